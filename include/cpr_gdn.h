@@ -1,0 +1,259 @@
+/*
+ * cpr_gdn.h -- C ABI of the Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet
+ * library for sm_103a (GB300).
+ *
+ * What the library computes.  Per (sequence, head) the gated delta rule
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t (scale q_t),       alpha_t = exp(g_t),
+ * with S_t of size d_v x d_k.  Source: page "IsoExec: 切换 SkyRL 中的训练器-
+ * 推理不匹配", section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet"
+ * (Gated DeltaNet; the recurrence is primary, parallelised across chunks of
+ * C tokens, and decode resynchronises the hidden state every C tokens), and
+ * the same page's "Bitwise Exact" row of its CPR table: trainer forward,
+ * rollout prefill and rollout decode must give identical bits.
+ *
+ * Execution contract.  Every call carries a cpr_contract and the SHA-256
+ * digest of its canonical serialisation.  The contract pins every choice
+ * that affects rounding (chunk size, dtypes, operand policy, reduction
+ * orders, chunk-to-state schedule, kernel build); the digest lets separate
+ * processes (trainer, rollout engine) prove they run the same numerical
+ * policy.  Source: page "IsoExec: bitpontos végrehajtással csökkentené az
+ * RL-rendszerek eltéréseit", section "Szerződés és közös modell" (contract
+ * fixing implementation, accumulation dtype, boundary dtype, reduction
+ * decomposition; SHA-256 digests), and page "IsoExec: 切换 SkyRL 中的训练器-
+ * 推理不匹配", section "合约结构与强制执行" (cases x regions, composition,
+ * claims, identities).  This library is one region with the cases
+ * trainer_fwd (cpr_gdn_fwd), engine_prefill (cpr_gdn_prefill) and decode
+ * (cpr_gdn_decode_step), plus the trainer backward (cpr_gdn_bwd).
+ *
+ * Layouts (all row-major, contiguous, token-major as a projection writes):
+ *     q, k          [n_tok, H, d_k]        io dtype
+ *     v             [n_tok, H, d_v]        io dtype
+ *     o             [n_tok, H, d_v]        out dtype (fp32)
+ *     g, beta       [n_tok, H]             fp32  (log-gate g <= 0; beta in (0,1))
+ *     h0, final     [n_seq, H, d_k, d_v]   fp32  (H = S^T, "state")
+ *     cu_seqlens    [n_seq + 1]            int32, cu[0] = 0, non-decreasing,
+ *                                          cu[n_seq] = n_tok (device memory)
+ *     decode tokens [n_seq, H, d]          one token per sequence per step
+ * Chunks restart at every sequence start; the last chunk of a sequence may
+ * be partial.
+ *
+ * Conventions.
+ *   - All pointers to tensors are DEVICE pointers owned by the caller; the
+ *     library never allocates or frees device memory and never synchronises
+ *     the host (except the functions that say so).
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t passed
+ *     as void*; NULL = legacy default stream).
+ *   - Tensor pointers must be 16-byte aligned (CPR_ERR_ALIGNMENT).  Token
+ *     tensors may be NULL when n_tok == 0.
+ *   - Host-side checks return an error code immediately and launch nothing.
+ *     Checks that need device data (cu_seqlens validity, the digest stored in
+ *     a decode cache) run on the device: on failure the kernels skip their
+ *     work and record the code in a device error word read by
+ *     cpr_get_device_error.  Nothing traps.
+ *   - cpr_last_error() returns a thread-local message for the last failure.
+ */
+#ifndef CPR_GDN_H
+#define CPR_GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define CPR_OK                     0
+#define CPR_ERR_INVALID_ARG        1  /* null/negative/inconsistent argument  */
+#define CPR_ERR_UNSUPPORTED        2  /* valid contract this build cannot run */
+#define CPR_ERR_ALIGNMENT          3  /* pointer not 16-byte aligned          */
+#define CPR_ERR_CONTRACT_MISMATCH  4  /* digest != SHA-256(contract), or a
+                                         decode cache made under another
+                                         contract (device-side)              */
+#define CPR_ERR_UNALIGNED          5  /* a prefill that does not start on a
+                                         chunk boundary                      */
+#define CPR_ERR_CUDA               6  /* a CUDA runtime call failed           */
+#define CPR_ERR_WORKSPACE          7  /* workspace null or too small          */
+#define CPR_ERR_BAD_SEQLENS        8  /* cu_seqlens invalid (device-side)     */
+
+/* ---- contract --------------------------------------------------------- */
+#define CPR_CONTRACT_VERSION 1u
+
+#define CPR_DTYPE_F32  1u
+#define CPR_DTYPE_BF16 2u
+
+/* operand_policy: how the within-chunk contractions are evaluated.
+ * SIMT_F32: every product and sum is an fp32 CUDA-core operation (fma
+ * chains in the order fixed by intra_order); io values are widened exactly. */
+#define CPR_POLICY_SIMT_F32 1u
+
+/* intra_order: id of the fixed within-chunk reduction orders.
+ * ROWSEQ_V1: gate prefix = serial fp32 sum in token order; every dot product
+ * an fma chain in ascending index order from +0; triangular solve by rows
+ * with the inner sums ascending.                                           */
+#define CPR_ORDER_ROWSEQ_V1 1u
+
+/* state_schedule: how chunk states are produced.
+ * SEQ_CHUNKS: H_{n+1} = f(H_n, chunk n) strictly in chunk order; d_v may be
+ * split across independent CTAs (columns of H evolve independently).       */
+#define CPR_SCHED_SEQ_CHUNKS 1u
+
+typedef struct cpr_contract {
+    uint32_t version;          /* CPR_CONTRACT_VERSION                          */
+    uint32_t chunk_size;       /* C; this build: 64                             */
+    uint32_t d_k;              /* this build: 64 or 128 (fp32 io: 64)           */
+    uint32_t d_v;              /* this build: equal to d_k                      */
+    uint32_t io_dtype;         /* q, k, v: CPR_DTYPE_BF16 or CPR_DTYPE_F32      */
+    uint32_t out_dtype;        /* o, dq, dk, dv: CPR_DTYPE_F32                  */
+    uint32_t gate_dtype;       /* g, beta, dg, dbeta: CPR_DTYPE_F32             */
+    uint32_t accum_dtype;      /* CPR_DTYPE_F32                                 */
+    uint32_t state_dtype;      /* chunk-boundary ("boundary dtype"): F32        */
+    uint32_t operand_policy;   /* CPR_POLICY_*                                  */
+    uint32_t intra_order;      /* CPR_ORDER_*                                   */
+    uint32_t state_schedule;   /* CPR_SCHED_*                                   */
+    uint32_t dv_splits;        /* CTAs per (seq, head) in the state pass: 1,2,4 */
+    float    scale;            /* multiplies q; finite                          */
+    uint32_t kernel_build_id;  /* must equal cpr_kernel_build_id()              */
+} cpr_contract;
+
+/* Identifier of this build's kernel arithmetic.  Bumped whenever any
+ * rounding-relevant detail of a kernel changes. */
+uint32_t cpr_kernel_build_id(void);
+
+/* Fill *c with this build's default contract for the given io dtype and head
+ * dims (C = 64, fp32 out/state/accumulation, SIMT_F32, ROWSEQ_V1,
+ * SEQ_CHUNKS, dv_splits = 4 for d_v = 128 else 2, scale = 1). */
+int cpr_contract_init_default(cpr_contract* c, uint32_t io_dtype, uint32_t d_k, uint32_t d_v);
+
+/* Canonical serialisation: the 16-byte tag "CPR-GDN-CONTRACT" followed by
+ * the 15 fields in declaration order, each as 4 little-endian bytes (scale
+ * as its IEEE-754 bit pattern) -- 76 bytes.  Writes the byte count to *len
+ * and, if out != NULL and *len was large enough on entry, the bytes. */
+int cpr_contract_serialize(const cpr_contract* c, uint8_t* out, size_t* len);
+
+/* SHA-256 (FIPS 180-4) of the canonical serialisation: the contract's
+ * numerical_policy identity. */
+int cpr_contract_digest(const cpr_contract* c, uint8_t out[32]);
+
+/* CPR_OK if this build can execute the contract, else INVALID_ARG or
+ * UNSUPPORTED with a message in cpr_last_error(). */
+int cpr_contract_check(const cpr_contract* c);
+
+/* Plain SHA-256 of a byte string (exposed so callers and tests can check the
+ * implementation against other SHA-256 implementations). */
+int cpr_sha256(const void* data, size_t len, uint8_t out[32]);
+
+/* ---- workspace and decode cache sizes --------------------------------- */
+#define CPR_OP_FWD 1   /* cpr_gdn_fwd and cpr_gdn_prefill */
+#define CPR_OP_BWD 2   /* cpr_gdn_bwd                     */
+
+/* Bytes of device workspace an op needs for a batch with n_seq sequences and
+ * n_tok tokens in total (an upper bound valid for any split of n_tok). */
+int cpr_gdn_workspace_size(const cpr_contract* c, int op, int n_seq, int64_t n_tok, int H,
+                           size_t* bytes);
+
+/* Decode cache: one caller-owned device blob per batch of n_seq sequences.
+ * It holds, per sequence, the position inside the current chunk and, per
+ * (sequence, head), the chunk-start state H_n plus the rows of the current
+ * partial chunk that the next decode steps need.  Sections (byte offsets
+ * from the blob start, each 256-byte aligned) are reported by
+ * cpr_decode_cache_layout. */
+typedef struct cpr_cache_layout {
+    size_t total_bytes;
+    size_t header;      /* 256 B: magic, version, digest[32], n_seq, H, C, d_k, d_v */
+    size_t pos;         /* int32  [n_seq]            tokens in the current chunk   */
+    size_t done;        /* uint32 [n_seq]            internal step counter (zero)  */
+    size_t state;       /* fp32   [n_seq, H, d_k, d_v] chunk-start state H_n      */
+    size_t k_rows;      /* io     [n_seq, H, C, d_k]                               */
+    size_t v_rows;      /* io     [n_seq, H, C, d_v]                               */
+    size_t gam_rows;    /* fp32   [n_seq, H, C]      in-chunk gate prefix          */
+    size_t beta_rows;   /* fp32   [n_seq, H, C]                                    */
+    size_t t_rows;      /* fp32   [n_seq, H, C, C]   rows of (I + A)^-1            */
+    size_t delta_rows;  /* fp32   [n_seq, H, C, d_v] rows of Delta                 */
+} cpr_cache_layout;
+
+int cpr_decode_cache_layout(const cpr_contract* c, int n_seq, int H, cpr_cache_layout* out);
+int cpr_decode_cache_bytes(const cpr_contract* c, int n_seq, int H, size_t* bytes);
+
+/* ---- compute entry points ---------------------------------------------- */
+
+/* Trainer forward (case trainer_fwd).  h0 and final_state may be NULL (h0 =
+ * zeros; final state not written).  o is required.  workspace: at least
+ * cpr_gdn_workspace_size(c, CPR_OP_FWD, ...) bytes, 256-byte aligned. */
+int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32],
+                const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                const float* h0, void* o, float* final_state,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Rollout prefill (case engine_prefill): the same arithmetic as cpr_gdn_fwd
+ * and, with the required cache, also initialises a decode cache (header with
+ * the digest, per-sequence position, the chunk-start state of each
+ * sequence's last chunk and that chunk's rows), so decoding continues exactly
+ * where the prefill stopped.  Every sequence starts on a chunk boundary (h0
+ * is the state at that boundary); a caller that continues a sequence from a
+ * cache whose position is not 0 must decode up to the boundary first. */
+int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32],
+                    const void* q, const void* k, const void* v, const float* g,
+                    const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
+                    int H, const float* h0, void* o, float* final_state, void* cache,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step (case decode) for n_seq sequences, one token each:
+ * q_t, k_t [n_seq, H, d_k], v_t [n_seq, H, d_v] (io dtype), g_t, beta_t
+ * [n_seq, H] fp32, o_t [n_seq, H, d_v] (out dtype).  Uses the same per-row
+ * arithmetic as the prefill's chunk kernels, so o_t and every committed
+ * chunk-boundary state equal a one-shot prefill's bits.  When a chunk fills,
+ * the step commits H_{n+1} into the cache (the resynchronisation every C
+ * tokens).  The cache's stored digest is checked on the device; on mismatch
+ * nothing is written and CPR_ERR_CONTRACT_MISMATCH is recorded. */
+int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32],
+                        const void* q_t, const void* k_t, const void* v_t, const float* g_t,
+                        const float* beta_t, int n_seq, int H, void* cache, void* o_t,
+                        void* stream);
+
+/* Trainer backward of cpr_gdn_fwd for the loss  <dO, o> + <dHT, final>.
+ * dHT and h0 may be NULL (zeros).  Outputs dq, dk [n_tok,H,d_k], dv
+ * [n_tok,H,d_v] (out dtype), dg, dbeta [n_tok,H] fp32, dh0 [n_seq,H,d_k,d_v]
+ * fp32 are all required.  workspace: cpr_gdn_workspace_size(c, CPR_OP_BWD). */
+int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32],
+                const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                const float* h0, const float* dO, const float* dHT,
+                void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- kernel timing ------------------------------------------------------ */
+
+/* Per-kernel timing collected with CUDA events recorded on the launching
+ * stream around every kernel this library launches between
+ * cpr_profile_begin and cpr_profile_end (process-wide).  Recording adds one
+ * event pair per launch; results are per kernel name. */
+typedef struct cpr_kernel_time {
+    char name[40];
+    uint32_t launches;
+    double total_ms;
+} cpr_kernel_time;
+
+/* Starts recording (discarding earlier records). */
+int cpr_profile_begin(void);
+
+/* Stops recording, SYNCHRONISES the device, and writes up to max_entries
+ * per-kernel totals to out (*n_entries = number of distinct kernels). */
+int cpr_profile_end(cpr_kernel_time* out, int max_entries, int* n_entries);
+
+/* ---- errors ------------------------------------------------------------ */
+
+/* Reads (and, if clear != 0, resets) the device error word of the current
+ * device.  SYNCHRONISES the device.  *code = CPR_OK if no kernel recorded an
+ * error since the last clear. */
+int cpr_get_device_error(uint32_t* code, int clear);
+
+/* Thread-local message describing the last non-OK return on this thread. */
+const char* cpr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPR_GDN_H */

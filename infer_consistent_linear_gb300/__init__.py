@@ -1,0 +1,313 @@
+"""Python binding of the CPR Gated DeltaNet library (libcpr_gdn.so).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/cpr_gdn.h.  PyTorch provides
+device memory and the current stream.  There is no fallback: if the shared
+library is missing or cannot be loaded, every entry point raises.
+
+Functions carry the C names: cpr_gdn_fwd, cpr_gdn_prefill,
+cpr_gdn_decode_step, cpr_gdn_bwd.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcpr_gdn.so")
+
+CPR_OK = 0
+ERRORS = {
+    1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CONTRACT_MISMATCH",
+    5: "UNALIGNED", 6: "CUDA", 7: "WORKSPACE", 8: "BAD_SEQLENS",
+}
+CPR_DTYPE_F32 = 1
+CPR_DTYPE_BF16 = 2
+CPR_POLICY_SIMT_F32 = 1
+CPR_ORDER_ROWSEQ_V1 = 1
+CPR_SCHED_SEQ_CHUNKS = 1
+CPR_OP_FWD = 1
+CPR_OP_BWD = 2
+
+
+class CprError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Contract(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint32) for n in (
+        "version", "chunk_size", "d_k", "d_v", "io_dtype", "out_dtype", "gate_dtype",
+        "accum_dtype", "state_dtype", "operand_policy", "intra_order", "state_schedule",
+        "dv_splits")] + [("scale", ctypes.c_float), ("kernel_build_id", ctypes.c_uint32)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class CacheLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "total_bytes", "header", "pos", "done", "state", "k_rows", "v_rows", "gam_rows",
+        "beta_rows", "t_rows", "delta_rows")]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_uint32),
+                ("total_ms", ctypes.c_double)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads the shared library (raises if it is absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"CPR GDN CUDA library not built: {path} is missing "
+                          "(run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P, I, U32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_int64, ctypes.c_size_t
+    CP = ctypes.POINTER(Contract)
+    sig = {
+        "cpr_kernel_build_id": (U32, []),
+        "cpr_contract_init_default": (I, [CP, U32, U32, U32]),
+        "cpr_contract_serialize": (I, [CP, P, ctypes.POINTER(SZ)]),
+        "cpr_contract_digest": (I, [CP, P]),
+        "cpr_contract_check": (I, [CP]),
+        "cpr_sha256": (I, [P, SZ, P]),
+        "cpr_gdn_workspace_size": (I, [CP, I, I, I64, I, ctypes.POINTER(SZ)]),
+        "cpr_decode_cache_layout": (I, [CP, I, I, ctypes.POINTER(CacheLayout)]),
+        "cpr_decode_cache_bytes": (I, [CP, I, I, ctypes.POINTER(SZ)]),
+        "cpr_gdn_fwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
+        "cpr_gdn_prefill": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, SZ, P]),
+        "cpr_gdn_decode_step": (I, [CP, P, P, P, P, P, P, I, I, P, P, P]),
+        "cpr_gdn_bwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
+                            P, SZ, P]),
+        "cpr_profile_begin": (I, []),
+        "cpr_profile_end": (I, [P, I, ctypes.POINTER(I)]),
+        "cpr_get_device_error": (I, [ctypes.POINTER(U32), I]),
+        "cpr_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != CPR_OK:
+        raise CprError(rc, _lib.cpr_last_error().decode())
+
+
+def kernel_build_id() -> int:
+    return load_library().cpr_kernel_build_id()
+
+
+def default_contract(io_dtype=torch.bfloat16, d_k: int = 128, d_v: Optional[int] = None,
+                     **overrides) -> Contract:
+    lib = load_library()
+    c = Contract()
+    dt = CPR_DTYPE_BF16 if io_dtype == torch.bfloat16 else CPR_DTYPE_F32
+    rc = lib.cpr_contract_init_default(ctypes.byref(c), dt, d_k, d_v or d_k)
+    for k_, v_ in overrides.items():
+        setattr(c, k_, v_)
+    if overrides:
+        rc = lib.cpr_contract_check(ctypes.byref(c))
+    _check(rc)
+    return c
+
+
+def contract_bytes(c: Contract) -> bytes:
+    lib = load_library()
+    n = ctypes.c_size_t(76)
+    buf = (ctypes.c_uint8 * 76)()
+    _check(lib.cpr_contract_serialize(ctypes.byref(c), buf, ctypes.byref(n)))
+    return bytes(buf[: n.value])
+
+
+def contract_digest(c: Contract) -> bytes:
+    lib = load_library()
+    out = (ctypes.c_uint8 * 32)()
+    _check(lib.cpr_contract_digest(ctypes.byref(c), out))
+    return bytes(out)
+
+
+def sha256(data: bytes) -> bytes:
+    lib = load_library()
+    out = (ctypes.c_uint8 * 32)()
+    buf = ctypes.create_string_buffer(data, len(data))
+    _check(lib.cpr_sha256(buf, len(data), out))
+    return bytes(out)
+
+
+def workspace_bytes(c: Contract, op: int, n_seq: int, n_tok: int, H: int) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib.cpr_gdn_workspace_size(ctypes.byref(c), op, n_seq, n_tok, H, ctypes.byref(n)))
+    return n.value
+
+
+def cache_layout(c: Contract, n_seq: int, H: int) -> CacheLayout:
+    lib = load_library()
+    out = CacheLayout()
+    _check(lib.cpr_decode_cache_layout(ctypes.byref(c), n_seq, H, ctypes.byref(out)))
+    return out
+
+
+def profile_begin():
+    """Start recording CUDA-event timings around every library kernel launch."""
+    _check(load_library().cpr_profile_begin())
+
+
+def profile_end() -> dict:
+    """Stop recording (synchronises); returns {kernel: (launches, total_ms)}."""
+    lib = load_library()
+    arr = (KernelTime * 32)()
+    n = ctypes.c_int(0)
+    _check(lib.cpr_profile_end(arr, 32, ctypes.byref(n)))
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, 32))}
+
+
+def get_device_error(clear: bool = True) -> int:
+    """Reads (and clears) the device error word.  Synchronises the device."""
+    lib = load_library()
+    code = ctypes.c_uint32(0)
+    _check(lib.cpr_get_device_error(ctypes.byref(code), int(clear)))
+    return code.value
+
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None or t.numel() == 0:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dig(c: Contract, digest: Optional[bytes]):
+    d = digest if digest is not None else contract_digest(c)
+    return (ctypes.c_uint8 * 32).from_buffer_copy(d)
+
+
+def _ws(c, op, n_seq, n_tok, H, device, workspace):
+    need = workspace_bytes(c, op, n_seq, n_tok, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel()
+
+
+@dataclass
+class DecodeCache:
+    """A caller-owned decode cache blob plus its section layout."""
+    blob: torch.Tensor
+    layout: CacheLayout
+    n_seq: int
+    H: int
+    d_k: int
+    d_v: int
+
+    def state(self) -> torch.Tensor:
+        """Chunk-start states H_n, [n_seq, H, d_k, d_v] fp32 (a view)."""
+        n = self.n_seq * self.H * self.d_k * self.d_v
+        o = self.layout.state
+        return self.blob[o:o + 4 * n].view(torch.float32).view(self.n_seq, self.H, self.d_k, self.d_v)
+
+    def pos(self) -> torch.Tensor:
+        o = self.layout.pos
+        return self.blob[o:o + 4 * self.n_seq].view(torch.int32)
+
+
+def new_decode_cache(c: Contract, n_seq: int, H: int, device) -> DecodeCache:
+    lay = cache_layout(c, n_seq, H)
+    blob = torch.zeros(lay.total_bytes, dtype=torch.uint8, device=device)
+    return DecodeCache(blob, lay, n_seq, H, c.d_k, c.d_v)
+
+
+def _shape_args(q, v, cu_seqlens):
+    n_tok, H, _ = q.shape
+    return int(n_tok), int(H), int(cu_seqlens.numel() - 1)
+
+
+def cpr_gdn_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
+                digest: Optional[bytes] = None, want_final: bool = True, out=None,
+                final=None, workspace=None):
+    """Trainer forward.  Returns (o [n_tok,H,d_v] fp32, final [n_seq,H,d_k,d_v] or None)."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    o = out if out is not None else torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
+    fin = final if final is not None else (
+        torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device) if want_final else None)
+    ws, wsb = _ws(c, CPR_OP_FWD, n_seq, n_tok, H, q.device, workspace)
+    _check(lib.cpr_gdn_fwd(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                           _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
+                           _ptr(fin), _ptr(ws), wsb, _stream()))
+    return o, fin
+
+
+def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
+                    digest: Optional[bytes] = None, want_final: bool = True, cache=None,
+                    out=None, workspace=None):
+    """Rollout prefill.  Returns (o, final or None, DecodeCache)."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    o = out if out is not None else torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
+    fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device) if want_final else None
+    cache = cache or new_decode_cache(c, n_seq, H, q.device)
+    ws, wsb = _ws(c, CPR_OP_FWD, n_seq, n_tok, H, q.device, workspace)
+    _check(lib.cpr_gdn_prefill(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v),
+                               _ptr(g), _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0),
+                               _ptr(o), _ptr(fin), _ptr(cache.blob), _ptr(ws), wsb, _stream()))
+    return o, fin, cache
+
+
+def cpr_gdn_decode_step(q_t, k_t, v_t, g_t, beta_t, cache: DecodeCache,
+                        contract: Optional[Contract] = None, digest: Optional[bytes] = None,
+                        out=None):
+    """One decode step; tokens [n_seq, H, d].  Returns o_t [n_seq, H, d_v] fp32."""
+    lib = load_library()
+    c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
+    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
+    o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
+    _check(lib.cpr_gdn_decode_step(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t),
+                                   _ptr(v_t), _ptr(g_t), _ptr(beta_t), n_seq, H,
+                                   _ptr(cache.blob), _ptr(o), _stream()))
+    return o
+
+
+def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
+                contract: Optional[Contract] = None, digest: Optional[bytes] = None,
+                workspace=None, outs=None):
+    """Trainer backward.  Returns dict dq, dk, dv (fp32), dg, dbeta, dh0."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    dev = q.device
+    if outs is None:
+        outs = dict(dq=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
+                    dk=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
+                    dv=torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=dev),
+                    dg=torch.empty(n_tok, H, dtype=torch.float32, device=dev),
+                    dbeta=torch.empty(n_tok, H, dtype=torch.float32, device=dev),
+                    dh0=torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=dev))
+    ws, wsb = _ws(c, CPR_OP_BWD, n_seq, n_tok, H, dev, workspace)
+    _check(lib.cpr_gdn_bwd(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                           _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(dO),
+                           _ptr(dHT), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]),
+                           _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),
+                           wsb, _stream()))
+    return outs

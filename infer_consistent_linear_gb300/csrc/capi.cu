@@ -1,0 +1,447 @@
+// C ABI of the CPR Gated DeltaNet library: contract handling, argument and
+// claim checks, workspace / cache layouts and kernel dispatch.  Declarations
+// and their documentation are in include/cpr_gdn.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "cpr_gdn.h"
+#include "profile.h"
+#include "sha256.h"
+#include "simt_launch.cuh"
+
+namespace {
+
+// Bumped whenever any rounding-relevant detail of a kernel changes.
+constexpr uint32_t kKernelBuildId = 1u;
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+}  // namespace
+
+// Device error word: first recorded error code, 0 = none.
+__device__ uint32_t g_cpr_device_error = 0u;
+
+namespace {
+
+uint32_t* device_error_ptr() {
+    static std::mutex mu;
+    static uint32_t* ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_cpr_device_error) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<uint32_t*>(p);
+    }
+    return ptrs[dev];
+}
+
+size_t io_size(uint32_t dt) { return dt == CPR_DTYPE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+void serialize(const cpr_contract& c, uint8_t out[76]) {
+    static const char tag[17] = "CPR-GDN-CONTRACT";
+    std::memcpy(out, tag, 16);
+    uint32_t f[15];
+    f[0] = c.version; f[1] = c.chunk_size; f[2] = c.d_k; f[3] = c.d_v; f[4] = c.io_dtype;
+    f[5] = c.out_dtype; f[6] = c.gate_dtype; f[7] = c.accum_dtype; f[8] = c.state_dtype;
+    f[9] = c.operand_policy; f[10] = c.intra_order; f[11] = c.state_schedule;
+    f[12] = c.dv_splits;
+    std::memcpy(&f[13], &c.scale, 4);
+    f[14] = c.kernel_build_id;
+    for (int i = 0; i < 15; ++i)
+        for (int b = 0; b < 4; ++b) out[16 + 4 * i + b] = (uint8_t)(f[i] >> (8 * b));
+}
+
+int check_contract(const cpr_contract* c) {
+    if (!c) return fail(CPR_ERR_INVALID_ARG, "contract is NULL");
+    if (c->version != CPR_CONTRACT_VERSION) return fail(CPR_ERR_UNSUPPORTED, "contract version %u", c->version);
+    if (c->chunk_size != 64) return fail(CPR_ERR_UNSUPPORTED, "chunk_size %u (this build: 64)", c->chunk_size);
+    if (c->d_k != c->d_v) return fail(CPR_ERR_UNSUPPORTED, "d_k != d_v");
+    if (c->io_dtype == CPR_DTYPE_BF16) {
+        if (c->d_k != 64 && c->d_k != 128) return fail(CPR_ERR_UNSUPPORTED, "d_k %u (bf16: 64 or 128)", c->d_k);
+    } else if (c->io_dtype == CPR_DTYPE_F32) {
+        if (c->d_k != 64) return fail(CPR_ERR_UNSUPPORTED, "d_k %u (fp32 io: 64)", c->d_k);
+    } else {
+        return fail(CPR_ERR_UNSUPPORTED, "io_dtype %u", c->io_dtype);
+    }
+    if (c->out_dtype != CPR_DTYPE_F32 || c->gate_dtype != CPR_DTYPE_F32 ||
+        c->accum_dtype != CPR_DTYPE_F32 || c->state_dtype != CPR_DTYPE_F32)
+        return fail(CPR_ERR_UNSUPPORTED, "out/gate/accum/state dtype must be F32");
+    if (c->operand_policy != CPR_POLICY_SIMT_F32) return fail(CPR_ERR_UNSUPPORTED, "operand_policy %u", c->operand_policy);
+    if (c->intra_order != CPR_ORDER_ROWSEQ_V1) return fail(CPR_ERR_UNSUPPORTED, "intra_order %u", c->intra_order);
+    if (c->state_schedule != CPR_SCHED_SEQ_CHUNKS) return fail(CPR_ERR_UNSUPPORTED, "state_schedule %u", c->state_schedule);
+    if (c->dv_splits != 1 && c->dv_splits != 2 && c->dv_splits != 4)
+        return fail(CPR_ERR_UNSUPPORTED, "dv_splits %u (1, 2 or 4)", c->dv_splits);
+    if (!std::isfinite(c->scale)) return fail(CPR_ERR_INVALID_ARG, "scale not finite");
+    if (c->kernel_build_id != kKernelBuildId)
+        return fail(CPR_ERR_UNSUPPORTED, "kernel_build_id %u (this build: %u)", c->kernel_build_id, kKernelBuildId);
+    return CPR_OK;
+}
+
+int check_digest(const cpr_contract* c, const uint8_t* digest) {
+    int rc = check_contract(c);
+    if (rc) return rc;
+    if (!digest) return fail(CPR_ERR_INVALID_ARG, "digest is NULL");
+    uint8_t buf[76], d[32];
+    serialize(*c, buf);
+    cpr::sha256(buf, sizeof(buf), d);
+    if (std::memcmp(d, digest, 32) != 0)
+        return fail(CPR_ERR_CONTRACT_MISMATCH, "digest does not match SHA-256 of the contract");
+    return CPR_OK;
+}
+
+struct WsLayout {
+    size_t chunk_off, W, U, P, gam, T, Kd, Hn, dH, total;
+    int64_t cmax;
+};
+
+WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int H) {
+    WsLayout w{};
+    const size_t C = c.chunk_size, dk = c.d_k, dv = c.d_v;
+    w.cmax = n_tok / (int64_t)C + n_seq;
+    const size_t ch = (size_t)w.cmax * (size_t)H;
+    size_t off = 0;
+    auto add = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
+    add(w.chunk_off, sizeof(int32_t) * (n_seq + 1));
+    add(w.W, ch * C * dk * 4);
+    add(w.U, ch * C * dv * 4);
+    add(w.P, ch * C * C * 4);
+    add(w.gam, ch * C * 4);
+    if (op == CPR_OP_BWD) {
+        add(w.T, ch * C * C * 4);
+        add(w.Kd, ch * C * C * 4);
+        add(w.Hn, ch * dk * dv * 4);
+        add(w.dH, ch * dk * dv * 4);
+    }
+    w.total = off;
+    return w;
+}
+
+cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
+    cpr_cache_layout l{};
+    const size_t C = c.chunk_size, dk = c.d_k, dv = c.d_v, io = io_size(c.io_dtype);
+    const size_t sh = (size_t)n_seq * H;
+    size_t off = 0;
+    auto add = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
+    add(l.header, 256);
+    add(l.pos, 4 * (size_t)n_seq);
+    add(l.done, 4 * (size_t)n_seq);
+    add(l.state, sh * dk * dv * 4);
+    add(l.k_rows, sh * C * dk * io);
+    add(l.v_rows, sh * C * dv * io);
+    add(l.gam_rows, sh * C * 4);
+    add(l.beta_rows, sh * C * 4);
+    add(l.t_rows, sh * C * C * 4);
+    add(l.delta_rows, sh * C * dv * 4);
+    l.total_bytes = off;
+    return l;
+}
+
+cpr::CacheOff to_off(const cpr_cache_layout& l) {
+    return cpr::CacheOff{l.header, l.pos, l.done, l.state, l.k_rows, l.v_rows,
+                         l.gam_rows, l.beta_rows, l.t_rows, l.delta_rows};
+}
+
+const cpr::SimtOps* ops_for(const cpr_contract& c) {
+    if (c.io_dtype == CPR_DTYPE_BF16) return c.d_k == 64 ? cpr::simt_ops_bf16_d64() : cpr::simt_ops_bf16_d128();
+    return cpr::simt_ops_f32_d64();
+}
+
+cpr::Digest digest_words(const uint8_t* d) {
+    cpr::Digest w;
+    std::memcpy(w.w, d, 32);
+    return w;
+}
+
+void header_words(const cpr_contract& c, int n_seq, int H, uint32_t out[7]) {
+    out[0] = (uint32_t)n_seq; out[1] = (uint32_t)H; out[2] = c.chunk_size; out[3] = c.d_k;
+    out[4] = c.d_v; out[5] = c.operand_policy; out[6] = c.io_dtype;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(CPR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define REQ_PTR(p)                                                             \
+    do {                                                                       \
+        if (!(p)) return fail(CPR_ERR_INVALID_ARG, "%s is NULL", #p);          \
+        if (!aligned16(p)) return fail(CPR_ERR_ALIGNMENT, "%s not 16-byte aligned", #p); \
+    } while (0)
+#define OPT_PTR(p)                                                             \
+    do {                                                                       \
+        if ((p) && !aligned16(p)) return fail(CPR_ERR_ALIGNMENT, "%s not 16-byte aligned", #p); \
+    } while (0)
+
+int check_sizes(int n_seq, int64_t n_tok, int H) {
+    if (n_seq < 0 || n_tok < 0 || H <= 0) return fail(CPR_ERR_INVALID_ARG, "n_seq/n_tok/H out of range");
+    if (n_tok > INT32_MAX) return fail(CPR_ERR_INVALID_ARG, "n_tok exceeds int32 (cu_seqlens is int32)");
+    if ((int64_t)n_seq * H > INT32_MAX / 4) return fail(CPR_ERR_INVALID_ARG, "n_seq * H too large");
+    return CPR_OK;
+}
+
+cudaError_t launch_setup(const cpr::simt::SetupArgs& sa, cudaStream_t st) {
+    cpr::ProfScope ps("cpr_setup", st);
+    cpr::simt::k_setup<<<1, 256, 0, st>>>(sa);
+    return cudaGetLastError();
+}
+
+// Shared by cpr_gdn_fwd and cpr_gdn_prefill: one code path, so the trainer
+// forward and the engine prefill run identical kernels.
+int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
+                 const void* v, const float* g, const float* beta, const int32_t* cu, int n_seq,
+                 int64_t n_tok, int H, const float* h0, void* o, float* final_state, void* cache,
+                 void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_digest(c, digest);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, n_tok, H);
+    if (rc) return rc;
+    REQ_PTR(cu);
+    if (n_tok > 0) {
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR(g); REQ_PTR(beta); REQ_PTR(o);
+    }
+    OPT_PTR(h0); OPT_PTR(final_state); OPT_PTR(cache);
+    const WsLayout w = ws_layout(*c, CPR_OP_FWD, n_seq, n_tok, H);
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return fail(CPR_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", w.total);
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+
+    cpr::simt::SetupArgs sa{};
+    sa.cu = cu; sa.n_seq = n_seq; sa.n_tok = n_tok;
+    sa.chunk_off = reinterpret_cast<int32_t*>(wsb + w.chunk_off);
+    sa.cache = static_cast<uint8_t*>(cache); sa.co = to_off(cl);
+    sa.digest = digest_words(digest); header_words(*c, n_seq, H, sa.hdr); sa.err = err;
+    cudaError_t e = launch_setup(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "setup launch");
+
+    cpr::simt::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu; a.chunk_off = sa.chunk_off;
+    a.n_seq = n_seq; a.H = H; a.scale = c->scale;
+    a.wsW = reinterpret_cast<float*>(wsb + w.W); a.wsU = reinterpret_cast<float*>(wsb + w.U);
+    a.wsP = reinterpret_cast<float*>(wsb + w.P); a.wsGam = reinterpret_cast<float*>(wsb + w.gam);
+    a.h0 = h0; a.o = o; a.final_state = final_state;
+    a.cache = static_cast<uint8_t*>(cache); a.co = to_off(cl); a.err = err;
+    cpr::LaunchCfg L{w.cmax, n_seq, H, (int)c->dv_splits, st};
+    e = ops_for(*c)->fwd(a, L);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return CPR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t cpr_kernel_build_id(void) { return kKernelBuildId; }
+
+int cpr_contract_init_default(cpr_contract* c, uint32_t io_dtype, uint32_t d_k, uint32_t d_v) {
+    if (!c) return fail(CPR_ERR_INVALID_ARG, "contract is NULL");
+    std::memset(c, 0, sizeof(*c));
+    c->version = CPR_CONTRACT_VERSION;
+    c->chunk_size = 64;
+    c->d_k = d_k;
+    c->d_v = d_v;
+    c->io_dtype = io_dtype;
+    c->out_dtype = CPR_DTYPE_F32;
+    c->gate_dtype = CPR_DTYPE_F32;
+    c->accum_dtype = CPR_DTYPE_F32;
+    c->state_dtype = CPR_DTYPE_F32;
+    c->operand_policy = CPR_POLICY_SIMT_F32;
+    c->intra_order = CPR_ORDER_ROWSEQ_V1;
+    c->state_schedule = CPR_SCHED_SEQ_CHUNKS;
+    c->dv_splits = d_v >= 128 ? 4 : 2;
+    c->scale = 1.0f;
+    c->kernel_build_id = kKernelBuildId;
+    return check_contract(c);
+}
+
+int cpr_contract_serialize(const cpr_contract* c, uint8_t* out, size_t* len) {
+    if (!c || !len) return fail(CPR_ERR_INVALID_ARG, "NULL argument");
+    const size_t need = 76;
+    const size_t have = *len;
+    *len = need;
+    if (out) {
+        if (have < need) return fail(CPR_ERR_INVALID_ARG, "buffer too small (%zu < 76)", have);
+        serialize(*c, out);
+    }
+    return CPR_OK;
+}
+
+int cpr_contract_digest(const cpr_contract* c, uint8_t out[32]) {
+    if (!c || !out) return fail(CPR_ERR_INVALID_ARG, "NULL argument");
+    uint8_t buf[76];
+    serialize(*c, buf);
+    cpr::sha256(buf, sizeof(buf), out);
+    return CPR_OK;
+}
+
+int cpr_contract_check(const cpr_contract* c) { return check_contract(c); }
+
+int cpr_sha256(const void* data, size_t len, uint8_t out[32]) {
+    if ((!data && len) || !out) return fail(CPR_ERR_INVALID_ARG, "NULL argument");
+    cpr::sha256(data, len, out);
+    return CPR_OK;
+}
+
+int cpr_gdn_workspace_size(const cpr_contract* c, int op, int n_seq, int64_t n_tok, int H,
+                           size_t* bytes) {
+    int rc = check_contract(c);
+    if (rc) return rc;
+    if (!bytes) return fail(CPR_ERR_INVALID_ARG, "bytes is NULL");
+    if (op != CPR_OP_FWD && op != CPR_OP_BWD) return fail(CPR_ERR_INVALID_ARG, "op %d", op);
+    rc = check_sizes(n_seq, n_tok, H);
+    if (rc) return rc;
+    *bytes = ws_layout(*c, op, n_seq, n_tok, H).total;
+    return CPR_OK;
+}
+
+int cpr_decode_cache_layout(const cpr_contract* c, int n_seq, int H, cpr_cache_layout* out) {
+    int rc = check_contract(c);
+    if (rc) return rc;
+    if (!out) return fail(CPR_ERR_INVALID_ARG, "out is NULL");
+    rc = check_sizes(n_seq, 0, H);
+    if (rc) return rc;
+    *out = cache_layout(*c, n_seq, H);
+    return CPR_OK;
+}
+
+int cpr_decode_cache_bytes(const cpr_contract* c, int n_seq, int H, size_t* bytes) {
+    if (!bytes) return fail(CPR_ERR_INVALID_ARG, "bytes is NULL");
+    cpr_cache_layout l;
+    int rc = cpr_decode_cache_layout(c, n_seq, H, &l);
+    if (rc) return rc;
+    *bytes = l.total_bytes;
+    return CPR_OK;
+}
+
+int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32], const void* q, const void* k,
+                const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                int n_seq, int64_t n_tok, int H, const float* h0, void* o, float* final_state,
+                void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                        final_state, nullptr, workspace, workspace_bytes, stream);
+}
+
+int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                    const void* k, const void* v, const float* g, const float* beta,
+                    const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H, const float* h0,
+                    void* o, float* final_state, void* cache, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (!cache) return fail(CPR_ERR_INVALID_ARG, "cache is NULL (use cpr_gdn_fwd without a cache)");
+    return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                        final_state, cache, workspace, workspace_bytes, stream);
+}
+
+int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
+                        const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
+                        int n_seq, int H, void* cache, void* o_t, void* stream) {
+    int rc = check_digest(c, digest);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, 0, H);
+    if (rc) return rc;
+    REQ_PTR(cache);
+    if (n_seq > 0) {
+        REQ_PTR(q_t); REQ_PTR(k_t); REQ_PTR(v_t); REQ_PTR(g_t); REQ_PTR(beta_t); REQ_PTR(o_t);
+    }
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+    cpr::simt::DecArgs a{};
+    a.q = q_t; a.k = k_t; a.v = v_t; a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
+    a.scale = c->scale; a.cache = static_cast<uint8_t*>(cache); a.co = to_off(cl);
+    a.digest = digest_words(digest); header_words(*c, n_seq, H, a.hdr);
+    a.o = static_cast<float*>(o_t); a.err = err;
+    cpr::LaunchCfg L{0, n_seq, H, (int)c->dv_splits, static_cast<cudaStream_t>(stream)};
+    const cudaError_t e = ops_for(*c)->decode(a, L);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return CPR_OK;
+}
+
+int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, const void* k,
+                const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
+                const float* dHT, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_digest(c, digest);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, n_tok, H);
+    if (rc) return rc;
+    REQ_PTR(cu_seqlens);
+    if (n_seq > 0) REQ_PTR(dh0);
+    if (n_tok > 0) {
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR(g); REQ_PTR(beta);
+        REQ_PTR(dO); REQ_PTR(dq); REQ_PTR(dk); REQ_PTR(dv); REQ_PTR(dg); REQ_PTR(dbeta);
+    }
+    OPT_PTR(h0); OPT_PTR(dHT);
+    const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
+    if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(CPR_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", w.total);
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+
+    cpr::simt::SetupArgs sa{};
+    sa.cu = cu_seqlens; sa.n_seq = n_seq; sa.n_tok = n_tok;
+    sa.chunk_off = reinterpret_cast<int32_t*>(wsb + w.chunk_off); sa.err = err;
+    cudaError_t e = launch_setup(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "setup launch");
+
+    cpr::simt::FwdArgs fa{};
+    fa.q = q; fa.k = k; fa.v = v; fa.g = g; fa.beta = beta; fa.cu = cu_seqlens;
+    fa.chunk_off = sa.chunk_off; fa.n_seq = n_seq; fa.H = H; fa.scale = c->scale;
+    fa.wsW = reinterpret_cast<float*>(wsb + w.W); fa.wsU = reinterpret_cast<float*>(wsb + w.U);
+    fa.wsP = reinterpret_cast<float*>(wsb + w.P); fa.wsGam = reinterpret_cast<float*>(wsb + w.gam);
+    fa.wsT = reinterpret_cast<float*>(wsb + w.T); fa.wsKd = reinterpret_cast<float*>(wsb + w.Kd);
+    fa.wsHn = reinterpret_cast<float*>(wsb + w.Hn);
+    fa.h0 = h0; fa.o = nullptr; fa.final_state = nullptr; fa.cache = nullptr; fa.err = err;
+
+    cpr::simt::BwdArgs ba{};
+    ba.q = q; ba.k = k; ba.v = v; ba.g = g; ba.beta = beta; ba.cu = cu_seqlens;
+    ba.chunk_off = sa.chunk_off; ba.n_seq = n_seq; ba.H = H; ba.scale = c->scale;
+    ba.dO = dO; ba.dHT = dHT;
+    ba.wsW = fa.wsW; ba.wsU = fa.wsU; ba.wsP = fa.wsP; ba.wsGam = fa.wsGam; ba.wsT = fa.wsT;
+    ba.wsKd = fa.wsKd; ba.wsHn = fa.wsHn; ba.wsdH = reinterpret_cast<float*>(wsb + w.dH);
+    ba.dq = static_cast<float*>(dq); ba.dk = static_cast<float*>(dk); ba.dv = static_cast<float*>(dv);
+    ba.dg = dg; ba.dbeta = dbeta; ba.dh0 = dh0; ba.err = err;
+    cpr::LaunchCfg L{w.cmax, n_seq, H, (int)c->dv_splits, st};
+    e = ops_for(*c)->bwd(fa, ba, L);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return CPR_OK;
+}
+
+int cpr_get_device_error(uint32_t* code, int clear) {
+    if (!code) return fail(CPR_ERR_INVALID_ARG, "code is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "synchronize");
+    e = cudaMemcpyFromSymbol(code, g_cpr_device_error, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "read device error");
+    if (clear) {
+        const uint32_t zero = 0u;
+        e = cudaMemcpyToSymbol(g_cpr_device_error, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error");
+    }
+    return CPR_OK;
+}
+
+const char* cpr_last_error(void) { return g_msg; }
+
+}  // extern "C"

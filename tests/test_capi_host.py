@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and
+exports every function include/cpr_gdn.h declares; contract serialisation,
+SHA-256 digest and claim checks; layouts; argument validation paths that
+return before any CUDA call."""
+import ctypes
+import hashlib
+import os
+import re
+import struct
+
+import pytest
+import torch
+
+import infer_consistent_linear_gb300 as cpr
+from infer_consistent_linear_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cpr_gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return cpr.load_library()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpr_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@pytest.mark.parametrize("n", [0, 1, 3, 55, 56, 63, 64, 65, 119, 120, 1000])
+def test_sha256_matches_hashlib(lib, n):
+    data = bytes((i * 37 + 11) & 0xFF for i in range(n))
+    assert cpr.sha256(data) == hashlib.sha256(data).digest()
+
+
+def test_contract_serialisation_and_digest(lib):
+    c = cpr.default_contract(torch.bfloat16, 128)
+    raw = cpr.contract_bytes(c)
+    assert len(raw) == 76 and raw[:16] == b"CPR-GDN-CONTRACT"
+    fields = struct.unpack("<13IfI", raw[16:])
+    assert fields[0] == 1 and fields[1] == 64 and fields[2] == 128 and fields[3] == 128
+    assert fields[13] == 1.0 and fields[14] == cpr.kernel_build_id()
+    assert cpr.contract_digest(c) == hashlib.sha256(raw).digest()
+
+
+def test_digest_changes_with_every_field(lib):
+    base = cpr.default_contract(torch.bfloat16, 128)
+    seen = {cpr.contract_digest(base)}
+    for name, _ in cpr.Contract._fields_:
+        c = cpr.Contract.from_buffer_copy(base)
+        if name == "scale":
+            c.scale = 0.5
+        else:
+            setattr(c, name, getattr(c, name) + 1)
+        d = cpr.contract_digest(c)
+        assert d not in seen, name
+        seen.add(d)
+
+
+def test_contract_checks(lib):
+    c = cpr.default_contract(torch.bfloat16, 128)
+    assert lib.cpr_contract_check(ctypes.byref(c)) == 0
+    for field, val in [("chunk_size", 32), ("d_k", 96), ("operand_policy", 9), ("dv_splits", 3),
+                       ("kernel_build_id", 999), ("version", 2), ("out_dtype", cpr.CPR_DTYPE_BF16)]:
+        x = cpr.Contract.from_buffer_copy(c)
+        setattr(x, field, val)
+        assert lib.cpr_contract_check(ctypes.byref(x)) == 2, field
+    x = cpr.Contract.from_buffer_copy(c)
+    x.scale = float("nan")
+    assert lib.cpr_contract_check(ctypes.byref(x)) == 1
+    with pytest.raises(cpr.CprError):
+        cpr.default_contract(torch.float32, 128)  # fp32 io: d = 64 only
+
+
+def test_workspace_and_cache_layout(lib):
+    c = cpr.default_contract(torch.bfloat16, 128)
+    f = cpr.workspace_bytes(c, cpr.CPR_OP_FWD, 4, 4 * 4096, 16)
+    b = cpr.workspace_bytes(c, cpr.CPR_OP_BWD, 4, 4 * 4096, 16)
+    chunks = (4 * 4096) // 64 + 4
+    assert f >= chunks * 16 * (64 * 128 * 4 * 2 + 64 * 64 * 4)
+    assert b > f
+    lay = cpr.cache_layout(c, 64, 32)
+    offs = [lay.header, lay.pos, lay.done, lay.state, lay.k_rows, lay.v_rows, lay.gam_rows,
+            lay.beta_rows, lay.t_rows, lay.delta_rows]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lay.k_rows - lay.state >= 64 * 32 * 128 * 128 * 4
+    assert lay.total_bytes >= lay.delta_rows + 64 * 32 * 64 * 128 * 4
+
+
+def _call_fwd(lib, c, digest, ptrs, n_seq=1, n_tok=64, H=1, ws_bytes=1 << 30):
+    q, k, v, g, beta, cu, o, ws = ptrs
+    return lib.cpr_gdn_fwd(ctypes.byref(c), digest, q, k, v, g, beta, cu, n_seq, n_tok, H, None, o,
+                           None, ws, ws_bytes, None)
+
+
+def test_host_argument_errors(lib):
+    c = cpr.default_contract(torch.bfloat16, 128)
+    dig = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(c))
+    good = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    bad = (ctypes.c_uint8 * 32).from_buffer_copy(bytes(32))
+    assert _call_fwd(lib, c, bad, good) == 4          # digest mismatch
+    p = list(good)
+    p[0] = None
+    assert _call_fwd(lib, c, dig, p) == 1             # null q
+    p = list(good)
+    p[2] = ctypes.c_void_p(0x10008)
+    assert _call_fwd(lib, c, dig, p) == 3             # misaligned v
+    assert _call_fwd(lib, c, dig, good, H=0) == 1
+    assert _call_fwd(lib, c, dig, good, n_seq=-1) == 1
+    assert _call_fwd(lib, c, dig, good, ws_bytes=16) == 7
+    p = list(good)
+    p[7] = ctypes.c_void_p(0x10010)
+    assert _call_fwd(lib, c, dig, p) == 7             # workspace not 256-aligned
+    x = cpr.Contract.from_buffer_copy(c)
+    x.chunk_size = 128
+    dx = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(x))
+    assert _call_fwd(lib, x, dx, good) == 2           # unsupported, even with its own digest
+    assert "chunk_size" in lib.cpr_last_error().decode()
+    assert lib.cpr_gdn_prefill(ctypes.byref(c), dig, *good[:6], 1, 64, 1, None, good[6], None,
+                               None, good[7], 1 << 30, None) == 1   # cache required
+    assert lib.cpr_gdn_decode_step(ctypes.byref(c), dig, *good[:5], 1, 1, None, good[6], None) == 1
