@@ -44,8 +44,9 @@
  *     the host (except the functions that say so).
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t passed
  *     as void*; NULL = legacy default stream).
- *   - Tensor pointers must be 16-byte aligned (CPR_ERR_ALIGNMENT).  Token
- *     tensors may be NULL when n_tok == 0.
+ *   - Tensor pointers must be 16-byte aligned, except the per-token scalar
+ *     tensors (g, beta, dg, dbeta) and cu_seqlens, which need 4 bytes
+ *     (CPR_ERR_ALIGNMENT).  Token tensors may be NULL when n_tok == 0.
  *   - Host-side checks return an error code immediately and launch nothing.
  *     Checks that need device data (cu_seqlens validity, the digest stored in
  *     a decode cache) run on the device: on failure the kernels skip their

@@ -183,6 +183,11 @@ int cuda_fail(cudaError_t e, const char* what) {
         if (!(p)) return fail(CPR_ERR_INVALID_ARG, "%s is NULL", #p);          \
         if (!aligned16(p)) return fail(CPR_ERR_ALIGNMENT, "%s not 16-byte aligned", #p); \
     } while (0)
+#define REQ_PTR4(p)                                                            \
+    do {                                                                       \
+        if (!(p)) return fail(CPR_ERR_INVALID_ARG, "%s is NULL", #p);          \
+        if (reinterpret_cast<uintptr_t>(p) & 3u) return fail(CPR_ERR_ALIGNMENT, "%s not 4-byte aligned", #p); \
+    } while (0)
 #define OPT_PTR(p)                                                             \
     do {                                                                       \
         if ((p) && !aligned16(p)) return fail(CPR_ERR_ALIGNMENT, "%s not 16-byte aligned", #p); \
@@ -211,9 +216,9 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
     if (rc) return rc;
     rc = check_sizes(n_seq, n_tok, H);
     if (rc) return rc;
-    REQ_PTR(cu);
+    REQ_PTR4(cu);
     if (n_tok > 0) {
-        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR(g); REQ_PTR(beta); REQ_PTR(o);
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta); REQ_PTR(o);
     }
     OPT_PTR(h0); OPT_PTR(final_state); OPT_PTR(cache);
     const WsLayout w = ws_layout(*c, CPR_OP_FWD, n_seq, n_tok, H);
@@ -359,7 +364,7 @@ int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const v
     if (rc) return rc;
     REQ_PTR(cache);
     if (n_seq > 0) {
-        REQ_PTR(q_t); REQ_PTR(k_t); REQ_PTR(v_t); REQ_PTR(g_t); REQ_PTR(beta_t); REQ_PTR(o_t);
+        REQ_PTR(q_t); REQ_PTR(k_t); REQ_PTR(v_t); REQ_PTR4(g_t); REQ_PTR4(beta_t); REQ_PTR(o_t);
     }
     uint32_t* err = device_error_ptr();
     if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
@@ -384,11 +389,11 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
     if (rc) return rc;
     rc = check_sizes(n_seq, n_tok, H);
     if (rc) return rc;
-    REQ_PTR(cu_seqlens);
+    REQ_PTR4(cu_seqlens);
     if (n_seq > 0) REQ_PTR(dh0);
     if (n_tok > 0) {
-        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR(g); REQ_PTR(beta);
-        REQ_PTR(dO); REQ_PTR(dq); REQ_PTR(dk); REQ_PTR(dv); REQ_PTR(dg); REQ_PTR(dbeta);
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta);
+        REQ_PTR(dO); REQ_PTR(dq); REQ_PTR(dk); REQ_PTR(dv); REQ_PTR4(dg); REQ_PTR4(dbeta);
     }
     OPT_PTR(h0); OPT_PTR(dHT);
     const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
