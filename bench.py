@@ -207,6 +207,7 @@ class OurStep:
             self.tok = [t.index_select(0, idx).view(n_decode_steps, n_seq, *t.shape[1:]).contiguous()
                         for t in (xd.q, xd.k, xd.v, xd.g, xd.beta)]
             self.o_steps = torch.empty(n_decode_steps, n_seq, H, d, device=dev)
+            self.blob0 = self.cache.blob.clone()   # cache right after the prefill
             self.xd_full = xd
             self.t = 0
             torch.cuda.synchronize()
@@ -368,15 +369,12 @@ def time_e2e(step, K, W, world):
                 ho.copy_(do, non_blocking=True)
 
     if step.op == "decode":
-        # replay from a fresh copy of the cache so positions line up
-        step.t = 0
-        blob0 = step.cache.blob.clone()
+        # replay the same token sequence from the post-prefill cache
+        step.cache.blob.copy_(step.blob0)
         for i in range(min(W, total)):
             one(i)
-        torch.cuda.synchronize()
-        step.cache.blob.copy_(blob0)
-        K = min(K, total)
-        start = 0
+        start = min(W, total)
+        K = min(K, total - start)
     else:
         for i in range(W):
             one(i)
@@ -394,4 +392,246 @@ def time_e2e(step, K, W, world):
            else sum(t.numel() * t.element_size() for t in host_out))
     return max_over_ranks(s.elapsed_time(e) / K, world), int(h2d), int(d2h)
 
-# CPR_BENCH_PART4
+
+# ------------------------------------------------------------ roofline
+def load_traffic():
+    try:
+        with open(TRAFFIC_FILE) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def roofline_for(step, prof, pk):
+    """Roofline of the dominant kernel (largest share of device time)."""
+    if not prof:
+        return None
+    name, (launches, total_ms) = max(prof.items(), key=lambda kv: kv[1][1])
+    avg_s = total_ms / launches / 1e3
+    units = step.kernel_units(name)
+    traffic = None
+    tr = load_traffic().get(f"{name}/{step.name}")
+    if tr and tr.get("kernel_build_id") == step.cpr.kernel_build_id():
+        traffic = tr.get("bytes_per_launch")
+    if name == "cpr_decode":
+        byt = DECODE_ALGO_BYTES_PER_SEQ_HEAD * units
+        ach = byt / avg_s / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "avg_launch_us": round(avg_s * 1e6, 2), "algo_bytes_per_launch": byt}
+    fl = simt_kernel_flops_per_chunk(name, step.d)
+    if fl is None:
+        return None
+    flops = fl * units
+    alu_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # fp32 FMA lanes x clock
+    ach = flops / avg_s / 1e12
+    return {"kernel": name, "bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak, 2),
+            "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4), "traffic": traffic,
+            "avg_launch_us": round(avg_s * 1e6, 2), "algo_flops_per_launch": flops,
+            "peak_source": "152 SMs x 128 fp32 lanes x 2 FLOP x max SM clock"}
+
+
+def path_roofline(step, ms, pk):
+    """The method's roofline for the whole step: the slower of its bytes at
+    HBM bandwidth and its dense-contraction FLOPs at the bf16 tensor peak."""
+    byt, fl = step.algo()
+    t_hbm = byt / (pk["hbm_gbs"] * 1e9)
+    t_mma = fl / (pk["bf16_tflops"] * 1e12)
+    t = max(t_hbm, t_mma)
+    return {"bound": "hbm" if t_hbm >= t_mma else "tensor", "roofline_us": round(t * 1e6, 2),
+            "measured_us": round(ms * 1e3, 2), "frac": round(t / (ms / 1e3), 4),
+            "algo_bytes": int(byt), "algo_flops": int(fl), "peaks": pk["source"]}
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_sample(name, n_steps_hint=1):
+    """Oracle run on a bounded sample of the workload; returns (units, seconds, desc, cores)."""
+    import oracle
+    from infer_consistent_linear_gb300.synth import make_inputs
+    oracle.build()
+    cores = oracle.default_threads()
+    w = WORKLOADS[name]
+    H, d = w["H"], w["d"]
+    if w["op"] == "decode":
+        # one decode step for every (sequence, head): one token from a full state
+        n_seq = len(workload_lens(name))
+        x = make_inputs([1] * n_seq, H, d, d, io_dtype=torch.bfloat16, seed=0, h0_std=0.1)
+        t0 = time.perf_counter()
+        oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
+        dt = time.perf_counter() - t0
+        return 1, dt, f"one decode step: {n_seq} sequences x {H} heads, fp64 recurrence", cores
+    lens = workload_lens(name)
+    if w["op"] == "fwd":
+        sample = lens[:2]
+    else:
+        sample = lens[:1]
+    x = make_inputs(sample, H, d, d, io_dtype=torch.bfloat16, seed=0, with_grad=(w["op"] == "fwdbwd"))
+    t0 = time.perf_counter()
+    oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)
+    if w["op"] == "fwdbwd":
+        oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO)
+    dt = time.perf_counter() - t0
+    return sum(sample), dt, (f"{len(sample)} of {len(lens)} sequences ({sum(sample)} tokens) x {H} "
+                             f"heads, fp64 {'fwd+bwd' if w['op'] == 'fwdbwd' else 'fwd'}"), cores
+
+
+def unit_of(name):
+    return ("us/step", False) if WORKLOADS[name]["op"] == "decode" else ("tokens/s", True)
+
+
+def value_of(name, ms, tokens_per_step, world):
+    if WORKLOADS[name]["op"] == "decode":
+        return round(ms * 1e3, 3)
+    return round(world * tokens_per_step / (ms / 1e3), 1)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    name = args.workload
+    unit, hib = unit_of(name)
+    times, units = [], 0
+    desc = cores = None
+    for i in range(args.warmup + args.steps):
+        u, dt, desc, cores = cpu_sample(name)
+        if i >= args.warmup:
+            times.append(dt)
+            units += u
+    total = sum(times)
+    if WORKLOADS[name]["op"] == "decode":
+        value = round(total / len(times) * 1e6, 3)
+    else:
+        value = round(units / total, 1)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 3),
+            "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOADS[name]["desc"], "sample": desc},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def measure(step, K, W, world, local):
+    """Device-timed region with clock sampling; re-measured once if the clock
+    record shows a hardware/thermal slowdown."""
+    for attempt in range(2):
+        clocks = ClockSampler(local)
+        clocks.start()
+        ms, prof = time_device(step, K, W, world, profile=True)
+        clocks.stop()
+        ck = clocks.summary()
+        if not (set(ck["reasons"]) & BAD_REASONS):
+            break
+        if step.op == "decode":
+            break  # tokens are consumed; keep the record and report it
+    ck["attempts"] = attempt + 1
+    return ms, prof, ck
+
+
+def kernel_table(prof, ms_total):
+    tot = sum(v[1] for v in prof.values()) or 1.0
+    return {k: {"launches": n, "avg_us": round(t / n * 1e3, 2), "share": round(t / tot, 4)}
+            for k, (n, t) in prof.items()}
+
+
+def decode_bitwise(step, n_done):
+    """Decode outputs vs a one-shot forward over the full sequences (bits)."""
+    cpr = step.cpr
+    xd = step.xd_full
+    o_full, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=step.c,
+                                digest=step.dig, want_final=False)
+    cu = xd.cu_seqlens.tolist()
+    idx = torch.tensor([[cu[b] + step.lens[b] + t for b in range(len(step.lens))]
+                        for t in range(n_done)], device=o_full.device).reshape(-1)
+    ref = o_full.index_select(0, idx).view_as(step.o_steps[:n_done])
+    return bool(torch.equal(ref.view(torch.int32), step.o_steps[:n_done].contiguous().view(torch.int32)))
+
+
+def secondary(name, dev, world, local, steps, warmup, pk):
+    n_dec = steps + warmup if WORKLOADS[name]["op"] == "decode" else 0
+    st = OurStep(name, dev, n_decode_steps=n_dec)
+    ms, prof = time_device(st, steps, warmup, world, profile=True)
+    unit, hib = unit_of(name)
+    res = {"workload": WORKLOADS[name]["desc"], "value": value_of(name, ms, st.tokens_per_step(), world),
+           "unit": unit, "higher_is_better": hib, "ms_per_step": round(ms, 4), "steps": steps,
+           "path_roofline": path_roofline(st, ms, pk), "roofline": roofline_for(st, prof, pk),
+           "kernels": kernel_table(prof, ms)}
+    if WORKLOADS[name]["op"] == "decode":
+        res["bitwise_decode_vs_prefill"] = decode_bitwise(st, n_dec)
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill")
+    ap.add_argument("--no-secondary", action="store_true", help="only the headline workload")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import infer_consistent_linear_gb300 as cpr
+    from infer_consistent_linear_gb300 import _build
+    _build.build()
+    cpr.load_library()
+    pk = peaks()
+    name = args.workload
+    K, W = args.steps, max(args.warmup, 0)
+    n_dec = K + W if WORKLOADS[name]["op"] == "decode" else 0
+    step = OurStep(name, dev, n_decode_steps=n_dec)
+    ms, prof, ck = measure(step, K, W, world, local)
+    unit, hib = unit_of(name)
+    value = value_of(name, ms, step.tokens_per_step(), world)
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(step, K, W, world)
+        e2e = {"value": value_of(name, e_ms, step.tokens_per_step(), world), "unit": unit,
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    extra = {}
+    if WORKLOADS[name]["op"] == "decode":
+        extra["bitwise_decode_vs_prefill"] = decode_bitwise(step, n_dec)
+    line ={"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms, 4), "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOADS[name]["desc"], "l2": "working set > 129 MB L2, no flush",
+                       "contract": {k: v for k, v in step.c.as_dict().items()},
+                       "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+            "clocks": ck, "e2e": e2e, "gpu_launches": int(sum(n for n, _ in prof.values())),
+            "roofline": roofline_for(step, prof, pk), "path_roofline": path_roofline(step, ms, pk),
+            "kernels": kernel_table(prof, ms), **extra}
+    del step
+    torch.cuda.empty_cache()
+    if not args.no_secondary:
+        sec = {}
+        plan = [("trainer", 5, 3), ("decode", 512, 3), ("varlen", 3, 3)]
+        for nm, s, w in plan:
+            if nm != name:
+                sec[nm] = secondary(nm, dev, world, local, s, w, pk)
+        line["workloads"] = sec
+    if rank == 0 and world == 1:
+        u, dt, desc, cores = cpu_sample(name)
+        cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)
+        line["cpu_baseline"] = {"value": cv, "unit": unit, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
