@@ -225,6 +225,31 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32],
                 void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free trainer forward.  The pages have no counterpart for this
+ * entry point: it exists for callers that cannot allocate device memory at
+ * the point of the call -- for example code running inside a host callback or
+ * a custom allocator hook, where cudaMalloc is forbidden or would deadlock, or
+ * embedders whose memory pools are fixed at start-up and have no room for a
+ * per-call workspace.
+ *
+ * Same arguments and result bits as cpr_gdn_fwd minus the workspace: the
+ * scratch lives in a fixed device array of CPR_NOALLOC_SCRATCH_BYTES inside
+ * this library (every GPU that loads the library holds it until the process
+ * exits).  A batch whose forward workspace (cpr_gdn_workspace_size with
+ * CPR_OP_FWD) exceeds that size is rejected with CPR_ERR_WORKSPACE before
+ * anything is launched.  The first call on a device looks up the array's
+ * device address with that device current; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (the forward writes every scratch word before reading it,
+ * so nothing needs clearing); calls that overlap on the GPU -- on two streams,
+ * or from two host threads -- race on it and must be serialised by the
+ * caller.  Allocates nothing (no cudaMalloc / cudaFree). */
+#define CPR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int cpr_gdn_fwd_noalloc(const cpr_contract* c, const uint8_t digest[32],
+                        const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
+                        int H, const float* h0, void* o, float* final_state, void* stream);
+
 /* ---- kernel timing ------------------------------------------------------ */
 
 /* Per-kernel timing collected with CUDA events recorded on the launching

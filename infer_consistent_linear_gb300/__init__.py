@@ -90,6 +90,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_decode_step": (I, [CP, P, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gdn_bwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                             P, SZ, P]),
+        "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_profile_begin": (I, []),
         "cpr_profile_end": (I, [P, I, ctypes.POINTER(I)]),
         "cpr_get_device_error": (I, [ctypes.POINTER(U32), I]),

@@ -29,6 +29,17 @@ int fail(int code, const char* fmt, ...) {
 
 }  // namespace
 
+namespace cpr {
+// Records a message for cpr_last_error() from other translation units.
+int record_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+}  // namespace cpr
+
 // Device error word: first recorded error code, 0 = none.
 __device__ uint32_t g_cpr_device_error = 0u;
 
