@@ -402,6 +402,17 @@ def load_traffic():
         return {}
 
 
+def kernel_src_sha():
+    """Hash of the kernel sources the stored ncu traffic figures belong to."""
+    import hashlib
+    csrc = os.path.join(ROOT, "infer_consistent_linear_gb300", "csrc")
+    h = hashlib.sha256()
+    for s in ("common.cuh", "simt_fwd.cuh", "simt_bwd.cuh"):
+        with open(os.path.join(csrc, s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def roofline_for(step, prof, pk):
     """Roofline of the dominant kernel (largest share of device time)."""
     if not prof:
@@ -411,7 +422,7 @@ def roofline_for(step, prof, pk):
     units = step.kernel_units(name)
     traffic = None
     tr = load_traffic().get(f"{name}/{step.name}")
-    if tr and tr.get("kernel_build_id") == step.cpr.kernel_build_id():
+    if tr and tr.get("kernel_src_sha") == kernel_src_sha():
         traffic = tr.get("bytes_per_launch")
     if name == "cpr_decode":
         byt = DECODE_ALGO_BYTES_PER_SEQ_HEAD * units
