@@ -77,6 +77,8 @@ extern "C" {
 #define CPR_ERR_CUDA               6  /* a CUDA runtime call failed           */
 #define CPR_ERR_WORKSPACE          7  /* workspace null or too small          */
 #define CPR_ERR_BAD_SEQLENS        8  /* cu_seqlens invalid (device-side)     */
+#define CPR_ERR_DEVICE_TIMEOUT     9  /* a bounded device-side wait expired;
+                                         the kernel gave up (device-side)     */
 
 /* ---- contract --------------------------------------------------------- */
 #define CPR_CONTRACT_VERSION 1u
@@ -88,6 +90,16 @@ extern "C" {
  * SIMT_F32: every product and sum is an fp32 CUDA-core operation (fma
  * chains in the order fixed by intra_order); io values are widened exactly. */
 #define CPR_POLICY_SIMT_F32 1u
+/* TC_BF16X3: every within-chunk contraction is a 5th-generation tensor-core
+ * MMA (tcgen05, kind::f16, fp32 accumulation).  bf16 inputs (q, k, v) enter
+ * exactly; every fp32 operand x is split into bf16 hi = bf16(x) and
+ * lo = bf16(x - hi) and a product of two split operands is the fixed
+ * sequence hi*hi + hi*lo + lo*hi (one exact operand: hi + lo).  Gate prefix,
+ * exponentials, the triangular solve and all epilogues are fp32 CUDA-core
+ * operations.  Decode re-issues the same MMA instructions (same shapes, same
+ * row positions) on the zero-padded partial chunk.  This build: bf16 io,
+ * d_k = d_v = 128, dv_splits 2 or 4. */
+#define CPR_POLICY_TC_BF16X3 2u
 
 /* intra_order: id of the fixed within-chunk reduction orders.
  * ROWSEQ_V1: gate prefix = serial fp32 sum in token order; every dot product

@@ -28,6 +28,7 @@ ERRORS = {
 CPR_DTYPE_F32 = 1
 CPR_DTYPE_BF16 = 2
 CPR_POLICY_SIMT_F32 = 1
+CPR_POLICY_TC_BF16X3 = 2
 CPR_ORDER_ROWSEQ_V1 = 1
 CPR_SCHED_SEQ_CHUNKS = 1
 CPR_OP_FWD = 1

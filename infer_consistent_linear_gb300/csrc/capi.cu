@@ -11,11 +11,13 @@
 #include "profile.h"
 #include "sha256.h"
 #include "simt_launch.cuh"
+#include "tc_decode.cuh"
+#include "tc_launch.h"
 
 namespace {
 
 // Bumped whenever any rounding-relevant detail of a kernel changes.
-constexpr uint32_t kKernelBuildId = 1u;
+constexpr uint32_t kKernelBuildId = 2u;
 
 thread_local char g_msg[512] = "";
 
@@ -94,7 +96,14 @@ int check_contract(const cpr_contract* c) {
     if (c->out_dtype != CPR_DTYPE_F32 || c->gate_dtype != CPR_DTYPE_F32 ||
         c->accum_dtype != CPR_DTYPE_F32 || c->state_dtype != CPR_DTYPE_F32)
         return fail(CPR_ERR_UNSUPPORTED, "out/gate/accum/state dtype must be F32");
-    if (c->operand_policy != CPR_POLICY_SIMT_F32) return fail(CPR_ERR_UNSUPPORTED, "operand_policy %u", c->operand_policy);
+    if (c->operand_policy == CPR_POLICY_TC_BF16X3) {
+        if (c->io_dtype != CPR_DTYPE_BF16 || c->d_k != 128)
+            return fail(CPR_ERR_UNSUPPORTED, "TC_BF16X3 needs bf16 io and d_k = d_v = 128");
+        if (c->dv_splits != 2 && c->dv_splits != 4)
+            return fail(CPR_ERR_UNSUPPORTED, "TC_BF16X3 needs dv_splits 2 or 4");
+    } else if (c->operand_policy != CPR_POLICY_SIMT_F32) {
+        return fail(CPR_ERR_UNSUPPORTED, "operand_policy %u", c->operand_policy);
+    }
     if (c->intra_order != CPR_ORDER_ROWSEQ_V1) return fail(CPR_ERR_UNSUPPORTED, "intra_order %u", c->intra_order);
     if (c->state_schedule != CPR_SCHED_SEQ_CHUNKS) return fail(CPR_ERR_UNSUPPORTED, "state_schedule %u", c->state_schedule);
     if (c->dv_splits != 1 && c->dv_splits != 2 && c->dv_splits != 4)
@@ -130,6 +139,11 @@ WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int 
     size_t off = 0;
     auto add = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
     add(w.chunk_off, sizeof(int32_t) * (n_seq + 1));
+    if (op == CPR_OP_FWD && c.operand_policy == CPR_POLICY_TC_BF16X3) {
+        add(w.W, ch * cpr::tc::kBlock);  // per (chunk, head) operand blocks
+        w.total = off;
+        return w;
+    }
     add(w.W, ch * C * dk * 4);
     add(w.U, ch * C * dv * 4);
     add(w.P, ch * C * C * 4);
@@ -248,6 +262,19 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
     sa.digest = digest_words(digest); header_words(*c, n_seq, H, sa.hdr); sa.err = err;
     cudaError_t e = launch_setup(sa, st);
     if (e != cudaSuccess) return cuda_fail(e, "setup launch");
+
+    if (c->operand_policy == CPR_POLICY_TC_BF16X3) {
+        cpr::tc::TcArgs t{};
+        t.q = static_cast<const __nv_bfloat16*>(q); t.k = static_cast<const __nv_bfloat16*>(k);
+        t.v = static_cast<const __nv_bfloat16*>(v); t.g = g; t.beta = beta; t.cu = cu;
+        t.chunk_off = sa.chunk_off; t.n_seq = n_seq; t.H = H; t.dvs = (int)(c->d_v / c->dv_splits);
+        t.scale = c->scale; t.ws = wsb + w.W; t.h0 = h0; t.o = static_cast<float*>(o);
+        t.final_state = final_state; t.cache = static_cast<uint8_t*>(cache); t.co = to_off(cl);
+        t.err = err;
+        e = cpr::tc_forward(t, w.cmax, n_seq, H, st);
+        if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+        return CPR_OK;
+    }
 
     cpr::simt::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu; a.chunk_off = sa.chunk_off;
@@ -380,6 +407,18 @@ int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const v
     uint32_t* err = device_error_ptr();
     if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
     const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+    if (c->operand_policy == CPR_POLICY_TC_BF16X3) {
+        cpr::tc::TcDecArgs t{};
+        t.q = static_cast<const __nv_bfloat16*>(q_t); t.k = static_cast<const __nv_bfloat16*>(k_t);
+        t.v = static_cast<const __nv_bfloat16*>(v_t); t.g = g_t; t.beta = beta_t;
+        t.n_seq = n_seq; t.H = H; t.scale = c->scale; t.cache = static_cast<uint8_t*>(cache);
+        t.co = to_off(cl); t.digest = digest_words(digest); header_words(*c, n_seq, H, t.hdr);
+        t.o = static_cast<float*>(o_t); t.err = err;
+        const cudaError_t e = cpr::tc_decode_step(t, (int)(c->d_v / c->dv_splits),
+                                                  static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+        return CPR_OK;
+    }
     cpr::simt::DecArgs a{};
     a.q = q_t; a.k = k_t; a.v = v_t; a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
     a.scale = c->scale; a.cache = static_cast<uint8_t*>(cache); a.co = to_off(cl);

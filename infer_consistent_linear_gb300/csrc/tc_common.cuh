@@ -1,0 +1,180 @@
+// sm_103a tensor-core building blocks (inline PTX): TMEM allocation, tcgen05.mma
+// (kind::f16, bf16 operands, fp32 accumulation), commit to mbarrier, TMEM loads,
+// bulk async copies, and the shared-memory operand layout they use.
+//
+// Operand layout ("core-matrix K-major, no swizzle"): an R x K bf16 tile is a
+// grid of 8-row x 8-element (8 x 16 B) core matrices stored row-group-major:
+// core matrix (rg, kg) at byte ((rg * K/8) + kg) * 128, row i of it at +16 i.
+// In the shared-memory descriptor the leading byte offset (LBO) is the stride
+// between core matrices adjacent along K (128 B) and the stride byte offset
+// (SBO) the stride between 8-row groups (K/8 * 128 B).  One MMA instruction
+// consumes K = 16 (two core matrices along K); the next k-step starts 256 B
+// further.  Accumulator rows: M = 128 -> TMEM lane r; M = 64 -> lane
+// (r / 16) * 32 + r % 16 (16 rows in each warp's lane quarter).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cpr {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Byte offset of element (r, k) in an R x K core-matrix K-major bf16 tile.
+__host__ __device__ __forceinline__ uint32_t cm_off(int r, int k, int K) {
+    return (uint32_t)((((r >> 3) * (K >> 3)) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// TMEM lane holding accumulator row r for an M = 64 MMA.
+__device__ __forceinline__ int lane_m64(int r) { return ((r >> 4) << 5) + (r & 15); }
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, int K) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;                  // LBO: along K
+    d |= (uint64_t)((((uint32_t)K >> 3) * 128u >> 4) & 0x3FFFu) << 32;  // SBO: along M/N
+    d |= (uint64_t)1 << 46;                                          // descriptor version
+    return d;
+}
+
+// kind::f16 instruction descriptor: D f32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- TMEM --------------------------------------------------------------------
+// Whole-warp operations.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor core, bulk copies).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// CTA barrier that also orders tcgen05 operations around it.
+__device__ __forceinline__ void tc_sync() {
+    fence_before();
+    __syncthreads();
+    fence_after();
+}
+
+// ---- MMA -----------------------------------------------------------------------
+// D[tmem] (+)= A[smem] * B[smem]^T over K = 16 (one instruction).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Issues the k-steps of A (M x K) * B (N x K)^T into d_tmem in ascending K
+// order; accumulates onto the existing D when `accumulate` is set.
+template <int M, int N, int K>
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, const void* a_tile, const void* b_tile,
+                                         bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(M, N);
+    const uint32_t a0 = smem_u32(a_tile), b0 = smem_u32(b_tile);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        mma_bf16(d_tmem, smem_desc(a0 + ks * 256, K), smem_desc(b0 + ks * 256, K), idesc,
+                 (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+// Arrives on `mbar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(mbar)) : "memory");
+}
+
+// ---- mbarrier ----------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(mbar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+    return ok;
+}
+// Bounded wait for the phase with the given parity.  Returns false (and
+// records CPR_ERR_DEVICE_TIMEOUT) if it does not complete within the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t* err) {
+    for (uint32_t it = 0; it < (1u << 22); ++it)
+        if (mbar_try_wait(mbar, parity)) return true;
+    set_error(err, CPR_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+// ---- bulk async copy (global -> shared), completion on an mbarrier ----------------
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(mbar)) : "memory");
+}
+
+// ---- TMEM -> registers ---------------------------------------------------------------
+// 32 consecutive columns of this warp's lane quarter: thread i gets lane (32w + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// TMEM address of (warp's lane quarter, column c).
+__device__ __forceinline__ uint32_t taddr_of(uint32_t base, int warp, int col) {
+    return base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)col;
+}
+
+// ---- bf16 hi/lo split -------------------------------------------------------------------
+// x ~= hi + lo with hi = bf16(x), lo = bf16(x - hi); x - hi is exact in fp32.
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(hi)));
+}
+
+// Stores 8 fp32 values (consecutive along K) as one 16-byte core-matrix row,
+// split into hi and lo tiles at the same offset.
+__device__ __forceinline__ void store8_split(unsigned char* hi_tile, unsigned char* lo_tile,
+                                             uint32_t off, const float (&x)[8]) {
+    __align__(16) __nv_bfloat16 h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) split_bf16(x[i], h[i], l[i]);
+    *reinterpret_cast<uint4*>(hi_tile + off) = *reinterpret_cast<const uint4*>(h);
+    *reinterpret_cast<uint4*>(lo_tile + off) = *reinterpret_cast<const uint4*>(l);
+}
+
+}  // namespace tc
+}  // namespace cpr

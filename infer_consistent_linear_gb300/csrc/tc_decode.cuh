@@ -1,0 +1,393 @@
+// CPR Gated DeltaNet decode step on the tensor cores (policy TC_BF16X3).
+//
+// One CTA per (sequence, head).  For the new row p of the current chunk it
+// re-issues exactly the MMA instructions of the prefill kernels (k_tc_prep,
+// k_tc_state): same shapes, same operand tiles and row positions, same k-step
+// and hi/lo pass order, with the rows of the chunk that do not exist yet set
+// to zero.  An output row of an MMA depends only on its own A row and on B,
+// and zero rows of B only meet zero entries of the row's A (T, P are lower
+// triangular), so row p gets the prefill's bits.  The fp32 parts (gate prefix,
+// exponentials, T row, epilogues) are the same operation sequences as the
+// prefill's.  When the chunk fills (p = C - 1) the step commits the next
+// chunk-start state with the prefill's commit MMAs: the resynchronisation
+// every C tokens (page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配", section
+// "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet").
+#pragma once
+
+#include "tc_fwd.cuh"
+
+namespace cpr {
+namespace tc {
+
+struct DecSmem {
+    static constexpr size_t Hhi = 0, Hlo = 32768;   // H^T, 128 x 128 bf16 each
+    static constexpr size_t Kt = 65536;              // K^T, 128 x 64
+    static constexpr size_t R1 = 81920;              // 64 KB, reused by phase
+    static constexpr size_t F = R1 + 65536;          // fp32 scratch
+    // fp32 arrays (floats from F)
+    static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
+                         fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fEnd = 960;
+    static constexpr size_t Bar = F + fEnd * 4;
+    static constexpr size_t Total = Bar + 64;
+};
+
+struct TcDecArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    int n_seq;
+    int H;
+    float scale;
+    uint8_t* cache;
+    CacheOff co;
+    Digest digest;
+    uint32_t hdr[7];
+    float* o;
+    uint32_t* err;
+};
+
+template <int DVS>
+__global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
+    using S = DecSmem;
+    constexpr int NSPLIT = D / DVS;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    float* F = reinterpret_cast<float*>(sm + S::F);
+    float *gams = F + S::fGam, *bets = F + S::fBet, *bgs = F + S::fBg, *arow = F + S::fArow,
+          *prow = F + S::fProw, *trow = F + S::fTrow, *decs = F + S::fDec, *Wp = F + S::fWp,
+          *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
+    __shared__ int ok_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H;
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const uint32_t* hdr = reinterpret_cast<const uint32_t*>(a.cache + a.co.header);
+    int32_t* pos = reinterpret_cast<int32_t*>(a.cache + a.co.pos);
+    uint32_t* done = reinterpret_cast<uint32_t*>(a.cache + a.co.done);
+    if (tid == 0) {
+        bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
+        for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
+        for (int i = 0; i < 7; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
+        const int p = ok ? pos[b] : -1;
+        if (!(p >= 0 && p < C)) ok = false;
+        if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
+        ok_s = ok ? 1 + p : 0;
+    }
+    __syncthreads();
+    if (!ok_s) return;
+    const int p = ok_s - 1;
+    const size_t sh = (size_t)b * H + h;
+    const __nv_bfloat16* ck = reinterpret_cast<const __nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
+    const __nv_bfloat16* cv = reinterpret_cast<const __nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
+    float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
+    float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
+    float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
+    float* cd = reinterpret_cast<float*>(a.cache + a.co.delta_rows) + sh * C * D;
+    float* Hst = reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D;
+    const __nv_bfloat16* qt = a.q + sh * D;
+    const __nv_bfloat16* kt = a.k + sh * D;
+    const __nv_bfloat16* vt = a.v + sh * D;
+    unsigned char* R1 = sm + S::R1;
+
+    if (warp == 0) tmem_alloc(tbase, 256);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init_fence();
+    }
+    // token row s of the chunk (k or v): cache rows below p, the new token at p, zero above
+    auto row_ptr = [&](const __nv_bfloat16* cache_rows, const __nv_bfloat16* tok, int s) {
+        return s < p ? cache_rows + (size_t)s * D : tok;
+    };
+    // H^T split into hi / lo (rows j, K dim d), from the fp32 chunk-start state
+    for (int i = tid; i < 16 * 16; i += 128) {
+        const int j8 = i / 16, d8 = i % 16;
+        float rows[8][8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float4 x0 = *reinterpret_cast<const float4*>(Hst + (size_t)(d8 * 8 + r) * D + j8 * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(Hst + (size_t)(d8 * 8 + r) * D + j8 * 8 + 4);
+            rows[r][0] = x0.x; rows[r][1] = x0.y; rows[r][2] = x0.z; rows[r][3] = x0.w;
+            rows[r][4] = x1.x; rows[r][5] = x1.y; rows[r][6] = x1.z; rows[r][7] = x1.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float x[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) x[r] = rows[r][c];
+            store8_split(sm + S::Hhi, sm + S::Hlo, cm_off(j8 * 8 + c, d8 * 8, D), x);
+        }
+    }
+    // [K; Q] tile for S1: rows s <= p of K, row 64 + p = q_p, all else zero
+    for (int i = tid; i < 128 * (D / 8); i += 128) {
+        const int r = i / (D / 8), d8 = i % (D / 8);
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < 64 && r <= p) val = *reinterpret_cast<const uint4*>(row_ptr(ck, kt, r) + d8 * 8);
+        if (r == 64 + p) val = *reinterpret_cast<const uint4*>(qt + d8 * 8);
+        *reinterpret_cast<uint4*>(R1 + cm_off(r, d8 * 8, D)) = val;
+    }
+    // K^T (sKt) and V^T (R1 + 32 KB): 8 x 8 transposes of the rows s <= p
+    for (int i = tid; i < 2 * 8 * (D / 8); i += 128) {
+        const int which = i / (8 * (D / 8));
+        const int s8 = (i / (D / 8)) % 8, d8 = i % (D / 8);
+        uint4 rows[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = s8 * 8 + j;
+            rows[j] = s <= p ? *reinterpret_cast<const uint4*>(row_ptr(which ? cv : ck, which ? vt : kt, s) + d8 * 8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+        transpose8_store(rows, (which ? R1 + 32768 : sm + S::Kt) + cm_off(d8 * 8, s8 * 8, C));
+    }
+    if (tid < p) {
+        gams[tid] = cg[tid];
+        bets[tid] = cb[tid];
+    }
+    if (tid == 0) {
+        gams[p] = __fadd_rn(p > 0 ? cg[p - 1] : 0.f, a.g[sh]);
+        bets[p] = a.beta[sh];
+    }
+    fence_async_smem();
+    tc_sync();
+    const uint32_t tmem = *tbase;
+    uint32_t phase = 0;
+    bool ok = true;
+    auto mma_wait = [&]() {
+        const bool w = mbar_wait(mbar, phase, a.err);
+        fence_after();
+        phase ^= 1u;
+        return !__syncthreads_or(!w);
+    };
+    if (tid == 0) {
+        mma_tile<128, 64, D>(tmem, R1, R1, false);
+        mma_commit(mbar);
+    }
+    if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid]);
+    ok = mma_wait();
+    if (!ok) goto cleanup;
+    {
+        const float gp = gams[p], bp = bets[p];
+        float v[32];
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            tmem_ld32(taddr_of(tmem, warp, c0), v);
+            if (tid == p) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c0 + j;
+                    arow[s] = (s < p) ? simt::a_entry(bp, gp, gams[s], v[j]) : 0.f;
+                }
+            } else if (tid == 64 + p) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c0 + j;
+                    prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, gams[s]), __fmul_rn(a.scale, v[j])) : 0.f;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < C) {  // T row p
+        const int j = tid;
+        float t = 0.f;
+        if (j < p) {
+            float acc = 0.f;
+            for (int s = j; s < p; ++s) acc = __fmaf_rn(arow[s], ct[s * C + j], acc);
+            t = -acc;
+        } else if (j == p) {
+            t = 1.f;
+        }
+        trow[j] = t;
+    }
+    // X tiles (R1 + 0 .. 32 KB): zero except row p
+    for (int i = tid; i < 2048; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < 16) {
+        const int which = tid >> 3, s8 = tid & 7;
+        unsigned char* xhi = R1 + which * 16384;
+        const float* sc = which ? bets : bgs;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int s = s8 * 8 + e;
+            x[e] = s <= p ? __fmul_rn(trow[s], sc[s]) : 0.f;
+        }
+        store8_split(xhi, xhi + 8192, cm_off(p, s8 * 8, C), x);
+    }
+    fence_async_smem();
+    tc_sync();
+    if (tid == 0) {
+        mma_tile<64, D, C>(tmem, R1, sm + S::Kt, false);
+        mma_tile<64, D, C>(tmem, R1 + 8192, sm + S::Kt, true);
+        mma_tile<64, D, C>(tmem + 128, R1 + 16384, R1 + 32768, false);
+        mma_tile<64, D, C>(tmem + 128, R1 + 24576, R1 + 32768, true);
+        mma_commit(mbar);
+    }
+    ok = mma_wait();
+    if (!ok) goto cleanup;
+    {
+        const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
+        float v[32];
+        for (int c0 = 0; c0 < 2 * D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem, warp, c0), v);
+            if (mine) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (c0 < D) Wp[c0 + j] = v[j];
+                    else Up[c0 - D + j] = v[j];
+                }
+            }
+        }
+    }
+    // A4 tiles (R1: hi at +0, lo at +32 KB): row p = W'_p, row 64 + p = q_p
+    for (int i = tid; i < 4096; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < 16) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = Wp[tid * 8 + e];
+        store8_split(R1, R1 + 32768, cm_off(p, tid * 8, D), x);
+    } else if (tid < 32) {
+        const int d8 = tid - 16;
+        *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, d8 * 8, D)) = *reinterpret_cast<const uint4*>(qt + d8 * 8);
+    }
+    fence_async_smem();
+    tc_sync();
+    if (tid == 0) {
+#pragma unroll
+        for (int sp = 0; sp < NSPLIT; ++sp) {
+            const uint32_t acc = tmem + sp * DVS;
+            mma_tile<128, DVS, D>(acc, R1, sm + S::Hhi + sp * DVS * 256, false);
+            mma_tile<128, DVS, D>(acc, R1, sm + S::Hlo + sp * DVS * 256, true);
+            mma_tile<128, DVS, D>(acc, R1 + 32768, sm + S::Hhi + sp * DVS * 256, true);
+        }
+        mma_commit(mbar);
+    }
+    ok = mma_wait();
+    if (!ok) goto cleanup;
+    {
+        const float Gp = simt::gate(gams[p]);
+        float v[32];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem, warp, c0), v);
+            if (tid == p) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Dp[c0 + j] = __fsub_rn(Up[c0 + j], v[j]);
+            } else if (tid == 64 + p) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Qs[c0 + j] = __fmul_rn(Gp, __fmul_rn(a.scale, v[j]));
+            }
+        }
+    }
+    __syncthreads();
+    // P tiles (R1 + 0: hi, + 8 KB: lo; zero except row p) and Delta^T (R1 + 16 KB: hi, + 32 KB: lo)
+    for (int i = tid; i < 1024; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < C * D; i += 128) {
+        const int s = i / D, j = i % D;
+        const float x = s < p ? cd[(size_t)s * D + j] : (s == p ? Dp[j] : 0.f);
+        __nv_bfloat16 hi, lo;
+        split_bf16(x, hi, lo);
+        *reinterpret_cast<__nv_bfloat16*>(R1 + 16384 + cm_off(j, s, C)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(R1 + 32768 + cm_off(j, s, C)) = lo;
+    }
+    __syncthreads();
+    if (tid < 8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = prow[tid * 8 + e];
+        store8_split(R1, R1 + 8192, cm_off(p, tid * 8, C), x);
+    }
+    fence_async_smem();
+    tc_sync();
+    if (tid == 0) {
+#pragma unroll
+        for (int sp = 0; sp < NSPLIT; ++sp) {
+            const uint32_t acc = tmem + 128 + sp * DVS;
+            mma_tile<64, DVS, C>(acc, R1, R1 + 16384 + sp * DVS * 128, false);
+            mma_tile<64, DVS, C>(acc, R1, R1 + 32768 + sp * DVS * 128, true);
+            mma_tile<64, DVS, C>(acc, R1 + 8192, R1 + 16384 + sp * DVS * 128, true);
+        }
+        mma_commit(mbar);
+    }
+    ok = mma_wait();
+    if (!ok) goto cleanup;
+    {
+        const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
+        float v[32];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem, warp, 128 + c0), v);
+            if (mine) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a.o[sh * D + c0 + j] = __fadd_rn(Qs[c0 + j], v[j]);
+            }
+        }
+    }
+    __syncthreads();
+    {
+        // append row p to the cache
+        __nv_bfloat16* ckw = const_cast<__nv_bfloat16*>(ck);
+        __nv_bfloat16* cvw = const_cast<__nv_bfloat16*>(cv);
+        if (tid < 16) *reinterpret_cast<uint4*>(ckw + (size_t)p * D + tid * 8) = *reinterpret_cast<const uint4*>(kt + tid * 8);
+        else if (tid < 32) *reinterpret_cast<uint4*>(cvw + (size_t)p * D + (tid - 16) * 8) = *reinterpret_cast<const uint4*>(vt + (tid - 16) * 8);
+        cd[(size_t)p * D + tid] = Dp[tid];
+        if (tid < C) ct[p * C + tid] = trow[tid];
+        if (tid == 0) {
+            cg[p] = gams[p];
+            cb[p] = bets[p];
+        }
+    }
+    if (p == C - 1) {  // resynchronise: commit the next chunk-start state
+        const int Lr = C - 1;
+        if (tid < C) decs[tid] = simt::decay(gams[Lr], gams[tid]);
+        __syncthreads();
+        for (int i = tid; i < C * D; i += 128) {
+            const int s = i / D, j = i % D;
+            const float x = __fmul_rn(decs[s], s < p ? cd[(size_t)s * D + j] : Dp[j]);
+            __nv_bfloat16 hi, lo;
+            split_bf16(x, hi, lo);
+            *reinterpret_cast<__nv_bfloat16*>(R1 + 16384 + cm_off(j, s, C)) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(R1 + 32768 + cm_off(j, s, C)) = lo;
+        }
+        fence_async_smem();
+        tc_sync();
+        if (tid == 0) {
+#pragma unroll
+            for (int sp = 0; sp < NSPLIT; ++sp) {
+                const uint32_t acc = tmem + sp * DVS;
+                mma_tile<128, DVS, C>(acc, sm + S::Kt, R1 + 16384 + sp * DVS * 128, false);
+                mma_tile<128, DVS, C>(acc, sm + S::Kt, R1 + 32768 + sp * DVS * 128, true);
+            }
+            mma_commit(mbar);
+        }
+        ok = mma_wait();
+        if (!ok) goto cleanup;
+        const float GL = simt::gate(gams[Lr]);
+        float v[32];
+        const int d = tid;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem, warp, c0), v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                float* hp = Hst + (size_t)d * D + c0 + j;
+                *hp = __fadd_rn(__fmul_rn(GL, *hp), v[j]);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {  // advance the position once every head of the sequence is done
+        __threadfence();
+        const uint32_t prev = atomicAdd(&done[b], 1u);
+        if (prev == (uint32_t)H - 1) {
+            pos[b] = (p + 1) % C;
+            done[b] = 0u;
+            __threadfence();
+        }
+    }
+cleanup:
+    tc_sync();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace tc
+}  // namespace cpr

@@ -1,0 +1,70 @@
+// Launch sequences of the TC_BF16X3 policy (tensor-core prep, state pass and
+// decode; bf16 io, d = 128).
+#include "profile.h"
+#include "tc_decode.cuh"
+#include "tc_launch.h"
+
+namespace cpr {
+
+namespace {
+
+template <class K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int DVS>
+cudaError_t state(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
+    auto kern = tc::k_tc_state<DVS>;
+    const size_t sm = tc::StateSmem<DVS>::Total;
+    cudaError_t e = set_smem(kern, sm);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
+    if (grid > 0) {
+        ProfScope ps("cpr_tc_state", st);
+        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template <int DVS>
+cudaError_t decode(const tc::TcDecArgs& a, cudaStream_t st) {
+    auto kern = tc::k_tc_decode<DVS>;
+    const size_t sm = tc::DecSmem::Total;
+    cudaError_t e = set_smem(kern, sm);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)a.n_seq * a.H;
+    if (grid > 0) {
+        ProfScope ps("cpr_tc_decode", st);
+        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st) {
+    cudaError_t e = set_smem(tc::k_tc_prep, tc::kPrepSmem);
+    if (e != cudaSuccess) return e;
+    if (cmax > 0) {
+        ProfScope ps("cpr_tc_prep", st);
+        tc::k_tc_prep<<<dim3((unsigned)cmax, H), 128, tc::kPrepSmem, st>>>(a);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (a.dvs) {
+        case 64: return state<64>(a, n_seq, H, st);
+        case 32: return state<32>(a, n_seq, H, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st) {
+    switch (dvs) {
+        case 64: return decode<64>(a, st);
+        case 32: return decode<32>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace cpr

@@ -81,6 +81,22 @@ def test_contract_checks(lib):
         cpr.default_contract(torch.float32, 128)  # fp32 io: d = 64 only
 
 
+def test_tensor_core_contract_rules(lib):
+    c = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
+                             dv_splits=2)
+    assert lib.cpr_contract_check(ctypes.byref(c)) == 0
+    assert cpr.contract_digest(c) != cpr.contract_digest(cpr.default_contract(torch.bfloat16, 128, dv_splits=2))
+    for field, val in [("dv_splits", 1), ("d_k", 64), ("io_dtype", cpr.CPR_DTYPE_F32)]:
+        x = cpr.Contract.from_buffer_copy(c)
+        setattr(x, field, val)
+        if field == "d_k":
+            x.d_v = 64
+        assert lib.cpr_contract_check(ctypes.byref(x)) == 2, field
+    # the TC forward workspace is one operand block per (chunk, head)
+    n_chunks = 4 * 4096 // 64 + 4
+    assert cpr.workspace_bytes(c, cpr.CPR_OP_FWD, 4, 4 * 4096, 16) >= n_chunks * 16 * 114944
+
+
 def test_workspace_and_cache_layout(lib):
     c = cpr.default_contract(torch.bfloat16, 128)
     f = cpr.workspace_bytes(c, cpr.CPR_OP_FWD, 4, 4 * 4096, 16)

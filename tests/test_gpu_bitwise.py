@@ -21,11 +21,11 @@ def _gpu():
     require_gpu()
 
 
-def _decode_vs_prefill(io, d, pre_lens, n_steps, H, check_oracle_tol=None):
+def _decode_vs_prefill(io, d, pre_lens, n_steps, H, check_oracle_tol=None, **contract_overrides):
     n_seq = len(pre_lens)
     full_lens = [L + n_steps for L in pre_lens]
     x = make_inputs(full_lens, H, d, d, io_dtype=io, seed=7, h0_std=0.1).to(DEV)
-    c = cpr.default_contract(io, d)
+    c = cpr.default_contract(io, d, **contract_overrides)
     o_full, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
     cu = x.cu_seqlens.tolist()
     sel = torch.cat([torch.arange(cu[b], cu[b] + pre_lens[b]) for b in range(n_seq)]).to(DEV)

@@ -1,0 +1,105 @@
+"""GPU tests of the tensor-core operand policy (TC_BF16X3: tcgen05 MMAs with
+bf16 hi/lo operand splitting): parity with the fp64 oracle and bit identity
+across prefill, decode, chunk-aligned splits and batch composition under one
+TC contract."""
+import pytest
+import torch
+
+import infer_consistent_linear_gb300 as cpr
+import oracle
+from infer_consistent_linear_gb300.synth import make_inputs
+from gpu_helpers import TOL_BF16, assert_bitwise, assert_close, require_gpu
+from test_gpu_bitwise import _decode_vs_prefill
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TC = dict(operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _tc(splits=2):
+    return cpr.default_contract(torch.bfloat16, 128, dv_splits=splits, **TC)
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_tc_fwd_parity_ragged(splits):
+    lens = [200, 64, 1, 130, 0, 257]
+    x = make_inputs(lens, 3, 128, 128, io_dtype=torch.bfloat16, seed=3, h0_std=0.1)
+    xd = x.to(DEV)
+    o, fin = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0,
+                             contract=_tc(splits))
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    o_ref, h_ref = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
+    assert_close("o", o, o_ref, TOL_BF16)
+    assert_close("final_state", fin, h_ref, TOL_BF16)
+
+
+def test_tc_fwd_parity_long_sequence_scale():
+    x = make_inputs([1000], 2, 128, 128, io_dtype=torch.bfloat16, seed=8, h0_std=0.2)
+    xd = x.to(DEV)
+    c = cpr.default_contract(torch.bfloat16, 128, dv_splits=2, scale=0.5, **TC)
+    o, fin = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    o_ref, h_ref = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, scale=0.5)
+    assert_close("o", o, o_ref, TOL_BF16)
+    assert_close("final_state", fin, h_ref, TOL_BF16)
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_tc_decode_equals_prefill(splits):
+    _decode_vs_prefill(torch.bfloat16, 128, [100, 64, 0, 1, 63], 70, 2, check_oracle_tol=TOL_BF16,
+                       operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=splits)
+
+
+def test_tc_chunk_aligned_split_and_batch_invariance():
+    c = _tc()
+    lens = [300, 77, 1, 128]
+    x = make_inputs(lens, 2, 128, 128, io_dtype=torch.bfloat16, seed=2, h0_std=0.1).to(DEV)
+    o, fin = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
+    cu = x.cu_seqlens.tolist()
+    for b, L in enumerate(lens):
+        sl = slice(cu[b], cu[b + 1])
+        cub = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+        ob, fb = cpr.cpr_gdn_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl], cub,
+                                 h0=x.h0[b:b + 1].contiguous(), contract=c)
+        assert_bitwise(f"o seq {b}", ob, o[sl])
+        assert_bitwise(f"final seq {b}", fb, fin[b:b + 1])
+    # chunk-aligned split of sequence 0
+    T1 = 128
+    s0 = slice(0, T1)
+    s1 = slice(T1, 300)
+    o1, f1 = cpr.cpr_gdn_fwd(x.q[s0], x.k[s0], x.v[s0], x.g[s0], x.beta[s0],
+                             torch.tensor([0, T1], dtype=torch.int32, device=DEV),
+                             h0=x.h0[0:1].contiguous(), contract=c)
+    o2, f2 = cpr.cpr_gdn_fwd(x.q[s1], x.k[s1], x.v[s1], x.g[s1], x.beta[s1],
+                             torch.tensor([0, 300 - T1], dtype=torch.int32, device=DEV), h0=f1,
+                             contract=c)
+    assert_bitwise("split o1", o1, o[s0])
+    assert_bitwise("split o2", o2, o[s1])
+    assert_bitwise("split final", f2, fin[0:1])
+
+
+def test_tc_prefill_cache_refused_by_simt_decode():
+    x = make_inputs([70], 1, 128, 128, io_dtype=torch.bfloat16, seed=1).to(DEV)
+    cu = torch.tensor([0, 69], dtype=torch.int32, device=DEV)
+    _, _, cache = cpr.cpr_gdn_prefill(x.q[:69], x.k[:69], x.v[:69], x.g[:69], x.beta[:69], cu,
+                                      contract=_tc())
+    cpr.get_device_error(clear=True)
+    simt = cpr.default_contract(torch.bfloat16, 128, dv_splits=2)
+    cpr.cpr_gdn_decode_step(x.q[69:], x.k[69:], x.v[69:], x.g[69:], x.beta[69:], cache, contract=simt)
+    assert cpr.get_device_error(clear=True) == 4
+
+
+def test_tc_contract_backward_parity():
+    x = make_inputs([150, 64, 1], 2, 128, 128, io_dtype=torch.bfloat16, seed=5, h0_std=0.1,
+                    with_grad=True)
+    xd = x.to(DEV)
+    got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0,
+                          contract=_tc())
+    ref = oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0)
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        assert_close(n, got[n], ref[n], TOL_BF16)
