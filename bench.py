@@ -167,6 +167,18 @@ def simt_kernel_flops_per_chunk(name, d, Cc=C):
     return None
 
 
+def tc_kernel_flops_per_chunk(name, d, Cc=C):
+    """Algorithmic dense-contraction FLOPs each tensor-core kernel carries per
+    (chunk, head): prep K K^T, Q K^T, T-applied K and V (4 C^2 d MACs); state
+    W'H, QH, K^T Delta (3 C d^2) and P Delta (C^2 d).  The hi/lo split passes
+    the kernels issue on top of these are not counted."""
+    if name == "cpr_tc_prep":
+        return 2 * 4 * Cc * Cc * d
+    if name == "cpr_tc_state":
+        return 2 * (3 * Cc * d * d + Cc * Cc * d)
+    return None
+
+
 def chunk_count(lens):
     return sum((L + C - 1) // C for L in lens)
 
@@ -175,7 +187,7 @@ def chunk_count(lens):
 class OurStep:
     """Device-resident inputs, outputs and workspaces for one workload."""
 
-    def __init__(self, name, dev, n_decode_steps=0):
+    def __init__(self, name, dev, n_decode_steps=0, policy="tc"):
         import infer_consistent_linear_gb300 as cpr
         from infer_consistent_linear_gb300.synth import make_inputs
         self.cpr = cpr
@@ -184,7 +196,11 @@ class OurStep:
         self.lens = workload_lens(name)
         self.H, self.d, self.op = self.w["H"], self.w["d"], self.w["op"]
         H, d = self.H, self.d
-        self.c = cpr.default_contract(torch.bfloat16, d)
+        if policy == "tc":
+            self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2,
+                                          operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        else:
+            self.c = cpr.default_contract(torch.bfloat16, d)
         self.dig = cpr.contract_digest(self.c)
         self.dev = dev
         if self.op == "decode":
@@ -267,7 +283,7 @@ class OurStep:
 
     def kernel_units(self, kname):
         """Units (chunk-heads, or (seq, head) pairs for decode) one launch processes."""
-        if kname == "cpr_decode":
+        if kname in ("cpr_decode", "cpr_tc_decode"):
             return len(self.lens) * self.H
         return chunk_count(self.lens) * self.H
 
@@ -424,7 +440,15 @@ def roofline_for(step, prof, pk):
     tr = load_traffic().get(f"{name}/{step.name}")
     if tr and tr.get("kernel_src_sha") == kernel_src_sha():
         traffic = tr.get("bytes_per_launch")
-    if name == "cpr_decode":
+    tfl = tc_kernel_flops_per_chunk(name, step.d)
+    if tfl is not None:
+        flops = tfl * units
+        ach = flops / avg_s / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
+                "avg_launch_us": round(avg_s * 1e6, 2), "algo_flops_per_launch": flops,
+                "peak_source": "measured bf16 dense (burst)"}
+    if name in ("cpr_decode", "cpr_tc_decode"):
         byt = DECODE_ALGO_BYTES_PER_SEQ_HEAD * units
         ach = byt / avg_s / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
@@ -562,9 +586,9 @@ def decode_bitwise(step, n_done):
     return bool(torch.equal(ref.view(torch.int32), step.o_steps[:n_done].contiguous().view(torch.int32)))
 
 
-def secondary(name, dev, world, local, steps, warmup, pk):
+def secondary(name, dev, world, local, steps, warmup, pk, policy):
     n_dec = steps + warmup if WORKLOADS[name]["op"] == "decode" else 0
-    st = OurStep(name, dev, n_decode_steps=n_dec)
+    st = OurStep(name, dev, n_decode_steps=n_dec, policy=policy)
     ms, prof = time_device(st, steps, warmup, world, profile=True)
     unit, hib = unit_of(name)
     res = {"workload": WORKLOADS[name]["desc"], "value": value_of(name, ms, st.tokens_per_step(), world),
@@ -587,6 +611,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill")
     ap.add_argument("--no-secondary", action="store_true", help="only the headline workload")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--policy", choices=["tc", "simt"], default="tc",
+                    help="operand policy of the contract (tc: tcgen05 tensor cores; simt: fp32 CUDA cores)")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     if args.impl == "reference":
@@ -602,7 +628,7 @@ def main():
     name = args.workload
     K, W = args.steps, max(args.warmup, 0)
     n_dec = K + W if WORKLOADS[name]["op"] == "decode" else 0
-    step = OurStep(name, dev, n_decode_steps=n_dec)
+    step = OurStep(name, dev, n_decode_steps=n_dec, policy=args.policy)
     ms, prof, ck = measure(step, K, W, world, local)
     unit, hib = unit_of(name)
     value = value_of(name, ms, step.tokens_per_step(), world)
@@ -616,7 +642,8 @@ def main():
         extra["bitwise_decode_vs_prefill"] = decode_bitwise(step, n_dec)
     line ={"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms, 4), "higher_is_better": hib, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16x3 MMA, f32 accumulate" if args.policy == "tc" else "f32",
+            "data": "synthetic",
             "config": {"workload": WORKLOADS[name]["desc"], "l2": "working set > 129 MB L2, no flush",
                        "contract": {k: v for k, v in step.c.as_dict().items()},
                        "parallelism": f"replicas x{world} (independent sequences per GPU)"},
@@ -630,7 +657,7 @@ def main():
         plan = [("trainer", 5, 3), ("decode", 512, 3), ("varlen", 3, 3)]
         for nm, s, w in plan:
             if nm != name:
-                sec[nm] = secondary(nm, dev, world, local, s, w, pk)
+                sec[nm] = secondary(nm, dev, world, local, s, w, pk, args.policy)
         line["workloads"] = sec
     if rank == 0 and world == 1:
         u, dt, desc, cores = cpu_sample(name)
