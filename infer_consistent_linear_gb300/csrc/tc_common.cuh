@@ -94,6 +94,44 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, const void* a_tile, co
     }
 }
 
+// MN-major ("transposed") tiles: an MN x K bf16 tile stored as core matrices
+// of 8 K-rows x 8 MN-elements (16 B per K-row), MN-groups contiguous:
+// element (mn, k) at ((k / 8) * (MN / 8) + mn / 8) * 128 + (k % 8) * 16 + (mn % 8) * 2.
+// Descriptor: LBO = K-direction core-matrix stride ((MN/8) * 128 B), SBO = 128 B;
+// one k-step (K = 16) advances the start by 2 * LBO.  A row of the source
+// matrix with MN contiguous (e.g. a token's k or v, a row of H) is stored with
+// 16-byte vector writes.  Results are bit-identical to the K-major layout.
+__host__ __device__ __forceinline__ uint32_t mn_off(int mn, int k, int MN) {
+    return (uint32_t)((((k >> 3) * (MN >> 3)) + (mn >> 3)) * 128 + (k & 7) * 16 + (mn & 7) * 2);
+}
+
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, int MN) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((((uint32_t)MN >> 3) * 128u >> 4) & 0x3FFFu) << 16;  // LBO: along K
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 32;                        // SBO: along MN
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_bf16(M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
+}
+
+// As mma_tile, with each operand either K-major (false) or MN-major (true).
+template <int M, int N, int K, bool AMN, bool BMN>
+__device__ __forceinline__ void mma_tile_mj(uint32_t d_tmem, const void* a_tile, const void* b_tile,
+                                            bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16_major(M, N, AMN, BMN);
+    const uint32_t a0 = smem_u32(a_tile), b0 = smem_u32(b_tile);
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t da = AMN ? smem_desc_mn(a0 + ks * 2 * (M / 8) * 128, M) : smem_desc(a0 + ks * 256, K);
+        const uint64_t db = BMN ? smem_desc_mn(b0 + ks * 2 * (N / 8) * 128, N) : smem_desc(b0 + ks * 256, K);
+        mma_bf16(d_tmem, da, db, idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
 // Arrives on `mbar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"

@@ -2,16 +2,16 @@
 //
 // One CTA per (sequence, head).  For the new row p of the current chunk it
 // re-issues exactly the MMA instructions of the prefill kernels (k_tc_prep,
-// k_tc_state): same shapes, same operand tiles and row positions, same k-step
-// and hi/lo pass order, with the rows of the chunk that do not exist yet set
-// to zero.  An output row of an MMA depends only on its own A row and on B,
-// and zero rows of B only meet zero entries of the row's A (T, P are lower
-// triangular), so row p gets the prefill's bits.  The fp32 parts (gate prefix,
-// exponentials, T row, epilogues) are the same operation sequences as the
-// prefill's.  When the chunk fills (p = C - 1) the step commits the next
-// chunk-start state with the prefill's commit MMAs: the resynchronisation
-// every C tokens (page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配", section
-// "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet").
+// k_tc_state): same shapes, same operand tiles, layouts and row positions,
+// same k-step and hi/lo pass order, with the rows of the chunk that do not
+// exist yet set to zero.  An output row of an MMA depends only on its own A
+// row and on B, and zero rows of B only meet zero entries of the row's A (T
+// and P are lower triangular), so row p gets the prefill's bits.  The fp32
+// parts (gate prefix, exponentials, T row, epilogues) are the same operation
+// sequences as the prefill's.  When the chunk fills (p = C - 1) the step
+// commits the next chunk-start state with the prefill's commit MMAs: the
+// resynchronisation every C tokens (page "IsoExec: 切换 SkyRL 中的训练器-
+// 推理不匹配", section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet").
 #pragma once
 
 #include "tc_fwd.cuh"
@@ -20,13 +20,13 @@ namespace cpr {
 namespace tc {
 
 struct DecSmem {
-    static constexpr size_t Hhi = 0, Hlo = 32768;   // H^T, 128 x 128 bf16 each
-    static constexpr size_t Kt = 65536;              // K^T, 128 x 64
+    static constexpr size_t Hhi = 0, Hlo = 32768;   // per split: MN-major DVS (j) x 128 (d)
+    static constexpr size_t Kmn = 65536;             // K, MN-major 128 (d) x 64 (token)
     static constexpr size_t R1 = 81920;              // 64 KB, reused by phase
     static constexpr size_t F = R1 + 65536;          // fp32 scratch
-    // fp32 arrays (floats from F)
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
-                         fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fEnd = 960;
+                         fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
+                         fRow2 = 1088, fEnd = 1216;
     static constexpr size_t Bar = F + fEnd * 4;
     static constexpr size_t Total = Bar + 64;
 };
@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     float* F = reinterpret_cast<float*>(sm + S::F);
     float *gams = F + S::fGam, *bets = F + S::fBet, *bgs = F + S::fBg, *arow = F + S::fArow,
           *prow = F + S::fProw, *trow = F + S::fTrow, *decs = F + S::fDec, *Wp = F + S::fWp,
-          *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs;
+          *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs, *row1 = F + S::fRow,
+          *row2 = F + S::fRow2;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
     __shared__ int ok_s;
@@ -80,8 +81,8 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     if (!ok_s) return;
     const int p = ok_s - 1;
     const size_t sh = (size_t)b * H + h;
-    const __nv_bfloat16* ck = reinterpret_cast<const __nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
-    const __nv_bfloat16* cv = reinterpret_cast<const __nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
+    __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
+    __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
     float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
     float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
     float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
@@ -97,49 +98,33 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         mbar_init(mbar, 1);
         mbar_init_fence();
     }
-    // token row s of the chunk (k or v): cache rows below p, the new token at p, zero above
-    auto row_ptr = [&](const __nv_bfloat16* cache_rows, const __nv_bfloat16* tok, int s) {
-        return s < p ? cache_rows + (size_t)s * D : tok;
-    };
-    // H^T split into hi / lo (rows j, K dim d), from the fp32 chunk-start state
-    for (int i = tid; i < 16 * 16; i += 128) {
-        const int j8 = i / 16, d8 = i % 16;
-        float rows[8][8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float4 x0 = *reinterpret_cast<const float4*>(Hst + (size_t)(d8 * 8 + r) * D + j8 * 8);
-            const float4 x1 = *reinterpret_cast<const float4*>(Hst + (size_t)(d8 * 8 + r) * D + j8 * 8 + 4);
-            rows[r][0] = x0.x; rows[r][1] = x0.y; rows[r][2] = x0.z; rows[r][3] = x0.w;
-            rows[r][4] = x1.x; rows[r][5] = x1.y; rows[r][6] = x1.z; rows[r][7] = x1.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            float x[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) x[r] = rows[r][c];
-            store8_split(sm + S::Hhi, sm + S::Hlo, cm_off(j8 * 8 + c, d8 * 8, D), x);
+    // H rows -> per-split MN-major hi/lo tiles (row d = tid)
+    {
+        const int d = tid;
+#pragma unroll 4
+        for (int j8 = 0; j8 < D / 8; ++j8) {
+            const float4 x0 = *reinterpret_cast<const float4*>(Hst + (size_t)d * D + j8 * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(Hst + (size_t)d * D + j8 * 8 + 4);
+            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+            const size_t tile = (size_t)sp * DVS * 128 * 2;
+            store8_split(sm + S::Hhi + tile, sm + S::Hlo + tile, mn_off(jl, d, DVS), x);
         }
     }
-    // [K; Q] tile for S1: rows s <= p of K, row 64 + p = q_p, all else zero
+    // [K; Q] (R1, K-major): rows s <= p of K, row 64 + p = q_p; K and V as MN-major tiles
     for (int i = tid; i < 128 * (D / 8); i += 128) {
         const int r = i / (D / 8), d8 = i % (D / 8);
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (r < 64 && r <= p) val = *reinterpret_cast<const uint4*>(row_ptr(ck, kt, r) + d8 * 8);
-        if (r == 64 + p) val = *reinterpret_cast<const uint4*>(qt + d8 * 8);
-        *reinterpret_cast<uint4*>(R1 + cm_off(r, d8 * 8, D)) = val;
-    }
-    // K^T (sKt) and V^T (R1 + 32 KB): 8 x 8 transposes of the rows s <= p
-    for (int i = tid; i < 2 * 8 * (D / 8); i += 128) {
-        const int which = i / (8 * (D / 8));
-        const int s8 = (i / (D / 8)) % 8, d8 = i % (D / 8);
-        uint4 rows[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int s = s8 * 8 + j;
-            rows[j] = s <= p ? *reinterpret_cast<const uint4*>(row_ptr(which ? cv : ck, which ? vt : kt, s) + d8 * 8)
-                             : make_uint4(0u, 0u, 0u, 0u);
+        uint4 x = make_uint4(0u, 0u, 0u, 0u), y = make_uint4(0u, 0u, 0u, 0u);
+        if (r < 64 && r <= p) {
+            x = *reinterpret_cast<const uint4*>((r < p ? ck + (size_t)r * D : kt) + d8 * 8);
+            y = *reinterpret_cast<const uint4*>((r < p ? cv + (size_t)r * D : vt) + d8 * 8);
         }
-        transpose8_store(rows, (which ? R1 + 32768 : sm + S::Kt) + cm_off(d8 * 8, s8 * 8, C));
+        if (r == 64 + p) x = *reinterpret_cast<const uint4*>(qt + d8 * 8);
+        *reinterpret_cast<uint4*>(R1 + cm_off(r, d8 * 8, D)) = x;
+        if (r < 64) {
+            *reinterpret_cast<uint4*>(sm + S::Kmn + mn_off(d8 * 8, r, D)) = x;
+            *reinterpret_cast<uint4*>(R1 + 32768 + mn_off(d8 * 8, r, D)) = y;
+        }
     }
     if (tid < p) {
         gams[tid] = cg[tid];
@@ -149,6 +134,10 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         gams[p] = __fadd_rn(p > 0 ? cg[p - 1] : 0.f, a.g[sh]);
         bets[p] = a.beta[sh];
     }
+    // this thread's column of the cached T rows (for the T row chain), loaded early
+    float tcol[C];
+#pragma unroll
+    for (int s = 0; s < C; ++s) tcol[s] = (tid < C && s < p) ? ct[s * C + tid] : 0.f;
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
@@ -168,40 +157,36 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     ok = mma_wait();
     if (!ok) goto cleanup;
     {
-        const float gp = gams[p], bp = bets[p];
         float v[32];
         for (int c0 = 0; c0 < C; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
             if (tid == p) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c0 + j;
-                    arow[s] = (s < p) ? simt::a_entry(bp, gp, gams[s], v[j]) : 0.f;
-                }
+                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
             } else if (tid == 64 + p) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c0 + j;
-                    prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, gams[s]), __fmul_rn(a.scale, v[j])) : 0.f;
-                }
+                for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
             }
         }
     }
     __syncthreads();
-    if (tid < C) {  // T row p
-        const int j = tid;
-        float t = 0.f;
-        if (j < p) {
-            float acc = 0.f;
-            for (int s = j; s < p; ++s) acc = __fmaf_rn(arow[s], ct[s * C + j], acc);
-            t = -acc;
-        } else if (j == p) {
-            t = 1.f;
-        }
-        trow[j] = t;
+    if (tid < C) {
+        const int s = tid;
+        const float gp = gams[p], bp = bets[p];
+        arow[s] = (s < p) ? simt::a_entry(bp, gp, gams[s], row1[s]) : 0.f;
+        prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, gams[s]), __fmul_rn(a.scale, row2[s])) : 0.f;
     }
-    // X tiles (R1 + 0 .. 32 KB): zero except row p
+    // X tiles (R1 + 0 .. 32 KB) and the T row: zero the tiles first
+    __syncthreads();
     for (int i = tid; i < 2048; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < C) {  // T row p: T_pj = -(sum_{s=j}^{p-1} a_ps T_sj), ascending s
+        const int j = tid;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < C; ++s)
+            if (s >= j && s < p) acc = __fmaf_rn(arow[s], tcol[s], acc);
+        trow[j] = (j < p) ? -acc : (j == p ? 1.f : 0.f);
+    }
     __syncthreads();
     if (tid < 16) {
         const int which = tid >> 3, s8 = tid & 7;
@@ -218,10 +203,10 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        mma_tile<64, D, C>(tmem, R1, sm + S::Kt, false);
-        mma_tile<64, D, C>(tmem, R1 + 8192, sm + S::Kt, true);
-        mma_tile<64, D, C>(tmem + 128, R1 + 16384, R1 + 32768, false);
-        mma_tile<64, D, C>(tmem + 128, R1 + 24576, R1 + 32768, true);
+        mma_tile_mj<64, D, C, false, true>(tmem, R1, sm + S::Kmn, false);
+        mma_tile_mj<64, D, C, false, true>(tmem, R1 + 8192, sm + S::Kmn, true);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 16384, R1 + 32768, false);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 24576, R1 + 32768, true);
         mma_commit(mbar);
     }
     ok = mma_wait();
@@ -258,45 +243,62 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
 #pragma unroll
         for (int sp = 0; sp < NSPLIT; ++sp) {
             const uint32_t acc = tmem + sp * DVS;
-            mma_tile<128, DVS, D>(acc, R1, sm + S::Hhi + sp * DVS * 256, false);
-            mma_tile<128, DVS, D>(acc, R1, sm + S::Hlo + sp * DVS * 256, true);
-            mma_tile<128, DVS, D>(acc, R1 + 32768, sm + S::Hhi + sp * DVS * 256, true);
+            const size_t tile = (size_t)sp * DVS * 128 * 2;
+            mma_tile_mj<128, DVS, D, false, true>(acc, R1, sm + S::Hhi + tile, false);
+            mma_tile_mj<128, DVS, D, false, true>(acc, R1, sm + S::Hlo + tile, true);
+            mma_tile_mj<128, DVS, D, false, true>(acc, R1 + 32768, sm + S::Hhi + tile, true);
         }
         mma_commit(mbar);
     }
     ok = mma_wait();
     if (!ok) goto cleanup;
     {
-        const float Gp = simt::gate(gams[p]);
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
             if (tid == p) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Dp[c0 + j] = __fsub_rn(Up[c0 + j], v[j]);
+                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
             } else if (tid == 64 + p) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Qs[c0 + j] = __fmul_rn(Gp, __fmul_rn(a.scale, v[j]));
+                for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
             }
         }
     }
     __syncthreads();
-    // P tiles (R1 + 0: hi, + 8 KB: lo; zero except row p) and Delta^T (R1 + 16 KB: hi, + 32 KB: lo)
-    for (int i = tid; i < 1024; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = tid; i < C * D; i += 128) {
-        const int s = i / D, j = i % D;
-        const float x = s < p ? cd[(size_t)s * D + j] : (s == p ? Dp[j] : 0.f);
-        __nv_bfloat16 hi, lo;
-        split_bf16(x, hi, lo);
-        *reinterpret_cast<__nv_bfloat16*>(R1 + 16384 + cm_off(j, s, C)) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(R1 + 32768 + cm_off(j, s, C)) = lo;
+    {
+        const float Gp = simt::gate(gams[p]);
+        const int j = tid;  // D == 128 == blockDim
+        Dp[j] = __fsub_rn(Up[j], row1[j]);
+        Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
     }
+    // P tiles (R1 + 0: hi, + 8 KB: lo; zero except row p); Delta (MN-major per split)
+    for (int i = tid; i < 1024; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    if (tid < 8) {
+    if (tid < C) {
+        const int s = tid;
+#pragma unroll 4
+        for (int j8 = 0; j8 < D / 8; ++j8) {
+            float x[8];
+            if (s < p) {
+                const float4 x0 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8);
+                const float4 x1 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8 + 4);
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (s == p) ? Dp[j8 * 8 + e] : 0.f;
+            }
+            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+            const size_t tile = (size_t)sp * DVS * 64 * 2;
+            store8_split(R1 + 16384 + tile, R1 + 32768 + tile, mn_off(jl, s, DVS), x);
+        }
+    } else if (tid < C + 8) {
+        const int s8 = tid - C;
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = prow[tid * 8 + e];
-        store8_split(R1, R1 + 8192, cm_off(p, tid * 8, C), x);
+        for (int e = 0; e < 8; ++e) x[e] = prow[s8 * 8 + e];
+        store8_split(R1, R1 + 8192, cm_off(p, s8 * 8, C), x);
     }
     fence_async_smem();
     tc_sync();
@@ -304,9 +306,10 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
 #pragma unroll
         for (int sp = 0; sp < NSPLIT; ++sp) {
             const uint32_t acc = tmem + 128 + sp * DVS;
-            mma_tile<64, DVS, C>(acc, R1, R1 + 16384 + sp * DVS * 128, false);
-            mma_tile<64, DVS, C>(acc, R1, R1 + 32768 + sp * DVS * 128, true);
-            mma_tile<64, DVS, C>(acc, R1 + 8192, R1 + 16384 + sp * DVS * 128, true);
+            const size_t tile = (size_t)sp * DVS * 64 * 2;
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1, R1 + 16384 + tile, false);
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1, R1 + 32768 + tile, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1 + 8192, R1 + 16384 + tile, true);
         }
         mma_commit(mbar);
     }
@@ -319,17 +322,16 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
             tmem_ld32(taddr_of(tmem, warp, 128 + c0), v);
             if (mine) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a.o[sh * D + c0 + j] = __fadd_rn(Qs[c0 + j], v[j]);
+                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
             }
         }
     }
     __syncthreads();
+    a.o[sh * D + tid] = __fadd_rn(Qs[tid], row1[tid]);
     {
         // append row p to the cache
-        __nv_bfloat16* ckw = const_cast<__nv_bfloat16*>(ck);
-        __nv_bfloat16* cvw = const_cast<__nv_bfloat16*>(cv);
-        if (tid < 16) *reinterpret_cast<uint4*>(ckw + (size_t)p * D + tid * 8) = *reinterpret_cast<const uint4*>(kt + tid * 8);
-        else if (tid < 32) *reinterpret_cast<uint4*>(cvw + (size_t)p * D + (tid - 16) * 8) = *reinterpret_cast<const uint4*>(vt + (tid - 16) * 8);
+        if (tid < 16) *reinterpret_cast<uint4*>(ck + (size_t)p * D + tid * 8) = *reinterpret_cast<const uint4*>(kt + tid * 8);
+        else if (tid < 32) *reinterpret_cast<uint4*>(cv + (size_t)p * D + (tid - 16) * 8) = *reinterpret_cast<const uint4*>(vt + (tid - 16) * 8);
         cd[(size_t)p * D + tid] = Dp[tid];
         if (tid < C) ct[p * C + tid] = trow[tid];
         if (tid == 0) {
@@ -341,13 +343,27 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         const int Lr = C - 1;
         if (tid < C) decs[tid] = simt::decay(gams[Lr], gams[tid]);
         __syncthreads();
-        for (int i = tid; i < C * D; i += 128) {
-            const int s = i / D, j = i % D;
-            const float x = __fmul_rn(decs[s], s < p ? cd[(size_t)s * D + j] : Dp[j]);
-            __nv_bfloat16 hi, lo;
-            split_bf16(x, hi, lo);
-            *reinterpret_cast<__nv_bfloat16*>(R1 + 16384 + cm_off(j, s, C)) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(R1 + 32768 + cm_off(j, s, C)) = lo;
+        if (tid < C) {
+            const int s = tid;
+            const float ds = decs[s];
+#pragma unroll 4
+            for (int j8 = 0; j8 < D / 8; ++j8) {
+                float x[8];
+                if (s < p) {
+                    const float4 x0 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8);
+                    const float4 x1 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8 + 4);
+                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                    x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = Dp[j8 * 8 + e];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(ds, x[e]);
+                const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+                const size_t tile = (size_t)sp * DVS * 64 * 2;
+                store8_split(R1 + 16384 + tile, R1 + 32768 + tile, mn_off(jl, s, DVS), x);
+            }
         }
         fence_async_smem();
         tc_sync();
@@ -355,8 +371,9 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
 #pragma unroll
             for (int sp = 0; sp < NSPLIT; ++sp) {
                 const uint32_t acc = tmem + sp * DVS;
-                mma_tile<128, DVS, C>(acc, sm + S::Kt, R1 + 16384 + sp * DVS * 128, false);
-                mma_tile<128, DVS, C>(acc, sm + S::Kt, R1 + 32768 + sp * DVS * 128, true);
+                const size_t tile = (size_t)sp * DVS * 64 * 2;
+                mma_tile_mj<128, DVS, C, true, true>(acc, sm + S::Kmn, R1 + 16384 + tile, false);
+                mma_tile_mj<128, DVS, C, true, true>(acc, sm + S::Kmn, R1 + 32768 + tile, true);
             }
             mma_commit(mbar);
         }
@@ -368,9 +385,13 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float* hp = Hst + (size_t)d * D + c0 + j;
-                *hp = __fadd_rn(__fmul_rn(GL, *hp), v[j]);
+            for (int j4 = 0; j4 < 8; ++j4) {
+                float4* hp = reinterpret_cast<float4*>(Hst + (size_t)d * D + c0 + 4 * j4);
+                const float4 h4 = *hp;
+                *hp = make_float4(__fadd_rn(__fmul_rn(GL, h4.x), v[4 * j4]),
+                                  __fadd_rn(__fmul_rn(GL, h4.y), v[4 * j4 + 1]),
+                                  __fadd_rn(__fmul_rn(GL, h4.z), v[4 * j4 + 2]),
+                                  __fadd_rn(__fmul_rn(GL, h4.w), v[4 * j4 + 3]));
             }
         }
     }

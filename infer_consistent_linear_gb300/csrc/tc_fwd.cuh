@@ -7,7 +7,7 @@
 //   S1   = [K; Q] K^T                      (exact bf16 inputs, one MMA group)
 //   a_rs = (b_r exp(gam_r - gam_s)) kk_rs       s < r
 //   p_rs = exp(gam_r - gam_s) (scale qk_rs)     s <= r
-//   T    = (I + A)^-1                       (fp32 column chains)
+//   T    = (I + A)^-1                       (fp32, T_rj = -sum_{s=j}^{r-1} a_rs T_sj, ascending s)
 //   W'   = (T diag(b G)) K,   U = (T diag(b)) V     (split A operand: hi + lo)
 //   acc4 = [W'; Q] H                        (hi*hi + hi*lo + lo*hi)
 //   D    = U - acc4[rows 0..63],   qh = acc4[rows 64..127]
@@ -18,7 +18,8 @@
 // H, written to the workspace in the operand layouts the tensor core reads)
 // and k_tc_state (one CTA per (sequence, head, d_v split), strictly in chunk
 // order, the H-dependent part with the workspace tiles streamed in by bulk
-// async copies).
+// async copies).  Token rows (k, v, a row of H or of Delta) feed MN-major
+// operand tiles directly, so no kernel transposes anything.
 #pragma once
 
 #include "simt_fwd.cuh"
@@ -31,11 +32,11 @@ constexpr int D = 128;
 constexpr int C = kChunk;
 
 // Per (chunk, head) workspace block (bytes).
-constexpr size_t kOffA4hi = 0;        // 128 x 128 bf16: rows 0..63 W'_hi, 64..127 Q
-constexpr size_t kOffA4lo = 32768;    // 64 x 128 bf16: W'_lo
-constexpr size_t kOffKt = 49152;      // 128 x 64 bf16: K^T (rows d, K dim s)
-constexpr size_t kOffPhi = 65536;     // 64 x 64 bf16
-constexpr size_t kOffPlo = 73728;     // 64 x 64 bf16
+constexpr size_t kOffA4hi = 0;        // 128 x 128 bf16 K-major: rows 0..63 W'_hi, 64..127 Q
+constexpr size_t kOffA4lo = 32768;    // 64 x 128 bf16 K-major: W'_lo
+constexpr size_t kOffKmn = 49152;     // K as an MN-major 128 (d) x 64 (token) tile
+constexpr size_t kOffPhi = 65536;     // 64 x 64 bf16 K-major
+constexpr size_t kOffPlo = 73728;     // 64 x 64 bf16 K-major
 constexpr size_t kOffU = 81920;       // 64 x 128 fp32, stored [split][64][DVS]
 constexpr size_t kOffGam = 114688;    // 64 fp32
 constexpr size_t kBlock = 114944;
@@ -61,40 +62,53 @@ struct TcArgs {
     uint32_t* err;
 };
 
-// Transposes an 8 x 8 bf16 block: in[j] holds row j (8 values); writes the
-// 8 rows of the transpose (row i = {in[0][i], ..., in[7][i]}) as one core matrix.
-__device__ __forceinline__ void transpose8_store(const uint4 (&in)[8], unsigned char* core) {
-    const __nv_bfloat16* e[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) e[j] = reinterpret_cast<const __nv_bfloat16*>(&in[j]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        __align__(16) __nv_bfloat16 row[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) row[j] = e[j][i];
-        *reinterpret_cast<uint4*>(core + 16 * i) = *reinterpret_cast<const uint4*>(row);
-    }
-}
-
 __device__ __forceinline__ uint4 ld16_or_zero(const __nv_bfloat16* p, bool valid) {
     return valid ? *reinterpret_cast<const uint4*>(p) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// T = (I + A)^-1 for one column j (the calling thread), all rows at once:
+// row r's sum runs over s = j, j+1, ..., r-1 in ascending order exactly as the
+// column chain T_rj = -(sum_{s=j}^{r-1} a_rs T_sj) does, but every row takes
+// its term s in the same step, so the dependent path is one fma per step.
+// At holds A transposed (At[s * 64 + r] = a_rs); writes T rows < nrows of
+// column j to Tout[r * ldT + j] (rows >= nrows get 0).
+__device__ __forceinline__ void t_solve_column(const float* At, float* Tout, int ldT, int j, int nrows) {
+    float acc[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) acc[r] = 0.f;
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+        const float Tt = (t < j) ? 0.f : (t == j ? 1.f : -acc[t]);
+        Tout[t * ldT + j] = (t < nrows) ? Tt : 0.f;
+        if (t >= j) {
+#pragma unroll
+            for (int r4 = (t + 1) / 4; r4 < C / 4; ++r4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(At + t * C + 4 * r4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * r4 + e > t) acc[4 * r4 + e] = __fmaf_rn(av[e], Tt, acc[4 * r4 + e]);
+            }
+        }
+    }
+}
+
 // ---- prep: everything of a chunk that does not depend on H ------------------------
-constexpr size_t kPrepSmem = 65536 + 2 * 64 * 65 * 4 + 4 * 64 * 4 + 64;
+constexpr size_t kPrepOffKmn = 32768, kPrepOffVmn = 49152, kPrepOffAt = 65536,
+                 kPrepOffT = 65536 + 16384, kPrepOffVec = kPrepOffT + 64 * 65 * 4;
+constexpr size_t kPrepSmem = kPrepOffVec + 3 * 64 * 4 + 64;
 
 static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char* tKQ = sm;            // 128 x 128 bf16; later the four X tiles
-    unsigned char* tKt = sm + 32768;    // 128 x 64
-    unsigned char* tVt = sm + 49152;    // 128 x 64
-    float* Afp = reinterpret_cast<float*>(sm + 65536);  // [64][65]
-    float* Tfp = Afp + 64 * 65;
-    float* gam = Tfp + 64 * 65;
+    unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; later the X tiles
+    unsigned char* tKmn = sm + kPrepOffKmn;        // K, MN-major 128 (d) x 64 (token)
+    unsigned char* tVmn = sm + kPrepOffVmn;        // V, MN-major
+    float* At = reinterpret_cast<float*>(sm + kPrepOffAt);   // [64][64], At[s][r] = a_rs
+    float* Tfp = reinterpret_cast<float*>(sm + kPrepOffT);   // [64][65]
+    float* gam = reinterpret_cast<float*>(sm + kPrepOffVec);
     float* bet = gam + 64;
     float* bg = bet + 64;
-    float* spare = bg + 64;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(spare + 64);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(bg + 64);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
 
     const int total = a.chunk_off[a.n_seq];
@@ -114,25 +128,17 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
         mbar_init(mbar, 1);
         mbar_init_fence();
     }
-    // [K; Q] rows (K-major: row = token, K dim = d)
+    // [K; Q] rows (K-major), K and V token rows into MN-major tiles
     for (int i = tid; i < 128 * (D / 8); i += 128) {
         const int r = i / (D / 8), d8 = i % (D / 8);
         const int tr = r & 63;
-        const __nv_bfloat16* src = (r < 64 ? a.k : a.q) + ((size_t)(t0 + tr) * H + h) * D + d8 * 8;
-        *reinterpret_cast<uint4*>(tKQ + cm_off(r, d8 * 8, D)) = ld16_or_zero(src, tr < nrows);
-    }
-    // K^T and V^T (rows = d, K dim = token): 8 x 8 block transposes
-    for (int i = tid; i < 2 * 8 * (D / 8); i += 128) {
-        const int which = i / (8 * (D / 8));
-        const int s8 = (i / (D / 8)) % 8, d8 = i % (D / 8);
-        const __nv_bfloat16* base = which ? a.v : a.k;
-        uint4 rows[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int s = s8 * 8 + j;
-            rows[j] = ld16_or_zero(base + ((size_t)(t0 + s) * H + h) * D + d8 * 8, s < nrows);
+        const size_t src = ((size_t)(t0 + tr) * H + h) * D + d8 * 8;
+        const uint4 x = ld16_or_zero((r < 64 ? a.k : a.q) + src, tr < nrows);
+        *reinterpret_cast<uint4*>(tKQ + cm_off(r, d8 * 8, D)) = x;
+        if (r < 64) {
+            *reinterpret_cast<uint4*>(tKmn + mn_off(d8 * 8, tr, D)) = x;
+            *reinterpret_cast<uint4*>(tVmn + mn_off(d8 * 8, tr, D)) = ld16_or_zero(a.v + src, tr < nrows);
         }
-        transpose8_store(rows, (which ? tVt : tKt) + cm_off(d8 * 8, s8 * 8, C));
     }
     if (tid < C) {
         gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
@@ -153,19 +159,21 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
         mma_tile<128, 64, D>(tmem, tKQ, tKQ, false);  // B = rows 0..63 of [K; Q] = K
         mma_commit(mbar);
     }
+    int outstanding = 0;  // mbarrier phase an in-flight MMA group will complete, or -1
     if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid]) : 0.f;
-    // Q rows and K^T go to the workspace as the state pass's operand tiles
+    // Q rows and K (MN-major) go to the workspace as the state pass's operand tiles
     for (int i = tid; i < 1024; i += 128) {
         reinterpret_cast<uint4*>(blk + kOffA4hi + 16384)[i] = reinterpret_cast<const uint4*>(tKQ + 16384)[i];
-        reinterpret_cast<uint4*>(blk + kOffKt)[i] = reinterpret_cast<const uint4*>(tKt)[i];
+        reinterpret_cast<uint4*>(blk + kOffKmn)[i] = reinterpret_cast<const uint4*>(tKmn)[i];
     }
-    int outstanding = 0;  // mbarrier phase an in-flight MMA group will complete, or -1
-    const bool ok1 = mbar_wait(mbar, 0, a.err);
-    fence_after();
-    if (__syncthreads_or(!ok1)) goto done;
+    {
+        const bool ok1 = mbar_wait(mbar, 0, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok1)) goto done;
+    }
     outstanding = -1;
     {
-        // S1 epilogue: thread = TMEM lane = row (0..63: K rows, 64..127: Q rows)
+        // S1 epilogue: thread = TMEM lane = row (0..63: K rows -> A, 64..127: Q rows -> P)
         float v[32];
         const int r = tid & 63;
         for (int c0 = 0; c0 < C; c0 += 32) {
@@ -174,7 +182,7 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int s = c0 + j;
-                    Afp[r * 65 + s] = (s < r && r < nrows) ? simt::a_entry(bet[r], gam[r], gam[s], v[j]) : 0.f;
+                    At[s * C + r] = (s < r && r < nrows) ? simt::a_entry(bet[r], gam[r], gam[s], v[j]) : 0.f;
                 }
             } else {
 #pragma unroll
@@ -193,16 +201,7 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
         }
     }
     __syncthreads();
-    // T = (I + A)^-1 by columns: T_rj = -(sum_{s=j}^{r-1} a_rs T_sj), ascending s
-    if (tid < C) {
-        const int j = tid;
-        for (int r = 0; r < C; ++r) Tfp[r * 65 + j] = (r == j && r < nrows) ? 1.f : 0.f;
-        for (int r = j + 1; r < nrows; ++r) {
-            float acc = 0.f;
-            for (int s = j; s < r; ++s) acc = __fmaf_rn(Afp[r * 65 + s], Tfp[s * 65 + j], acc);
-            Tfp[r * 65 + j] = -acc;
-        }
-    }
+    if (tid < C) t_solve_column(At, Tfp, 65, tid, nrows);
     __syncthreads();
     {
         // X1 = T diag(b G) (threads 0..63), X2 = T diag(b) (threads 64..127), split
@@ -239,10 +238,10 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        mma_tile<64, D, C>(tmem, tKQ, tKt, false);                // W' = X1_hi K
-        mma_tile<64, D, C>(tmem, tKQ + 8192, tKt, true);          //    + X1_lo K
-        mma_tile<64, D, C>(tmem + 128, tKQ + 16384, tVt, false);  // U  = X2_hi V
-        mma_tile<64, D, C>(tmem + 128, tKQ + 24576, tVt, true);   //    + X2_lo V
+        mma_tile_mj<64, D, C, false, true>(tmem, tKQ, tKmn, false);                // W' = X1_hi K
+        mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 8192, tKmn, true);          //    + X1_lo K
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, tKQ + 16384, tVmn, false);  // U  = X2_hi V
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, tKQ + 24576, tVmn, true);   //    + X2_lo V
         mma_commit(mbar);
     }
     outstanding = 1;
@@ -293,20 +292,21 @@ done:
 // ---- state pass: one CTA per (sequence, head, d_v split), chunks in order -----------
 template <int DVS>
 struct StateSmem {
-    static constexpr size_t A4hi = 0, A4lo = 32768, Kt = 65536, Phi = 81920, Plo = 90112;
+    static constexpr size_t A4hi = 0, A4lo = 32768, Kmn = 65536, Phi = 81920, Plo = 90112;
     static constexpr size_t U = 98304;                       // 64 x DVS fp32
-    static constexpr size_t Hhi = U + 64 * DVS * 4;          // DVS x 128 bf16
+    static constexpr size_t Hhi = U + 64 * DVS * 4;          // H as MN-major DVS (j) x 128 (d)
     static constexpr size_t Hlo = Hhi + DVS * 128 * 2;
-    static constexpr size_t Dhi = Hlo + DVS * 128 * 2;       // DVS x 64 bf16
+    static constexpr size_t Dhi = Hlo + DVS * 128 * 2;       // Delta, MN-major DVS (j) x 64 (token)
     static constexpr size_t Dlo = Dhi + DVS * 64 * 2;
-    static constexpr size_t Bhi = Dlo + DVS * 64 * 2;
+    static constexpr size_t Bhi = Dlo + DVS * 64 * 2;        // decay * Delta, same layout
     static constexpr size_t Blo = Bhi + DVS * 64 * 2;
     static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32
     static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 (bulk copied)
     static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
-    static constexpr size_t Bar = Dec + 256;                 // 2 mbarriers + TMEM base
+    static constexpr size_t Bar = Dec + 256;                 // 3 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
-    static constexpr uint32_t LoadBytes = 32768 + 16384 + 16384 + 8192 + 8192 + 64 * DVS * 4 + 256;
+    static constexpr uint32_t LoadA = 32768 + 16384;
+    static constexpr uint32_t LoadB = 16384 + 8192 + 8192 + 64 * DVS * 4 + 256;
 };
 
 template <int DVS>
@@ -320,8 +320,9 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     float* Gm = reinterpret_cast<float*>(sm + L::Gm);
     float* dec = reinterpret_cast<float*>(sm + L::Dec);
     uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);
-    uint64_t* bar_ld = bar_mma + 1;
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 2);
+    uint64_t* bar_ldA = bar_mma + 1;
+    uint64_t* bar_ldB = bar_mma + 2;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 3);
 
     const int total = a.chunk_off[a.n_seq];
     if (total < 0) return;
@@ -339,7 +340,8 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     if (warp == 0) tmem_alloc(tbase, 256);
     if (tid == 0) {
         mbar_init(bar_mma, 1);
-        mbar_init(bar_ld, 1);
+        mbar_init(bar_ldA, 1);
+        mbar_init(bar_ldB, 1);
         mbar_init_fence();
     }
     for (int i = tid; i < 1024; i += 128)  // rows 64..127 of the W'_lo operand stay zero
@@ -348,39 +350,57 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     float Hreg[DVS];
     const int d = tid;
 #pragma unroll
-    for (int j = 0; j < DVS; ++j) Hreg[j] = a.h0 ? a.h0[(sh * D + d) * D + j0 + j] : 0.f;
-#pragma unroll
-    for (int j = 0; j < DVS; ++j) {
-        __nv_bfloat16 hi, lo;
-        split_bf16(Hreg[j], hi, lo);
-        *reinterpret_cast<__nv_bfloat16*>(sm + L::Hhi + cm_off(j, d, D)) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(sm + L::Hlo + cm_off(j, d, D)) = lo;
+    for (int j4 = 0; j4 < DVS / 4; ++j4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.h0) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + 4 * j4);
+        Hreg[4 * j4] = x.x; Hreg[4 * j4 + 1] = x.y; Hreg[4 * j4 + 2] = x.z; Hreg[4 * j4 + 3] = x.w;
     }
-    if (nch == 0 && cstate) {
+    auto put_h = [&]() {
 #pragma unroll
-        for (int j = 0; j < DVS; ++j) cstate[d * D + j0 + j] = Hreg[j];
-    }
+        for (int j8 = 0; j8 < DVS / 8; ++j8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = Hreg[j8 * 8 + e];
+            store8_split(sm + L::Hhi, sm + L::Hlo, mn_off(j8 * 8, d, DVS), x);
+        }
+    };
+    auto put_state = [&](float* dst) {
+#pragma unroll
+        for (int j4 = 0; j4 < DVS / 4; ++j4)
+            *reinterpret_cast<float4*>(dst + (size_t)d * D + j0 + 4 * j4) =
+                make_float4(Hreg[4 * j4], Hreg[4 * j4 + 1], Hreg[4 * j4 + 2], Hreg[4 * j4 + 3]);
+    };
+    put_h();
+    if (nch == 0 && cstate) put_state(cstate);
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
     const uint32_t acc4 = tmem, acc5 = tmem + DVS, acc6 = tmem + 2 * DVS;
-    uint32_t ph_mma = 0, ph_ld = 0;
-    bool pending = false, failed = false, mma_out = false;
+    uint32_t ph_mma = 0, ph_ldA = 0, ph_ldB = 0;
+    bool pendA = false, pendB = false, failed = false, mma_out = false;
 
-    auto issue_loads = [&](int n) {
-        const unsigned char* blk = a.ws + ((size_t)(a.chunk_off[b] + n) * H + h) * kBlock;
-        mbar_expect_tx(bar_ld, L::LoadBytes);
-        bulk_g2s(sm + L::A4hi, blk + kOffA4hi, 32768, bar_ld);
-        bulk_g2s(sm + L::A4lo, blk + kOffA4lo, 16384, bar_ld);
-        bulk_g2s(sm + L::Kt, blk + kOffKt, 16384, bar_ld);
-        bulk_g2s(sm + L::Phi, blk + kOffPhi, 8192, bar_ld);
-        bulk_g2s(sm + L::Plo, blk + kOffPlo, 8192, bar_ld);
-        bulk_g2s(sm + L::U, blk + kOffU + (size_t)sp * 64 * DVS * 4, 64 * DVS * 4, bar_ld);
-        bulk_g2s(sm + L::Gam, blk + kOffGam, 256, bar_ld);
+    auto blk_of = [&](int n) { return a.ws + ((size_t)(a.chunk_off[b] + n) * H + h) * kBlock; };
+    auto issue_A = [&](int n) {
+        const unsigned char* blk = blk_of(n);
+        mbar_expect_tx(bar_ldA, L::LoadA);
+        bulk_g2s(sm + L::A4hi, blk + kOffA4hi, 32768, bar_ldA);
+        bulk_g2s(sm + L::A4lo, blk + kOffA4lo, 16384, bar_ldA);
+    };
+    auto issue_B = [&](int n) {
+        const unsigned char* blk = blk_of(n);
+        mbar_expect_tx(bar_ldB, L::LoadB);
+        bulk_g2s(sm + L::Kmn, blk + kOffKmn, 16384, bar_ldB);
+        bulk_g2s(sm + L::Phi, blk + kOffPhi, 8192, bar_ldB);
+        bulk_g2s(sm + L::Plo, blk + kOffPlo, 8192, bar_ldB);
+        bulk_g2s(sm + L::U, blk + kOffU + (size_t)sp * 64 * DVS * 4, 64 * DVS * 4, bar_ldB);
+        bulk_g2s(sm + L::Gam, blk + kOffGam, 256, bar_ldB);
     };
     if (nch > 0) {
-        if (tid == 0) issue_loads(0);
-        pending = true;
+        if (tid == 0) {
+            issue_A(0);
+            issue_B(0);
+        }
+        pendA = pendB = true;
     }
 
     for (int n = 0; n < nch; ++n) {
@@ -388,19 +408,23 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         const int nrows = min(C, T - n * C);
         const int Lr = nrows - 1;
         const bool last = (n == nch - 1);
-        bool ok = mbar_wait(bar_ld, ph_ld, a.err);
-        pending = !ok;
+        bool ok = mbar_wait(bar_ldB, ph_ldB, a.err);
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_ld ^= 1u;
+        ph_ldB ^= 1u;
+        pendB = false;
         if (tid < C) {
             Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
             dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
         }
         const float GL = simt::gate(gam[Lr]);
+        ok = mbar_wait(bar_ldA, ph_ldA, a.err);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_ldA ^= 1u;
+        pendA = false;
         if (tid == 0) {
-            mma_tile<128, DVS, D>(acc4, sm + L::A4hi, sm + L::Hhi, false);
-            mma_tile<128, DVS, D>(acc4, sm + L::A4hi, sm + L::Hlo, true);
-            mma_tile<128, DVS, D>(acc4, sm + L::A4lo, sm + L::Hhi, true);
+            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4hi, sm + L::Hhi, false);
+            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4hi, sm + L::Hlo, true);
+            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4lo, sm + L::Hhi, true);
             mma_commit(bar_mma);
         }
         mma_out = true;
@@ -409,6 +433,11 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_mma ^= 1u;
         mma_out = false;
+        if (tid == 0 && n + 1 < nch) {  // the A4 operand tiles of chunk n are consumed
+            fence_async_smem();
+            issue_A(n + 1);
+        }
+        pendA = (n + 1 < nch);
         {
             // rows 0..63: Delta = U - W'H ; rows 64..127: qh
             const int r = tid;
@@ -419,41 +448,47 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
                 if (r < 64) {
                     const bool in = r < nrows;
                     float* cd = (a.cache && last && nrows < C && in)
-                                    ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0
+                                    ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0 + c0
                                     : nullptr;
+                    const float dr = dec[r];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int jj = c0 + j;
-                        const float dl = in ? __fsub_rn(sU[r * DVS + jj], v[j]) : 0.f;
-                        __nv_bfloat16 hi, lo;
-                        split_bf16(dl, hi, lo);
-                        *reinterpret_cast<__nv_bfloat16*>(sm + L::Dhi + cm_off(jj, r, C)) = hi;
-                        *reinterpret_cast<__nv_bfloat16*>(sm + L::Dlo + cm_off(jj, r, C)) = lo;
-                        split_bf16(__fmul_rn(dec[r], dl), hi, lo);
-                        *reinterpret_cast<__nv_bfloat16*>(sm + L::Bhi + cm_off(jj, r, C)) = hi;
-                        *reinterpret_cast<__nv_bfloat16*>(sm + L::Blo + cm_off(jj, r, C)) = lo;
-                        if (cd) cd[jj] = dl;
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float x[8], y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int jj = c0 + j8 * 8 + e;
+                            x[e] = in ? __fsub_rn(sU[r * DVS + jj], v[j8 * 8 + e]) : 0.f;
+                            y[e] = __fmul_rn(dr, x[e]);
+                        }
+                        store8_split(sm + L::Dhi, sm + L::Dlo, mn_off(c0 + j8 * 8, r, DVS), x);
+                        store8_split(sm + L::Bhi, sm + L::Blo, mn_off(c0 + j8 * 8, r, DVS), y);
+                        if (cd) {
+                            *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
+                            *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                        }
                     }
                 } else {
                     const int rr = r - 64;
+                    const float gr = Gm[rr];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        sQ[rr * DVS + c0 + j] = __fmul_rn(Gm[rr], __fmul_rn(a.scale, v[j]));
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        *reinterpret_cast<float4*>(sQ + rr * DVS + c0 + 4 * j4) =
+                            make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
+                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
+                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
+                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
                 }
             }
-            if (cstate && last && nrows < C) {
-#pragma unroll
-                for (int j = 0; j < DVS; ++j) cstate[d * D + j0 + j] = Hreg[j];
-            }
+            if (cstate && last && nrows < C) put_state(cstate);
         }
         fence_async_smem();
         tc_sync();
         if (tid == 0) {
-            mma_tile<64, DVS, C>(acc5, sm + L::Phi, sm + L::Dhi, false);
-            mma_tile<64, DVS, C>(acc5, sm + L::Phi, sm + L::Dlo, true);
-            mma_tile<64, DVS, C>(acc5, sm + L::Plo, sm + L::Dhi, true);
-            mma_tile<128, DVS, C>(acc6, sm + L::Kt, sm + L::Bhi, false);
-            mma_tile<128, DVS, C>(acc6, sm + L::Kt, sm + L::Blo, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Phi, sm + L::Dhi, false);
+            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Phi, sm + L::Dlo, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Plo, sm + L::Dhi, true);
+            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Bhi, false);
+            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Blo, true);
             mma_commit(bar_mma);
         }
         mma_out = true;
@@ -462,11 +497,11 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_mma ^= 1u;
         mma_out = false;
-        if (tid == 0 && n + 1 < nch) {  // every operand tile of chunk n has been consumed
+        if (tid == 0 && n + 1 < nch) {  // K, P, U and gam of chunk n are consumed
             fence_async_smem();
-            issue_loads(n + 1);
+            issue_B(n + 1);
         }
-        pending = (n + 1 < nch);
+        pendB = (n + 1 < nch);
         {
             float v[32];
             // o rows: M = 64 accumulator, row r = 16 * warp + lane for lanes < 16
@@ -478,12 +513,10 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
                     float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + c0;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        float4 x;
-                        x.x = __fadd_rn(sQ[r * DVS + c0 + 4 * j4 + 0], v[4 * j4 + 0]);
-                        x.y = __fadd_rn(sQ[r * DVS + c0 + 4 * j4 + 1], v[4 * j4 + 1]);
-                        x.z = __fadd_rn(sQ[r * DVS + c0 + 4 * j4 + 2], v[4 * j4 + 2]);
-                        x.w = __fadd_rn(sQ[r * DVS + c0 + 4 * j4 + 3], v[4 * j4 + 3]);
-                        if (a.o) *reinterpret_cast<float4*>(orow + 4 * j4) = x;
+                        const float4 q4 = *reinterpret_cast<const float4*>(sQ + r * DVS + c0 + 4 * j4);
+                        *reinterpret_cast<float4*>(orow + 4 * j4) =
+                            make_float4(__fadd_rn(q4.x, v[4 * j4]), __fadd_rn(q4.y, v[4 * j4 + 1]),
+                                        __fadd_rn(q4.z, v[4 * j4 + 2]), __fadd_rn(q4.w, v[4 * j4 + 3]));
                     }
                 }
             }
@@ -492,30 +525,19 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
             for (int c0 = 0; c0 < DVS; c0 += 32) {
                 tmem_ld32(taddr_of(acc6, warp, c0), v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float hn = __fadd_rn(__fmul_rn(GL, Hreg[c0 + j]), v[j]);
-                    Hreg[c0 + j] = hn;
-                    __nv_bfloat16 hi, lo;
-                    split_bf16(hn, hi, lo);
-                    *reinterpret_cast<__nv_bfloat16*>(sm + L::Hhi + cm_off(c0 + j, d, D)) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(sm + L::Hlo + cm_off(c0 + j, d, D)) = lo;
-                }
+                for (int j = 0; j < 32; ++j) Hreg[c0 + j] = __fadd_rn(__fmul_rn(GL, Hreg[c0 + j]), v[j]);
             }
-            if (cstate && last && nrows == C) {
-#pragma unroll
-                for (int j = 0; j < DVS; ++j) cstate[d * D + j0 + j] = Hreg[j];
-            }
+            put_h();
+            if (cstate && last && nrows == C) put_state(cstate);
         }
         fence_async_smem();
         tc_sync();
     }
-    if (!failed && a.final_state) {
-#pragma unroll
-        for (int j = 0; j < DVS; ++j) a.final_state[(sh * D + d) * D + j0 + j] = Hreg[j];
-    }
+    if (!failed && a.final_state) put_state(a.final_state + sh * D * D);
     if (failed) {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
-        if (pending) mbar_wait(bar_ld, ph_ld, a.err);
+        if (pendA) mbar_wait(bar_ldA, ph_ldA, a.err);
+        if (pendB) mbar_wait(bar_ldB, ph_ldB, a.err);
         if (mma_out) mbar_wait(bar_mma, ph_mma, a.err);
     }
     tc_sync();
