@@ -172,6 +172,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
                  :: "r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(mbar)) : "memory");
 }
 
+// ---- 16-byte asynchronous copies (global -> shared), zero-filled when !valid ----------
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(smem_u32(dst_smem)), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- TMEM -> registers ---------------------------------------------------------------
 // 32 consecutive columns of this warp's lane quarter: thread i gets lane (32w + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

@@ -27,7 +27,8 @@ struct DecSmem {
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
                          fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
                          fRow2 = 1088, fEnd = 1216;
-    static constexpr size_t Bar = F + fEnd * 4;
+    static constexpr size_t Stage = 153600;          // 64 KB fp32: H, later the cached Delta rows
+    static constexpr size_t Bar = Stage + 65536;
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -59,7 +60,9 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
           *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs, *row1 = F + S::fRow,
           *row2 = F + S::fRow2;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* bar_ld = mbar + 1;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 2);
+    float* stage = reinterpret_cast<float*>(sm + S::Stage);
     __shared__ int ok_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -96,34 +99,24 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     if (warp == 0) tmem_alloc(tbase, 256);
     if (tid == 0) {
         mbar_init(mbar, 1);
+        mbar_init(bar_ld, 1);
         mbar_init_fence();
+        mbar_expect_tx(bar_ld, 65536);  // the chunk-start state, one contiguous 64 KB block
+        bulk_g2s(stage, Hst, 65536, bar_ld);
     }
-    // H rows -> per-split MN-major hi/lo tiles (row d = tid)
-    {
-        const int d = tid;
-#pragma unroll 4
-        for (int j8 = 0; j8 < D / 8; ++j8) {
-            const float4 x0 = *reinterpret_cast<const float4*>(Hst + (size_t)d * D + j8 * 8);
-            const float4 x1 = *reinterpret_cast<const float4*>(Hst + (size_t)d * D + j8 * 8 + 4);
-            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
-            const size_t tile = (size_t)sp * DVS * 128 * 2;
-            store8_split(sm + S::Hhi + tile, sm + S::Hlo + tile, mn_off(jl, d, DVS), x);
-        }
-    }
-    // [K; Q] (R1, K-major): rows s <= p of K, row 64 + p = q_p; K and V as MN-major tiles
+    // [K; Q] (R1, K-major): rows s <= p of K, row 64 + p = q_p; K and V as MN-major
+    // tiles; every other row zero-filled by the copies themselves
     for (int i = tid; i < 128 * (D / 8); i += 128) {
         const int r = i / (D / 8), d8 = i % (D / 8);
-        uint4 x = make_uint4(0u, 0u, 0u, 0u), y = make_uint4(0u, 0u, 0u, 0u);
-        if (r < 64 && r <= p) {
-            x = *reinterpret_cast<const uint4*>((r < p ? ck + (size_t)r * D : kt) + d8 * 8);
-            y = *reinterpret_cast<const uint4*>((r < p ? cv + (size_t)r * D : vt) + d8 * 8);
-        }
-        if (r == 64 + p) x = *reinterpret_cast<const uint4*>(qt + d8 * 8);
-        *reinterpret_cast<uint4*>(R1 + cm_off(r, d8 * 8, D)) = x;
         if (r < 64) {
-            *reinterpret_cast<uint4*>(sm + S::Kmn + mn_off(d8 * 8, r, D)) = x;
-            *reinterpret_cast<uint4*>(R1 + 32768 + mn_off(d8 * 8, r, D)) = y;
+            const bool in = r <= p;
+            const __nv_bfloat16* ks = (r < p ? ck + (size_t)r * D : kt) + d8 * 8;
+            const __nv_bfloat16* vs = (r < p ? cv + (size_t)r * D : vt) + d8 * 8;
+            cp_async16(R1 + cm_off(r, d8 * 8, D), ks, in);
+            cp_async16(sm + S::Kmn + mn_off(d8 * 8, r, D), ks, in);
+            cp_async16(R1 + 32768 + mn_off(d8 * 8, r, D), vs, in);
+        } else {
+            cp_async16(R1 + cm_off(r, d8 * 8, D), qt + d8 * 8, r == 64 + p);
         }
     }
     if (tid < p) {
@@ -138,11 +131,14 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     float tcol[C];
 #pragma unroll
     for (int s = 0; s < C; ++s) tcol[s] = (tid < C && s < p) ? ct[s * C + tid] : 0.f;
+    cp_async_wait_all();
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
     uint32_t phase = 0;
     bool ok = true;
+    bool ld_pending = true;   // the state copy is in flight from the start
+    uint32_t ld_phase = 0;
     auto mma_wait = [&]() {
         const bool w = mbar_wait(mbar, phase, a.err);
         fence_after();
@@ -237,6 +233,33 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         const int d8 = tid - 16;
         *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, d8 * 8, D)) = *reinterpret_cast<const uint4*>(qt + d8 * 8);
     }
+    {
+        // the staged chunk-start state -> per-split MN-major hi/lo tiles (row d = tid)
+        const bool okh = mbar_wait(bar_ld, 0, a.err);
+        if (__syncthreads_or(!okh)) goto cleanup;
+        ld_pending = false;
+        ld_phase = 1;
+        const int d = tid;
+#pragma unroll 4
+        for (int jj = 0; jj < D / 8; ++jj) {
+            const int j8 = (jj + d) & (D / 8 - 1);  // staggered columns: no bank conflicts
+            const float4 x0 = *reinterpret_cast<const float4*>(stage + d * D + j8 * 8);
+            const float4 x1 = *reinterpret_cast<const float4*>(stage + d * D + j8 * 8 + 4);
+            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+            const size_t tile = (size_t)sp * DVS * 128 * 2;
+            store8_split(sm + S::Hhi + tile, sm + S::Hlo + tile, mn_off(jl, d, DVS), x);
+        }
+    }
+    __syncthreads();
+    if (p > 0) {  // the cached Delta rows of this chunk -> the staging area (during the A4 MMA)
+        ld_pending = true;
+        if (tid == 0) {
+            fence_async_smem();
+            mbar_expect_tx(bar_ld, (uint32_t)p * D * 4);
+            bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_ld);
+        }
+    }
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
@@ -274,15 +297,21 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     }
     // P tiles (R1 + 0: hi, + 8 KB: lo; zero except row p); Delta (MN-major per split)
     for (int i = tid; i < 1024; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (p > 0) {
+        const bool okd = mbar_wait(bar_ld, 1, a.err);
+        if (__syncthreads_or(!okd)) goto cleanup;
+        ld_pending = false;
+    }
     __syncthreads();
     if (tid < C) {
         const int s = tid;
 #pragma unroll 4
-        for (int j8 = 0; j8 < D / 8; ++j8) {
+        for (int jj = 0; jj < D / 8; ++jj) {
+            const int j8 = (jj + s) & (D / 8 - 1);
             float x[8];
             if (s < p) {
-                const float4 x0 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8);
-                const float4 x1 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8 + 4);
+                const float4 x0 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8);
+                const float4 x1 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8 + 4);
                 x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
                 x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
             } else {
@@ -347,11 +376,12 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
             const int s = tid;
             const float ds = decs[s];
 #pragma unroll 4
-            for (int j8 = 0; j8 < D / 8; ++j8) {
+            for (int jj = 0; jj < D / 8; ++jj) {
+                const int j8 = (jj + s) & (D / 8 - 1);
                 float x[8];
                 if (s < p) {
-                    const float4 x0 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8);
-                    const float4 x1 = *reinterpret_cast<const float4*>(cd + (size_t)s * D + j8 * 8 + 4);
+                    const float4 x0 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8);
+                    const float4 x1 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8 + 4);
                     x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
                     x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
                 } else {
@@ -406,6 +436,7 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         }
     }
 cleanup:
+    if (ld_pending) mbar_wait(bar_ld, ld_phase, a.err);  // bounded: let the copy land
     tc_sync();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }

@@ -128,22 +128,22 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
         mbar_init(mbar, 1);
         mbar_init_fence();
     }
-    // [K; Q] rows (K-major), K and V token rows into MN-major tiles
-    for (int i = tid; i < 128 * (D / 8); i += 128) {
-        const int r = i / (D / 8), d8 = i % (D / 8);
-        const int tr = r & 63;
-        const size_t src = ((size_t)(t0 + tr) * H + h) * D + d8 * 8;
-        const uint4 x = ld16_or_zero((r < 64 ? a.k : a.q) + src, tr < nrows);
-        *reinterpret_cast<uint4*>(tKQ + cm_off(r, d8 * 8, D)) = x;
-        if (r < 64) {
-            *reinterpret_cast<uint4*>(tKmn + mn_off(d8 * 8, tr, D)) = x;
-            *reinterpret_cast<uint4*>(tVmn + mn_off(d8 * 8, tr, D)) = ld16_or_zero(a.v + src, tr < nrows);
-        }
+    // [K; Q] rows (K-major), K and V token rows into MN-major tiles: all copies
+    // in flight at once, rows past the chunk's end zero-filled
+    for (int i = tid; i < 64 * (D / 8); i += 128) {
+        const int tr = i / (D / 8), d8 = i % (D / 8);
+        const bool in = tr < nrows;
+        const size_t src = in ? ((size_t)(t0 + tr) * H + h) * D + d8 * 8 : 0;
+        cp_async16(tKQ + cm_off(tr, d8 * 8, D), a.k + src, in);
+        cp_async16(tKQ + cm_off(64 + tr, d8 * 8, D), a.q + src, in);
+        cp_async16(tKmn + mn_off(d8 * 8, tr, D), a.k + src, in);
+        cp_async16(tVmn + mn_off(d8 * 8, tr, D), a.v + src, in);
     }
     if (tid < C) {
         gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
         bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     }
+    cp_async_wait_all();
     __syncthreads();
     if (tid == 0) {  // gate prefix: serial fp32 sum in token order
         float acc = 0.f;
@@ -305,8 +305,8 @@ struct StateSmem {
     static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
     static constexpr size_t Bar = Dec + 256;                 // 3 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
-    static constexpr uint32_t LoadA = 32768 + 16384;
-    static constexpr uint32_t LoadB = 16384 + 8192 + 8192 + 64 * DVS * 4 + 256;
+    static constexpr uint32_t LoadA = 32768 + 16384 + 256;               // A4 tiles + gam
+    static constexpr uint32_t LoadB = 16384 + 8192 + 8192 + 64 * DVS * 4;  // K, P, U
 };
 
 template <int DVS>
@@ -379,12 +379,14 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     uint32_t ph_mma = 0, ph_ldA = 0, ph_ldB = 0;
     bool pendA = false, pendB = false, failed = false, mma_out = false;
 
-    auto blk_of = [&](int n) { return a.ws + ((size_t)(a.chunk_off[b] + n) * H + h) * kBlock; };
+    const int coff = a.chunk_off[b];
+    auto blk_of = [&](int n) { return a.ws + ((size_t)(coff + n) * H + h) * kBlock; };
     auto issue_A = [&](int n) {
         const unsigned char* blk = blk_of(n);
         mbar_expect_tx(bar_ldA, L::LoadA);
         bulk_g2s(sm + L::A4hi, blk + kOffA4hi, 32768, bar_ldA);
         bulk_g2s(sm + L::A4lo, blk + kOffA4lo, 16384, bar_ldA);
+        bulk_g2s(sm + L::Gam, blk + kOffGam, 256, bar_ldA);
     };
     auto issue_B = [&](int n) {
         const unsigned char* blk = blk_of(n);
@@ -393,7 +395,6 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         bulk_g2s(sm + L::Phi, blk + kOffPhi, 8192, bar_ldB);
         bulk_g2s(sm + L::Plo, blk + kOffPlo, 8192, bar_ldB);
         bulk_g2s(sm + L::U, blk + kOffU + (size_t)sp * 64 * DVS * 4, 64 * DVS * 4, bar_ldB);
-        bulk_g2s(sm + L::Gam, blk + kOffGam, 256, bar_ldB);
     };
     if (nch > 0) {
         if (tid == 0) {
@@ -408,16 +409,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         const int nrows = min(C, T - n * C);
         const int Lr = nrows - 1;
         const bool last = (n == nch - 1);
-        bool ok = mbar_wait(bar_ldB, ph_ldB, a.err);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_ldB ^= 1u;
-        pendB = false;
-        if (tid < C) {
-            Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
-            dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
-        }
-        const float GL = simt::gate(gam[Lr]);
-        ok = mbar_wait(bar_ldA, ph_ldA, a.err);
+        bool ok = mbar_wait(bar_ldA, ph_ldA, a.err);
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_ldA ^= 1u;
         pendA = false;
@@ -428,6 +420,15 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
             mma_commit(bar_mma);
         }
         mma_out = true;
+        if (tid < C) {
+            Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
+            dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
+        }
+        const float GL = simt::gate(gam[Lr]);
+        ok = mbar_wait(bar_ldB, ph_ldB, a.err);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_ldB ^= 1u;
+        pendB = false;
         ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
