@@ -64,12 +64,17 @@ def peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_max_mhz=2070.0, source="fallback")
 
 
+N_SEQ_OVERRIDE = None   # --n-seq: first n sequences only (small cases for profiler captures)
+
+
 def workload_lens(name):
     w = WORKLOADS[name]
     if w["lens"] is not None:
-        return list(w["lens"])
-    from infer_consistent_linear_gb300.synth import varlen_lengths
-    return varlen_lengths(48, 128, 8192, seed=0)
+        lens = list(w["lens"])
+    else:
+        from infer_consistent_linear_gb300.synth import varlen_lengths
+        lens = varlen_lengths(48, 128, 8192, seed=0)
+    return lens[:N_SEQ_OVERRIDE] if N_SEQ_OVERRIDE else lens
 
 
 # ---------------------------------------------------------------- clocks
@@ -423,9 +428,10 @@ def kernel_src_sha():
     import hashlib
     csrc = os.path.join(ROOT, "infer_consistent_linear_gb300", "csrc")
     h = hashlib.sha256()
-    for s in ("common.cuh", "simt_fwd.cuh", "simt_bwd.cuh"):
-        with open(os.path.join(csrc, s), "rb") as f:
-            h.update(f.read())
+    for s in sorted(os.listdir(csrc)):
+        if s.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, s), "rb") as f:
+                h.update(s.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -613,7 +619,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--policy", choices=["tc", "simt"], default="tc",
                     help="operand policy of the contract (tc: tcgen05 tensor cores; simt: fp32 CUDA cores)")
+    ap.add_argument("--n-seq", type=int, default=None,
+                    help="run only the first n sequences of the workload (a smaller case for "
+                         "profiler captures; the line then does not describe the named workload)")
     args = ap.parse_args()
+    global N_SEQ_OVERRIDE
+    N_SEQ_OVERRIDE = args.n_seq
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
@@ -644,7 +655,9 @@ def main():
             "ms_per_step": round(ms, 4), "higher_is_better": hib, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16x3 MMA, f32 accumulate" if args.policy == "tc" else "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOADS[name]["desc"], "l2": "working set > 129 MB L2, no flush",
+            "config": {"workload": WORKLOADS[name]["desc"] + (f" [first {args.n_seq} sequences only]"
+                                                               if args.n_seq else ""),
+                       "l2": "working set > 129 MB L2, no flush",
                        "contract": {k: v for k, v in step.c.as_dict().items()},
                        "parallelism": f"replicas x{world} (independent sequences per GPU)"},
             "clocks": ck, "e2e": e2e, "gpu_launches": int(sum(n for n, _ in prof.values())),

@@ -22,7 +22,7 @@ namespace tc {
 struct DecSmem {
     static constexpr size_t Hhi = 0, Hlo = 32768;   // per split: MN-major DVS (j) x 128 (d)
     static constexpr size_t Kmn = 65536;             // K, MN-major 128 (d) x 64 (token)
-    static constexpr size_t R1 = 81920;              // 64 KB, reused by phase
+    static constexpr size_t R1 = 81920;              // 64 KB right after Kmn, reused by phase
     static constexpr size_t F = R1 + 65536;          // fp32 scratch
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
                          fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
@@ -104,21 +104,20 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         mbar_expect_tx(bar_ld, 65536);  // the chunk-start state, one contiguous 64 KB block
         bulk_g2s(stage, Hst, 65536, bar_ld);
     }
-    // [K; Q] (R1, K-major): rows s <= p of K, row 64 + p = q_p; K and V as MN-major
-    // tiles; every other row zero-filled by the copies themselves
-    for (int i = tid; i < 128 * (D / 8); i += 128) {
+    // K and V rows s <= p as MN-major tiles (Kmn; R1 + 32 KB), later rows zero-filled
+    // by the copies themselves.  The K tile read K-major is the [K; Q] operand's
+    // first 64 rows (the two layouts are byte-identical); its rows 64.. are
+    // R1's first 16 KB, of which only row 64 + p = q_p is written: other rows of
+    // an A operand reach only accumulator rows this step never reads.
+    for (int i = tid; i < 64 * (D / 8); i += 128) {
         const int r = i / (D / 8), d8 = i % (D / 8);
-        if (r < 64) {
-            const bool in = r <= p;
-            const __nv_bfloat16* ks = (r < p ? ck + (size_t)r * D : kt) + d8 * 8;
-            const __nv_bfloat16* vs = (r < p ? cv + (size_t)r * D : vt) + d8 * 8;
-            cp_async16(R1 + cm_off(r, d8 * 8, D), ks, in);
-            cp_async16(sm + S::Kmn + mn_off(d8 * 8, r, D), ks, in);
-            cp_async16(R1 + 32768 + mn_off(d8 * 8, r, D), vs, in);
-        } else {
-            cp_async16(R1 + cm_off(r, d8 * 8, D), qt + d8 * 8, r == 64 + p);
-        }
+        const bool in = r <= p;
+        const __nv_bfloat16* ks = (r < p ? ck + (size_t)r * D : kt) + d8 * 8;
+        const __nv_bfloat16* vs = (r < p ? cv + (size_t)r * D : vt) + d8 * 8;
+        cp_async16(sm + S::Kmn + mn_off(d8 * 8, r, D), ks, in);
+        cp_async16(R1 + 32768 + mn_off(d8 * 8, r, D), vs, in);
     }
+    if (tid < D / 8) cp_async16(R1 + cm_off(p, tid * 8, D), qt + tid * 8, true);
     if (tid < p) {
         gams[tid] = cg[tid];
         bets[tid] = cb[tid];
@@ -146,7 +145,7 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         return !__syncthreads_or(!w);
     };
     if (tid == 0) {
-        mma_tile<128, 64, D>(tmem, R1, R1, false);
+        mma_tile<128, 64, D>(tmem, sm + S::Kmn, sm + S::Kmn, false);
         mma_commit(mbar);
     }
     if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid]);
@@ -172,9 +171,8 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         arow[s] = (s < p) ? simt::a_entry(bp, gp, gams[s], row1[s]) : 0.f;
         prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, gams[s]), __fmul_rn(a.scale, row2[s])) : 0.f;
     }
-    // X tiles (R1 + 0 .. 32 KB) and the T row: zero the tiles first
+    // X tiles (R1 + 0 .. 32 KB, row p only) and the T row
     __syncthreads();
-    for (int i = tid; i < 2048; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < C) {  // T row p: T_pj = -(sum_{s=j}^{p-1} a_ps T_sj), ascending s
         const int j = tid;
         float acc = 0.f;
@@ -222,7 +220,6 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         }
     }
     // A4 tiles (R1: hi at +0, lo at +32 KB): row p = W'_p, row 64 + p = q_p
-    for (int i = tid; i < 4096; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     if (tid < 16) {
         float x[8];
@@ -232,6 +229,8 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     } else if (tid < 32) {
         const int d8 = tid - 16;
         *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, d8 * 8, D)) = *reinterpret_cast<const uint4*>(qt + d8 * 8);
+    } else if (tid < 48) {  // q_p has no lo part: that row of the lo tile is zero, as in the prefill
+        *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(64 + p, (tid - 32) * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
     }
     {
         // the staged chunk-start state -> per-split MN-major hi/lo tiles (row d = tid)
@@ -295,8 +294,7 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         Dp[j] = __fsub_rn(Up[j], row1[j]);
         Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
     }
-    // P tiles (R1 + 0: hi, + 8 KB: lo; zero except row p); Delta (MN-major per split)
-    for (int i = tid; i < 1024; i += 128) reinterpret_cast<uint4*>(R1)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // P tiles (R1 + 0: hi, + 8 KB: lo; row p); Delta (MN-major per split, rows > p zero)
     if (p > 0) {
         const bool okd = mbar_wait(bar_ld, 1, a.err);
         if (__syncthreads_or(!okd)) goto cleanup;

@@ -37,7 +37,7 @@ constexpr size_t kOffA4lo = 32768;    // 64 x 128 bf16 K-major: W'_lo
 constexpr size_t kOffKmn = 49152;     // K as an MN-major 128 (d) x 64 (token) tile
 constexpr size_t kOffPhi = 65536;     // 64 x 64 bf16 K-major
 constexpr size_t kOffPlo = 73728;     // 64 x 64 bf16 K-major
-constexpr size_t kOffU = 81920;       // 64 x 128 fp32, stored [split][64][DVS]
+constexpr size_t kOffU = 81920;       // 64 x 128 fp32, [split][DVS/4][64 rows] float4 groups
 constexpr size_t kOffGam = 114688;    // 64 fp32
 constexpr size_t kBlock = 114944;
 
@@ -94,14 +94,16 @@ __device__ __forceinline__ void t_solve_column(const float* At, float* Tout, int
 }
 
 // ---- prep: everything of a chunk that does not depend on H ------------------------
-constexpr size_t kPrepOffKmn = 32768, kPrepOffVmn = 49152, kPrepOffAt = 65536,
-                 kPrepOffT = 65536 + 16384, kPrepOffVec = kPrepOffT + 64 * 65 * 4;
+// [K; Q] K-major (32 KB; the K rows double as the MN-major d x token K tile, the
+// two layouts being byte-identical), V MN-major, A^T, T, gate vectors.
+constexpr size_t kPrepOffVmn = 32768, kPrepOffAt = 49152, kPrepOffT = 49152 + 16384,
+                 kPrepOffVec = kPrepOffT + 64 * 65 * 4;
 constexpr size_t kPrepSmem = kPrepOffVec + 3 * 64 * 4 + 64;
 
 static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; later the X tiles
-    unsigned char* tKmn = sm + kPrepOffKmn;        // K, MN-major 128 (d) x 64 (token)
+    unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later X1
+    unsigned char* tKmn = sm;                      // the K rows read as an MN-major 128 (d) x 64 tile
     unsigned char* tVmn = sm + kPrepOffVmn;        // V, MN-major
     float* At = reinterpret_cast<float*>(sm + kPrepOffAt);   // [64][64], At[s][r] = a_rs
     float* Tfp = reinterpret_cast<float*>(sm + kPrepOffT);   // [64][65]
@@ -128,15 +130,14 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
         mbar_init(mbar, 1);
         mbar_init_fence();
     }
-    // [K; Q] rows (K-major), K and V token rows into MN-major tiles: all copies
-    // in flight at once, rows past the chunk's end zero-filled
+    // [K; Q] rows (K-major) and V token rows (MN-major): all copies in flight at
+    // once, rows past the chunk's end zero-filled
     for (int i = tid; i < 64 * (D / 8); i += 128) {
         const int tr = i / (D / 8), d8 = i % (D / 8);
         const bool in = tr < nrows;
         const size_t src = in ? ((size_t)(t0 + tr) * H + h) * D + d8 * 8 : 0;
         cp_async16(tKQ + cm_off(tr, d8 * 8, D), a.k + src, in);
         cp_async16(tKQ + cm_off(64 + tr, d8 * 8, D), a.q + src, in);
-        cp_async16(tKmn + mn_off(d8 * 8, tr, D), a.k + src, in);
         cp_async16(tVmn + mn_off(d8 * 8, tr, D), a.v + src, in);
     }
     if (tid < C) {
@@ -204,9 +205,10 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     if (tid < C) t_solve_column(At, Tfp, 65, tid, nrows);
     __syncthreads();
     {
-        // X1 = T diag(b G) (threads 0..63), X2 = T diag(b) (threads 64..127), split
+        // X1 = T diag(b G) (threads 0..63, into the Q rows' space), X2 = T diag(b)
+        // (threads 64..127, into the A^T space), split
         const int r = tid & 63, which = tid >> 6;
-        unsigned char* xhi = tKQ + which * 16384;
+        unsigned char* xhi = which ? reinterpret_cast<unsigned char*>(At) : tKQ + 16384;
         unsigned char* xlo = xhi + 8192;
         const float* sc = which ? bet : bg;
         for (int s8 = 0; s8 < C / 8; ++s8) {
@@ -238,10 +240,11 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        mma_tile_mj<64, D, C, false, true>(tmem, tKQ, tKmn, false);                // W' = X1_hi K
-        mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 8192, tKmn, true);          //    + X1_lo K
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, tKQ + 16384, tVmn, false);  // U  = X2_hi V
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, tKQ + 24576, tVmn, true);   //    + X2_lo V
+        unsigned char* x2 = reinterpret_cast<unsigned char*>(At);
+        mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 16384, tKmn, false);        // W' = X1_hi K
+        mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 24576, tKmn, true);         //    + X1_lo K
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, x2, tVmn, false);           // U  = X2_hi V
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, x2 + 8192, tVmn, true);     //    + X2_lo V
         mma_commit(mbar);
     }
     outstanding = 1;
@@ -276,7 +279,7 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const int j = c0 + j4 * 4;
                     const int sp = j / dvs, jl = j % dvs;
-                    *reinterpret_cast<float4*>(U + ((size_t)sp * 64 + r) * dvs + jl) =
+                    *reinterpret_cast<float4*>(U + (((size_t)sp * (dvs / 4) + jl / 4) * 64 + r) * 4) =
                         make_float4(v[j4 * 4], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
                 }
             }
@@ -293,14 +296,14 @@ done:
 template <int DVS>
 struct StateSmem {
     static constexpr size_t A4hi = 0, A4lo = 32768, Kmn = 65536, Phi = 81920, Plo = 90112;
-    static constexpr size_t U = 98304;                       // 64 x DVS fp32
+    static constexpr size_t U = 98304;                       // 64 x DVS fp32, [DVS/4][64] float4
     static constexpr size_t Hhi = U + 64 * DVS * 4;          // H as MN-major DVS (j) x 128 (d)
     static constexpr size_t Hlo = Hhi + DVS * 128 * 2;
     static constexpr size_t Dhi = Hlo + DVS * 128 * 2;       // Delta, MN-major DVS (j) x 64 (token)
     static constexpr size_t Dlo = Dhi + DVS * 64 * 2;
     static constexpr size_t Bhi = Dlo + DVS * 64 * 2;        // decay * Delta, same layout
     static constexpr size_t Blo = Bhi + DVS * 64 * 2;
-    static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32
+    static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32, [DVS/4][64] float4
     static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 (bulk copied)
     static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
     static constexpr size_t Bar = Dec + 256;                 // 3 mbarriers + TMEM base
@@ -455,10 +458,12 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
 #pragma unroll
                     for (int j8 = 0; j8 < 4; ++j8) {
                         float x[8], y[8];
+                        const float4 u0 = reinterpret_cast<const float4*>(sU)[((c0 + j8 * 8) / 4) * 64 + r];
+                        const float4 u1 = reinterpret_cast<const float4*>(sU)[((c0 + j8 * 8) / 4 + 1) * 64 + r];
+                        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            const int jj = c0 + j8 * 8 + e;
-                            x[e] = in ? __fsub_rn(sU[r * DVS + jj], v[j8 * 8 + e]) : 0.f;
+                            x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
                             y[e] = __fmul_rn(dr, x[e]);
                         }
                         store8_split(sm + L::Dhi, sm + L::Dlo, mn_off(c0 + j8 * 8, r, DVS), x);
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
                     const float gr = Gm[rr];
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4)
-                        *reinterpret_cast<float4*>(sQ + rr * DVS + c0 + 4 * j4) =
+                        reinterpret_cast<float4*>(sQ)[(c0 / 4 + j4) * 64 + rr] =
                             make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
                                         __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
                                         __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
                     float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + c0;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(sQ + r * DVS + c0 + 4 * j4);
+                        const float4 q4 = reinterpret_cast<const float4*>(sQ)[(c0 / 4 + j4) * 64 + r];
                         *reinterpret_cast<float4*>(orow + 4 * j4) =
                             make_float4(__fadd_rn(q4.x, v[4 * j4]), __fadd_rn(q4.y, v[4 * j4 + 1]),
                                         __fadd_rn(q4.z, v[4 * j4 + 2]), __fadd_rn(q4.w, v[4 * j4 + 3]));
