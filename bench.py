@@ -181,6 +181,10 @@ def tc_kernel_flops_per_chunk(name, d, Cc=C):
         return 2 * 4 * Cc * Cc * d
     if name == "cpr_tc_state":
         return 2 * (3 * Cc * d * d + Cc * Cc * d)
+    if name == "cpr_tc_state_bwd":   # P^T dO, T^T dDelta (C^2 d); K dH', Q^T dO, K^T dR (C d^2)
+        return 2 * (2 * Cc * Cc * d + 3 * Cc * d * d)
+    if name == "cpr_tc_grad":        # [Q;K]K^T, [dO;dR]Delta^T, G1 K, G1^T Q, M2 K; [dO;dR]H^T, Delta dH'^T
+        return 2 * (7 * Cc * Cc * d + 3 * Cc * d * d)
     return None
 
 

@@ -139,8 +139,8 @@ WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int 
     size_t off = 0;
     auto add = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
     add(w.chunk_off, sizeof(int32_t) * (n_seq + 1));
-    if (op == CPR_OP_FWD && c.operand_policy == CPR_POLICY_TC_BF16X3) {
-        add(w.W, ch * cpr::tc::kBlock);  // per (chunk, head) operand blocks
+    if (c.operand_policy == CPR_POLICY_TC_BF16X3) {  // per (chunk, head) operand blocks
+        add(w.W, ch * (op == CPR_OP_BWD ? cpr::tc::kBlockTrain : cpr::tc::kBlock));
         w.total = off;
         return w;
     }
@@ -268,7 +268,8 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
         t.q = static_cast<const __nv_bfloat16*>(q); t.k = static_cast<const __nv_bfloat16*>(k);
         t.v = static_cast<const __nv_bfloat16*>(v); t.g = g; t.beta = beta; t.cu = cu;
         t.chunk_off = sa.chunk_off; t.n_seq = n_seq; t.H = H; t.dvs = (int)(c->d_v / c->dv_splits);
-        t.scale = c->scale; t.ws = wsb + w.W; t.h0 = h0; t.o = static_cast<float*>(o);
+        t.scale = c->scale; t.ws = wsb + w.W; t.blk_bytes = cpr::tc::kBlock; t.train = false;
+        t.h0 = h0; t.o = static_cast<float*>(o);
         t.final_state = final_state; t.cache = static_cast<uint8_t*>(cache); t.co = to_off(cl);
         t.err = err;
         e = cpr::tc_forward(t, w.cmax, n_seq, H, st);
@@ -459,6 +460,23 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
     sa.chunk_off = reinterpret_cast<int32_t*>(wsb + w.chunk_off); sa.err = err;
     cudaError_t e = launch_setup(sa, st);
     if (e != cudaSuccess) return cuda_fail(e, "setup launch");
+
+    if (c->operand_policy == CPR_POLICY_TC_BF16X3) {
+        cpr::tc::TcArgs t{};
+        t.q = static_cast<const __nv_bfloat16*>(q); t.k = static_cast<const __nv_bfloat16*>(k);
+        t.v = static_cast<const __nv_bfloat16*>(v); t.g = g; t.beta = beta; t.cu = cu_seqlens;
+        t.chunk_off = sa.chunk_off; t.n_seq = n_seq; t.H = H; t.dvs = (int)(c->d_v / c->dv_splits);
+        t.scale = c->scale; t.ws = wsb + w.W; t.blk_bytes = cpr::tc::kBlockTrain; t.train = true;
+        t.h0 = h0; t.o = nullptr; t.final_state = nullptr; t.cache = nullptr; t.err = err;
+        cpr::tc::TcBwdArgs tb{};
+        tb.q = t.q; tb.k = t.k; tb.v = t.v; tb.g = g; tb.beta = beta; tb.cu = cu_seqlens;
+        tb.chunk_off = sa.chunk_off; tb.n_seq = n_seq; tb.H = H; tb.scale = c->scale; tb.ws = t.ws;
+        tb.dO = dO; tb.dHT = dHT; tb.dq = static_cast<float*>(dq); tb.dk = static_cast<float*>(dk);
+        tb.dv = static_cast<float*>(dv); tb.dg = dg; tb.dbeta = dbeta; tb.dh0 = dh0; tb.err = err;
+        e = cpr::tc_backward(t, tb, w.cmax, n_seq, H, st);
+        if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+        return CPR_OK;
+    }
 
     cpr::simt::FwdArgs fa{};
     fa.q = q; fa.k = k; fa.v = v; fa.g = g; fa.beta = beta; fa.cu = cu_seqlens;

@@ -1,0 +1,768 @@
+// CPR Gated DeltaNet backward on the tensor cores (operand policy TC_BF16X3).
+//
+// The backward of the forward chunk form (derived here; the pages give the
+// trainer forward+backward stage only as a timing, page "IsoExec: 切换 SkyRL
+// 中的训练器-推理不匹配", section "Chunkwise-Parallel Recurrent (CPR) Gated
+// DeltaNet", stage table).  Per chunk, with start state H, dH' = dL/dH_{n+1},
+// E_rs = exp(gam_r - gam_s), dec_s = E_Ls, bg_s = b_s G_s, R = diag(b)(V - diag(G) K H)
+// (so that Delta = T R):
+//   dDelta = P^T dO + diag(dec) (K dH')
+//   dR     = T^T dDelta
+//   dH     = G_L dH' + Q^T diag(G scale) dO - K^T diag(bg) dR        (previous chunk's dH')
+//   dP_rs  =  dO_r . Delta_s  (s <= r),   dA_rs = -dR_r . Delta_s  (s < r)
+//   dq     = scale (diag(G) dO H^T + (E . dP) K)
+//   dk     = -diag(bg) dR H^T + diag(dec) Delta dH'^T + (E . dP)^T Q^ + (G2 + G2^T) K,
+//            G2_rs = b_r E_rs dA_rs
+//   dv     = diag(b) dR
+//   db_r   = dR_r . v_r - G_r k_r . (dR H^T)_r + sum_{s<r} dA_rs E_rs kk_rs
+//   dgam_r = G_r (q^_r . (dO H^T)_r - b_r k_r . (dR H^T)_r) + rowE_r - colE_r - e_r
+//            (+ G_L <dH', H> + sum_{s<L} e_s at r = L),
+//            e_s = dec_s k_s . (Delta dH'^T)_s,  t_rs = dP_rs P_rs + b_r dA_rs E_rs kk_rs,
+//            rowE_r = sum_{s<r} t_rs,  colE_s = sum_{r>s} t_rs
+//   dg_s   = sum_{r=s}^{L} dgam_r
+// Kernels: k_tc_state_bwd (one CTA per (sequence, head, d_v split), chunks in
+// reverse order: the dH chain; stores dH' and dR per chunk) and k_tc_grad (one
+// CTA per chunk and head, all d_v columns: every per-token gradient).  The
+// training forward (k_tc_prep, k_tc_state with `train`) leaves T, H_n and Delta
+// in each chunk's workspace block; every fp32 x fp32 product is three bf16 MMA
+// passes (hi hi, hi lo, lo hi), fp32 x exact-bf16 two.  No bitwise coupling to
+// another path: deterministic (fixed orders, no atomics) and batch-invariant
+// (one CTA per chunk or per sequence).
+#pragma once
+
+#include "tc_fwd.cuh"
+
+namespace cpr {
+namespace tc {
+
+struct TcBwdArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    const int32_t* chunk_off;
+    int n_seq;
+    int H;
+    float scale;
+    unsigned char* ws;    // kBlockTrain blocks from the training forward
+    const float* dO;
+    const float* dHT;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dg;
+    float* dbeta;
+    float* dh0;
+    uint32_t* err;
+};
+
+// ---- reverse state pass ---------------------------------------------------------------
+template <int DVS>
+struct SbSmem {
+    static constexpr size_t Phi = 0, Plo = 8192;             // P, K-major (r, s); read as P^T
+    static constexpr size_t Thi = 16384, Tlo = 24576;        // T, K-major (r, j); read as T^T
+    static constexpr size_t KQ0 = 32768, KQ1 = 65536;        // [K | Q] K-major, two buffers
+    static constexpr size_t dHhi = 98304;                    // dH', MN-major (j, d)
+    static constexpr size_t dHlo = dHhi + DVS * 128 * 2;
+    static constexpr size_t B1hi = dHlo + DVS * 128 * 2;     // dO, then dDelta: MN-major (j, t)
+    static constexpr size_t B1lo = B1hi + DVS * 64 * 2;
+    static constexpr size_t B2hi = B1lo + DVS * 64 * 2;      // G scale dO, then -bg dR
+    static constexpr size_t B2lo = B2hi + DVS * 64 * 2;
+    static constexpr size_t Stage = B2lo + DVS * 64 * 2;     // dO rows fp32, [DVS/4][64] float4
+    static constexpr size_t Vec = Stage + 64 * DVS * 4;      // gam, Gm, dec, bg (64 fp32 each)
+    static constexpr size_t Bar = Vec + 4 * 256;             // 5 mbarriers + TMEM base
+    static constexpr size_t Total = Bar + 64;
+};
+
+template <int DVS>
+__global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
+    using L = SbSmem<DVS>;
+    constexpr int NSPLIT = D / DVS;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    float* gam = reinterpret_cast<float*>(sm + L::Vec);
+    float* Gm = gam + 64;
+    float* dec = Gm + 64;
+    float* bgv = dec + 64;
+    uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);
+    uint64_t* bar_P = bar_mma + 1;
+    uint64_t* bar_T = bar_mma + 2;
+    uint64_t* bar_KQ = bar_mma + 3;  // two
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 5);
+
+    const int total = a.chunk_off[a.n_seq];
+    if (total < 0) return;
+    const int H = a.H;
+    const int sp = blockIdx.x % NSPLIT;
+    const int h = (blockIdx.x / NSPLIT) % H;
+    const int b = blockIdx.x / (NSPLIT * H);
+    const int j0 = sp * DVS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
+    const int coff = a.chunk_off[b];
+    const int nch = a.chunk_off[b + 1] - coff;
+    const size_t sh = (size_t)b * H + h;
+    auto blk_of = [&](int n) { return a.ws + ((size_t)(coff + n) * H + h) * kBlockTrain; };
+
+    if (warp == 0) tmem_alloc(tbase, 256);
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(bar_mma + i, 1);
+        mbar_init_fence();
+    }
+    // dL/dH of the last chunk's end state, row d = tid, columns j0..j0+DVS
+    float dHreg[DVS];
+    const int d = tid;
+#pragma unroll
+    for (int j4 = 0; j4 < DVS / 4; ++j4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.dHT) x = *reinterpret_cast<const float4*>(a.dHT + (sh * D + d) * D + j0 + 4 * j4);
+        dHreg[4 * j4] = x.x; dHreg[4 * j4 + 1] = x.y; dHreg[4 * j4 + 2] = x.z; dHreg[4 * j4 + 3] = x.w;
+    }
+    // dH' as the B operand of K dH'; also chunk nn's dH' tiles for k_tc_grad
+    auto put_dh = [&](int nn) {
+        unsigned char* g = (nn >= 0) ? blk_of(nn) + kOffdH : nullptr;
+#pragma unroll
+        for (int j8 = 0; j8 < DVS / 8; ++j8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = dHreg[j8 * 8 + e];
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4*>(sm + L::dHhi + mn_off(j8 * 8, d, DVS)) = hi;
+            *reinterpret_cast<uint4*>(sm + L::dHlo + mn_off(j8 * 8, d, DVS)) = lo;
+            if (g) {
+                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + j8 * 8, D)) = hi;
+                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + j8 * 8, D)) = lo;
+            }
+        }
+    };
+    auto issue_P = [&](int n) {
+        const unsigned char* blk = blk_of(n);
+        mbar_expect_tx(bar_P, 16384 + 256);
+        bulk_g2s(sm + L::Phi, blk + kOffPhi, 16384, bar_P);
+        bulk_g2s(gam, blk + kOffGam, 256, bar_P);
+    };
+    auto issue_T = [&](int n) {
+        mbar_expect_tx(bar_T, 16384);
+        bulk_g2s(sm + L::Thi, blk_of(n) + kOffT, 16384, bar_T);
+    };
+    auto issue_KQ = [&](int n) {
+        const unsigned char* blk = blk_of(n);
+        unsigned char* dst = sm + ((n & 1) ? L::KQ1 : L::KQ0);
+        uint64_t* bar = bar_KQ + (n & 1);
+        mbar_expect_tx(bar, 32768);
+        bulk_g2s(dst, blk + kOffKmn, 16384, bar);
+        bulk_g2s(dst + 16384, blk + kOffA4hi + 16384, 16384, bar);
+    };
+    // dO rows of chunk n (columns j0..j0+DVS) into the staging area, zero past the end
+    auto issue_dO = [&](int n) {
+        const int t0 = seq0 + n * C, nrows = min(C, T - n * C);
+        for (int i = tid; i < 64 * (DVS / 4); i += 128) {
+            const int r = i / (DVS / 4), q4 = i % (DVS / 4);  // a row's 16-byte pieces side by side
+            const bool in = r < nrows;
+            const float* src = a.dO + (in ? ((size_t)(t0 + r) * H + h) * D + j0 + 4 * q4 : 0);
+            cp_async16(sm + L::Stage + ((size_t)q4 * 64 + r) * 16, src, in);
+        }
+    };
+    auto beta_of = [&](int n) {
+        const int t0 = seq0 + n * C, nrows = min(C, T - n * C);
+        return (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    };
+
+    put_dh(nch - 1);
+    float bcur = 0.f;
+    if (nch > 0) {
+        if (tid == 0) {
+            issue_P(nch - 1);
+            issue_T(nch - 1);
+            issue_KQ(nch - 1);
+            if (nch > 1) issue_KQ(nch - 2);
+        }
+        issue_dO(nch - 1);
+        bcur = beta_of(nch - 1);
+    }
+    fence_async_smem();
+    tc_sync();
+    const uint32_t tmem = *tbase;
+    const uint32_t tD1 = tmem, tD2 = tmem + DVS, tR = tmem + 2 * DVS, tH = tmem + 3 * DVS;
+    uint32_t ph_mma = 0, ph_P = 0, ph_T = 0, ph_KQ[2] = {0u, 0u};
+    bool pendP = nch > 0, pendT = nch > 0, pendKQ[2] = {nch > 0, nch > 1}, mma_out = false;
+    if (nch > 0 && ((nch - 1) & 1)) { pendKQ[0] = nch > 1; pendKQ[1] = true; }
+    bool failed = false;
+    const float scale = a.scale;
+    // M = 64 accumulator rows: lanes 0..15 of each warp
+    const int r64 = warp * 16 + lane;
+
+    for (int it = 0; it < nch; ++it) {
+        const int n = nch - 1 - it;
+        const int nrows = min(C, T - n * C);
+        const int Lr = nrows - 1;
+        const int cur = n & 1;
+        unsigned char* KQ = sm + (cur ? L::KQ1 : L::KQ0);
+        bool ok = mbar_wait(bar_P, ph_P, a.err);
+        cp_async_wait_all();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_P ^= 1u;
+        pendP = false;
+        if (tid < C) {
+            const bool in = tid < nrows;
+            const float gr = gam[tid];
+            Gm[tid] = in ? simt::gate(gr) : 0.f;
+            dec[tid] = in ? simt::decay(gam[Lr], gr) : 0.f;
+            bgv[tid] = in ? simt::bg_entry(bcur, gr) : 0.f;
+            // dO (B1) and G scale dO (B2) rows, MN-major (j, t)
+            const float gs = __fmul_rn(Gm[tid], scale);
+#pragma unroll
+            for (int j8 = 0; j8 < DVS / 8; ++j8) {
+                const float4 u0 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8) * 64 + tid];
+                const float4 u1 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8 + 1) * 64 + tid];
+                const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(gs, x[e]);
+                store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(j8 * 8, tid, DVS), x);
+                store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(j8 * 8, tid, DVS), y);
+            }
+        }
+        const float GL = simt::gate(gam[Lr]);
+        __syncthreads();  // the staging area is consumed
+        if (n > 0) {
+            issue_dO(n - 1);
+            bcur = beta_of(n - 1);
+        }
+        fence_async_smem();
+        ok = mbar_wait(bar_KQ + cur, ph_KQ[cur], a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_KQ[cur] ^= 1u;
+        pendKQ[cur] = false;
+        if (tid == 0) {
+            mma_tile_mj<64, DVS, C, true, true>(tD1, sm + L::Phi, sm + L::B1hi, false);   // P^T dO
+            mma_tile_mj<64, DVS, C, true, true>(tD1, sm + L::Phi, sm + L::B1lo, true);
+            mma_tile_mj<64, DVS, C, true, true>(tD1, sm + L::Plo, sm + L::B1hi, true);
+            mma_tile_mj<64, DVS, D, false, true>(tD2, KQ, sm + L::dHhi, false);            // K dH'
+            mma_tile_mj<64, DVS, D, false, true>(tD2, KQ, sm + L::dHlo, true);
+            mma_tile_mj<128, DVS, C, true, true>(tH, KQ + 16384, sm + L::B2hi, false);     // Q^T G scale dO
+            mma_tile_mj<128, DVS, C, true, true>(tH, KQ + 16384, sm + L::B2lo, true);
+            mma_commit(bar_mma);
+        }
+        mma_out = true;
+        ok = mbar_wait(bar_mma, ph_mma, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_mma ^= 1u;
+        mma_out = false;
+        if (tid == 0 && n > 0) {  // P and gam of chunk n are consumed
+            fence_async_smem();
+            issue_P(n - 1);
+        }
+        pendP = n > 0;
+        {
+            // dDelta = P^T dO + dec . (K dH') -> B1 (MN-major (j, t))
+            float v1[32], v2[32];
+#pragma unroll
+            for (int c0 = 0; c0 < DVS; c0 += 32) {
+                tmem_ld32(taddr_of(tD1, warp, c0), v1);
+                tmem_ld32(taddr_of(tD2, warp, c0), v2);
+                if (lane < 16) {
+                    const float dr = dec[r64];
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = __fmaf_rn(dr, v2[j8 * 8 + e], v1[j8 * 8 + e]);
+                        store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(c0 + j8 * 8, r64, DVS), x);
+                    }
+                }
+            }
+        }
+        fence_async_smem();
+        tc_sync();
+        ok = mbar_wait(bar_T, ph_T, a.err);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_T ^= 1u;
+        pendT = false;
+        if (tid == 0) {
+            mma_tile_mj<64, DVS, C, true, true>(tR, sm + L::Thi, sm + L::B1hi, false);    // T^T dDelta
+            mma_tile_mj<64, DVS, C, true, true>(tR, sm + L::Thi, sm + L::B1lo, true);
+            mma_tile_mj<64, DVS, C, true, true>(tR, sm + L::Tlo, sm + L::B1hi, true);
+            mma_commit(bar_mma);
+        }
+        mma_out = true;
+        ok = mbar_wait(bar_mma, ph_mma, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_mma ^= 1u;
+        mma_out = false;
+        if (tid == 0 && n > 0) {
+            fence_async_smem();
+            issue_T(n - 1);
+        }
+        pendT = n > 0;
+        {
+            // dR rows: to the workspace (K-major (r, j) hi/lo) and -bg . dR -> B2
+            unsigned char* gdr = blk_of(n) + kOffdR;
+            float v1[32];
+#pragma unroll
+            for (int c0 = 0; c0 < DVS; c0 += 32) {
+                tmem_ld32(taddr_of(tR, warp, c0), v1);
+                if (lane < 16) {
+                    const float nb = -bgv[r64];
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float x[8], y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            x[e] = v1[j8 * 8 + e];
+                            y[e] = __fmul_rn(nb, x[e]);
+                        }
+                        uint4 hi, lo;
+                        split8(x, hi, lo);
+                        *reinterpret_cast<uint4*>(gdr + cm_off(r64, j0 + c0 + j8 * 8, D)) = hi;
+                        *reinterpret_cast<uint4*>(gdr + 16384 + cm_off(r64, j0 + c0 + j8 * 8, D)) = lo;
+                        store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(c0 + j8 * 8, r64, DVS), y);
+                    }
+                }
+            }
+        }
+        fence_async_smem();
+        tc_sync();
+        if (tid == 0) {
+            mma_tile_mj<128, DVS, C, true, true>(tH, KQ, sm + L::B2hi, true);   // += K^T (-bg dR)
+            mma_tile_mj<128, DVS, C, true, true>(tH, KQ, sm + L::B2lo, true);
+            mma_commit(bar_mma);
+        }
+        mma_out = true;
+        ok = mbar_wait(bar_mma, ph_mma, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_mma ^= 1u;
+        mma_out = false;
+        if (tid == 0 && n >= 2) {  // K and Q of chunk n are consumed: chunk n - 2 takes the buffer
+            fence_async_smem();
+            issue_KQ(n - 2);
+        }
+        if (n >= 2) pendKQ[cur] = true;
+        {
+            // dH = G_L dH' + acc, row d = tid
+            float v1[32];
+#pragma unroll
+            for (int c0 = 0; c0 < DVS; c0 += 32) {
+                tmem_ld32(taddr_of(tH, warp, c0), v1);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dHreg[c0 + j] = __fmaf_rn(GL, dHreg[c0 + j], v1[j]);
+            }
+            put_dh(n - 1);
+        }
+        fence_async_smem();
+        tc_sync();
+    }
+    if (!failed) {
+#pragma unroll
+        for (int j4 = 0; j4 < DVS / 4; ++j4)
+            *reinterpret_cast<float4*>(a.dh0 + (sh * D + d) * D + j0 + 4 * j4) =
+                make_float4(dHreg[4 * j4], dHreg[4 * j4 + 1], dHreg[4 * j4 + 2], dHreg[4 * j4 + 3]);
+    } else {
+        // let in-flight copies and MMAs finish (bounded) before TMEM is released
+        cp_async_wait_all();
+        if (pendP) mbar_wait(bar_P, ph_P, a.err);
+        if (pendT) mbar_wait(bar_T, ph_T, a.err);
+        if (pendKQ[0]) mbar_wait(bar_KQ, ph_KQ[0], a.err);
+        if (pendKQ[1]) mbar_wait(bar_KQ + 1, ph_KQ[1], a.err);
+        if (mma_out) mbar_wait(bar_mma, ph_mma, a.err);
+    }
+    tc_sync();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---- per-chunk gradients -------------------------------------------------------------------
+struct GradSmem {
+    static constexpr size_t QK = 0;            // [Q | K] K-major: Q rows 0..63, K rows 64..127
+    static constexpr size_t Rhi = 32768;       // [dO | dR | Delta] K-major 192 x 128, hi
+    static constexpr size_t Rlo = 81920;       // lo
+    static constexpr size_t Bt = 131072;       // H_n, then dH': K-major (d, j), hi then lo
+    static constexpr size_t Scr = 196608;      // 64 x 65 fp32
+    static constexpr size_t Vec = Scr + 64 * 65 * 4;
+    static constexpr int kVec = 13;            // 64-float vectors
+    static constexpr size_t Red = Vec + kVec * 256;
+    static constexpr size_t Bar = Red + 1024;  // 2 mbarriers + TMEM base
+    static constexpr size_t Total = Bar + 64;
+};
+
+static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
+    using L = GradSmem;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char* QK = sm + L::QK;
+    unsigned char* Rhi = sm + L::Rhi;
+    unsigned char* Rlo = sm + L::Rlo;
+    unsigned char* Bt = sm + L::Bt;
+    float* scr = reinterpret_cast<float*>(sm + L::Scr);
+    float* vec = reinterpret_cast<float*>(sm + L::Vec);
+    float *gam = vec, *Gm = vec + 64, *bet = vec + 128, *bgv = vec + 192, *dec = vec + 256,
+          *qh = vec + 320, *kh = vec + 384, *rowB = vec + 448, *colE = vec + 512, *eL = vec + 576,
+          *dbA = vec + 640, *dRv = vec + 704, *dgam = vec + 768;
+    float* red = reinterpret_cast<float*>(sm + L::Red);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + L::Bar);
+    uint64_t* bar_mma = bar_ld + 1;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_ld + 2);
+
+    const int total = a.chunk_off[a.n_seq];
+    const int cidx = blockIdx.x, h = blockIdx.y, H = a.H;
+    if (total < 0 || cidx >= total) return;
+    const int b = find_seq(a.chunk_off, a.n_seq, cidx);
+    const int n = cidx - a.chunk_off[b];
+    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
+    const int t0 = seq0 + n * C;
+    const int nrows = min(C, T - n * C);
+    const int Lr = nrows - 1;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const unsigned char* blk = a.ws + ((size_t)cidx * H + h) * kBlockTrain;
+    const float scale = a.scale;
+
+    if (warp == 0) tmem_alloc(tbase, 512);
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+        mbar_expect_tx(bar_ld, 6 * 16384 + 65536 + 256);
+        bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_ld);     // Q rows
+        bulk_g2s(QK + 16384, blk + kOffKmn, 16384, bar_ld);      // K rows
+        bulk_g2s(Rhi + 16384, blk + kOffdR, 16384, bar_ld);
+        bulk_g2s(Rlo + 16384, blk + kOffdR + 16384, 16384, bar_ld);
+        bulk_g2s(Rhi + 32768, blk + kOffDl, 16384, bar_ld);
+        bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_ld);
+        bulk_g2s(Bt, blk + kOffHn, 65536, bar_ld);
+        bulk_g2s(gam, blk + kOffGam, 256, bar_ld);
+    }
+    // dO rows (zero past the chunk's end) split into R rows 0..63
+    for (int i = tid; i < 64 * (D / 8); i += 128) {
+        const int r = i / (D / 8), d8 = i % (D / 8);
+        float x[8];
+        if (r < nrows) {
+            const float4* src = reinterpret_cast<const float4*>(a.dO + ((size_t)(t0 + r) * H + h) * D + d8 * 8);
+            const float4 u0 = src[0], u1 = src[1];
+            x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+            x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        store8_split(Rhi, Rlo, cm_off(r, d8 * 8, D), x);
+    }
+    if (tid < C) bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    const uint32_t tX1 = 0, tG = 128, tS1 = 192, tX2 = 256, tdq = 384, tdk = 128;
+    uint32_t tmem = 0;
+    int ld_out = 0, mma_out = -1;   // mbarrier phases still to complete (-1: none)
+    float rowA = 0.f;               // sum_{s<r} dP_rs P_rs of row r = tid (tid < 64)
+    {
+        const bool ok = mbar_wait(bar_ld, 0, a.err);
+        fence_async_smem();
+        tc_sync();
+        tmem = *tbase;
+        if (__syncthreads_or(!ok)) goto done;
+    }
+    ld_out = -1;
+    if (tid < C) {
+        const bool in = tid < nrows;
+        const float gr = gam[tid];
+        Gm[tid] = in ? simt::gate(gr) : 0.f;
+        dec[tid] = in ? simt::decay(gam[Lr], gr) : 0.f;
+        bgv[tid] = in ? simt::bg_entry(bet[tid], gr) : 0.f;
+    }
+    if (tid == 0) {
+        mma_tile<128, 64, D>(tmem + tS1, QK, QK + 16384, false);            // [Q; K] K^T
+        mma_tile<128, 128, D>(tmem + tX1, Rhi, Bt, false);                  // [dO; dR] H^T
+        mma_tile<128, 128, D>(tmem + tX1, Rhi, Bt + 32768, true);
+        mma_tile<128, 128, D>(tmem + tX1, Rlo, Bt, true);
+        mma_tile<128, 64, D>(tmem + tG, Rhi, Rhi + 32768, false);           // [dO; dR] Delta^T
+        mma_tile<128, 64, D>(tmem + tG, Rhi, Rlo + 32768, true);
+        mma_tile<128, 64, D>(tmem + tG, Rlo, Rhi + 32768, true);
+        mma_commit(bar_mma);
+    }
+    mma_out = 0;
+    {
+        const bool ok = mbar_wait(bar_mma, 0, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) goto done;
+    }
+    mma_out = -1;
+    if (tid == 0) {  // H_n is consumed: dH' takes its place
+        fence_async_smem();
+        mbar_expect_tx(bar_ld, 65536);
+        bulk_g2s(Bt, blk + kOffdH, 65536, bar_ld);
+    }
+    ld_out = 1;
+    // ---- phase A: row quantities (thread r < 64: the dO / Q rows; 64 + r: the dR / K rows)
+    {
+        const int r = tid & 63;
+        const bool top = tid < 64;
+        const float gr = gam[r], br = bet[r];
+        float v1[32], v2[32];
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tS1, warp, c0), v1);
+            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
+            if (top) {
+#pragma unroll
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = c0 + j8 * 8 + e, j = j8 * 8 + e;
+                        const bool in = s <= r && r < nrows;
+                        const float E = in ? simt::decay(gr, gam[s]) : 0.f;
+                        const float P = __fmul_rn(E, __fmul_rn(scale, v1[j]));
+                        const float dP = in ? v2[j] : 0.f;
+                        const float t = (s < r) ? __fmul_rn(dP, P) : 0.f;
+                        scr[r * 65 + s] = t;
+                        if (s < r) rowA = __fadd_rn(rowA, t);
+                        x[e] = __fmul_rn(E, dP);   // G1 = E . dP
+                    }
+                    store8_split(Rhi, Rlo, cm_off(r, c0 + j8 * 8, C), x);
+                }
+            } else {
+                float sa = 0.f, sb = 0.f;
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c0 + j;
+                    const bool in = s < r && r < nrows;
+                    const float Kd = in ? __fmul_rn(simt::decay(gr, gam[s]), v1[j]) : 0.f;
+                    const float dA = in ? -v2[j] : 0.f;
+                    sa = __fmaf_rn(dA, Kd, sa);
+                    sb = __fmaf_rn(__fmul_rn(br, dA), Kd, sb);
+                }
+                if (c0 == 0) { dbA[r] = sa; rowB[r] = sb; }
+                else { dbA[r] = __fadd_rn(dbA[r], sa); rowB[r] = __fadd_rn(rowB[r], sb); }
+            }
+        }
+        // q^_r . (dO H^T)_r (top) and k_r . (dR H^T)_r (bottom)
+        const unsigned char* qrow = QK + (top ? 0 : 16384);
+        float acc = 0.f;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tX1, warp, c0), v1);
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) {
+                float qv[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + cm_off(r, c0 + j8 * 8, D)), qv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc = __fmaf_rn(top ? __fmul_rn(scale, qv[e]) : qv[e], v1[j8 * 8 + e], acc);
+            }
+        }
+        if (top) {
+            qh[r] = acc;
+        } else {
+            kh[r] = acc;
+            // dR row: dv = b dR, and dR . v
+            float dv8[8], s = 0.f;
+            const bool in = r < nrows;
+            for (int d8 = 0; d8 < D / 8; ++d8) {
+                const uint32_t off = cm_off(r, d8 * 8, D);
+                join8(*reinterpret_cast<const uint4*>(Rhi + 16384 + off),
+                      *reinterpret_cast<const uint4*>(Rlo + 16384 + off), dv8);
+                if (in) {
+                    float vv[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.v + ((size_t)(t0 + r) * H + h) * D + d8 * 8), vv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s = __fmaf_rn(dv8[e], vv[e], s);
+                    float* dvr = a.dv + ((size_t)(t0 + r) * H + h) * D + d8 * 8;
+                    *reinterpret_cast<float4*>(dvr) = make_float4(__fmul_rn(br, dv8[0]), __fmul_rn(br, dv8[1]),
+                                                                  __fmul_rn(br, dv8[2]), __fmul_rn(br, dv8[3]));
+                    *reinterpret_cast<float4*>(dvr + 4) = make_float4(__fmul_rn(br, dv8[4]), __fmul_rn(br, dv8[5]),
+                                                                      __fmul_rn(br, dv8[6]), __fmul_rn(br, dv8[7]));
+                }
+            }
+            dRv[r] = s;
+        }
+    }
+    {
+        // dH' has arrived: X2 = [dR; Delta] dH'^T (rows 64.. are Delta dH'^T)
+        const bool ok = mbar_wait(bar_ld, 1, a.err);
+        if (__syncthreads_or(!ok)) goto done;
+    }
+    ld_out = -1;
+    if (tid == 0) {
+        mma_tile<128, 128, D>(tmem + tX2, Rhi + 16384, Bt, false);
+        mma_tile<128, 128, D>(tmem + tX2, Rhi + 16384, Bt + 32768, true);
+        mma_tile<128, 128, D>(tmem + tX2, Rlo + 16384, Bt, true);
+        mma_commit(bar_mma);
+    }
+    mma_out = 1;
+    // ---- phase B: t_rs += b_r dA_rs Kd_rs (the bottom rows' half of the E terms)
+    {
+        const int r = tid & 63;
+        float v1[32], v2[32];
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tS1, warp, c0), v1);
+            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
+            if (tid >= 64) {
+                const float gr = gam[r], br = bet[r];
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c0 + j;
+                    if (s < r && r < nrows) {
+                        const float Kd = __fmul_rn(simt::decay(gr, gam[s]), v1[j]);
+                        scr[r * 65 + s] = __fadd_rn(scr[r * 65 + s], __fmul_rn(__fmul_rn(br, -v2[j]), Kd));
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < C) {  // phase C: column sums
+        const int s = tid;
+        float acc = 0.f;
+        for (int r = s + 1; r < nrows; ++r) acc = __fadd_rn(acc, scr[r * 65 + s]);
+        colE[s] = acc;
+    }
+    __syncthreads();
+    {
+        // phase D: G2_rs = b_r E_rs dA_rs (bottom rows) into the scratch; <dH', H_n> partials
+        const int r = tid & 63;
+        float v2[32];
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
+            if (tid >= 64) {
+                const float gr = gam[r], br = bet[r];
+                for (int j = 0; j < 32; ++j) {
+                    const int s = c0 + j;
+                    const bool in = s < r && r < nrows;
+                    scr[r * 65 + s] = in ? __fmul_rn(__fmul_rn(br, simt::decay(gr, gam[s])), -v2[j]) : 0.f;
+                }
+            }
+        }
+        const int d = tid;
+        float acc = 0.f;
+        for (int j8 = 0; j8 < D / 8; ++j8) {
+            const uint32_t off = cm_off(d, j8 * 8, D);
+            float hv[8], dv8[8];
+            join8(*reinterpret_cast<const uint4*>(blk + kOffHn + off),
+                  *reinterpret_cast<const uint4*>(blk + kOffHn + 32768 + off), hv);
+            join8(*reinterpret_cast<const uint4*>(Bt + off), *reinterpret_cast<const uint4*>(Bt + 32768 + off), dv8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = __fmaf_rn(dv8[e], hv[e], acc);
+        }
+        red[d] = acc;
+    }
+    {
+        const bool ok = mbar_wait(bar_mma, 1, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) goto done;
+    }
+    mma_out = -1;
+    {
+        // phase E: A tiles of the last MMA group (R rows 16 KB.. are free now), e_s
+        const int r = tid & 63;
+        if (tid < 64) {  // (scale G1)^T, MN-major (mn = 64 + s, k = r)
+            for (int s8 = 0; s8 < C / 8; ++s8) {
+                float x[8];
+                join8(*reinterpret_cast<const uint4*>(Rhi + cm_off(r, s8 * 8, C)),
+                      *reinterpret_cast<const uint4*>(Rlo + cm_off(r, s8 * 8, C)), x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(scale, x[e]);
+                store8_split(Rhi + 16384, Rlo + 16384, mn_off(64 + s8 * 8, r, 128), x);
+            }
+        } else {  // G2 + G2^T, MN-major (mn = 64 + s, k = r)
+            for (int s8 = 0; s8 < C / 8; ++s8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s = s8 * 8 + e;
+                    x[e] = __fadd_rn(scr[s * 65 + r], scr[r * 65 + s]);
+                }
+                store8_split(Rhi + 32768, Rlo + 32768, mn_off(64 + s8 * 8, r, 128), x);
+            }
+        }
+        float v1[32], acc = 0.f;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tX2, warp, c0), v1);
+            if (tid >= 64) {
+#pragma unroll
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    float kv[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(QK + 16384 + cm_off(r, c0 + j8 * 8, D)), kv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = __fmaf_rn(kv[e], v1[j8 * 8 + e], acc);
+                }
+            }
+        }
+        if (tid >= 64) eL[r] = (r < Lr) ? __fmul_rn(dec[r], acc) : 0.f;
+        if (tid == 0) {
+            float s = 0.f;
+            for (int i = 0; i < 128; ++i) s = __fadd_rn(s, red[i]);
+            red[128] = s;
+        }
+    }
+    fence_async_smem();
+    tc_sync();
+    if (tid == 0) {
+        mma_tile_mj<128, 128, C, false, true>(tmem + tdq, Rhi, QK + 16384, false);          // G1 K
+        mma_tile_mj<128, 128, C, false, true>(tmem + tdq, Rlo, QK + 16384, true);
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rhi + 16384, QK, false);           // (s G1)^T Q
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 16384, QK, true);
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rhi + 32768, QK + 16384, true);    // (G2 + G2^T) K
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 32768, QK + 16384, true);
+        mma_commit(bar_mma);
+    }
+    mma_out = 0;
+    if (tid < C) {  // gate and beta gradients of row r
+        const int r = tid;
+        const float kr = kh[r];
+        const float dG = __fsub_rn(qh[r], __fmul_rn(bet[r], kr));
+        const float dbR = __fsub_rn(dRv[r], __fmul_rn(Gm[r], kr));
+        float dgr = __fsub_rn(__fadd_rn(__fmul_rn(Gm[r], dG), __fadd_rn(rowA, rowB[r])), colE[r]);
+        dgr = __fsub_rn(dgr, eL[r]);
+        if (r == Lr) {
+            float sumL = 0.f;
+            for (int s = 0; s < Lr; ++s) sumL = __fadd_rn(sumL, eL[s]);
+            dgr = __fadd_rn(dgr, __fadd_rn(__fmul_rn(Gm[Lr], red[128]), sumL));
+        }
+        if (r < nrows) a.dbeta[(size_t)(t0 + r) * H + h] = __fadd_rn(dbR, dbA[r]);
+        dgam[r] = (r < nrows) ? dgr : 0.f;
+    }
+    __syncthreads();
+    if (tid < nrows) {  // dg_s = sum_{r=s}^{L} dgam_r, from the last row down
+        float acc = 0.f;
+        for (int r = Lr; r >= tid; --r) acc = __fadd_rn(acc, dgam[r]);
+        a.dg[(size_t)(t0 + tid) * H + h] = acc;
+    }
+    {
+        const bool ok = mbar_wait(bar_mma, 0, a.err);
+        fence_after();
+        if (__syncthreads_or(!ok)) goto done;
+    }
+    mma_out = -1;
+    {
+        // dq rows (top), dk rows (bottom)
+        const int r = tid & 63;
+        const bool top = tid < 64;
+        const bool in = r < nrows;
+        float x1[32], y[32], z[32];
+        float* out = (top ? a.dq : a.dk) + ((size_t)(t0 + r) * H + h) * D;
+        const float gr = Gm[r], nb = -bgv[r], dr = dec[r];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            tmem_ld32(taddr_of(tmem + tX1, warp, c0), x1);
+            tmem_ld32(taddr_of(tmem + (top ? tdq : tdk), warp, c0), y);
+            tmem_ld32(taddr_of(tmem + tX2, warp, c0), z);
+            if (in) {
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * j4 + e;
+                        o4[e] = top ? __fmul_rn(scale, __fmaf_rn(gr, x1[j], y[j]))
+                                    : __fadd_rn(__fmaf_rn(nb, x1[j], __fmul_rn(dr, z[j])), y[j]);
+                    }
+                    *reinterpret_cast<float4*>(out + c0 + 4 * j4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+        }
+    }
+done:
+    if (ld_out >= 0) mbar_wait(bar_ld, (uint32_t)ld_out, a.err);    // bounded
+    if (mma_out >= 0) mbar_wait(bar_mma, (uint32_t)mma_out, a.err);
+    tc_sync();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace tc
+}  // namespace cpr

@@ -210,15 +210,38 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
     lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(hi)));
 }
 
+// Splits 8 fp32 values into packed hi and lo bf16 vectors.
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+    __align__(16) __nv_bfloat16 h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) split_bf16(x[i], h[i], l[i]);
+    hi = *reinterpret_cast<const uint4*>(h);
+    lo = *reinterpret_cast<const uint4*>(l);
+}
+
 // Stores 8 fp32 values (consecutive along K) as one 16-byte core-matrix row,
 // split into hi and lo tiles at the same offset.
 __device__ __forceinline__ void store8_split(unsigned char* hi_tile, unsigned char* lo_tile,
                                              uint32_t off, const float (&x)[8]) {
-    __align__(16) __nv_bfloat16 h[8], l[8];
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    *reinterpret_cast<uint4*>(hi_tile + off) = hi;
+    *reinterpret_cast<uint4*>(lo_tile + off) = lo;
+}
+
+// Packed hi/lo vectors back to 8 fp32 values (hi + lo).
+__device__ __forceinline__ void join8(const uint4& hi, const uint4& lo, float (&x)[8]) {
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&hi);
+    const __nv_bfloat16* l = reinterpret_cast<const __nv_bfloat16*>(&lo);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split_bf16(x[i], h[i], l[i]);
-    *reinterpret_cast<uint4*>(hi_tile + off) = *reinterpret_cast<const uint4*>(h);
-    *reinterpret_cast<uint4*>(lo_tile + off) = *reinterpret_cast<const uint4*>(l);
+    for (int i = 0; i < 8; ++i) x[i] = __fadd_rn(__bfloat162float(h[i]), __bfloat162float(l[i]));
+}
+
+// 8 bf16 values (16 bytes) to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&x)[8]) {
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(h[i]);
 }
 
 }  // namespace tc

@@ -40,6 +40,14 @@ constexpr size_t kOffPlo = 73728;     // 64 x 64 bf16 K-major
 constexpr size_t kOffU = 81920;       // 64 x 128 fp32, [split][DVS/4][64 rows] float4 groups
 constexpr size_t kOffGam = 114688;    // 64 fp32
 constexpr size_t kBlock = 114944;
+// Training blocks (the backward) append, all as hi/lo bf16 tile pairs in the
+// K-major core-matrix layout the backward kernels read with bulk copies:
+constexpr size_t kOffT = kBlock;               // T, 64 x 64 (r, j): hi, lo (8 KB each)
+constexpr size_t kOffHn = kOffT + 16384;       // chunk-start state H_n, 128 x 128 (d, j): hi, lo
+constexpr size_t kOffDl = kOffHn + 65536;      // Delta, 64 x 128 (s, j): hi, lo
+constexpr size_t kOffdH = kOffDl + 32768;      // dL/dH_{n+1}, 128 x 128 (d, j): hi, lo
+constexpr size_t kOffdR = kOffdH + 65536;      // dL/dR, 64 x 128 (r, j): hi, lo
+constexpr size_t kBlockTrain = kOffdR + 32768;
 
 struct TcArgs {
     const __nv_bfloat16* q;
@@ -53,7 +61,9 @@ struct TcArgs {
     int H;
     int dvs;              // d_v columns per state CTA
     float scale;
-    unsigned char* ws;    // [chunks * H] blocks of kBlock bytes
+    unsigned char* ws;    // [chunks * H] blocks of blk_bytes bytes
+    size_t blk_bytes;     // kBlock (forward) or kBlockTrain (recompute for the backward)
+    bool train;           // also write T, H_n and Delta tiles for the backward
     const float* h0;
     float* o;
     float* final_state;
@@ -123,7 +133,7 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
     const int nrows = min(C, T - n * C);
     const bool last = (n * C + nrows == T);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char* blk = a.ws + ((size_t)cidx * H + h) * kBlock;
+    unsigned char* blk = a.ws + ((size_t)cidx * H + h) * a.blk_bytes;
 
     if (warp == 0) tmem_alloc(tbase, 256);
     if (tid == 0) {
@@ -216,6 +226,14 @@ static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(Tfp[r * 65 + s8 * 8 + e], sc[s8 * 8 + e]);
             store8_split(xhi, xlo, cm_off(r, s8 * 8, C), x);
+        }
+        if (a.train && which == 0) {  // T itself, for dR = T^T dDelta in the backward
+            for (int s8 = 0; s8 < C / 8; ++s8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = Tfp[r * 65 + s8 * 8 + e];
+                store8_split(blk + kOffT, blk + kOffT + 8192, cm_off(r, s8 * 8, C), x);
+            }
         }
     }
     if (a.cache && last && nrows < C) {  // decode cache: rows of the last, partial chunk
@@ -358,13 +376,25 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         if (a.h0) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + 4 * j4);
         Hreg[4 * j4] = x.x; Hreg[4 * j4 + 1] = x.y; Hreg[4 * j4 + 2] = x.z; Hreg[4 * j4 + 3] = x.w;
     }
-    auto put_h = [&]() {
+    const int coff = a.chunk_off[b];
+    auto blk_of = [&](int n) { return a.ws + ((size_t)(coff + n) * H + h) * a.blk_bytes; };
+    // H as the B operand of the next chunk; for training also chunk nn's start
+    // state as K-major (d, j) hi/lo tiles in its workspace block
+    auto put_h = [&](int nn) {
+        unsigned char* g = (a.train && nn < nch) ? blk_of(nn) + kOffHn : nullptr;
 #pragma unroll
         for (int j8 = 0; j8 < DVS / 8; ++j8) {
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = Hreg[j8 * 8 + e];
-            store8_split(sm + L::Hhi, sm + L::Hlo, mn_off(j8 * 8, d, DVS), x);
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4*>(sm + L::Hhi + mn_off(j8 * 8, d, DVS)) = hi;
+            *reinterpret_cast<uint4*>(sm + L::Hlo + mn_off(j8 * 8, d, DVS)) = lo;
+            if (g) {
+                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + j8 * 8, D)) = hi;
+                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + j8 * 8, D)) = lo;
+            }
         }
     };
     auto put_state = [&](float* dst) {
@@ -373,7 +403,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
             *reinterpret_cast<float4*>(dst + (size_t)d * D + j0 + 4 * j4) =
                 make_float4(Hreg[4 * j4], Hreg[4 * j4 + 1], Hreg[4 * j4 + 2], Hreg[4 * j4 + 3]);
     };
-    put_h();
+    put_h(0);
     if (nch == 0 && cstate) put_state(cstate);
     fence_async_smem();
     tc_sync();
@@ -382,8 +412,6 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     uint32_t ph_mma = 0, ph_ldA = 0, ph_ldB = 0;
     bool pendA = false, pendB = false, failed = false, mma_out = false;
 
-    const int coff = a.chunk_off[b];
-    auto blk_of = [&](int n) { return a.ws + ((size_t)(coff + n) * H + h) * kBlock; };
     auto issue_A = [&](int n) {
         const unsigned char* blk = blk_of(n);
         mbar_expect_tx(bar_ldA, L::LoadA);
@@ -466,7 +494,17 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
                             x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
                             y[e] = __fmul_rn(dr, x[e]);
                         }
-                        store8_split(sm + L::Dhi, sm + L::Dlo, mn_off(c0 + j8 * 8, r, DVS), x);
+                        {
+                            uint4 hi, lo;
+                            split8(x, hi, lo);
+                            *reinterpret_cast<uint4*>(sm + L::Dhi + mn_off(c0 + j8 * 8, r, DVS)) = hi;
+                            *reinterpret_cast<uint4*>(sm + L::Dlo + mn_off(c0 + j8 * 8, r, DVS)) = lo;
+                            if (a.train) {  // Delta rows for the backward, K-major (s, j)
+                                unsigned char* g = blk_of(n) + kOffDl + cm_off(r, j0 + c0 + j8 * 8, D);
+                                *reinterpret_cast<uint4*>(g) = hi;
+                                *reinterpret_cast<uint4*>(g + 16384) = lo;
+                            }
+                        }
                         store8_split(sm + L::Bhi, sm + L::Blo, mn_off(c0 + j8 * 8, r, DVS), y);
                         if (cd) {
                             *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
@@ -515,7 +553,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
 #pragma unroll
             for (int c0 = 0; c0 < DVS; c0 += 32) {
                 tmem_ld32(taddr_of(acc5, warp, c0), v);
-                if (lane < 16 && r < nrows) {
+                if (lane < 16 && r < nrows && a.o) {
                     float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + c0;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
@@ -533,7 +571,7 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) Hreg[c0 + j] = __fadd_rn(__fmul_rn(GL, Hreg[c0 + j]), v[j]);
             }
-            put_h();
+            put_h(n + 1);
             if (cstate && last && nrows == C) put_state(cstate);
         }
         fence_async_smem();

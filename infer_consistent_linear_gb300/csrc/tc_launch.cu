@@ -1,6 +1,7 @@
 // Launch sequences of the TC_BF16X3 policy (tensor-core prep, state pass and
 // decode; bf16 io, d = 128).
 #include "profile.h"
+#include "tc_bwd.cuh"
 #include "tc_decode.cuh"
 #include "tc_launch.h"
 
@@ -41,6 +42,20 @@ cudaError_t decode(const tc::TcDecArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+template <int DVS>
+cudaError_t state_bwd(const tc::TcBwdArgs& a, int n_seq, int H, cudaStream_t st) {
+    auto kern = tc::k_tc_state_bwd<DVS>;
+    const size_t sm = tc::SbSmem<DVS>::Total;
+    cudaError_t e = set_smem(kern, sm);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
+    if (grid > 0) {
+        ProfScope ps("cpr_tc_state_bwd", st);
+        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st) {
@@ -65,6 +80,25 @@ cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st) {
         case 32: return decode<32>(a, st);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cmax, int n_seq, int H,
+                        cudaStream_t st) {
+    cudaError_t e = tc_forward(f, cmax, n_seq, H, st);
+    if (e != cudaSuccess) return e;
+    switch (f.dvs) {
+        case 64: e = state_bwd<64>(b, n_seq, H, st); break;
+        case 32: e = state_bwd<32>(b, n_seq, H, st); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    e = set_smem(tc::k_tc_grad, tc::GradSmem::Total);
+    if (e != cudaSuccess) return e;
+    if (cmax > 0) {
+        ProfScope ps("cpr_tc_grad", st);
+        tc::k_tc_grad<<<dim3((unsigned)cmax, H), 128, tc::GradSmem::Total, st>>>(b);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace cpr

@@ -2,7 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
-#include "tc_fwd.cuh"
+#include "tc_bwd.cuh"
 
 namespace cpr {
 namespace tc {
@@ -11,4 +11,9 @@ struct TcDecArgs;
 // setup must already have run on `st`; a.dvs selects the state-pass split width.
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st);
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st);
+// Training forward (prep + state pass writing the backward's tiles), reverse
+// state pass and per-chunk gradients; `f` must have train set and
+// blk_bytes = kBlockTrain, `b.ws` the same workspace blocks.
+cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cmax, int n_seq, int H,
+                        cudaStream_t st);
 }  // namespace cpr

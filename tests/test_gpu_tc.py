@@ -94,12 +94,55 @@ def test_tc_prefill_cache_refused_by_simt_decode():
     assert cpr.get_device_error(clear=True) == 4
 
 
-def test_tc_contract_backward_parity():
-    x = make_inputs([150, 64, 1], 2, 128, 128, io_dtype=torch.bfloat16, seed=5, h0_std=0.1,
-                    with_grad=True)
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def _tc_bwd(x, c, dHT=None):
     xd = x.to(DEV)
     got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0,
-                          contract=_tc())
-    ref = oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0)
-    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+                          dHT=None if dHT is None else dHT.to(DEV), contract=c)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    return got
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_tc_backward_parity_ragged_with_dHT(splits):
+    lens = [150, 64, 1, 0, 200]
+    x = make_inputs(lens, 2, 128, 128, io_dtype=torch.bfloat16, seed=5, h0_std=0.1, with_grad=True)
+    gen = torch.Generator().manual_seed(11)
+    dHT = torch.randn(len(lens), 2, 128, 128, generator=gen)
+    got = _tc_bwd(x, _tc(splits), dHT)
+    ref = oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, dHT=dHT)
+    for n in GRADS:
         assert_close(n, got[n], ref[n], TOL_BF16)
+
+
+def test_tc_backward_parity_no_dHT_scale():
+    x = make_inputs([300, 65], 3, 128, 128, io_dtype=torch.bfloat16, seed=6, h0_std=0.2, with_grad=True)
+    c = cpr.default_contract(torch.bfloat16, 128, dv_splits=2, scale=0.5, **TC)
+    got = _tc_bwd(x, c)
+    ref = oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, scale=0.5)
+    for n in GRADS:
+        assert_close(n, got[n], ref[n], TOL_BF16)
+
+
+def test_tc_backward_deterministic_and_batch_invariant():
+    lens = [130, 64, 257, 5]
+    x = make_inputs(lens, 2, 128, 128, io_dtype=torch.bfloat16, seed=7, h0_std=0.1, with_grad=True)
+    c = _tc()
+    a = _tc_bwd(x, c)
+    b = _tc_bwd(x, c)
+    for n in GRADS:
+        assert_bitwise(n, a[n], b[n])
+    cu = x.cu_seqlens.tolist()
+    for i in range(len(lens)):
+        lo, hi = cu[i], cu[i + 1]
+        xs = make_inputs([lens[i]], 2, 128, 128, io_dtype=torch.bfloat16, seed=0, with_grad=True)
+        for f in ("q", "k", "v", "g", "beta", "dO"):
+            setattr(xs, f, getattr(x, f)[lo:hi].clone())
+        xs.h0 = x.h0[i:i + 1].clone()
+        one = _tc_bwd(xs, c)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            assert_bitwise(f"{n}[seq {i}]", one[n], a[n][lo:hi])
+        assert_bitwise(f"dh0[seq {i}]", one["dh0"], a["dh0"][i:i + 1])
