@@ -211,6 +211,7 @@ class OurStep:
         else:
             self.c = cpr.default_contract(torch.bfloat16, d)
         self.dig = cpr.contract_digest(self.c)
+        self.saved = policy == "tc"
         self.dev = dev
         if self.op == "decode":
             full = [L + n_decode_steps for L in self.lens]
@@ -267,11 +268,15 @@ class OurStep:
             self.t += 1
             return
         x = xd if xd is not None else self.xd
+        # the trainer step: a training forward that keeps its tiles for the backward
+        # (tensor-core contract), or forward + backward-with-recompute (SIMT contract)
+        train = self.op == "fwdbwd" and self.saved
         cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c, digest=self.dig,
-                        out=self.o, final=self.fin, workspace=self.ws)
+                        out=self.o, final=self.fin, workspace=self.wsb if train else self.ws,
+                        train=train)
         if self.op == "fwdbwd":
             cpr.cpr_gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, contract=self.c,
-                            digest=self.dig, workspace=self.wsb, outs=self.gouts)
+                            digest=self.dig, workspace=self.wsb, outs=self.gouts, saved=train)
 
     def tokens_per_step(self):
         return len(self.lens) if self.op == "decode" else sum(self.lens)

@@ -159,7 +159,7 @@ int cpr_sha256(const void* data, size_t len, uint8_t out[32]);
 
 /* ---- workspace and decode cache sizes --------------------------------- */
 #define CPR_OP_FWD 1   /* cpr_gdn_fwd and cpr_gdn_prefill */
-#define CPR_OP_BWD 2   /* cpr_gdn_bwd                     */
+#define CPR_OP_BWD 2   /* cpr_gdn_bwd, cpr_gdn_fwd_train, cpr_gdn_bwd_saved */
 
 /* Bytes of device workspace an op needs for a batch with n_seq sequences and
  * n_tok tokens in total (an upper bound valid for any split of n_tok). */
@@ -236,6 +236,34 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32],
                 const float* h0, const float* dO, const float* dHT,
                 void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Training forward: the outputs of cpr_gdn_fwd (same arithmetic, same bits)
+ * and, in the workspace, the per-chunk tiles the backward reads (chunk-start
+ * states, Delta, (I + A)^-1 and the operand tiles), so that
+ * cpr_gdn_bwd_saved need not recompute the forward -- the trainer's
+ * forward-then-backward step of the stage table (page "IsoExec: 切换 SkyRL
+ * 中的训练器-推理不匹配", section "Chunkwise-Parallel Recurrent (CPR) Gated
+ * DeltaNet", "Trainer Fwd+Bwd").  workspace: cpr_gdn_workspace_size(c,
+ * CPR_OP_BWD, ...) bytes, 256-byte aligned, owned by the caller until the
+ * matching cpr_gdn_bwd_saved has run.  CPR_POLICY_TC_BF16X3 contracts only
+ * (CPR_ERR_UNSUPPORTED otherwise). */
+int cpr_gdn_fwd_train(const cpr_contract* c, const uint8_t digest[32],
+                      const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
+                      int H, const float* h0, void* o, float* final_state,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward from a training forward's workspace: the same arguments and
+ * results as cpr_gdn_bwd, but the forward is not recomputed; `workspace`
+ * must be the one cpr_gdn_fwd_train filled for the same contract, inputs and
+ * h0, unchanged since (the library cannot check this).  Results are
+ * bit-identical to cpr_gdn_bwd's.  CPR_POLICY_TC_BF16X3 contracts only. */
+int cpr_gdn_bwd_saved(const cpr_contract* c, const uint8_t digest[32],
+                      const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
+                      int H, const float* h0, const float* dO, const float* dHT,
+                      void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free trainer forward.  The pages have no counterpart for this
  * entry point: it exists for callers that cannot allocate device memory at

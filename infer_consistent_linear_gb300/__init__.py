@@ -23,8 +23,10 @@ LIB_PATH = os.path.join(_PKG, "libcpr_gdn.so")
 CPR_OK = 0
 ERRORS = {
     1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CONTRACT_MISMATCH",
-    5: "UNALIGNED", 6: "CUDA", 7: "WORKSPACE", 8: "BAD_SEQLENS",
+    5: "UNALIGNED", 6: "CUDA", 7: "WORKSPACE", 8: "BAD_SEQLENS", 9: "DEVICE_TIMEOUT",
 }
+CPR_ERR_INVALID_ARG = 1
+CPR_ERR_UNSUPPORTED = 2
 CPR_DTYPE_F32 = 1
 CPR_DTYPE_BF16 = 2
 CPR_POLICY_SIMT_F32 = 1
@@ -91,6 +93,9 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_decode_step": (I, [CP, P, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gdn_bwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                             P, SZ, P]),
+        "cpr_gdn_fwd_train": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
+        "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
+                                  P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_profile_begin": (I, []),
         "cpr_profile_end": (I, [P, I, ctypes.POINTER(I)]),
@@ -245,18 +250,24 @@ def _shape_args(q, v, cu_seqlens):
 
 def cpr_gdn_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
                 digest: Optional[bytes] = None, want_final: bool = True, out=None,
-                final=None, workspace=None):
-    """Trainer forward.  Returns (o [n_tok,H,d_v] fp32, final [n_seq,H,d_k,d_v] or None)."""
+                final=None, workspace=None, train: bool = False):
+    """Trainer forward.  Returns (o [n_tok,H,d_v] fp32, final [n_seq,H,d_k,d_v] or None).
+    With train=True (cpr_gdn_fwd_train) the workspace -- CPR_OP_BWD-sized, required -- also
+    keeps the tiles cpr_gdn_bwd(..., saved=True) reads instead of recomputing the forward."""
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
     n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
     o = out if out is not None else torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
     fin = final if final is not None else (
         torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device) if want_final else None)
-    ws, wsb = _ws(c, CPR_OP_FWD, n_seq, n_tok, H, q.device, workspace)
-    _check(lib.cpr_gdn_fwd(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                           _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
-                           _ptr(fin), _ptr(ws), wsb, _stream()))
+    if train and workspace is None:
+        raise CprError(CPR_ERR_INVALID_ARG, "train=True needs a caller-owned CPR_OP_BWD workspace "
+                                            "(passed on to the saved backward)")
+    ws, wsb = _ws(c, CPR_OP_BWD if train else CPR_OP_FWD, n_seq, n_tok, H, q.device, workspace)
+    fn = lib.cpr_gdn_fwd_train if train else lib.cpr_gdn_fwd
+    _check(fn(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+              _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
+              _ptr(fin), _ptr(ws), wsb, _stream()))
     return o, fin
 
 
@@ -293,8 +304,12 @@ def cpr_gdn_decode_step(q_t, k_t, v_t, g_t, beta_t, cache: DecodeCache,
 
 def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                 contract: Optional[Contract] = None, digest: Optional[bytes] = None,
-                workspace=None, outs=None):
-    """Trainer backward.  Returns dict dq, dk, dv (fp32), dg, dbeta, dh0."""
+                workspace=None, outs=None, saved: bool = False):
+    """Trainer backward.  Returns dict dq, dk, dv (fp32), dg, dbeta, dh0.  With saved=True
+    (cpr_gdn_bwd_saved) `workspace` is the one a cpr_gdn_fwd(..., train=True) call filled
+    for the same inputs; the forward is then not recomputed."""
+    if saved and workspace is None:
+        raise CprError(CPR_ERR_INVALID_ARG, "saved=True needs the training forward's workspace")
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
     n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
@@ -307,7 +322,8 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                     dbeta=torch.empty(n_tok, H, dtype=torch.float32, device=dev),
                     dh0=torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=dev))
     ws, wsb = _ws(c, CPR_OP_BWD, n_seq, n_tok, H, dev, workspace)
-    _check(lib.cpr_gdn_bwd(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+    fn = lib.cpr_gdn_bwd_saved if saved else lib.cpr_gdn_bwd
+    _check(fn(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                            _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(dO),
                            _ptr(dHT), _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]),
                            _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),

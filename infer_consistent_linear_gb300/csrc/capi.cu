@@ -233,12 +233,16 @@ cudaError_t launch_setup(const cpr::simt::SetupArgs& sa, cudaStream_t st) {
 
 // Shared by cpr_gdn_fwd and cpr_gdn_prefill: one code path, so the trainer
 // forward and the engine prefill run identical kernels.
+// `train`: also leave the backward's per-chunk tiles in the (CPR_OP_BWD-sized)
+// workspace; the kernels and the outputs' arithmetic are the same.
 int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
                  const void* v, const float* g, const float* beta, const int32_t* cu, int n_seq,
                  int64_t n_tok, int H, const float* h0, void* o, float* final_state, void* cache,
-                 void* ws, size_t ws_bytes, void* stream) {
+                 void* ws, size_t ws_bytes, void* stream, bool train = false) {
     int rc = check_digest(c, digest);
     if (rc) return rc;
+    if (train && c->operand_policy != CPR_POLICY_TC_BF16X3)
+        return fail(CPR_ERR_UNSUPPORTED, "training forward: tensor-core operand policy only");
     rc = check_sizes(n_seq, n_tok, H);
     if (rc) return rc;
     REQ_PTR4(cu);
@@ -246,7 +250,7 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
         REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta); REQ_PTR(o);
     }
     OPT_PTR(h0); OPT_PTR(final_state); OPT_PTR(cache);
-    const WsLayout w = ws_layout(*c, CPR_OP_FWD, n_seq, n_tok, H);
+    const WsLayout w = ws_layout(*c, train ? CPR_OP_BWD : CPR_OP_FWD, n_seq, n_tok, H);
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
         return fail(CPR_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", w.total);
     uint32_t* err = device_error_ptr();
@@ -268,7 +272,8 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
         t.q = static_cast<const __nv_bfloat16*>(q); t.k = static_cast<const __nv_bfloat16*>(k);
         t.v = static_cast<const __nv_bfloat16*>(v); t.g = g; t.beta = beta; t.cu = cu;
         t.chunk_off = sa.chunk_off; t.n_seq = n_seq; t.H = H; t.dvs = (int)(c->d_v / c->dv_splits);
-        t.scale = c->scale; t.ws = wsb + w.W; t.blk_bytes = cpr::tc::kBlock; t.train = false;
+        t.scale = c->scale; t.ws = wsb + w.W; t.train = train;
+        t.blk_bytes = train ? cpr::tc::kBlockTrain : cpr::tc::kBlock;
         t.h0 = h0; t.o = static_cast<float*>(o);
         t.final_state = final_state; t.cache = static_cast<uint8_t*>(cache); t.co = to_off(cl);
         t.err = err;
@@ -384,6 +389,15 @@ int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
                         final_state, nullptr, workspace, workspace_bytes, stream);
 }
 
+int cpr_gdn_fwd_train(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                      const void* k, const void* v, const float* g, const float* beta,
+                      const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                      const float* h0, void* o, float* final_state, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                        final_state, nullptr, workspace, workspace_bytes, stream, true);
+}
+
 int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32], const void* q,
                     const void* k, const void* v, const float* g, const float* beta,
                     const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H, const float* h0,
@@ -431,13 +445,16 @@ int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const v
     return CPR_OK;
 }
 
-int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, const void* k,
-                const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
-                int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
-                const float* dHT, void* dq, void* dk, void* dv, float* dg, float* dbeta,
-                float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+// `saved`: the workspace holds a training forward's tiles; skip the recompute.
+static int backward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
+                  const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                  int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
+                  const float* dHT, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  float* dh0, void* workspace, size_t workspace_bytes, void* stream, bool saved) {
     int rc = check_digest(c, digest);
     if (rc) return rc;
+    if (saved && c->operand_policy != CPR_POLICY_TC_BF16X3)
+        return fail(CPR_ERR_UNSUPPORTED, "backward from saved tiles: tensor-core operand policy only");
     rc = check_sizes(n_seq, n_tok, H);
     if (rc) return rc;
     REQ_PTR4(cu_seqlens);
@@ -473,7 +490,7 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
         tb.chunk_off = sa.chunk_off; tb.n_seq = n_seq; tb.H = H; tb.scale = c->scale; tb.ws = t.ws;
         tb.dO = dO; tb.dHT = dHT; tb.dq = static_cast<float*>(dq); tb.dk = static_cast<float*>(dk);
         tb.dv = static_cast<float*>(dv); tb.dg = dg; tb.dbeta = dbeta; tb.dh0 = dh0; tb.err = err;
-        e = cpr::tc_backward(t, tb, w.cmax, n_seq, H, st);
+        e = cpr::tc_backward(t, tb, w.cmax, n_seq, H, st, !saved);
         if (e != cudaSuccess) return cuda_fail(e, "backward launch");
         return CPR_OK;
     }
@@ -499,6 +516,25 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
     e = ops_for(*c)->bwd(fa, ba, L);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return CPR_OK;
+}
+
+int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32], const void* q, const void* k,
+                const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
+                const float* dHT, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+    return backward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, dO, dHT,
+                         dq, dk, dv, dg, dbeta, dh0, workspace, workspace_bytes, stream, false);
+}
+
+int cpr_gdn_bwd_saved(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                      const void* k, const void* v, const float* g, const float* beta,
+                      const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                      const float* h0, const float* dO, const float* dHT, void* dq, void* dk,
+                      void* dv, float* dg, float* dbeta, float* dh0, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return backward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, dO, dHT,
+                         dq, dk, dv, dg, dbeta, dh0, workspace, workspace_bytes, stream, true);
 }
 
 int cpr_get_device_error(uint32_t* code, int clear) {

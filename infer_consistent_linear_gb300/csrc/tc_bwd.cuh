@@ -436,6 +436,7 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(gam, blk + kOffGam, 256, bar_ld);
     }
     // dO rows (zero past the chunk's end) split into R rows 0..63
+#pragma unroll 8
     for (int i = tid; i < 64 * (D / 8); i += 128) {
         const int r = i / (D / 8), d8 = i % (D / 8);
         float x[8];
@@ -555,6 +556,7 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
             // dR row: dv = b dR, and dR . v
             float dv8[8], s = 0.f;
             const bool in = r < nrows;
+#pragma unroll 4
             for (int d8 = 0; d8 < D / 8; ++d8) {
                 const uint32_t off = cm_off(r, d8 * 8, D);
                 join8(*reinterpret_cast<const uint4*>(Rhi + 16384 + off),
@@ -631,6 +633,7 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
         }
         const int d = tid;
         float acc = 0.f;
+#pragma unroll 8
         for (int j8 = 0; j8 < D / 8; ++j8) {
             const uint32_t off = cm_off(d, j8 * 8, D);
             float hv[8], dv8[8];

@@ -311,6 +311,11 @@ done:
 }
 
 // ---- state pass: one CTA per (sequence, head, d_v split), chunks in order -----------
+// 256 threads: warp w reads TMEM lane quarter w % 4; the two warps of a quarter
+// take one half of the DVS columns each.  Per chunk the dependent chain is
+// A4 MMA -> Delta epilogue -> H' MMA -> H' epilogue; the output rows of chunk n
+// (P Delta and the Q H rows) are read while chunk n + 1's A4 MMA runs, from
+// double-buffered accumulators.
 template <int DVS>
 struct StateSmem {
     static constexpr size_t A4hi = 0, A4lo = 32768, Kmn = 65536, Phi = 81920, Plo = 90112;
@@ -324,26 +329,31 @@ struct StateSmem {
     static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32, [DVS/4][64] float4
     static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 (bulk copied)
     static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
-    static constexpr size_t Bar = Dec + 256;                 // 3 mbarriers + TMEM base
+    static constexpr size_t Bar = Dec + 256;                 // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
-    static constexpr uint32_t LoadA = 32768 + 16384 + 256;               // A4 tiles + gam
-    static constexpr uint32_t LoadB = 16384 + 8192 + 8192 + 64 * DVS * 4;  // K, P, U
+    static constexpr uint32_t LoadA = 32768 + 16384 + 256;   // A4 tiles + gam
+    static constexpr uint32_t LoadB = 16384 + 64 * DVS * 4;  // K, U
+    static constexpr uint32_t LoadP = 16384;                 // P hi, lo
+    static constexpr uint32_t TmemCols = 5 * DVS > 256 ? 512 : 256;
 };
 
 template <int DVS>
-__global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
+__global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
     using L = StateSmem<DVS>;
     constexpr int NSPLIT = D / DVS;
+    constexpr int HALF = DVS / 2;  // columns per thread
     extern __shared__ __align__(1024) unsigned char sm[];
     float* sU = reinterpret_cast<float*>(sm + L::U);
     float* sQ = reinterpret_cast<float*>(sm + L::Q);
     float* gam = reinterpret_cast<float*>(sm + L::Gam);
     float* Gm = reinterpret_cast<float*>(sm + L::Gm);
     float* dec = reinterpret_cast<float*>(sm + L::Dec);
-    uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);
-    uint64_t* bar_ldA = bar_mma + 1;
-    uint64_t* bar_ldB = bar_mma + 2;
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 3);
+    uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);   // A4 and H' groups
+    uint64_t* bar_pd = bar_mma + 1;                                   // P Delta groups
+    uint64_t* bar_ldA = bar_mma + 2;
+    uint64_t* bar_ldB = bar_mma + 3;
+    uint64_t* bar_ldP = bar_mma + 4;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 5);
 
     const int total = a.chunk_off[a.n_seq];
     if (total < 0) return;
@@ -353,27 +363,27 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     const int b = blockIdx.x / (NSPLIT * H);
     const int j0 = sp * DVS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int cb = half * HALF;                 // this thread's first column (within the split)
     const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
     const int nch = a.chunk_off[b + 1] - a.chunk_off[b];
     const size_t sh = (size_t)b * H + h;
     float* cstate = a.cache ? reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D : nullptr;
 
-    if (warp == 0) tmem_alloc(tbase, 256);
+    if (warp == 0) tmem_alloc(tbase, L::TmemCols);
     if (tid == 0) {
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_ldA, 1);
-        mbar_init(bar_ldB, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bar_mma + i, 1);
         mbar_init_fence();
     }
-    for (int i = tid; i < 1024; i += 128)  // rows 64..127 of the W'_lo operand stay zero
+    for (int i = tid; i < 1024; i += 256)  // rows 64..127 of the W'_lo operand stay zero
         reinterpret_cast<uint4*>(sm + L::A4lo + 16384)[i] = make_uint4(0u, 0u, 0u, 0u);
-    // state columns j0..j0+DVS of row d = tid, fp32, kept in registers
-    float Hreg[DVS];
-    const int d = tid;
+    // state row d = 32 quarter + lane, columns j0 + cb .. + HALF, fp32 in registers
+    float Hreg[HALF];
+    const int d = quarter * 32 + lane;
 #pragma unroll
-    for (int j4 = 0; j4 < DVS / 4; ++j4) {
+    for (int j4 = 0; j4 < HALF / 4; ++j4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.h0) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + 4 * j4);
+        if (a.h0) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + cb + 4 * j4);
         Hreg[4 * j4] = x.x; Hreg[4 * j4 + 1] = x.y; Hreg[4 * j4 + 2] = x.z; Hreg[4 * j4 + 3] = x.w;
     }
     const int coff = a.chunk_off[b];
@@ -383,24 +393,25 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     auto put_h = [&](int nn) {
         unsigned char* g = (a.train && nn < nch) ? blk_of(nn) + kOffHn : nullptr;
 #pragma unroll
-        for (int j8 = 0; j8 < DVS / 8; ++j8) {
+        for (int j8 = 0; j8 < HALF / 8; ++j8) {
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = Hreg[j8 * 8 + e];
             uint4 hi, lo;
             split8(x, hi, lo);
-            *reinterpret_cast<uint4*>(sm + L::Hhi + mn_off(j8 * 8, d, DVS)) = hi;
-            *reinterpret_cast<uint4*>(sm + L::Hlo + mn_off(j8 * 8, d, DVS)) = lo;
+            const int jj = cb + j8 * 8;
+            *reinterpret_cast<uint4*>(sm + L::Hhi + mn_off(jj, d, DVS)) = hi;
+            *reinterpret_cast<uint4*>(sm + L::Hlo + mn_off(jj, d, DVS)) = lo;
             if (g) {
-                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + j8 * 8, D)) = hi;
-                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + j8 * 8, D)) = lo;
+                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + jj, D)) = hi;
+                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + jj, D)) = lo;
             }
         }
     };
     auto put_state = [&](float* dst) {
 #pragma unroll
-        for (int j4 = 0; j4 < DVS / 4; ++j4)
-            *reinterpret_cast<float4*>(dst + (size_t)d * D + j0 + 4 * j4) =
+        for (int j4 = 0; j4 < HALF / 4; ++j4)
+            *reinterpret_cast<float4*>(dst + (size_t)d * D + j0 + cb + 4 * j4) =
                 make_float4(Hreg[4 * j4], Hreg[4 * j4 + 1], Hreg[4 * j4 + 2], Hreg[4 * j4 + 3]);
     };
     put_h(0);
@@ -408,9 +419,11 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
-    const uint32_t acc4 = tmem, acc5 = tmem + DVS, acc6 = tmem + 2 * DVS;
-    uint32_t ph_mma = 0, ph_ldA = 0, ph_ldB = 0;
-    bool pendA = false, pendB = false, failed = false, mma_out = false;
+    auto acc4 = [&](int n) { return tmem + (uint32_t)((n & 1) * DVS); };
+    auto acc5 = [&](int n) { return tmem + (uint32_t)((2 + (n & 1)) * DVS); };
+    const uint32_t acc6 = tmem + 4 * DVS;
+    uint32_t ph_mma = 0, ph_pd = 0, ph_ldA = 0, ph_ldB = 0, ph_ldP = 0;
+    bool pendA = false, pendB = false, pendP = false, failed = false, mma_out = false, pd_out = false;
 
     auto issue_A = [&](int n) {
         const unsigned char* blk = blk_of(n);
@@ -423,20 +436,63 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         const unsigned char* blk = blk_of(n);
         mbar_expect_tx(bar_ldB, L::LoadB);
         bulk_g2s(sm + L::Kmn, blk + kOffKmn, 16384, bar_ldB);
-        bulk_g2s(sm + L::Phi, blk + kOffPhi, 8192, bar_ldB);
-        bulk_g2s(sm + L::Plo, blk + kOffPlo, 8192, bar_ldB);
         bulk_g2s(sm + L::U, blk + kOffU + (size_t)sp * 64 * DVS * 4, 64 * DVS * 4, bar_ldB);
+    };
+    auto issue_P = [&](int n) {
+        mbar_expect_tx(bar_ldP, L::LoadP);
+        bulk_g2s(sm + L::Phi, blk_of(n) + kOffPhi, 16384, bar_ldP);
+    };
+    // output rows of chunk m: o_r = G_r (scale qh_r) + (P Delta)_r
+    auto o_epilogue = [&](int m) -> bool {
+        const bool w = mbar_wait(bar_pd, ph_pd, a.err);
+        fence_after();
+        if (__syncthreads_or(!w)) return false;
+        ph_pd ^= 1u;
+        pd_out = false;
+        if (tid == 0 && m + 1 < nch) {  // P of chunk m is consumed
+            fence_async_smem();
+            issue_P(m + 1);
+        }
+        pendP = (m + 1 < nch);
+        const int t0 = seq0 + m * C, nrows = min(C, T - m * C);
+        float v[32];
+        if (quarter >= 2) {  // Q H rows (accumulator rows 64..127) -> sQ, scaled by G_r
+            tmem_ld32(taddr_of(acc4(m), warp, cb), v);
+            const int rr = d - 64;
+            const float gr = Gm[rr];
+#pragma unroll
+            for (int j4 = 0; j4 < HALF / 4; ++j4)
+                reinterpret_cast<float4*>(sQ)[(cb / 4 + j4) * 64 + rr] =
+                    make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
+                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
+                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
+                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
+        }
+        __syncthreads();
+        tmem_ld32(taddr_of(acc5(m), warp, cb), v);  // M = 64: row 16 quarter + lane, lanes < 16
+        const int r = quarter * 16 + lane;
+        if (lane < 16 && r < nrows && a.o) {
+            float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + cb;
+#pragma unroll
+            for (int j4 = 0; j4 < HALF / 4; ++j4) {
+                const float4 q4 = reinterpret_cast<const float4*>(sQ)[(cb / 4 + j4) * 64 + r];
+                *reinterpret_cast<float4*>(orow + 4 * j4) =
+                    make_float4(__fadd_rn(q4.x, v[4 * j4]), __fadd_rn(q4.y, v[4 * j4 + 1]),
+                                __fadd_rn(q4.z, v[4 * j4 + 2]), __fadd_rn(q4.w, v[4 * j4 + 3]));
+            }
+        }
+        return true;
     };
     if (nch > 0) {
         if (tid == 0) {
             issue_A(0);
             issue_B(0);
+            issue_P(0);
         }
-        pendA = pendB = true;
+        pendA = pendB = pendP = true;
     }
 
     for (int n = 0; n < nch; ++n) {
-        const int t0 = seq0 + n * C;
         const int nrows = min(C, T - n * C);
         const int Lr = nrows - 1;
         const bool last = (n == nch - 1);
@@ -445,12 +501,13 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         ph_ldA ^= 1u;
         pendA = false;
         if (tid == 0) {
-            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4hi, sm + L::Hhi, false);
-            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4hi, sm + L::Hlo, true);
-            mma_tile_mj<128, DVS, D, false, true>(acc4, sm + L::A4lo, sm + L::Hhi, true);
+            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hhi, false);
+            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hlo, true);
+            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4lo, sm + L::Hhi, true);
             mma_commit(bar_mma);
         }
         mma_out = true;
+        if (n > 0 && !o_epilogue(n - 1)) { failed = true; break; }
         if (tid < C) {
             Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
             dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
@@ -465,127 +522,101 @@ __global__ void __launch_bounds__(128) k_tc_state(TcArgs a) {
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_mma ^= 1u;
         mma_out = false;
-        if (tid == 0 && n + 1 < nch) {  // the A4 operand tiles of chunk n are consumed
+        if (tid == 0 && n + 1 < nch) {  // the A4 operand tiles and gam of chunk n are consumed
             fence_async_smem();
             issue_A(n + 1);
         }
         pendA = (n + 1 < nch);
-        {
-            // rows 0..63: Delta = U - W'H ; rows 64..127: qh
-            const int r = tid;
+        if (quarter < 2) {
+            // rows 0..63: Delta = U - W'H, columns cb .. cb + HALF
+            const int r = d;
             float v[32];
+            tmem_ld32(taddr_of(acc4(n), warp, cb), v);
+            const bool in = r < nrows;
+            float* cd = (a.cache && last && nrows < C && in)
+                            ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0 + cb
+                            : nullptr;
+            const float dr = dec[r];
 #pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(acc4, warp, c0), v);
-                if (r < 64) {
-                    const bool in = r < nrows;
-                    float* cd = (a.cache && last && nrows < C && in)
-                                    ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0 + c0
-                                    : nullptr;
-                    const float dr = dec[r];
+            for (int j8 = 0; j8 < HALF / 8; ++j8) {
+                float x[8], y[8];
+                const int jj = cb + j8 * 8;
+                const float4 u0 = reinterpret_cast<const float4*>(sU)[(jj / 4) * 64 + r];
+                const float4 u1 = reinterpret_cast<const float4*>(sU)[(jj / 4 + 1) * 64 + r];
+                const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-                    for (int j8 = 0; j8 < 4; ++j8) {
-                        float x[8], y[8];
-                        const float4 u0 = reinterpret_cast<const float4*>(sU)[((c0 + j8 * 8) / 4) * 64 + r];
-                        const float4 u1 = reinterpret_cast<const float4*>(sU)[((c0 + j8 * 8) / 4 + 1) * 64 + r];
-                        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
-                            y[e] = __fmul_rn(dr, x[e]);
-                        }
-                        {
-                            uint4 hi, lo;
-                            split8(x, hi, lo);
-                            *reinterpret_cast<uint4*>(sm + L::Dhi + mn_off(c0 + j8 * 8, r, DVS)) = hi;
-                            *reinterpret_cast<uint4*>(sm + L::Dlo + mn_off(c0 + j8 * 8, r, DVS)) = lo;
-                            if (a.train) {  // Delta rows for the backward, K-major (s, j)
-                                unsigned char* g = blk_of(n) + kOffDl + cm_off(r, j0 + c0 + j8 * 8, D);
-                                *reinterpret_cast<uint4*>(g) = hi;
-                                *reinterpret_cast<uint4*>(g + 16384) = lo;
-                            }
-                        }
-                        store8_split(sm + L::Bhi, sm + L::Blo, mn_off(c0 + j8 * 8, r, DVS), y);
-                        if (cd) {
-                            *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
-                            *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
-                        }
-                    }
-                } else {
-                    const int rr = r - 64;
-                    const float gr = Gm[rr];
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4)
-                        reinterpret_cast<float4*>(sQ)[(c0 / 4 + j4) * 64 + rr] =
-                            make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
-                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
-                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
-                                        __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
+                for (int e = 0; e < 8; ++e) {
+                    x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
+                    y[e] = __fmul_rn(dr, x[e]);
+                }
+                uint4 hi, lo;
+                split8(x, hi, lo);
+                *reinterpret_cast<uint4*>(sm + L::Dhi + mn_off(jj, r, DVS)) = hi;
+                *reinterpret_cast<uint4*>(sm + L::Dlo + mn_off(jj, r, DVS)) = lo;
+                if (a.train) {  // Delta rows for the backward, K-major (s, j)
+                    unsigned char* g = blk_of(n) + kOffDl + cm_off(r, j0 + jj, D);
+                    *reinterpret_cast<uint4*>(g) = hi;
+                    *reinterpret_cast<uint4*>(g + 16384) = lo;
+                }
+                store8_split(sm + L::Bhi, sm + L::Blo, mn_off(jj, r, DVS), y);
+                if (cd) {
+                    *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
+                    *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
                 }
             }
-            if (cstate && last && nrows < C) put_state(cstate);
         }
+        if (cstate && last && nrows < C) put_state(cstate);
         fence_async_smem();
         tc_sync();
+        ok = mbar_wait(bar_ldP, ph_ldP, a.err);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        ph_ldP ^= 1u;
+        pendP = false;
         if (tid == 0) {
-            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Phi, sm + L::Dhi, false);
-            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Phi, sm + L::Dlo, true);
-            mma_tile_mj<64, DVS, C, false, true>(acc5, sm + L::Plo, sm + L::Dhi, true);
-            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Bhi, false);
+            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Bhi, false);   // H' part
             mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Blo, true);
             mma_commit(bar_mma);
+            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Phi, sm + L::Dhi, false);  // P Delta
+            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Phi, sm + L::Dlo, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Plo, sm + L::Dhi, true);
+            mma_commit(bar_pd);
         }
         mma_out = true;
+        pd_out = true;
         ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_mma ^= 1u;
         mma_out = false;
-        if (tid == 0 && n + 1 < nch) {  // K, P, U and gam of chunk n are consumed
+        if (tid == 0 && n + 1 < nch) {  // K and U of chunk n are consumed
             fence_async_smem();
             issue_B(n + 1);
         }
         pendB = (n + 1 < nch);
         {
+            // H' = G_L H + K^T (dec . Delta): row d, columns cb .. cb + HALF
             float v[32];
-            // o rows: M = 64 accumulator, row r = 16 * warp + lane for lanes < 16
-            const int r = warp * 16 + lane;
+            tmem_ld32(taddr_of(acc6, warp, cb), v);
 #pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(acc5, warp, c0), v);
-                if (lane < 16 && r < nrows && a.o) {
-                    float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + c0;
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 q4 = reinterpret_cast<const float4*>(sQ)[(c0 / 4 + j4) * 64 + r];
-                        *reinterpret_cast<float4*>(orow + 4 * j4) =
-                            make_float4(__fadd_rn(q4.x, v[4 * j4]), __fadd_rn(q4.y, v[4 * j4 + 1]),
-                                        __fadd_rn(q4.z, v[4 * j4 + 2]), __fadd_rn(q4.w, v[4 * j4 + 3]));
-                    }
-                }
-            }
-            // H' = G_L H + K^T (dec . Delta): row d = tid
-#pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(acc6, warp, c0), v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) Hreg[c0 + j] = __fadd_rn(__fmul_rn(GL, Hreg[c0 + j]), v[j]);
-            }
+            for (int j = 0; j < HALF; ++j) Hreg[j] = __fadd_rn(__fmul_rn(GL, Hreg[j]), v[j]);
             put_h(n + 1);
             if (cstate && last && nrows == C) put_state(cstate);
         }
         fence_async_smem();
         tc_sync();
     }
+    if (!failed && nch > 0 && !o_epilogue(nch - 1)) failed = true;
     if (!failed && a.final_state) put_state(a.final_state + sh * D * D);
     if (failed) {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
         if (pendA) mbar_wait(bar_ldA, ph_ldA, a.err);
         if (pendB) mbar_wait(bar_ldB, ph_ldB, a.err);
+        if (pendP) mbar_wait(bar_ldP, ph_ldP, a.err);
         if (mma_out) mbar_wait(bar_mma, ph_mma, a.err);
+        if (pd_out) mbar_wait(bar_pd, ph_pd, a.err);
     }
     tc_sync();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, L::TmemCols);
 }
 
 }  // namespace tc

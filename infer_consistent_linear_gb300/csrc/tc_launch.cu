@@ -23,7 +23,7 @@ cudaError_t state(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
     const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
     if (grid > 0) {
         ProfScope ps("cpr_tc_state", st);
-        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+        kern<<<(unsigned)grid, 256, sm, st>>>(a);
     }
     return cudaGetLastError();
 }
@@ -83,9 +83,12 @@ cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st) {
 }
 
 cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cmax, int n_seq, int H,
-                        cudaStream_t st) {
-    cudaError_t e = tc_forward(f, cmax, n_seq, H, st);
-    if (e != cudaSuccess) return e;
+                        cudaStream_t st, bool recompute) {
+    cudaError_t e = cudaSuccess;
+    if (recompute) {
+        e = tc_forward(f, cmax, n_seq, H, st);
+        if (e != cudaSuccess) return e;
+    }
     switch (f.dvs) {
         case 64: e = state_bwd<64>(b, n_seq, H, st); break;
         case 32: e = state_bwd<32>(b, n_seq, H, st); break;

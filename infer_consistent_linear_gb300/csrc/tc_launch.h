@@ -13,7 +13,8 @@ cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cuda
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st);
 // Training forward (prep + state pass writing the backward's tiles), reverse
 // state pass and per-chunk gradients; `f` must have train set and
-// blk_bytes = kBlockTrain, `b.ws` the same workspace blocks.
+// blk_bytes = kBlockTrain, `b.ws` the same workspace blocks.  Without
+// `recompute` the blocks must already hold a training forward's tiles.
 cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cmax, int n_seq, int H,
-                        cudaStream_t st);
+                        cudaStream_t st, bool recompute = true);
 }  // namespace cpr

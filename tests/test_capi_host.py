@@ -144,3 +144,22 @@ def test_host_argument_errors(lib):
     assert lib.cpr_gdn_prefill(ctypes.byref(c), dig, *good[:6], 1, 64, 1, None, good[6], None,
                                None, good[7], 1 << 30, None) == 1   # cache required
     assert lib.cpr_gdn_decode_step(ctypes.byref(c), dig, *good[:5], 1, 1, None, good[6], None) == 1
+
+
+def test_training_forward_and_saved_backward_need_tc_contract(lib):
+    c = cpr.default_contract(torch.bfloat16, 128)          # SIMT policy
+    dig = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(c))
+    p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    rc = lib.cpr_gdn_fwd_train(ctypes.byref(c), dig, *p[:6], 1, 64, 1, None, p[6], None, p[7],
+                               1 << 40, None)
+    assert rc == 2 and "tensor-core" in lib.cpr_last_error().decode()
+    rc = lib.cpr_gdn_bwd_saved(ctypes.byref(c), dig, *p[:6], 1, 64, 1, None, p[6], None,
+                               *[ctypes.c_void_p(0x20000 * (i + 1)) for i in range(6)], p[7], 1 << 40, None)
+    assert rc == 2
+    t = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=2)
+    dt = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(t))
+    small = cpr.workspace_bytes(t, cpr.CPR_OP_FWD, 1, 64, 1)
+    assert cpr.workspace_bytes(t, cpr.CPR_OP_BWD, 1, 64, 1) > small
+    rc = lib.cpr_gdn_fwd_train(ctypes.byref(t), dt, *p[:6], 1, 64, 1, None, p[6], None, p[7],
+                               small, None)
+    assert rc == 7                                          # a forward-sized workspace is too small

@@ -146,3 +146,27 @@ def test_tc_backward_deterministic_and_batch_invariant():
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             assert_bitwise(f"{n}[seq {i}]", one[n], a[n][lo:hi])
         assert_bitwise(f"dh0[seq {i}]", one["dh0"], a["dh0"][i:i + 1])
+
+
+def test_tc_training_forward_and_saved_backward_are_bitwise_the_plain_calls():
+    lens = [200, 64, 1, 130]
+    x = make_inputs(lens, 2, 128, 128, io_dtype=torch.bfloat16, seed=9, h0_std=0.1, with_grad=True)
+    xd = x.to(DEV)
+    c = _tc()
+    gen = torch.Generator().manual_seed(3)
+    dHT = torch.randn(len(lens), 2, 128, 128, generator=gen).to(DEV)
+    o, fin = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    ref = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0, dHT=dHT,
+                          contract=c)
+    ws = torch.empty(cpr.workspace_bytes(c, cpr.CPR_OP_BWD, len(lens), sum(lens), 2),
+                     dtype=torch.uint8, device=DEV)
+    o2, fin2 = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c,
+                               workspace=ws, train=True)
+    got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0, dHT=dHT,
+                          contract=c, workspace=ws, saved=True)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    assert_bitwise("o", o2, o)
+    assert_bitwise("final", fin2, fin)
+    for n in GRADS:
+        assert_bitwise(n, got[n], ref[n])
