@@ -76,10 +76,13 @@ struct SbSmem {
     static constexpr size_t Total = Bar + 64;
 };
 
+// 256 threads: warp w reads TMEM lane quarter w % 4, the two warps of a
+// quarter one half of the DVS columns each.
 template <int DVS>
-__global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
+__global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
     using L = SbSmem<DVS>;
     constexpr int NSPLIT = D / DVS;
+    constexpr int HALF = DVS / 2;
     extern __shared__ __align__(1024) unsigned char sm[];
     float* gam = reinterpret_cast<float*>(sm + L::Vec);
     float* Gm = gam + 64;
@@ -99,6 +102,7 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
     const int b = blockIdx.x / (NSPLIT * H);
     const int j0 = sp * DVS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, cb = (warp >> 2) * HALF;
     const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
     const int coff = a.chunk_off[b];
     const int nch = a.chunk_off[b + 1] - coff;
@@ -110,30 +114,31 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
         for (int i = 0; i < 5; ++i) mbar_init(bar_mma + i, 1);
         mbar_init_fence();
     }
-    // dL/dH of the last chunk's end state, row d = tid, columns j0..j0+DVS
-    float dHreg[DVS];
-    const int d = tid;
+    // dL/dH of the last chunk's end state, row d, columns j0 + cb .. + HALF
+    float dHreg[HALF];
+    const int d = quarter * 32 + lane;
 #pragma unroll
-    for (int j4 = 0; j4 < DVS / 4; ++j4) {
+    for (int j4 = 0; j4 < HALF / 4; ++j4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.dHT) x = *reinterpret_cast<const float4*>(a.dHT + (sh * D + d) * D + j0 + 4 * j4);
+        if (a.dHT) x = *reinterpret_cast<const float4*>(a.dHT + (sh * D + d) * D + j0 + cb + 4 * j4);
         dHreg[4 * j4] = x.x; dHreg[4 * j4 + 1] = x.y; dHreg[4 * j4 + 2] = x.z; dHreg[4 * j4 + 3] = x.w;
     }
     // dH' as the B operand of K dH'; also chunk nn's dH' tiles for k_tc_grad
     auto put_dh = [&](int nn) {
         unsigned char* g = (nn >= 0) ? blk_of(nn) + kOffdH : nullptr;
 #pragma unroll
-        for (int j8 = 0; j8 < DVS / 8; ++j8) {
+        for (int j8 = 0; j8 < HALF / 8; ++j8) {
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = dHreg[j8 * 8 + e];
             uint4 hi, lo;
             split8(x, hi, lo);
-            *reinterpret_cast<uint4*>(sm + L::dHhi + mn_off(j8 * 8, d, DVS)) = hi;
-            *reinterpret_cast<uint4*>(sm + L::dHlo + mn_off(j8 * 8, d, DVS)) = lo;
+            const int jj = cb + j8 * 8;
+            *reinterpret_cast<uint4*>(sm + L::dHhi + mn_off(jj, d, DVS)) = hi;
+            *reinterpret_cast<uint4*>(sm + L::dHlo + mn_off(jj, d, DVS)) = lo;
             if (g) {
-                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + j8 * 8, D)) = hi;
-                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + j8 * 8, D)) = lo;
+                *reinterpret_cast<uint4*>(g + cm_off(d, j0 + jj, D)) = hi;
+                *reinterpret_cast<uint4*>(g + 32768 + cm_off(d, j0 + jj, D)) = lo;
             }
         }
     };
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
     // dO rows of chunk n (columns j0..j0+DVS) into the staging area, zero past the end
     auto issue_dO = [&](int n) {
         const int t0 = seq0 + n * C, nrows = min(C, T - n * C);
-        for (int i = tid; i < 64 * (DVS / 4); i += 128) {
+        for (int i = tid; i < 64 * (DVS / 4); i += 256) {
             const int r = i / (DVS / 4), q4 = i % (DVS / 4);  // a row's 16-byte pieces side by side
             const bool in = r < nrows;
             const float* src = a.dO + (in ? ((size_t)(t0 + r) * H + h) * D + j0 + 4 * q4 : 0);
@@ -191,8 +196,8 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
     if (nch > 0 && ((nch - 1) & 1)) { pendKQ[0] = nch > 1; pendKQ[1] = true; }
     bool failed = false;
     const float scale = a.scale;
-    // M = 64 accumulator rows: lanes 0..15 of each warp
-    const int r64 = warp * 16 + lane;
+    // M = 64 accumulator rows: lanes 0..15 of each lane quarter
+    const int r64 = quarter * 16 + lane;
 
     for (int it = 0; it < nch; ++it) {
         const int n = nch - 1 - it;
@@ -205,24 +210,29 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_P ^= 1u;
         pendP = false;
-        if (tid < C) {
-            const bool in = tid < nrows;
-            const float gr = gam[tid];
-            Gm[tid] = in ? simt::gate(gr) : 0.f;
-            dec[tid] = in ? simt::decay(gam[Lr], gr) : 0.f;
-            bgv[tid] = in ? simt::bg_entry(bcur, gr) : 0.f;
-            // dO (B1) and G scale dO (B2) rows, MN-major (j, t)
-            const float gs = __fmul_rn(Gm[tid], scale);
+        {
+            // token row rr, a quarter of the columns per thread: dO (B1) and G scale dO
+            // (B2) rows, MN-major (j, t)
+            const int rr = tid & 63, part = tid >> 6;
+            const bool in = rr < nrows;
+            const float gr = gam[rr];
+            const float Gr = in ? simt::gate(gr) : 0.f;
+            if (part == 0) {
+                Gm[rr] = Gr;
+                dec[rr] = in ? simt::decay(gam[Lr], gr) : 0.f;
+                bgv[rr] = in ? simt::bg_entry(bcur, gr) : 0.f;
+            }
+            const float gs = __fmul_rn(Gr, scale);
 #pragma unroll
-            for (int j8 = 0; j8 < DVS / 8; ++j8) {
-                const float4 u0 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8) * 64 + tid];
-                const float4 u1 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8 + 1) * 64 + tid];
+            for (int j8 = part * (DVS / 32); j8 < (part + 1) * (DVS / 32); ++j8) {
+                const float4 u0 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8) * 64 + rr];
+                const float4 u1 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8 + 1) * 64 + rr];
                 const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(gs, x[e]);
-                store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(j8 * 8, tid, DVS), x);
-                store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(j8 * 8, tid, DVS), y);
+                store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(j8 * 8, rr, DVS), x);
+                store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(j8 * 8, rr, DVS), y);
             }
         }
         const float GL = simt::gate(gam[Lr]);
@@ -259,21 +269,18 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
         }
         pendP = n > 0;
         {
-            // dDelta = P^T dO + dec . (K dH') -> B1 (MN-major (j, t))
+            // dDelta = P^T dO + dec . (K dH') -> B1 (MN-major (j, t)), this thread's columns
             float v1[32], v2[32];
+            tmem_ld32(taddr_of(tD1, warp, cb), v1);
+            tmem_ld32(taddr_of(tD2, warp, cb), v2);
+            if (lane < 16) {
+                const float dr = dec[r64];
 #pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(tD1, warp, c0), v1);
-                tmem_ld32(taddr_of(tD2, warp, c0), v2);
-                if (lane < 16) {
-                    const float dr = dec[r64];
+                for (int j8 = 0; j8 < HALF / 8; ++j8) {
+                    float x[8];
 #pragma unroll
-                    for (int j8 = 0; j8 < 4; ++j8) {
-                        float x[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = __fmaf_rn(dr, v2[j8 * 8 + e], v1[j8 * 8 + e]);
-                        store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(c0 + j8 * 8, r64, DVS), x);
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = __fmaf_rn(dr, v2[j8 * 8 + e], v1[j8 * 8 + e]);
+                    store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(cb + j8 * 8, r64, DVS), x);
                 }
             }
         }
@@ -304,25 +311,23 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
             // dR rows: to the workspace (K-major (r, j) hi/lo) and -bg . dR -> B2
             unsigned char* gdr = blk_of(n) + kOffdR;
             float v1[32];
+            tmem_ld32(taddr_of(tR, warp, cb), v1);
+            if (lane < 16) {
+                const float nb = -bgv[r64];
 #pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(tR, warp, c0), v1);
-                if (lane < 16) {
-                    const float nb = -bgv[r64];
+                for (int j8 = 0; j8 < HALF / 8; ++j8) {
+                    float x[8], y[8];
 #pragma unroll
-                    for (int j8 = 0; j8 < 4; ++j8) {
-                        float x[8], y[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            x[e] = v1[j8 * 8 + e];
-                            y[e] = __fmul_rn(nb, x[e]);
-                        }
-                        uint4 hi, lo;
-                        split8(x, hi, lo);
-                        *reinterpret_cast<uint4*>(gdr + cm_off(r64, j0 + c0 + j8 * 8, D)) = hi;
-                        *reinterpret_cast<uint4*>(gdr + 16384 + cm_off(r64, j0 + c0 + j8 * 8, D)) = lo;
-                        store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(c0 + j8 * 8, r64, DVS), y);
+                    for (int e = 0; e < 8; ++e) {
+                        x[e] = v1[j8 * 8 + e];
+                        y[e] = __fmul_rn(nb, x[e]);
                     }
+                    uint4 hi, lo;
+                    split8(x, hi, lo);
+                    const int jj = cb + j8 * 8;
+                    *reinterpret_cast<uint4*>(gdr + cm_off(r64, j0 + jj, D)) = hi;
+                    *reinterpret_cast<uint4*>(gdr + 16384 + cm_off(r64, j0 + jj, D)) = lo;
+                    store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(jj, r64, DVS), y);
                 }
             }
         }
@@ -345,14 +350,11 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
         }
         if (n >= 2) pendKQ[cur] = true;
         {
-            // dH = G_L dH' + acc, row d = tid
+            // dH = G_L dH' + acc, row d, this thread's columns
             float v1[32];
+            tmem_ld32(taddr_of(tH, warp, cb), v1);
 #pragma unroll
-            for (int c0 = 0; c0 < DVS; c0 += 32) {
-                tmem_ld32(taddr_of(tH, warp, c0), v1);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dHreg[c0 + j] = __fmaf_rn(GL, dHreg[c0 + j], v1[j]);
-            }
+            for (int j = 0; j < HALF; ++j) dHreg[j] = __fmaf_rn(GL, dHreg[j], v1[j]);
             put_dh(n - 1);
         }
         fence_async_smem();
@@ -360,8 +362,8 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
     }
     if (!failed) {
 #pragma unroll
-        for (int j4 = 0; j4 < DVS / 4; ++j4)
-            *reinterpret_cast<float4*>(a.dh0 + (sh * D + d) * D + j0 + 4 * j4) =
+        for (int j4 = 0; j4 < HALF / 4; ++j4)
+            *reinterpret_cast<float4*>(a.dh0 + (sh * D + d) * D + j0 + cb + 4 * j4) =
                 make_float4(dHreg[4 * j4], dHreg[4 * j4 + 1], dHreg[4 * j4 + 2], dHreg[4 * j4 + 3]);
     } else {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
@@ -377,20 +379,30 @@ __global__ void __launch_bounds__(128) k_tc_state_bwd(TcBwdArgs a) {
 }
 
 // ---- per-chunk gradients -------------------------------------------------------------------
+// 256 threads.  Accumulator row L (TMEM lane L) is read by warps L / 32 and
+// L / 32 + 4, each taking half of the columns.  Rows 0..63 ("top") carry the
+// dO / Q-side quantities of token r = L, rows 64..127 ("bottom") the dR /
+// K-side ones of token r = L - 64.
 struct GradSmem {
     static constexpr size_t QK = 0;            // [Q | K] K-major: Q rows 0..63, K rows 64..127
     static constexpr size_t Rhi = 32768;       // [dO | dR | Delta] K-major 192 x 128, hi
     static constexpr size_t Rlo = 81920;       // lo
     static constexpr size_t Bt = 131072;       // H_n, then dH': K-major (d, j), hi then lo
-    static constexpr size_t Scr = 196608;      // 64 x 65 fp32
+    static constexpr size_t Scr = 196608;      // 64 x 65 fp32: t_rs
     static constexpr size_t Vec = Scr + 64 * 65 * 4;
-    static constexpr int kVec = 13;            // 64-float vectors
-    static constexpr size_t Red = Vec + kVec * 256;
-    static constexpr size_t Bar = Red + 1024;  // 2 mbarriers + TMEM base
+    static constexpr int kVec = 22;            // 64-float vectors
+    static constexpr size_t Bar = Vec + kVec * 256;   // 2 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
 
-static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
+// Sum over the 32 lanes of a warp in a fixed tree (lane 0 gets the result).
+__device__ __forceinline__ float warp_sum_tree(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, o));
+    return x;
+}
+
+static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     using L = GradSmem;
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char* QK = sm + L::QK;
@@ -399,10 +411,11 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
     unsigned char* Bt = sm + L::Bt;
     float* scr = reinterpret_cast<float*>(sm + L::Scr);
     float* vec = reinterpret_cast<float*>(sm + L::Vec);
+    // [2][64] vectors hold the two column halves' partial sums of a row
     float *gam = vec, *Gm = vec + 64, *bet = vec + 128, *bgv = vec + 192, *dec = vec + 256,
-          *qh = vec + 320, *kh = vec + 384, *rowB = vec + 448, *colE = vec + 512, *eL = vec + 576,
-          *dbA = vec + 640, *dRv = vec + 704, *dgam = vec + 768;
-    float* red = reinterpret_cast<float*>(sm + L::Red);
+          *qh = vec + 320, *kh = vec + 448, *rowA = vec + 576, *rowB = vec + 704, *dbA = vec + 832,
+          *dRv = vec + 960, *colE = vec + 1024, *eL = vec + 1088, *dgam = vec + 1216,
+          *red = vec + 1280;   // red: 8 warp sums; 1288 floats in all
     uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + L::Bar);
     uint64_t* bar_mma = bar_ld + 1;
     uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_ld + 2);
@@ -416,7 +429,11 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
     const int t0 = seq0 + n * C;
     const int nrows = min(C, T - n * C);
     const int Lr = nrows - 1;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;       // accumulator row / TMEM lane
+    const bool top = row < 64;
+    const int r = row & 63;                    // token row of the chunk
     const unsigned char* blk = a.ws + ((size_t)cidx * H + h) * kBlockTrain;
     const float scale = a.scale;
 
@@ -436,12 +453,12 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(gam, blk + kOffGam, 256, bar_ld);
     }
     // dO rows (zero past the chunk's end) split into R rows 0..63
-#pragma unroll 8
-    for (int i = tid; i < 64 * (D / 8); i += 128) {
-        const int r = i / (D / 8), d8 = i % (D / 8);
+#pragma unroll 4
+    for (int i = tid; i < 64 * (D / 8); i += 256) {
+        const int rr = i / (D / 8), d8 = i % (D / 8);
         float x[8];
-        if (r < nrows) {
-            const float4* src = reinterpret_cast<const float4*>(a.dO + ((size_t)(t0 + r) * H + h) * D + d8 * 8);
+        if (rr < nrows) {
+            const float4* src = reinterpret_cast<const float4*>(a.dO + ((size_t)(t0 + rr) * H + h) * D + d8 * 8);
             const float4 u0 = src[0], u1 = src[1];
             x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
             x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
@@ -449,13 +466,13 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
-        store8_split(Rhi, Rlo, cm_off(r, d8 * 8, D), x);
+        store8_split(Rhi, Rlo, cm_off(rr, d8 * 8, D), x);
     }
     if (tid < C) bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     const uint32_t tX1 = 0, tG = 128, tS1 = 192, tX2 = 256, tdq = 384, tdk = 128;
     uint32_t tmem = 0;
     int ld_out = 0, mma_out = -1;   // mbarrier phases still to complete (-1: none)
-    float rowA = 0.f;               // sum_{s<r} dP_rs P_rs of row r = tid (tid < 64)
+    float bloc[32];                 // bottom rows: b_r dA_rs Kd_rs for this thread's columns
     {
         const bool ok = mbar_wait(bar_ld, 0, a.err);
         fence_async_smem();
@@ -494,51 +511,48 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(Bt, blk + kOffdH, 65536, bar_ld);
     }
     ld_out = 1;
-    // ---- phase A: row quantities (thread r < 64: the dO / Q rows; 64 + r: the dR / K rows)
     {
-        const int r = tid & 63;
-        const bool top = tid < 64;
+        // ---- phase A: one pass over this thread's 32 columns s of the row
+        const int s0 = hf * 32;
         const float gr = gam[r], br = bet[r];
         float v1[32], v2[32];
-        for (int c0 = 0; c0 < C; c0 += 32) {
-            tmem_ld32(taddr_of(tmem + tS1, warp, c0), v1);
-            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
-            if (top) {
+        tmem_ld32(taddr_of(tmem + tS1, warp, s0), v1);
+        tmem_ld32(taddr_of(tmem + tG, warp, s0), v2);
+        float sa = 0.f, sb = 0.f;
 #pragma unroll
-                for (int j8 = 0; j8 < 4; ++j8) {
-                    float x[8];
+        for (int j8 = 0; j8 < 4; ++j8) {
+            float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = c0 + j8 * 8 + e, j = j8 * 8 + e;
-                        const bool in = s <= r && r < nrows;
-                        const float E = in ? simt::decay(gr, gam[s]) : 0.f;
-                        const float P = __fmul_rn(E, __fmul_rn(scale, v1[j]));
-                        const float dP = in ? v2[j] : 0.f;
-                        const float t = (s < r) ? __fmul_rn(dP, P) : 0.f;
-                        scr[r * 65 + s] = t;
-                        if (s < r) rowA = __fadd_rn(rowA, t);
-                        x[e] = __fmul_rn(E, dP);   // G1 = E . dP
-                    }
-                    store8_split(Rhi, Rlo, cm_off(r, c0 + j8 * 8, C), x);
-                }
-            } else {
-                float sa = 0.f, sb = 0.f;
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c0 + j;
+            for (int e = 0; e < 8; ++e) {
+                const int s = s0 + j8 * 8 + e, j = j8 * 8 + e;
+                if (top) {
+                    const bool in = s <= r && r < nrows;
+                    const float E = in ? simt::decay(gr, gam[s]) : 0.f;
+                    const float P = __fmul_rn(E, __fmul_rn(scale, v1[j]));
+                    const float dP = in ? v2[j] : 0.f;
+                    const float t = (s < r) ? __fmul_rn(dP, P) : 0.f;
+                    scr[r * 65 + s] = t;
+                    sa = __fadd_rn(sa, t);
+                    x[e] = __fmul_rn(E, dP);                        // G1 = E . dP
+                } else {
                     const bool in = s < r && r < nrows;
-                    const float Kd = in ? __fmul_rn(simt::decay(gr, gam[s]), v1[j]) : 0.f;
+                    const float E = in ? simt::decay(gr, gam[s]) : 0.f;
+                    const float Kd = __fmul_rn(E, v1[j]);
                     const float dA = in ? -v2[j] : 0.f;
-                    sa = __fmaf_rn(dA, Kd, sa);
-                    sb = __fmaf_rn(__fmul_rn(br, dA), Kd, sb);
+                    sa = __fmaf_rn(dA, Kd, sa);                      // dbA part
+                    bloc[j] = __fmul_rn(__fmul_rn(br, dA), Kd);
+                    sb = __fadd_rn(sb, bloc[j]);                     // rowB part
+                    x[e] = __fmul_rn(__fmul_rn(br, E), dA);         // G2 = b E dA
                 }
-                if (c0 == 0) { dbA[r] = sa; rowB[r] = sb; }
-                else { dbA[r] = __fadd_rn(dbA[r], sa); rowB[r] = __fadd_rn(rowB[r], sb); }
             }
+            // [G1; G2] K-major 128 x 64 tile: G1 in rows 0..63, G2 in rows 64..127
+            store8_split(Rhi, Rlo, cm_off(row, s0 + j8 * 8, C), x);
         }
-        // q^_r . (dO H^T)_r (top) and k_r . (dR H^T)_r (bottom)
+        // q^_r . (dO H^T)_r (top) or k_r . (dR H^T)_r (bottom), this thread's 64 columns
         const unsigned char* qrow = QK + (top ? 0 : 16384);
         float acc = 0.f;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c = 0; c < 2; ++c) {
+            const int c0 = hf * 64 + c * 32;
             tmem_ld32(taddr_of(tmem + tX1, warp, c0), v1);
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {
@@ -550,30 +564,50 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
             }
         }
         if (top) {
-            qh[r] = acc;
+            rowA[hf * 64 + r] = sa;
+            qh[hf * 64 + r] = acc;
         } else {
-            kh[r] = acc;
-            // dR row: dv = b dR, and dR . v
-            float dv8[8], s = 0.f;
-            const bool in = r < nrows;
-#pragma unroll 4
-            for (int d8 = 0; d8 < D / 8; ++d8) {
-                const uint32_t off = cm_off(r, d8 * 8, D);
-                join8(*reinterpret_cast<const uint4*>(Rhi + 16384 + off),
-                      *reinterpret_cast<const uint4*>(Rlo + 16384 + off), dv8);
-                if (in) {
-                    float vv[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.v + ((size_t)(t0 + r) * H + h) * D + d8 * 8), vv);
+            dbA[hf * 64 + r] = sa;
+            rowB[hf * 64 + r] = sb;
+            kh[hf * 64 + r] = acc;
+        }
+    }
+    __syncthreads();
+    if (!top) {  // t_rs = dP_rs P_rs (written above) + b_r dA_rs Kd_rs
+        const int s0 = hf * 32;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) s = __fmaf_rn(dv8[e], vv[e], s);
-                    float* dvr = a.dv + ((size_t)(t0 + r) * H + h) * D + d8 * 8;
-                    *reinterpret_cast<float4*>(dvr) = make_float4(__fmul_rn(br, dv8[0]), __fmul_rn(br, dv8[1]),
-                                                                  __fmul_rn(br, dv8[2]), __fmul_rn(br, dv8[3]));
-                    *reinterpret_cast<float4*>(dvr + 4) = make_float4(__fmul_rn(br, dv8[4]), __fmul_rn(br, dv8[5]),
-                                                                      __fmul_rn(br, dv8[6]), __fmul_rn(br, dv8[7]));
-                }
+        for (int j = 0; j < 32; ++j) scr[r * 65 + s0 + j] = __fadd_rn(scr[r * 65 + s0 + j], bloc[j]);
+    }
+    __syncthreads();
+    if (tid < C) {  // column sums colE_s = sum_{r > s} t_rs
+        const int s = tid;
+        float acc = 0.f;
+        for (int rr = s + 1; rr < nrows; ++rr) acc = __fadd_rn(acc, scr[rr * 65 + s]);
+        colE[s] = acc;
+    } else if (tid >= 128) {
+        // dv = b dR and dR . v, a warp per row, 16-byte pieces side by side
+        const int t = tid - 128;
+        for (int rr = t >> 5; rr < nrows; rr += 4) {
+            const int c4 = (t & 31) * 4;
+            const uint32_t off = cm_off(rr, c4, D);
+            const uint2 hi = *reinterpret_cast<const uint2*>(Rhi + 16384 + off);
+            const uint2 lo = *reinterpret_cast<const uint2*>(Rlo + 16384 + off);
+            const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&hi);
+            const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&lo);
+            const size_t g = ((size_t)(t0 + rr) * H + h) * D + c4;
+            const uint2 vv = *reinterpret_cast<const uint2*>(a.v + g);
+            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vv);
+            const float brr = bet[rr];
+            float x[4], sdot = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[e] = __fadd_rn(__bfloat162float(hh[e]), __bfloat162float(ll[e]));
+                sdot = __fmaf_rn(x[e], __bfloat162float(vb[e]), sdot);
             }
-            dRv[r] = s;
+            *reinterpret_cast<float4*>(a.dv + g) =
+                make_float4(__fmul_rn(brr, x[0]), __fmul_rn(brr, x[1]), __fmul_rn(brr, x[2]), __fmul_rn(brr, x[3]));
+            sdot = warp_sum_tree(sdot);
+            if ((t & 31) == 0) dRv[rr] = sdot;
         }
     }
     {
@@ -589,52 +623,13 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
         mma_commit(bar_mma);
     }
     mma_out = 1;
-    // ---- phase B: t_rs += b_r dA_rs Kd_rs (the bottom rows' half of the E terms)
     {
-        const int r = tid & 63;
-        float v1[32], v2[32];
-        for (int c0 = 0; c0 < C; c0 += 32) {
-            tmem_ld32(taddr_of(tmem + tS1, warp, c0), v1);
-            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
-            if (tid >= 64) {
-                const float gr = gam[r], br = bet[r];
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c0 + j;
-                    if (s < r && r < nrows) {
-                        const float Kd = __fmul_rn(simt::decay(gr, gam[s]), v1[j]);
-                        scr[r * 65 + s] = __fadd_rn(scr[r * 65 + s], __fmul_rn(__fmul_rn(br, -v2[j]), Kd));
-                    }
-                }
-            }
-        }
-    }
-    __syncthreads();
-    if (tid < C) {  // phase C: column sums
-        const int s = tid;
+        // <dH', H_n>: row d = tid & 127, half of the columns per thread; H_n again from
+        // the workspace (just bulk-read, so mostly in L2), dH' from shared memory
+        const int d = tid & 127, jh = tid >> 7;
         float acc = 0.f;
-        for (int r = s + 1; r < nrows; ++r) acc = __fadd_rn(acc, scr[r * 65 + s]);
-        colE[s] = acc;
-    }
-    __syncthreads();
-    {
-        // phase D: G2_rs = b_r E_rs dA_rs (bottom rows) into the scratch; <dH', H_n> partials
-        const int r = tid & 63;
-        float v2[32];
-        for (int c0 = 0; c0 < C; c0 += 32) {
-            tmem_ld32(taddr_of(tmem + tG, warp, c0), v2);
-            if (tid >= 64) {
-                const float gr = gam[r], br = bet[r];
-                for (int j = 0; j < 32; ++j) {
-                    const int s = c0 + j;
-                    const bool in = s < r && r < nrows;
-                    scr[r * 65 + s] = in ? __fmul_rn(__fmul_rn(br, simt::decay(gr, gam[s])), -v2[j]) : 0.f;
-                }
-            }
-        }
-        const int d = tid;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int j8 = 0; j8 < D / 8; ++j8) {
+#pragma unroll
+        for (int j8 = jh * 8; j8 < jh * 8 + 8; ++j8) {
             const uint32_t off = cm_off(d, j8 * 8, D);
             float hv[8], dv8[8];
             join8(*reinterpret_cast<const uint4*>(blk + kOffHn + off),
@@ -643,7 +638,8 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc = __fmaf_rn(dv8[e], hv[e], acc);
         }
-        red[d] = acc;
+        acc = warp_sum_tree(acc);
+        if (lane == 0) red[warp] = acc;
     }
     {
         const bool ok = mbar_wait(bar_mma, 1, a.err);
@@ -652,32 +648,27 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
     }
     mma_out = -1;
     {
-        // phase E: A tiles of the last MMA group (R rows 16 KB.. are free now), e_s
-        const int r = tid & 63;
-        if (tid < 64) {  // (scale G1)^T, MN-major (mn = 64 + s, k = r)
-            for (int s8 = 0; s8 < C / 8; ++s8) {
-                float x[8];
-                join8(*reinterpret_cast<const uint4*>(Rhi + cm_off(r, s8 * 8, C)),
-                      *reinterpret_cast<const uint4*>(Rlo + cm_off(r, s8 * 8, C)), x);
+        // ---- phase E: MN-major A tiles (mn = 64 + s, k = r) of (scale G1)^T and G2^T from
+        // the [G1; G2] tile's rows, interleaved in the dR / Delta space (free now: X2 is done);
+        // e_s = dec_s k_s . (Delta dH'^T)_s
+        unsigned char* mhi = Rhi + 16384 + (top ? 0 : 1024);
+        unsigned char* mlo = Rlo + 16384 + (top ? 0 : 1024);
+#pragma unroll
+        for (int s8 = hf * 4; s8 < hf * 4 + 4; ++s8) {
+            float x[8];
+            join8(*reinterpret_cast<const uint4*>(Rhi + cm_off(row, s8 * 8, C)),
+                  *reinterpret_cast<const uint4*>(Rlo + cm_off(row, s8 * 8, C)), x);
+            if (top) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(scale, x[e]);
-                store8_split(Rhi + 16384, Rlo + 16384, mn_off(64 + s8 * 8, r, 128), x);
             }
-        } else {  // G2 + G2^T, MN-major (mn = 64 + s, k = r)
-            for (int s8 = 0; s8 < C / 8; ++s8) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = s8 * 8 + e;
-                    x[e] = __fadd_rn(scr[s * 65 + r], scr[r * 65 + s]);
-                }
-                store8_split(Rhi + 32768, Rlo + 32768, mn_off(64 + s8 * 8, r, 128), x);
-            }
+            store8_split(mhi, mlo, mn_off(64 + s8 * 8, r, 128), x);
         }
         float v1[32], acc = 0.f;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c = 0; c < 2; ++c) {
+            const int c0 = hf * 64 + c * 32;
             tmem_ld32(taddr_of(tmem + tX2, warp, c0), v1);
-            if (tid >= 64) {
+            if (!top) {
 #pragma unroll
                 for (int j8 = 0; j8 < 4; ++j8) {
                     float kv[8];
@@ -687,44 +678,53 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
                 }
             }
         }
-        if (tid >= 64) eL[r] = (r < Lr) ? __fmul_rn(dec[r], acc) : 0.f;
-        if (tid == 0) {
-            float s = 0.f;
-            for (int i = 0; i < 128; ++i) s = __fadd_rn(s, red[i]);
-            red[128] = s;
-        }
+        if (!top) eL[hf * 64 + r] = acc;
     }
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        mma_tile_mj<128, 128, C, false, true>(tmem + tdq, Rhi, QK + 16384, false);          // G1 K
+        // interleaved MN-major tiles: (scale G1)^T at +0, G2^T at +1 KB (its garbage halves
+        // lie on the other tile's rows, which no read of this accumulator uses)
+        mma_tile_mj<128, 128, C, false, true>(tmem + tdq, Rhi, QK + 16384, false);          // [G1; G2] K
         mma_tile_mj<128, 128, C, false, true>(tmem + tdq, Rlo, QK + 16384, true);
         mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rhi + 16384, QK, false);           // (s G1)^T Q
         mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 16384, QK, true);
-        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rhi + 32768, QK + 16384, true);    // (G2 + G2^T) K
-        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 32768, QK + 16384, true);
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rhi + 16384 + 1024, QK + 16384, true);  // G2^T K
+        mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 16384 + 1024, QK + 16384, true);
         mma_commit(bar_mma);
     }
     mma_out = 0;
-    if (tid < C) {  // gate and beta gradients of row r
-        const int r = tid;
-        const float kr = kh[r];
-        const float dG = __fsub_rn(qh[r], __fmul_rn(bet[r], kr));
-        const float dbR = __fsub_rn(dRv[r], __fmul_rn(Gm[r], kr));
-        float dgr = __fsub_rn(__fadd_rn(__fmul_rn(Gm[r], dG), __fadd_rn(rowA, rowB[r])), colE[r]);
-        dgr = __fsub_rn(dgr, eL[r]);
-        if (r == Lr) {
-            float sumL = 0.f;
-            for (int s = 0; s < Lr; ++s) sumL = __fadd_rn(sumL, eL[s]);
-            dgr = __fadd_rn(dgr, __fadd_rn(__fmul_rn(Gm[Lr], red[128]), sumL));
+    if (tid < C) {  // gate and beta gradients of row r = tid
+        const int rr = tid;
+        const float kr = __fadd_rn(kh[rr], kh[64 + rr]);
+        const float qr = __fadd_rn(qh[rr], qh[64 + rr]);
+        const float e_r = (rr < Lr) ? __fmul_rn(dec[rr], __fadd_rn(eL[rr], eL[64 + rr])) : 0.f;
+        dgam[rr] = e_r;   // e_s, read by row L below after the barrier
+        const float dG = __fsub_rn(qr, __fmul_rn(bet[rr], kr));
+        const float dbR = __fsub_rn(dRv[rr], __fmul_rn(Gm[rr], kr));
+        const float rowE = __fadd_rn(__fadd_rn(rowA[rr], rowA[64 + rr]), __fadd_rn(rowB[rr], rowB[64 + rr]));
+        float dgr = __fsub_rn(__fadd_rn(__fmul_rn(Gm[rr], dG), rowE), colE[rr]);
+        dgr = __fsub_rn(dgr, e_r);
+        if (rr < nrows)
+            a.dbeta[(size_t)(t0 + rr) * H + h] = __fadd_rn(dbR, __fadd_rn(dbA[rr], dbA[64 + rr]));
+        eL[rr] = dgr;     // this row's dgam before the row-L terms
+    }
+    __syncthreads();
+    if (tid < C) {
+        const int rr = tid;
+        float dgr = eL[rr];
+        if (rr == Lr) {
+            float sumL = 0.f, rs = 0.f;
+            for (int s = 0; s < Lr; ++s) sumL = __fadd_rn(sumL, dgam[s]);
+            for (int w = 0; w < 8; ++w) rs = __fadd_rn(rs, red[w]);
+            dgr = __fadd_rn(dgr, __fadd_rn(__fmul_rn(Gm[Lr], rs), sumL));
         }
-        if (r < nrows) a.dbeta[(size_t)(t0 + r) * H + h] = __fadd_rn(dbR, dbA[r]);
-        dgam[r] = (r < nrows) ? dgr : 0.f;
+        colE[rr] = (rr < nrows) ? dgr : 0.f;   // dgam_r
     }
     __syncthreads();
     if (tid < nrows) {  // dg_s = sum_{r=s}^{L} dgam_r, from the last row down
         float acc = 0.f;
-        for (int r = Lr; r >= tid; --r) acc = __fadd_rn(acc, dgam[r]);
+        for (int rr = Lr; rr >= tid; --rr) acc = __fadd_rn(acc, colE[rr]);
         a.dg[(size_t)(t0 + tid) * H + h] = acc;
     }
     {
@@ -734,17 +734,17 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
     }
     mma_out = -1;
     {
-        // dq rows (top), dk rows (bottom)
-        const int r = tid & 63;
-        const bool top = tid < 64;
+        // dq rows (top), dk rows (bottom); this thread's 64 columns
         const bool in = r < nrows;
-        float x1[32], y[32], z[32];
+        float x1[32], y[32], z[32], w2[32];
         float* out = (top ? a.dq : a.dk) + ((size_t)(t0 + r) * H + h) * D;
         const float gr = Gm[r], nb = -bgv[r], dr = dec[r];
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c = 0; c < 2; ++c) {
+            const int c0 = hf * 64 + c * 32;
             tmem_ld32(taddr_of(tmem + tX1, warp, c0), x1);
-            tmem_ld32(taddr_of(tmem + (top ? tdq : tdk), warp, c0), y);
+            tmem_ld32(taddr_of(tmem + tdq, warp, c0), y);
             tmem_ld32(taddr_of(tmem + tX2, warp, c0), z);
+            tmem_ld32(taddr_of(tmem + tdk, warp, c0), w2);
             if (in) {
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
@@ -752,8 +752,9 @@ static __global__ void __launch_bounds__(128) k_tc_grad(TcBwdArgs a) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int j = 4 * j4 + e;
+                        // bottom: -bg X1 + dec X2 + (s G1)^T Q + G2^T K + G2 K (the last from tdq)
                         o4[e] = top ? __fmul_rn(scale, __fmaf_rn(gr, x1[j], y[j]))
-                                    : __fadd_rn(__fmaf_rn(nb, x1[j], __fmul_rn(dr, z[j])), y[j]);
+                                    : __fadd_rn(__fadd_rn(__fmaf_rn(nb, x1[j], __fmul_rn(dr, z[j])), w2[j]), y[j]);
                     }
                     *reinterpret_cast<float4*>(out + c0 + 4 * j4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }

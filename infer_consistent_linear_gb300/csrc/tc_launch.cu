@@ -51,7 +51,7 @@ cudaError_t state_bwd(const tc::TcBwdArgs& a, int n_seq, int H, cudaStream_t st)
     const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
     if (grid > 0) {
         ProfScope ps("cpr_tc_state_bwd", st);
-        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+        kern<<<(unsigned)grid, 256, sm, st>>>(a);
     }
     return cudaGetLastError();
 }
@@ -99,7 +99,7 @@ cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cma
     if (e != cudaSuccess) return e;
     if (cmax > 0) {
         ProfScope ps("cpr_tc_grad", st);
-        tc::k_tc_grad<<<dim3((unsigned)cmax, H), 128, tc::GradSmem::Total, st>>>(b);
+        tc::k_tc_grad<<<dim3((unsigned)cmax, H), 256, tc::GradSmem::Total, st>>>(b);
     }
     return cudaGetLastError();
 }
