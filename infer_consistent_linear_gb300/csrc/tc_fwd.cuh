@@ -110,7 +110,7 @@ constexpr size_t kPrepOffVmn = 32768, kPrepOffAt = 49152, kPrepOffT = 49152 + 16
                  kPrepOffVec = kPrepOffT + 64 * 65 * 4;
 constexpr size_t kPrepSmem = kPrepOffVec + 3 * 64 * 4 + 64;
 
-static __global__ void __launch_bounds__(128) k_tc_prep(TcArgs a) {
+static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later X1
     unsigned char* tKmn = sm;                      // the K rows read as an MN-major 128 (d) x 64 tile
