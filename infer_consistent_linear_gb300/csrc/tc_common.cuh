@@ -210,13 +210,21 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
     lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(hi)));
 }
 
-// Splits 8 fp32 values into packed hi and lo bf16 vectors.
+// Splits 8 fp32 values into packed hi and lo bf16 vectors (the split of
+// split_bf16, two values per conversion: both round to nearest even, so the
+// bits are the same).
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-    __align__(16) __nv_bfloat16 h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split_bf16(x[i], h[i], l[i]);
-    hi = *reinterpret_cast<const uint4*>(h);
-    lo = *reinterpret_cast<const uint4*>(l);
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(hb);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(__fsub_rn(x[2 * i], hf.x), __fsub_rn(x[2 * i + 1], hf.y));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hb);
+        l[i] = *reinterpret_cast<const uint32_t*>(&lb);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Stores 8 fp32 values (consecutive along K) as one 16-byte core-matrix row,
