@@ -76,28 +76,37 @@ __device__ __forceinline__ uint4 ld16_or_zero(const __nv_bfloat16* p, bool valid
     return valid ? *reinterpret_cast<const uint4*>(p) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// T = (I + A)^-1 for one column j (the calling thread), all rows at once:
-// row r's sum runs over s = j, j+1, ..., r-1 in ascending order exactly as the
-// column chain T_rj = -(sum_{s=j}^{r-1} a_rs T_sj) does, but every row takes
-// its term s in the same step, so the dependent path is one fma per step.
-// At holds A transposed (At[s * 64 + r] = a_rs); writes T rows < nrows of
-// column j to Tout[r * ldT + j] (rows >= nrows get 0).
-__device__ __forceinline__ void t_solve_column(const float* At, float* Tout, int ldT, int j, int nrows) {
-    float acc[C];
+// T = (I + A)^-1 by the column wavefront: T_rj = -(sum_{s=j}^{r-1} a_rs T_sj), each
+// row's sum one fma chain in ascending s (the chain a decode step evaluates for its own
+// row).  Step t adds a_rt T_tj to every row r > t of column j.  Two threads per column
+// (lanes 2j and 2j + 1) keep the running sums of the even and odd rows in registers; the
+// owner of row t hands its final value to the partner with a shuffle.  At2 holds A
+// transposed with the rows of each parity together: At2[s * 64 + (r & 1) * 32 + r / 2] =
+// a_rs.  Writes T rows < nrows of column j to Tout[r * ldT + j] (rows >= nrows get 0).
+// 128 threads.
+__device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int ldT, int nrows) {
+    const int j = threadIdx.x >> 1, p = threadIdx.x & 1;
+    float acc[C / 2];
 #pragma unroll
-    for (int r = 0; r < C; ++r) acc[r] = 0.f;
+    for (int i = 0; i < C / 2; ++i) acc[i] = 0.f;
 #pragma unroll
     for (int t = 0; t < C; ++t) {
-        const float Tt = (t < j) ? 0.f : (t == j ? 1.f : -acc[t]);
-        Tout[t * ldT + j] = (t < nrows) ? Tt : 0.f;
+        const float mine = -acc[t >> 1];
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+        const float fin = ((t & 1) == p) ? mine : other;
+        const float Tt = (t < j) ? 0.f : (t == j ? 1.f : fin);
+        if ((t & 1) == p) Tout[t * ldT + j] = (t < nrows) ? Tt : 0.f;
         if (t >= j) {
+            const float* arow = At2 + t * C + p * (C / 2);
 #pragma unroll
-            for (int r4 = (t + 1) / 4; r4 < C / 4; ++r4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(At + t * C + 4 * r4);
+            for (int i4 = t / 8; i4 < C / 8; ++i4) {   // i >= t / 2 - 1 covers every row > t
+                const float4 a4 = *reinterpret_cast<const float4*>(arow + 4 * i4);
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (4 * r4 + e > t) acc[4 * r4 + e] = __fmaf_rn(av[e], Tt, acc[4 * r4 + e]);
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 4 * i4 + e;
+                    if (2 * i + 1 > t && 2 * i + p > t) acc[i] = __fmaf_rn(av[e], Tt, acc[i]);
+                }
             }
         }
     }
@@ -115,7 +124,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later X1
     unsigned char* tKmn = sm;                      // the K rows read as an MN-major 128 (d) x 64 tile
     unsigned char* tVmn = sm + kPrepOffVmn;        // V, MN-major
-    float* At = reinterpret_cast<float*>(sm + kPrepOffAt);   // [64][64], At[s][r] = a_rs
+    float* At = reinterpret_cast<float*>(sm + kPrepOffAt);   // [64][64], a_rs at s * 64 + (r & 1) * 32 + r / 2
     float* Tfp = reinterpret_cast<float*>(sm + kPrepOffT);   // [64][65]
     float* gam = reinterpret_cast<float*>(sm + kPrepOffVec);
     float* bet = gam + 64;
@@ -193,7 +202,8 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int s = c0 + j;
-                    At[s * C + r] = (s < r && r < nrows) ? simt::a_entry(bet[r], gam[r], gam[s], v[j]) : 0.f;
+                    At[s * C + (r & 1) * (C / 2) + (r >> 1)] =
+                        (s < r && r < nrows) ? simt::a_entry(bet[r], gam[r], gam[s], v[j]) : 0.f;
                 }
             } else {
 #pragma unroll
@@ -212,7 +222,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
         }
     }
     __syncthreads();
-    if (tid < C) t_solve_column(At, Tfp, 65, tid, nrows);
+    t_solve_pairs(At, Tfp, 65, nrows);
     __syncthreads();
     {
         // X1 = T diag(b G) (threads 0..63, into the Q rows' space), X2 = T diag(b)
