@@ -172,6 +172,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
                  :: "r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(mbar)) : "memory");
 }
 
+// ---- bulk async copy (shared -> global), completion tracked by bulk groups ----------------
+// Both addresses 16-byte aligned, bytes a multiple of 16.  The writes to shared memory that
+// produced the source must be made visible to the async proxy first (fence_async_smem).
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // ---- 16-byte asynchronous copies (global -> shared), zero-filled when !valid ----------
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"

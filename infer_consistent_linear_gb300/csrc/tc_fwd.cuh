@@ -178,14 +178,13 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     if (tid == 0) {
         mma_tile<128, 64, D>(tmem, tKQ, tKQ, false);  // B = rows 0..63 of [K; Q] = K
         mma_commit(mbar);
+        // Q rows and K go to the workspace as the later kernels' operand tiles
+        bulk_s2g(blk + kOffA4hi + 16384, tKQ + 16384, 16384);
+        bulk_s2g(blk + kOffKmn, tKmn, 16384);
+        bulk_commit();
     }
     int outstanding = 0;  // mbarrier phase an in-flight MMA group will complete, or -1
     if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid]) : 0.f;
-    // Q rows and K (MN-major) go to the workspace as the state pass's operand tiles
-    for (int i = tid; i < 1024; i += 128) {
-        reinterpret_cast<uint4*>(blk + kOffA4hi + 16384)[i] = reinterpret_cast<const uint4*>(tKQ + 16384)[i];
-        reinterpret_cast<uint4*>(blk + kOffKmn)[i] = reinterpret_cast<const uint4*>(tKmn)[i];
-    }
     {
         const bool ok1 = mbar_wait(mbar, 0, a.err);
         fence_after();
@@ -223,6 +222,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     }
     __syncthreads();
     t_solve_pairs(At, Tfp, 65, nrows);
+    if (tid == 0) bulk_wait_read();  // the Q rows' space takes X1 next
     __syncthreads();
     {
         // X1 = T diag(b G) (threads 0..63, into the Q rows' space), X2 = T diag(b)
@@ -283,7 +283,9 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     }
     outstanding = -1;
     {
-        // W' and U rows: M = 64 layout, row r = 16 * warp + lane for lanes < 16
+        // W' and U rows (M = 64 layout, row r = 16 * warp + lane for lanes < 16) are
+        // staged in the now free operand space in their workspace layouts, then
+        // bulk-stored: W' hi, lo over the [K; Q] tile, U over the V and A^T space
         const int r = warp * 16 + lane;
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -294,28 +296,37 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = v[j8 * 8 + e];
-                    store8_split(blk + kOffA4hi, blk + kOffA4lo, cm_off(r, c0 + j8 * 8, D), x);
+                    store8_split(tKQ, tKQ + 16384, cm_off(r, c0 + j8 * 8, D), x);
                 }
             }
         }
-        float* U = reinterpret_cast<float*>(blk + kOffU);
-        const int dvs = a.dvs;
+        float* U = reinterpret_cast<float*>(tVmn);
+        const int dvs = a.dvs, dsh = __ffs(dvs) - 1;   // dvs is a power of two
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, 128 + c0), v);
             if (lane < 16) {
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const int j = c0 + j4 * 4;
-                    const int sp = j / dvs, jl = j % dvs;
+                    const int sp = j >> dsh, jl = j & (dvs - 1);
                     *reinterpret_cast<float4*>(U + (((size_t)sp * (dvs / 4) + jl / 4) * 64 + r) * 4) =
                         make_float4(v[j4 * 4], v[j4 * 4 + 1], v[j4 * 4 + 2], v[j4 * 4 + 3]);
                 }
             }
         }
-        if (tid < C) reinterpret_cast<float*>(blk + kOffGam)[tid] = gam[tid];
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(blk + kOffA4hi, tKQ, 16384);
+            bulk_s2g(blk + kOffA4lo, tKQ + 16384, 16384);
+            bulk_s2g(blk + kOffU, tVmn, 32768);
+            bulk_s2g(blk + kOffGam, gam, 256);
+            bulk_commit();
+        }
     }
 done:
     if (outstanding >= 0) mbar_wait(mbar, (uint32_t)outstanding, a.err);  // bounded
+    if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
     tc_sync();
     if (warp == 0) tmem_dealloc(*tbase, 256);
 }
