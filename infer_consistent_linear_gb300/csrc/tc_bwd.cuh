@@ -416,42 +416,70 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
           *qh = vec + 320, *kh = vec + 448, *rowA = vec + 576, *rowB = vec + 704, *dbA = vec + 832,
           *dRv = vec + 960, *colE = vec + 1024, *eL = vec + 1088, *dgam = vec + 1216,
           *red = vec + 1280;   // red: 8 warp sums; 1288 floats in all
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + L::Bar);
-    uint64_t* bar_mma = bar_ld + 1;
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_ld + 2);
+    uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + L::Bar);   // Q, K, dR, Delta, gam
+    uint64_t* bar_hn = bar_in + 1;                                   // H_n
+    uint64_t* bar_dh = bar_in + 2;                                   // dH'
+    uint64_t* bar_mma = bar_in + 3;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_in + 4);
 
     const int total = a.chunk_off[a.n_seq];
-    const int cidx = blockIdx.x, h = blockIdx.y, H = a.H;
-    if (total < 0 || cidx >= total) return;
+    if (total < 0) return;
+    const int H = a.H;
+    const int nwork = total * H;           // (chunk, head) items, chunk-major
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int row = quarter * 32 + lane;       // accumulator row / TMEM lane
+    const bool top = row < 64;
+    const int r = row & 63;                    // token row of the chunk
+    const float scale = a.scale;
+    auto blk_of = [&](int w) { return a.ws + (size_t)w * kBlockTrain; };   // w = cidx * H + h
+    auto issue_in = [&](int w) {
+        const unsigned char* blk = blk_of(w);
+        mbar_expect_tx(bar_in, 6 * 16384 + 256);
+        bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_in);     // Q rows
+        bulk_g2s(QK + 16384, blk + kOffKmn, 16384, bar_in);      // K rows
+        bulk_g2s(Rhi + 16384, blk + kOffdR, 16384, bar_in);
+        bulk_g2s(Rlo + 16384, blk + kOffdR + 16384, 16384, bar_in);
+        bulk_g2s(Rhi + 32768, blk + kOffDl, 16384, bar_in);
+        bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_in);
+        bulk_g2s(gam, blk + kOffGam, 256, bar_in);
+    };
+    auto issue_hn = [&](int w) {
+        mbar_expect_tx(bar_hn, 65536);
+        bulk_g2s(Bt, blk_of(w) + kOffHn, 65536, bar_hn);
+    };
+
+    if (warp == 0) tmem_alloc(tbase, 512);
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(bar_in + i, 1);
+        mbar_init_fence();
+        if ((int)blockIdx.x < nwork) {
+            issue_in(blockIdx.x);
+            issue_hn(blockIdx.x);
+        }
+    }
+    tc_sync();
+    const uint32_t tmem = *tbase;
+    const uint32_t tX1 = 0, tG = 128, tS1 = 192, tX2 = 256, tdq = 384, tdk = 128;
+    uint32_t ph_mma = 0;
+    bool pend_in = (int)blockIdx.x < nwork, pend_hn = pend_in, pend_dh = false, mma_out = false;
+    uint32_t ph_in = 0, ph_hn = 0;  // parity the pending input / H_n copy completes
+    bool failed = false;
+    int it = 0;                    // this CTA's item count: the load barriers' phase parity
+    float bloc[32];                // bottom rows: b_r dA_rs Kd_rs for this thread's columns
+
+    for (int w = blockIdx.x; w < nwork; w += gridDim.x, ++it) {
+    const uint32_t ph = (uint32_t)(it & 1);
+    const int wn = w + (int)gridDim.x;         // the next item of this CTA
+    const int cidx = w / H, h = w % H;
     const int b = find_seq(a.chunk_off, a.n_seq, cidx);
     const int n = cidx - a.chunk_off[b];
     const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
     const int t0 = seq0 + n * C;
     const int nrows = min(C, T - n * C);
     const int Lr = nrows - 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, hf = warp >> 2;
-    const int row = quarter * 32 + lane;       // accumulator row / TMEM lane
-    const bool top = row < 64;
-    const int r = row & 63;                    // token row of the chunk
-    const unsigned char* blk = a.ws + ((size_t)cidx * H + h) * kBlockTrain;
-    const float scale = a.scale;
-
-    if (warp == 0) tmem_alloc(tbase, 512);
-    if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
-        mbar_init_fence();
-        mbar_expect_tx(bar_ld, 6 * 16384 + 65536 + 256);
-        bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_ld);     // Q rows
-        bulk_g2s(QK + 16384, blk + kOffKmn, 16384, bar_ld);      // K rows
-        bulk_g2s(Rhi + 16384, blk + kOffdR, 16384, bar_ld);
-        bulk_g2s(Rlo + 16384, blk + kOffdR + 16384, 16384, bar_ld);
-        bulk_g2s(Rhi + 32768, blk + kOffDl, 16384, bar_ld);
-        bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_ld);
-        bulk_g2s(Bt, blk + kOffHn, 65536, bar_ld);
-        bulk_g2s(gam, blk + kOffGam, 256, bar_ld);
-    }
+    const unsigned char* blk = blk_of(w);
+    tc_sync();   // the previous item's TMEM reads and shared-memory use are over
     // dO rows (zero past the chunk's end) split into R rows 0..63
 #pragma unroll 4
     for (int i = tid; i < 64 * (D / 8); i += 256) {
@@ -469,18 +497,13 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         store8_split(Rhi, Rlo, cm_off(rr, d8 * 8, D), x);
     }
     if (tid < C) bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    const uint32_t tX1 = 0, tG = 128, tS1 = 192, tX2 = 256, tdq = 384, tdk = 128;
-    uint32_t tmem = 0;
-    int ld_out = 0, mma_out = -1;   // mbarrier phases still to complete (-1: none)
-    float bloc[32];                 // bottom rows: b_r dA_rs Kd_rs for this thread's columns
     {
-        const bool ok = mbar_wait(bar_ld, 0, a.err);
+        const bool ok = mbar_wait(bar_in, ph, a.err) && mbar_wait(bar_hn, ph, a.err);
         fence_async_smem();
         tc_sync();
-        tmem = *tbase;
-        if (__syncthreads_or(!ok)) goto done;
+        if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    ld_out = -1;
+    pend_in = pend_hn = false;
     if (tid < C) {
         const bool in = tid < nrows;
         const float gr = gam[tid];
@@ -498,19 +521,20 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         mma_tile<128, 64, D>(tmem + tG, Rlo, Rhi + 32768, true);
         mma_commit(bar_mma);
     }
-    mma_out = 0;
+    mma_out = true;
     {
-        const bool ok = mbar_wait(bar_mma, 0, a.err);
+        const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
-        if (__syncthreads_or(!ok)) goto done;
+        if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    mma_out = -1;
+    ph_mma ^= 1u;
+    mma_out = false;
     if (tid == 0) {  // H_n is consumed: dH' takes its place
         fence_async_smem();
-        mbar_expect_tx(bar_ld, 65536);
-        bulk_g2s(Bt, blk + kOffdH, 65536, bar_ld);
+        mbar_expect_tx(bar_dh, 65536);
+        bulk_g2s(Bt, blk + kOffdH, 65536, bar_dh);
     }
-    ld_out = 1;
+    pend_dh = true;
     {
         // ---- phase A: one pass over this thread's 32 columns s of the row
         const int s0 = hf * 32;
@@ -585,18 +609,27 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         for (int rr = s + 1; rr < nrows; ++rr) acc = __fadd_rn(acc, scr[rr * 65 + s]);
         colE[s] = acc;
     } else if (tid >= 128) {
-        // dv = b dR and dR . v, a warp per row, 16-byte pieces side by side
-        const int t = tid - 128;
-        for (int rr = t >> 5; rr < nrows; rr += 4) {
-            const int c4 = (t & 31) * 4;
+        // dv = b dR and dR . v, a warp per row, 16-byte pieces side by side; every
+        // row's v loads are issued before any is used
+        const int t = tid - 128, w4 = t >> 5, c4 = (t & 31) * 4;
+        uint2 vrow[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int rr = w4 + 4 * k;
+            vrow[k] = (rr < nrows) ? *reinterpret_cast<const uint2*>(a.v + ((size_t)(t0 + rr) * H + h) * D + c4)
+                                   : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int rr = w4 + 4 * k;
+            if (rr >= nrows) break;
             const uint32_t off = cm_off(rr, c4, D);
             const uint2 hi = *reinterpret_cast<const uint2*>(Rhi + 16384 + off);
             const uint2 lo = *reinterpret_cast<const uint2*>(Rlo + 16384 + off);
             const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&hi);
             const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&lo);
             const size_t g = ((size_t)(t0 + rr) * H + h) * D + c4;
-            const uint2 vv = *reinterpret_cast<const uint2*>(a.v + g);
-            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vv);
+            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vrow[k]);
             const float brr = bet[rr];
             float x[4], sdot = 0.f;
 #pragma unroll
@@ -612,17 +645,17 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     }
     {
         // dH' has arrived: X2 = [dR; Delta] dH'^T (rows 64.. are Delta dH'^T)
-        const bool ok = mbar_wait(bar_ld, 1, a.err);
-        if (__syncthreads_or(!ok)) goto done;
+        const bool ok = mbar_wait(bar_dh, ph, a.err);
+        if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    ld_out = -1;
+    pend_dh = false;
     if (tid == 0) {
         mma_tile<128, 128, D>(tmem + tX2, Rhi + 16384, Bt, false);
         mma_tile<128, 128, D>(tmem + tX2, Rhi + 16384, Bt + 32768, true);
         mma_tile<128, 128, D>(tmem + tX2, Rlo + 16384, Bt, true);
         mma_commit(bar_mma);
     }
-    mma_out = 1;
+    mma_out = true;
     {
         // <dH', H_n>: row d = tid & 127, half of the columns per thread; H_n again from
         // the workspace (just bulk-read, so mostly in L2), dH' from shared memory
@@ -642,11 +675,18 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         if (lane == 0) red[warp] = acc;
     }
     {
-        const bool ok = mbar_wait(bar_mma, 1, a.err);
+        const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
-        if (__syncthreads_or(!ok)) goto done;
+        if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    mma_out = -1;
+    ph_mma ^= 1u;
+    mma_out = false;
+    if (tid == 0 && wn < nwork) {  // dH' is consumed: the next item's H_n goes to Bt already
+        fence_async_smem();
+        issue_hn(wn);
+    }
+    pend_hn = wn < nwork;
+    ph_hn = ph ^ 1u;
     {
         // ---- phase E: MN-major A tiles (mn = 64 + s, k = r) of (scale G1)^T and G2^T from
         // the [G1; G2] tile's rows, interleaved in the dR / Delta space (free now: X2 is done);
@@ -693,7 +733,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         mma_tile_mj<128, 128, C, true, true>(tmem + tdk, Rlo + 16384 + 1024, QK + 16384, true);
         mma_commit(bar_mma);
     }
-    mma_out = 0;
+    mma_out = true;
     if (tid < C) {  // gate and beta gradients of row r = tid
         const int rr = tid;
         const float kr = __fadd_rn(kh[rr], kh[64 + rr]);
@@ -728,11 +768,18 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         a.dg[(size_t)(t0 + tid) * H + h] = acc;
     }
     {
-        const bool ok = mbar_wait(bar_mma, 0, a.err);
+        const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
-        if (__syncthreads_or(!ok)) goto done;
+        if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    mma_out = -1;
+    ph_mma ^= 1u;
+    mma_out = false;
+    if (tid == 0 && wn < nwork) {  // Q, K, the R tiles and gam are consumed: next item's inputs
+        fence_async_smem();
+        issue_in(wn);
+    }
+    pend_in = wn < nwork;
+    ph_in = ph ^ 1u;
     {
         // dq rows (top), dk rows (bottom); this thread's 64 columns
         const bool in = r < nrows;
@@ -761,9 +808,13 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
             }
         }
     }
-done:
-    if (ld_out >= 0) mbar_wait(bar_ld, (uint32_t)ld_out, a.err);    // bounded
-    if (mma_out >= 0) mbar_wait(bar_mma, (uint32_t)mma_out, a.err);
+    }  // items
+    if (failed) {   // let in-flight copies and MMAs finish (bounded) before TMEM is released
+        if (pend_dh) mbar_wait(bar_dh, (uint32_t)(it & 1), a.err);
+        if (mma_out) mbar_wait(bar_mma, ph_mma, a.err);
+        if (pend_in) mbar_wait(bar_in, ph_in, a.err);
+        if (pend_hn) mbar_wait(bar_hn, ph_hn, a.err);
+    }
     tc_sync();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }

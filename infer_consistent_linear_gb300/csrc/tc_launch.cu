@@ -97,9 +97,17 @@ cudaError_t tc_backward(const tc::TcArgs& f, const tc::TcBwdArgs& b, int64_t cma
     if (e != cudaSuccess) return e;
     e = set_smem(tc::k_tc_grad, tc::GradSmem::Total);
     if (e != cudaSuccess) return e;
-    if (cmax > 0) {
+    // persistent: one CTA per SM walks the (chunk, head) items
+    int dev = 0, nsm = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t items = cmax * (int64_t)H;
+    const int grid = (int)(items < nsm ? items : nsm);
+    if (grid > 0) {
         ProfScope ps("cpr_tc_grad", st);
-        tc::k_tc_grad<<<dim3((unsigned)cmax, H), 256, tc::GradSmem::Total, st>>>(b);
+        tc::k_tc_grad<<<grid, 256, tc::GradSmem::Total, st>>>(b);
     }
     return cudaGetLastError();
 }
