@@ -184,6 +184,9 @@ typedef struct cpr_cache_layout {
     size_t beta_rows;   /* fp32   [n_seq, H, C]                                    */
     size_t t_rows;      /* fp32   [n_seq, H, C, C]   rows of (I + A)^-1            */
     size_t delta_rows;  /* fp32   [n_seq, H, C, d_v] rows of Delta                 */
+    size_t state_tiles; /* bf16   [n_seq, H] x 64 KB: H_n as hi/lo tensor-core operand
+                           tiles (tensor-core contracts; the fp32 copy stays authoritative) */
+    size_t delta_tiles; /* bf16   [n_seq, H] x 32 KB: the Delta rows as hi/lo operand tiles */
 } cpr_cache_layout;
 
 int cpr_decode_cache_layout(const cpr_contract* c, int n_seq, int H, cpr_cache_layout* out);

@@ -56,7 +56,7 @@ class Contract(ctypes.Structure):
 class CacheLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "total_bytes", "header", "pos", "done", "state", "k_rows", "v_rows", "gam_rows",
-        "beta_rows", "t_rows", "delta_rows")]
+        "beta_rows", "t_rows", "delta_rows", "state_tiles", "delta_tiles")]
 
 
 class KernelTime(ctypes.Structure):

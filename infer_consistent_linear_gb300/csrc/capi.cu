@@ -174,13 +174,15 @@ cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
     add(l.beta_rows, sh * C * 4);
     add(l.t_rows, sh * C * C * 4);
     add(l.delta_rows, sh * C * dv * 4);
+    add(l.state_tiles, sh * dk * dv * 4);   // bf16 hi + lo operand tiles of the state
+    add(l.delta_tiles, sh * C * dv * 4);    // bf16 hi + lo operand tiles of the Delta rows
     l.total_bytes = off;
     return l;
 }
 
 cpr::CacheOff to_off(const cpr_cache_layout& l) {
     return cpr::CacheOff{l.header, l.pos, l.done, l.state, l.k_rows, l.v_rows,
-                         l.gam_rows, l.beta_rows, l.t_rows, l.delta_rows};
+                         l.gam_rows, l.beta_rows, l.t_rows, l.delta_rows, l.state_tiles, l.delta_tiles};
 }
 
 const cpr::SimtOps* ops_for(const cpr_contract& c) {

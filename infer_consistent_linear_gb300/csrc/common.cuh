@@ -66,7 +66,8 @@ __device__ __forceinline__ int find_seq(const int32_t* chunk_off, int n_seq, int
 
 // ---- decode cache section offsets (bytes) ------------------------------------
 struct CacheOff {
-    size_t header, pos, done, state, k_rows, v_rows, gam_rows, beta_rows, t_rows, delta_rows;
+    size_t header, pos, done, state, k_rows, v_rows, gam_rows, beta_rows, t_rows, delta_rows,
+        state_tiles, delta_tiles;
 };
 
 struct Digest {

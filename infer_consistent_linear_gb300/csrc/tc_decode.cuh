@@ -20,15 +20,17 @@ namespace cpr {
 namespace tc {
 
 struct DecSmem {
-    static constexpr size_t Hhi = 0, Hlo = 32768;   // per split: MN-major DVS (j) x 128 (d)
+    static constexpr size_t Hhi = 0, Hlo = 32768;   // state tiles, per split MN-major DVS (j) x 128 (d)
     static constexpr size_t Kmn = 65536;             // K, MN-major 128 (d) x 64 (token)
     static constexpr size_t R1 = 81920;              // 64 KB right after Kmn, reused by phase
     static constexpr size_t F = R1 + 65536;          // fp32 scratch
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
                          fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
                          fRow2 = 1088, fEnd = 1216;
-    static constexpr size_t Stage = 153600;          // 64 KB fp32: H, later the cached Delta rows
-    static constexpr size_t Bar = Stage + 65536;
+    static constexpr size_t Dt = 153600;             // Delta tiles: hi (16 KB) | lo (16 KB), per split
+                                                     // MN-major DVS (j) x 64 (token); at a commit the
+                                                     // fp32 Delta rows
+    static constexpr size_t Bar = Dt + 32768;
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -49,6 +51,50 @@ struct TcDecArgs {
     uint32_t* err;
 };
 
+// After a prefill that writes a decode cache: the chunk-start state and the current
+// chunk's Delta rows (rows >= pos zero) as the decode's hi/lo operand tiles, per split
+// MN-major (split sp at sp * DVS * 256 / 128 bytes, lo tiles 32 KB / 16 KB after hi) --
+// split8 of the fp32 values the state pass left in the cache, so the decode reads the
+// same bits it would compute itself.  One CTA per (sequence, head).
+template <int DVS>
+__global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff co, const int32_t* chunk_off,
+                                                        int n_seq, int H) {
+    if (chunk_off[n_seq] < 0) return;   // rejected cu_seqlens: the prefill wrote nothing
+    const size_t sh = blockIdx.x;
+    const int b = (int)(sh / H);
+    const int p = reinterpret_cast<const int32_t*>(cache + co.pos)[b];
+    const float* Hs = reinterpret_cast<const float*>(cache + co.state) + sh * D * D;
+    const float* Dr = reinterpret_cast<const float*>(cache + co.delta_rows) + sh * C * D;
+    unsigned char* ct = cache + co.state_tiles + sh * 65536;
+    unsigned char* cdt = cache + co.delta_tiles + sh * 32768;
+    for (int i = threadIdx.x; i < (D + C) * (D / 8); i += blockDim.x) {
+        const bool st = i < D * (D / 8);
+        const int rr = (st ? i : i - D * (D / 8)) / (D / 8), j8 = i % (D / 8);
+        float x[8];
+        if (st || rr < p) {
+            const float4* src = reinterpret_cast<const float4*>((st ? Hs : Dr) + (size_t)rr * D + j8 * 8);
+            const float4 u0 = src[0], u1 = src[1];
+            x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+            x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+        if (st) {
+            const uint32_t off = (uint32_t)sp * DVS * 256 + mn_off(jl, rr, DVS);
+            *reinterpret_cast<uint4*>(ct + off) = hi;
+            *reinterpret_cast<uint4*>(ct + 32768 + off) = lo;
+        } else {
+            const uint32_t off = (uint32_t)sp * DVS * 128 + mn_off(jl, rr, DVS);
+            *reinterpret_cast<uint4*>(cdt + off) = hi;
+            *reinterpret_cast<uint4*>(cdt + 16384 + off) = lo;
+        }
+    }
+}
+
 template <int DVS>
 __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     using S = DecSmem;
@@ -62,7 +108,7 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);
     uint64_t* bar_ld = mbar + 1;
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 2);
-    float* stage = reinterpret_cast<float*>(sm + S::Stage);
+    float* stage = reinterpret_cast<float*>(sm + S::Dt);   // fp32 Delta rows at a commit
     __shared__ int ok_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -91,6 +137,10 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
     float* cd = reinterpret_cast<float*>(a.cache + a.co.delta_rows) + sh * C * D;
     float* Hst = reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D;
+    unsigned char* cst = a.cache + a.co.state_tiles + sh * 65536;     // state hi | lo tiles
+    unsigned char* cdt = a.cache + a.co.delta_tiles + sh * 32768;     // Delta hi | lo tiles
+    // bytes of each split's Delta tile holding rows < p (8-row core-matrix groups)
+    const uint32_t dpre = (uint32_t)((p + 7) / 8) * (DVS / 8) * 128;
     const __nv_bfloat16* qt = a.q + sh * D;
     const __nv_bfloat16* kt = a.k + sh * D;
     const __nv_bfloat16* vt = a.v + sh * D;
@@ -101,8 +151,17 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         mbar_init(mbar, 1);
         mbar_init(bar_ld, 1);
         mbar_init_fence();
-        mbar_expect_tx(bar_ld, 65536);  // the chunk-start state, one contiguous 64 KB block
-        bulk_g2s(stage, Hst, 65536, bar_ld);
+        // the chunk-start state as ready operand tiles, and the Delta rows < p
+        mbar_expect_tx(bar_ld, 65536 + 2u * NSPLIT * dpre);
+        bulk_g2s(sm + S::Hhi, cst, 65536, bar_ld);
+        if (dpre) {
+#pragma unroll
+            for (int sp = 0; sp < NSPLIT; ++sp) {
+                const uint32_t t = (uint32_t)sp * DVS * 128;
+                bulk_g2s(sm + S::Dt + t, cdt + t, dpre, bar_ld);
+                bulk_g2s(sm + S::Dt + 16384 + t, cdt + 16384 + t, dpre, bar_ld);
+            }
+        }
     }
     // K and V rows s <= p as MN-major tiles (Kmn; R1 + 32 KB), later rows zero-filled
     // by the copies themselves.  The K tile read K-major is the [K; Q] operand's
@@ -233,32 +292,21 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(64 + p, (tid - 32) * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
     }
     {
-        // the staged chunk-start state -> per-split MN-major hi/lo tiles (row d = tid)
+        // state tiles and the Delta rows < p have landed; rows >= p of every Delta tile are
+        // set to zero (row p is written below; rows past it only meet zero P entries)
         const bool okh = mbar_wait(bar_ld, 0, a.err);
         if (__syncthreads_or(!okh)) goto cleanup;
         ld_pending = false;
         ld_phase = 1;
-        const int d = tid;
-#pragma unroll 4
-        for (int jj = 0; jj < D / 8; ++jj) {
-            const int j8 = (jj + d) & (D / 8 - 1);  // staggered columns: no bank conflicts
-            const float4 x0 = *reinterpret_cast<const float4*>(stage + d * D + j8 * 8);
-            const float4 x1 = *reinterpret_cast<const float4*>(stage + d * D + j8 * 8 + 4);
-            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
-            const size_t tile = (size_t)sp * DVS * 128 * 2;
-            store8_split(sm + S::Hhi + tile, sm + S::Hlo + tile, mn_off(jl, d, DVS), x);
+        constexpr int CH = DVS / 8;                        // 16-byte chunks per tile row
+        for (int i = tid; i < (C - p) * CH * NSPLIT * 2; i += 128) {
+            const int sr = p + i / (CH * NSPLIT * 2), rem = i % (CH * NSPLIT * 2);
+            const int sp = (rem / CH) % NSPLIT, lohi = rem / (CH * NSPLIT), c8 = rem % CH;
+            *reinterpret_cast<uint4*>(sm + S::Dt + lohi * 16384 + sp * DVS * 128 + mn_off(c8 * 8, sr, DVS)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
     }
     __syncthreads();
-    if (p > 0) {  // the cached Delta rows of this chunk -> the staging area (during the A4 MMA)
-        ld_pending = true;
-        if (tid == 0) {
-            fence_async_smem();
-            mbar_expect_tx(bar_ld, (uint32_t)p * D * 4);
-            bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_ld);
-        }
-    }
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
@@ -294,34 +342,23 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         Dp[j] = __fsub_rn(Up[j], row1[j]);
         Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
     }
-    // P tiles (R1 + 0: hi, + 8 KB: lo; row p); Delta (MN-major per split, rows > p zero)
-    if (p > 0) {
-        const bool okd = mbar_wait(bar_ld, 1, a.err);
-        if (__syncthreads_or(!okd)) goto cleanup;
-        ld_pending = false;
-    }
+    // P row p (R1 + 0: hi, + 8 KB: lo); Delta row p into the Delta tiles and the cache
     __syncthreads();
-    if (tid < C) {
-        const int s = tid;
-#pragma unroll 4
-        for (int jj = 0; jj < D / 8; ++jj) {
-            const int j8 = (jj + s) & (D / 8 - 1);
-            float x[8];
-            if (s < p) {
-                const float4 x0 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8);
-                const float4 x1 = *reinterpret_cast<const float4*>(stage + s * D + j8 * 8 + 4);
-                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-            } else {
+    if (tid < D / 8) {
+        const int j8 = tid;
+        float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = (s == p) ? Dp[j8 * 8 + e] : 0.f;
-            }
-            const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
-            const size_t tile = (size_t)sp * DVS * 64 * 2;
-            store8_split(R1 + 16384 + tile, R1 + 32768 + tile, mn_off(jl, s, DVS), x);
-        }
-    } else if (tid < C + 8) {
-        const int s8 = tid - C;
+        for (int e = 0; e < 8; ++e) x[e] = Dp[j8 * 8 + e];
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
+        const uint32_t off = (uint32_t)sp * DVS * 128 + mn_off(jl, p, DVS);
+        *reinterpret_cast<uint4*>(sm + S::Dt + off) = hi;
+        *reinterpret_cast<uint4*>(sm + S::Dt + 16384 + off) = lo;
+        *reinterpret_cast<uint4*>(cdt + off) = hi;
+        *reinterpret_cast<uint4*>(cdt + 16384 + off) = lo;
+    } else if (tid >= 64 && tid < 64 + C / 8) {
+        const int s8 = tid - 64;
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = prow[s8 * 8 + e];
@@ -334,9 +371,9 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         for (int sp = 0; sp < NSPLIT; ++sp) {
             const uint32_t acc = tmem + 128 + sp * DVS;
             const size_t tile = (size_t)sp * DVS * 64 * 2;
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1, R1 + 16384 + tile, false);
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1, R1 + 32768 + tile, true);
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1 + 8192, R1 + 16384 + tile, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1, sm + S::Dt + tile, false);
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1, sm + S::Dt + 16384 + tile, true);
+            mma_tile_mj<64, DVS, C, false, true>(acc, R1 + 8192, sm + S::Dt + tile, true);
         }
         mma_commit(mbar);
     }
@@ -368,8 +405,18 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     }
     if (p == C - 1) {  // resynchronise: commit the next chunk-start state
         const int Lr = C - 1;
+        if (tid == 0) {  // the chunk's other fp32 Delta rows (the Delta tiles are consumed)
+            fence_async_smem();
+            mbar_expect_tx(bar_ld, (uint32_t)p * D * 4);
+            bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_ld);
+        }
+        ld_pending = true;
         if (tid < C) decs[tid] = simt::decay(gams[Lr], gams[tid]);
-        __syncthreads();
+        {
+            const bool okd = mbar_wait(bar_ld, 1, a.err);
+            if (__syncthreads_or(!okd)) goto cleanup;
+            ld_pending = false;
+        }
         if (tid < C) {
             const int s = tid;
             const float ds = decs[s];
@@ -413,13 +460,22 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-                float4* hp = reinterpret_cast<float4*>(Hst + (size_t)d * D + c0 + 4 * j4);
-                const float4 h4 = *hp;
-                *hp = make_float4(__fadd_rn(__fmul_rn(GL, h4.x), v[4 * j4]),
-                                  __fadd_rn(__fmul_rn(GL, h4.y), v[4 * j4 + 1]),
-                                  __fadd_rn(__fmul_rn(GL, h4.z), v[4 * j4 + 2]),
-                                  __fadd_rn(__fmul_rn(GL, h4.w), v[4 * j4 + 3]));
+            for (int j8 = 0; j8 < 4; ++j8) {
+                float4* hp = reinterpret_cast<float4*>(Hst + (size_t)d * D + c0 + 8 * j8);
+                const float4 h0 = hp[0], h1 = hp[1];
+                const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(__fmul_rn(GL, hv[e]), v[8 * j8 + e]);
+                hp[0] = make_float4(x[0], x[1], x[2], x[3]);
+                hp[1] = make_float4(x[4], x[5], x[6], x[7]);
+                // and the operand tiles the next steps load
+                uint4 hi, lo;
+                split8(x, hi, lo);
+                const int jc = c0 + 8 * j8, sp = jc / DVS, jl = jc - sp * DVS;
+                const uint32_t off = (uint32_t)sp * DVS * 256 + mn_off(jl, d, DVS);
+                *reinterpret_cast<uint4*>(cst + off) = hi;
+                *reinterpret_cast<uint4*>(cst + 32768 + off) = lo;
             }
         }
     }

@@ -29,6 +29,16 @@ cudaError_t state(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
 }
 
 template <int DVS>
+cudaError_t cache_tiles(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
+    const int64_t grid = (int64_t)n_seq * H;
+    if (grid > 0) {
+        ProfScope ps("cpr_tc_cache_tiles", st);
+        tc::k_tc_cache_tiles<DVS><<<(unsigned)grid, 256, 0, st>>>(a.cache, a.co, a.chunk_off, n_seq, H);
+    }
+    return cudaGetLastError();
+}
+
+template <int DVS>
 cudaError_t decode(const tc::TcDecArgs& a, cudaStream_t st) {
     auto kern = tc::k_tc_decode<DVS>;
     const size_t sm = tc::DecSmem::Total;
@@ -68,10 +78,12 @@ cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cuda
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (a.dvs) {
-        case 64: return state<64>(a, n_seq, H, st);
-        case 32: return state<32>(a, n_seq, H, st);
+        case 64: e = state<64>(a, n_seq, H, st); break;
+        case 32: e = state<32>(a, n_seq, H, st); break;
         default: return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess || !a.cache) return e;
+    return a.dvs == 64 ? cache_tiles<64>(a, n_seq, H, st) : cache_tiles<32>(a, n_seq, H, st);
 }
 
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st) {

@@ -106,10 +106,12 @@ def test_workspace_and_cache_layout(lib):
     assert b > f
     lay = cpr.cache_layout(c, 64, 32)
     offs = [lay.header, lay.pos, lay.done, lay.state, lay.k_rows, lay.v_rows, lay.gam_rows,
-            lay.beta_rows, lay.t_rows, lay.delta_rows]
+            lay.beta_rows, lay.t_rows, lay.delta_rows, lay.state_tiles, lay.delta_tiles]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lay.k_rows - lay.state >= 64 * 32 * 128 * 128 * 4
-    assert lay.total_bytes >= lay.delta_rows + 64 * 32 * 64 * 128 * 4
+    assert lay.state_tiles - lay.delta_rows >= 64 * 32 * 64 * 128 * 4
+    assert lay.delta_tiles - lay.state_tiles >= 64 * 32 * 128 * 128 * 4
+    assert lay.total_bytes >= lay.delta_tiles + 64 * 32 * 64 * 128 * 4
 
 
 def _call_fwd(lib, c, digest, ptrs, n_seq=1, n_tok=64, H=1, ws_bytes=1 << 30):
