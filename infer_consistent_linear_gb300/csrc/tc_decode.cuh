@@ -481,7 +481,8 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     }
     __syncthreads();
     if (tid == 0) {  // advance the position once every head of the sequence is done
-        __threadfence();
+        // No fence before the count: every CTA of the sequence read pos[b] (and used it)
+        // before its own increment, and the next step is a later launch.
         const uint32_t prev = atomicAdd(&done[b], 1u);
         if (prev == (uint32_t)H - 1) {
             pos[b] = (p + 1) % C;
