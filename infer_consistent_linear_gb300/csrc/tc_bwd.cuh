@@ -70,8 +70,7 @@ struct SbSmem {
     static constexpr size_t B1lo = B1hi + DVS * 64 * 2;
     static constexpr size_t B2hi = B1lo + DVS * 64 * 2;      // G scale dO, then -bg dR
     static constexpr size_t B2lo = B2hi + DVS * 64 * 2;
-    static constexpr size_t Stage = B2lo + DVS * 64 * 2;     // dO rows fp32, [DVS/4][64] float4
-    static constexpr size_t Vec = Stage + 64 * DVS * 4;      // gam, Gm, dec, bg (64 fp32 each)
+    static constexpr size_t Vec = B2lo + DVS * 64 * 2;      // gam, Gm, dec, bg (64 fp32 each)
     static constexpr size_t Bar = Vec + 4 * 256;             // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
@@ -160,14 +159,20 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         bulk_g2s(dst, blk + kOffKmn, 16384, bar);
         bulk_g2s(dst + 16384, blk + kOffA4hi + 16384, 16384, bar);
     };
-    // dO rows of chunk n (columns j0..j0+DVS) into the staging area, zero past the end
-    auto issue_dO = [&](int n) {
-        const int t0 = seq0 + n * C, nrows = min(C, T - n * C);
-        for (int i = tid; i < 64 * (DVS / 4); i += 256) {
-            const int r = i / (DVS / 4), q4 = i % (DVS / 4);  // a row's 16-byte pieces side by side
-            const bool in = r < nrows;
-            const float* src = a.dO + (in ? ((size_t)(t0 + r) * H + h) * D + j0 + 4 * q4 : 0);
-            cp_async16(sm + L::Stage + ((size_t)q4 * 64 + r) * 16, src, in);
+    // this thread's slice of chunk n's dO rows (token rr, 8-column groups j8 of its part),
+    // loaded into registers one chunk ahead; rows past the end are zero
+    constexpr int NJ8 = DVS / 32;                     // 8-column groups per thread
+    const int rr = tid & 63, part = tid >> 6;
+    float4 dOpre[2 * NJ8];
+    auto load_dO = [&](int n) {
+        const int t0 = seq0 + n * C;
+        const bool in = rr < min(C, T - n * C);
+        const float4* src = reinterpret_cast<const float4*>(a.dO + ((size_t)(t0 + (in ? rr : 0)) * H + h) * D + j0);
+#pragma unroll
+        for (int q = 0; q < NJ8; ++q) {
+            const int j8 = part * NJ8 + q;
+            dOpre[2 * q] = in ? src[2 * j8] : make_float4(0.f, 0.f, 0.f, 0.f);
+            dOpre[2 * q + 1] = in ? src[2 * j8 + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     auto beta_of = [&](int n) {
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             issue_KQ(nch - 1);
             if (nch > 1) issue_KQ(nch - 2);
         }
-        issue_dO(nch - 1);
+        load_dO(nch - 1);
         bcur = beta_of(nch - 1);
     }
     fence_async_smem();
@@ -206,14 +211,12 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         const int cur = n & 1;
         unsigned char* KQ = sm + (cur ? L::KQ1 : L::KQ0);
         bool ok = mbar_wait(bar_P, ph_P, a.err);
-        cp_async_wait_all();
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_P ^= 1u;
         pendP = false;
         {
             // token row rr, a quarter of the columns per thread: dO (B1) and G scale dO
             // (B2) rows, MN-major (j, t)
-            const int rr = tid & 63, part = tid >> 6;
             const bool in = rr < nrows;
             const float gr = gam[rr];
             const float Gr = in ? simt::gate(gr) : 0.f;
@@ -224,9 +227,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             }
             const float gs = __fmul_rn(Gr, scale);
 #pragma unroll
-            for (int j8 = part * (DVS / 32); j8 < (part + 1) * (DVS / 32); ++j8) {
-                const float4 u0 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8) * 64 + rr];
-                const float4 u1 = reinterpret_cast<const float4*>(sm + L::Stage)[(2 * j8 + 1) * 64 + rr];
+            for (int q = 0; q < NJ8; ++q) {
+                const int j8 = part * NJ8 + q;
+                const float4 u0 = dOpre[2 * q], u1 = dOpre[2 * q + 1];
                 const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float y[8];
 #pragma unroll
@@ -236,9 +239,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             }
         }
         const float GL = simt::gate(gam[Lr]);
-        __syncthreads();  // the staging area is consumed
-        if (n > 0) {
-            issue_dO(n - 1);
+        if (n > 0) {   // the next chunk's dO slice and beta, a chunk ahead
+            load_dO(n - 1);
             bcur = beta_of(n - 1);
         }
         fence_async_smem();
@@ -367,7 +369,6 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
                 make_float4(dHreg[4 * j4], dHreg[4 * j4 + 1], dHreg[4 * j4 + 2], dHreg[4 * j4 + 3]);
     } else {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
-        cp_async_wait_all();
         if (pendP) mbar_wait(bar_P, ph_P, a.err);
         if (pendT) mbar_wait(bar_T, ph_T, a.err);
         if (pendKQ[0]) mbar_wait(bar_KQ, ph_KQ[0], a.err);
