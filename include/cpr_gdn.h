@@ -322,6 +322,17 @@ int cpr_get_device_error(uint32_t* code, int clear);
 /* Thread-local message describing the last non-OK return on this thread. */
 const char* cpr_last_error(void);
 
+/* Test support for the device-side failure path.  Every wait of the kernels on
+ * an mbarrier (an async copy or MMA completing) polls at most a fixed number of
+ * times; on expiry the kernel records CPR_ERR_DEVICE_TIMEOUT in the device error
+ * word, lets its own copies and MMAs finish (bounded), frees its tensor memory
+ * and returns.  This call runs that path for real: one thread waits, with
+ * `poll_limit` polls, on an mbarrier nothing arrives on.  It allocates 4 bytes of
+ * device memory, synchronises the device, and sets *completed to 0 when the
+ * wait ran out (the expected result); CPR_ERR_DEVICE_TIMEOUT is then readable
+ * with cpr_get_device_error. */
+int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed);
+
 #ifdef __cplusplus
 }
 #endif

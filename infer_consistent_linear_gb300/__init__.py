@@ -94,6 +94,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_bwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                             P, SZ, P]),
         "cpr_gdn_fwd_train": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
+        "cpr_selftest_wait_timeout": (I, [U32, ctypes.POINTER(U32)]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -329,3 +330,12 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                            _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),
                            wsb, _stream()))
     return outs
+
+
+def selftest_wait_timeout(poll_limit: int = 4096) -> bool:
+    """Runs the device's bounded-wait expiry path once (see include/cpr_gdn.h);
+    returns True when the wait ran out as it must."""
+    lib = load_library()
+    done = ctypes.c_uint32(1)
+    _check(lib.cpr_selftest_wait_timeout(poll_limit, ctypes.byref(done)))
+    return done.value == 0

@@ -553,6 +553,20 @@ int cpr_get_device_error(uint32_t* code, int clear) {
     return CPR_OK;
 }
 
+int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
+    if (!completed) return fail(CPR_ERR_INVALID_ARG, "completed is NULL");
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    uint32_t* d_ok = nullptr;
+    cudaError_t e = cudaMalloc(&d_ok, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "selftest alloc");
+    e = cpr::tc_wait_timeout_selftest(err, poll_limit, d_ok, nullptr);
+    if (e == cudaSuccess) e = cudaMemcpy(completed, d_ok, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    cudaFree(d_ok);
+    if (e != cudaSuccess) return cuda_fail(e, "selftest");
+    return CPR_OK;
+}
+
 const char* cpr_last_error(void) { return g_msg; }
 
 }  // extern "C"

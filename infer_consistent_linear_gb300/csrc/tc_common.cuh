@@ -157,12 +157,15 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* mbar, uint32_t parit
     return ok;
 }
 // Bounded wait for the phase with the given parity.  Returns false (and
-// records CPR_ERR_DEVICE_TIMEOUT) if it does not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t* err) {
-    for (uint32_t it = 0; it < (1u << 22); ++it)
+// records CPR_ERR_DEVICE_TIMEOUT) if it does not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* mbar, uint32_t parity, uint32_t* err, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it)
         if (mbar_try_wait(mbar, parity)) return true;
     set_error(err, CPR_ERR_DEVICE_TIMEOUT);
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t* err) {
+    return mbar_wait_n(mbar, parity, err, 1u << 22);
 }
 
 // ---- bulk async copy (global -> shared), completion on an mbarrier ----------------

@@ -66,7 +66,24 @@ cudaError_t state_bwd(const tc::TcBwdArgs& a, int n_seq, int H, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// The timeout path of the bounded waits: one thread waits on an mbarrier that
+// nothing arrives on, with a short poll limit; it records CPR_ERR_DEVICE_TIMEOUT,
+// the kernel returns and the context stays usable.
+__global__ void k_wait_timeout(uint32_t* err, uint32_t limit, uint32_t* ok_out) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init_fence();
+    const bool ok = tc::mbar_wait_n(&bar, 0, err, limit);
+    *ok_out = ok ? 1u : 0u;
+}
+
 }  // namespace
+
+cudaError_t tc_wait_timeout_selftest(uint32_t* err, uint32_t limit, uint32_t* ok_out, cudaStream_t st) {
+    k_wait_timeout<<<1, 32, 0, st>>>(err, limit, ok_out);
+    return cudaGetLastError();
+}
 
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st) {
     cudaError_t e = set_smem(tc::k_tc_prep, tc::kPrepSmem);

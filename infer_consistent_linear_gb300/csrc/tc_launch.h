@@ -11,6 +11,8 @@ struct TcDecArgs;
 // setup must already have run on `st`; a.dvs selects the state-pass split width.
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st);
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st);
+// Test support: a bounded mbarrier wait that cannot complete (see cpr_selftest_wait_timeout).
+cudaError_t tc_wait_timeout_selftest(uint32_t* err, uint32_t limit, uint32_t* ok_out, cudaStream_t st);
 // Training forward (prep + state pass writing the backward's tiles), reverse
 // state pass and per-chunk gradients; `f` must have train set and
 // blk_bytes = kBlockTrain, `b.ws` the same workspace blocks.  Without

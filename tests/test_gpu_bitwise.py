@@ -164,3 +164,16 @@ def test_decode_rejects_cache_of_another_contract():
     cpr.cpr_gdn_decode_step(x.q[69:], x.k[69:], x.v[69:], x.g[69:], x.beta[69:], cache,
                             contract=ca, out=o)
     assert cpr.get_device_error(clear=True) == 0
+
+
+def test_bounded_wait_expires_with_device_timeout_and_context_stays_usable():
+    cpr.get_device_error(clear=True)
+    assert cpr.selftest_wait_timeout(4096)                 # the wait ran out
+    assert cpr.get_device_error(clear=True) == 9           # CPR_ERR_DEVICE_TIMEOUT recorded
+    c = cpr.default_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+    x = make_inputs([100], 2, 128, 128, io_dtype=torch.bfloat16, seed=3)
+    o, _ = cpr.cpr_gdn_fwd(*(t.to(DEV) for t in (x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)), contract=c)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    o_ref, _ = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)
+    assert_close("o after the timeout", o, o_ref, TOL_BF16)
