@@ -185,6 +185,13 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     }
     int outstanding = 0;  // mbarrier phase an in-flight MMA group will complete, or -1
     if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid]) : 0.f;
+    // E_rs = exp(gam_r - gam_s), s <= r, once per pair, spread evenly over the threads while
+    // the S1 MMA runs (rows p and 63 - p together hold 65 entries), into the T buffer
+    for (int i = tid; i < 32 * (C + 1); i += 128) {
+        const int pr = i / (C + 1), k = i % (C + 1);
+        const int r = (k <= pr) ? pr : C - 1 - pr, s_ = (k <= pr) ? k : k - pr - 1;
+        Tfp[r * 65 + s_] = simt::decay(gam[r], gam[s_]);
+    }
     {
         const bool ok1 = mbar_wait(mbar, 0, a.err);
         fence_after();
@@ -199,10 +206,10 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
             if (tid < 64) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 32; ++j) {   // a_rs = (b_r E_rs) kk_rs, as a_entry
                     const int s = c0 + j;
                     At[s * C + (r & 1) * (C / 2) + (r >> 1)] =
-                        (s < r && r < nrows) ? simt::a_entry(bet[r], gam[r], gam[s], v[j]) : 0.f;
+                        (s < r && r < nrows) ? __fmul_rn(__fmul_rn(bet[r], Tfp[r * 65 + s]), v[j]) : 0.f;
                 }
             } else {
 #pragma unroll
@@ -212,7 +219,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
                     for (int e = 0; e < 8; ++e) {
                         const int s = c0 + j8 * 8 + e;
                         x[e] = (s <= r && r < nrows)
-                                   ? __fmul_rn(simt::decay(gam[r], gam[s]), __fmul_rn(a.scale, v[j8 * 8 + e]))
+                                   ? __fmul_rn(Tfp[r * 65 + s], __fmul_rn(a.scale, v[j8 * 8 + e]))
                                    : 0.f;
                     }
                     store8_split(blk + kOffPhi, blk + kOffPlo, cm_off(r, c0 + j8 * 8, C), x);
