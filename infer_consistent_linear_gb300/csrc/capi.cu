@@ -492,6 +492,7 @@ static int backward_impl(const cpr_contract* c, const uint8_t* digest, const voi
         tb.chunk_off = sa.chunk_off; tb.n_seq = n_seq; tb.H = H; tb.scale = c->scale; tb.ws = t.ws;
         tb.dO = dO; tb.dHT = dHT; tb.dq = static_cast<float*>(dq); tb.dk = static_cast<float*>(dk);
         tb.dv = static_cast<float*>(dv); tb.dg = dg; tb.dbeta = dbeta; tb.dh0 = dh0; tb.err = err;
+        tb.nsplit = (int)c->dv_splits;
         e = cpr::tc_backward(t, tb, w.cmax, n_seq, H, st, !saved);
         if (e != cudaSuccess) return cuda_fail(e, "backward launch");
         return CPR_OK;

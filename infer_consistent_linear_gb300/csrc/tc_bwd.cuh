@@ -55,8 +55,16 @@ struct TcBwdArgs {
     float* dg;
     float* dbeta;
     float* dh0;
+    int nsplit;           // d_v splits of the reverse state pass (2 or 4)
     uint32_t* err;
 };
+
+// Sum over the 32 lanes of a warp in a fixed tree (lane 0 gets the result).
+__device__ __forceinline__ float warp_sum_tree(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, o));
+    return x;
+}
 
 // ---- reverse state pass ---------------------------------------------------------------
 template <int DVS>
@@ -70,8 +78,9 @@ struct SbSmem {
     static constexpr size_t B1lo = B1hi + DVS * 64 * 2;
     static constexpr size_t B2hi = B1lo + DVS * 64 * 2;      // G scale dO, then -bg dR
     static constexpr size_t B2lo = B2hi + DVS * 64 * 2;
-    static constexpr size_t Vec = B2lo + DVS * 64 * 2;      // gam, Gm, dec, bg (64 fp32 each)
-    static constexpr size_t Bar = Vec + 4 * 256;             // 5 mbarriers + TMEM base
+    static constexpr size_t Vec = B2lo + DVS * 64 * 2;      // gam, Gm, dec, bg (64 fp32 each),
+                                                             // 8 warp sums
+    static constexpr size_t Bar = Vec + 5 * 256;             // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -87,6 +96,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
     float* Gm = gam + 64;
     float* dec = Gm + 64;
     float* bgv = dec + 64;
+    float* red = bgv + 64;
     uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);
     uint64_t* bar_P = bar_mma + 1;
     uint64_t* bar_T = bar_mma + 2;
@@ -180,6 +190,18 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         return (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     };
 
+    // this thread's part of H_n (row d, its columns) for <dH', H_n>, loaded a chunk ahead
+    uint4 hn[HALF / 4];
+    auto load_hn = [&](int n) {
+        const unsigned char* g = blk_of(n) + kOffHn;
+#pragma unroll
+        for (int j8 = 0; j8 < HALF / 8; ++j8) {
+            const uint32_t off = cm_off(d, j0 + cb + j8 * 8, D);
+            hn[2 * j8] = *reinterpret_cast<const uint4*>(g + off);
+            hn[2 * j8 + 1] = *reinterpret_cast<const uint4*>(g + 32768 + off);
+        }
+    };
+    if (nch > 0) load_hn(nch - 1);
     put_dh(nch - 1);
     float bcur = 0.f;
     if (nch > 0) {
@@ -260,6 +282,21 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             mma_commit(bar_mma);
         }
         mma_out = true;
+        {
+            // <dH', H_n> over this thread's columns (dH' = dHreg, still chunk n's) while the
+            // MMAs run, then a fixed tree over the warp; the next chunk's H_n follows
+            float acc = 0.f;
+#pragma unroll
+            for (int j8 = 0; j8 < HALF / 8; ++j8) {
+                float hv[8];
+                join8(hn[2 * j8], hn[2 * j8 + 1], hv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = __fmaf_rn(dHreg[j8 * 8 + e], hv[e], acc);
+            }
+            acc = warp_sum_tree(acc);
+            if (lane == 0) red[warp] = acc;
+            if (n > 0) load_hn(n - 1);
+        }
         ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -288,6 +325,11 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         }
         fence_async_smem();
         tc_sync();
+        if (tid == 0) {  // this split's share of <dH', H_n>, warps in order
+            float s = 0.f;
+            for (int w = 0; w < 8; ++w) s = __fadd_rn(s, red[w]);
+            reinterpret_cast<float*>(blk_of(n) + kOffHdot)[sp] = s;
+        }
         ok = mbar_wait(bar_T, ph_T, a.err);
         if (__syncthreads_or(!ok)) { failed = true; break; }
         ph_T ^= 1u;
@@ -396,13 +438,6 @@ struct GradSmem {
     static constexpr size_t Total = Bar + 64;
 };
 
-// Sum over the 32 lanes of a warp in a fixed tree (lane 0 gets the result).
-__device__ __forceinline__ float warp_sum_tree(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xffffffffu, x, o));
-    return x;
-}
-
 static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     using L = GradSmem;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -416,7 +451,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     float *gam = vec, *Gm = vec + 64, *bet = vec + 128, *bgv = vec + 192, *dec = vec + 256,
           *qh = vec + 320, *kh = vec + 448, *rowA = vec + 576, *rowB = vec + 704, *dbA = vec + 832,
           *dRv = vec + 960, *colE = vec + 1024, *eL = vec + 1088, *dgam = vec + 1216,
-          *red = vec + 1280;   // red: 8 warp sums; 1288 floats in all
+          *red = vec + 1280;   // red: the d_v splits' shares of <dH', H_n>; 1284 floats in all
     uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + L::Bar);   // Q, K, dR, Delta, gam
     uint64_t* bar_hn = bar_in + 1;                                   // H_n
     uint64_t* bar_dh = bar_in + 2;                                   // dH'
@@ -436,7 +471,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     auto blk_of = [&](int w) { return a.ws + (size_t)w * kBlockTrain; };   // w = cidx * H + h
     auto issue_in = [&](int w) {
         const unsigned char* blk = blk_of(w);
-        mbar_expect_tx(bar_in, 6 * 16384 + 256);
+        mbar_expect_tx(bar_in, 6 * 16384 + 256 + 16);
         bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_in);     // Q rows
         bulk_g2s(QK + 16384, blk + kOffKmn, 16384, bar_in);      // K rows
         bulk_g2s(Rhi + 16384, blk + kOffdR, 16384, bar_in);
@@ -444,6 +479,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(Rhi + 32768, blk + kOffDl, 16384, bar_in);
         bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_in);
         bulk_g2s(gam, blk + kOffGam, 256, bar_in);
+        bulk_g2s(red, blk + kOffHdot, 16, bar_in);               // the splits' <dH', H_n>
     };
     auto issue_hn = [&](int w) {
         mbar_expect_tx(bar_hn, 65536);
@@ -658,24 +694,6 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     }
     mma_out = true;
     {
-        // <dH', H_n>: row d = tid & 127, half of the columns per thread; H_n again from
-        // the workspace (just bulk-read, so mostly in L2), dH' from shared memory
-        const int d = tid & 127, jh = tid >> 7;
-        float acc = 0.f;
-#pragma unroll
-        for (int j8 = jh * 8; j8 < jh * 8 + 8; ++j8) {
-            const uint32_t off = cm_off(d, j8 * 8, D);
-            float hv[8], dv8[8];
-            join8(*reinterpret_cast<const uint4*>(blk + kOffHn + off),
-                  *reinterpret_cast<const uint4*>(blk + kOffHn + 32768 + off), hv);
-            join8(*reinterpret_cast<const uint4*>(Bt + off), *reinterpret_cast<const uint4*>(Bt + 32768 + off), dv8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc = __fmaf_rn(dv8[e], hv[e], acc);
-        }
-        acc = warp_sum_tree(acc);
-        if (lane == 0) red[warp] = acc;
-    }
-    {
         const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -757,7 +775,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         if (rr == Lr) {
             float sumL = 0.f, rs = 0.f;
             for (int s = 0; s < Lr; ++s) sumL = __fadd_rn(sumL, dgam[s]);
-            for (int w = 0; w < 8; ++w) rs = __fadd_rn(rs, red[w]);
+            for (int w = 0; w < a.nsplit; ++w) rs = __fadd_rn(rs, red[w]);
             dgr = __fadd_rn(dgr, __fadd_rn(__fmul_rn(Gm[Lr], rs), sumL));
         }
         colE[rr] = (rr < nrows) ? dgr : 0.f;   // dgam_r

@@ -49,6 +49,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 // ---- TMEM --------------------------------------------------------------------
 // Whole-warp operations.
+// The CTA's only allocation (it gives up the permit to allocate again); blocks until
+// the columns are free.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");

@@ -47,7 +47,8 @@ constexpr size_t kOffHn = kOffT + 16384;       // chunk-start state H_n, 128 x 1
 constexpr size_t kOffDl = kOffHn + 65536;      // Delta, 64 x 128 (s, j): hi, lo
 constexpr size_t kOffdH = kOffDl + 32768;      // dL/dH_{n+1}, 128 x 128 (d, j): hi, lo
 constexpr size_t kOffdR = kOffdH + 65536;      // dL/dR, 64 x 128 (r, j): hi, lo
-constexpr size_t kBlockTrain = kOffdR + 32768;
+constexpr size_t kOffHdot = kOffdR + 32768;    // <dH', H_n> over each d_v split's columns (fp32 x 4)
+constexpr size_t kBlockTrain = kOffHdot + 256;
 
 struct TcArgs {
     const __nv_bfloat16* q;
@@ -113,18 +114,21 @@ __device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int
 }
 
 // ---- prep: everything of a chunk that does not depend on H ------------------------
-// [K; Q] K-major (32 KB; the K rows double as the MN-major d x token K tile, the
-// two layouts being byte-identical), V MN-major, A^T, T, gate vectors.
-constexpr size_t kPrepOffVmn = 32768, kPrepOffAt = 49152, kPrepOffT = 49152 + 16384,
-                 kPrepOffVec = kPrepOffT + 64 * 65 * 4;
+// Shared memory (65 KB, three CTAs per SM): [K; Q] K-major (32 KB; the K rows double
+// as the MN-major d x token K tile, the two layouts being byte-identical), V MN-major
+// (16 KB), the fp32 T buffer (E table, then T, then the X2 tiles), gate vectors.  A^T
+// and then the X1 tiles take the Q rows' space once the S1 MMA has read it.  The 256
+// TMEM columns are allocated once the copies are in flight: with three CTAs per SM
+// the third one's allocation waits for another CTA to finish, but its loads do not.
+constexpr size_t kPrepOffVmn = 32768, kPrepOffT = 49152, kPrepOffVec = kPrepOffT + 64 * 65 * 4;
 constexpr size_t kPrepSmem = kPrepOffVec + 3 * 64 * 4 + 64;
 
-static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
+static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later X1
+    unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later A^T, X1
     unsigned char* tKmn = sm;                      // the K rows read as an MN-major 128 (d) x 64 tile
     unsigned char* tVmn = sm + kPrepOffVmn;        // V, MN-major
-    float* At = reinterpret_cast<float*>(sm + kPrepOffAt);   // [64][64], a_rs at s * 64 + (r & 1) * 32 + r / 2
+    float* At = reinterpret_cast<float*>(sm + 16384);        // [64][64], a_rs at s * 64 + (r & 1) * 32 + r / 2
     float* Tfp = reinterpret_cast<float*>(sm + kPrepOffT);   // [64][65]
     float* gam = reinterpret_cast<float*>(sm + kPrepOffVec);
     float* bet = gam + 64;
@@ -144,7 +148,6 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned char* blk = a.ws + ((size_t)cidx * H + h) * a.blk_bytes;
 
-    if (warp == 0) tmem_alloc(tbase, 256);
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init_fence();
@@ -163,6 +166,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
         gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
         bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     }
+    if (warp == 0) tmem_alloc(tbase, 256);   // while the copies land
     cp_async_wait_all();
     __syncthreads();
     if (tid == 0) {  // gate prefix: serial fp32 sum in token order
@@ -175,6 +179,8 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
+    bool held = true;      // the TMEM columns, released before the last bulk stores
+    int outstanding = 0;   // mbarrier phase an in-flight MMA group will complete, or -1
     if (tid == 0) {
         mma_tile<128, 64, D>(tmem, tKQ, tKQ, false);  // B = rows 0..63 of [K; Q] = K
         mma_commit(mbar);
@@ -183,7 +189,6 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
         bulk_s2g(blk + kOffKmn, tKmn, 16384);
         bulk_commit();
     }
-    int outstanding = 0;  // mbarrier phase an in-flight MMA group will complete, or -1
     if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid]) : 0.f;
     // E_rs = exp(gam_r - gam_s), s <= r, once per pair, spread evenly over the threads while
     // the S1 MMA runs (rows p and 63 - p together hold 65 entries), into the T buffer
@@ -195,6 +200,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     {
         const bool ok1 = mbar_wait(mbar, 0, a.err);
         fence_after();
+        if (tid == 0) bulk_wait_read();  // the Q rows' space takes A^T next
         if (__syncthreads_or(!ok1)) goto done;
     }
     outstanding = -1;
@@ -229,37 +235,45 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     }
     __syncthreads();
     t_solve_pairs(At, Tfp, 65, nrows);
-    if (tid == 0) bulk_wait_read();  // the Q rows' space takes X1 next
     __syncthreads();
+    if (a.cache && last && nrows < C) {  // decode cache: T rows of the last, partial chunk
+        float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + ((size_t)b * H + h) * C * C;
+        for (int i = tid; i < nrows * C; i += 128) ct[i] = Tfp[(i / C) * 65 + (i % C)];
+    }
     {
         // X1 = T diag(b G) (threads 0..63, into the Q rows' space), X2 = T diag(b)
-        // (threads 64..127, into the A^T space), split
+        // (threads 64..127, over the T buffer once every row of T is in registers), split
         const int r = tid & 63, which = tid >> 6;
-        unsigned char* xhi = which ? reinterpret_cast<unsigned char*>(At) : tKQ + 16384;
+        float trow[C];
+#pragma unroll
+        for (int s = 0; s < C; ++s) trow[s] = Tfp[r * 65 + s];
+        __syncthreads();
+        unsigned char* xhi = which ? reinterpret_cast<unsigned char*>(Tfp) : tKQ + 16384;
         unsigned char* xlo = xhi + 8192;
         const float* sc = which ? bet : bg;
+#pragma unroll
         for (int s8 = 0; s8 < C / 8; ++s8) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(Tfp[r * 65 + s8 * 8 + e], sc[s8 * 8 + e]);
+            for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(trow[s8 * 8 + e], sc[s8 * 8 + e]);
             store8_split(xhi, xlo, cm_off(r, s8 * 8, C), x);
         }
         if (a.train && which == 0) {  // T itself, for dR = T^T dDelta in the backward
+#pragma unroll
             for (int s8 = 0; s8 < C / 8; ++s8) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = Tfp[r * 65 + s8 * 8 + e];
+                for (int e = 0; e < 8; ++e) x[e] = trow[s8 * 8 + e];
                 store8_split(blk + kOffT, blk + kOffT + 8192, cm_off(r, s8 * 8, C), x);
             }
         }
     }
-    if (a.cache && last && nrows < C) {  // decode cache: rows of the last, partial chunk
+    if (a.cache && last && nrows < C) {  // decode cache: the other rows of the last, partial chunk
         const size_t sh = (size_t)b * H + h;
         __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
         __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
         float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
         float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
-        float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
         for (int i = tid; i < nrows * (D / 8); i += 128) {
             const int r = i / (D / 8), d8 = i % (D / 8);
             const size_t src = ((size_t)(t0 + r) * H + h) * D + d8 * 8;
@@ -270,12 +284,11 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
             cg[tid] = gam[tid];
             cb[tid] = bet[tid];
         }
-        for (int i = tid; i < nrows * C; i += 128) ct[i] = Tfp[(i / C) * 65 + (i % C)];
     }
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        unsigned char* x2 = reinterpret_cast<unsigned char*>(At);
+        unsigned char* x2 = reinterpret_cast<unsigned char*>(Tfp);
         mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 16384, tKmn, false);        // W' = X1_hi K
         mma_tile_mj<64, D, C, false, true>(tmem, tKQ + 24576, tKmn, true);         //    + X1_lo K
         mma_tile_mj<64, D, C, false, true>(tmem + 128, x2, tVmn, false);           // U  = X2_hi V
@@ -292,7 +305,7 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
     {
         // W' and U rows (M = 64 layout, row r = 16 * warp + lane for lanes < 16) are
         // staged in the now free operand space in their workspace layouts, then
-        // bulk-stored: W' hi, lo over the [K; Q] tile, U over the V and A^T space
+        // bulk-stored: W' hi, lo over the [K; Q] tile, U over the V tile and the T buffer
         const int r = warp * 16 + lane;
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -322,7 +335,9 @@ static __global__ void __launch_bounds__(128, 2) k_tc_prep(TcArgs a) {
             }
         }
         fence_async_smem();
-        __syncthreads();
+        tc_sync();
+        if (warp == 0) tmem_dealloc(tmem, 256);
+        held = false;
         if (tid == 0) {
             bulk_s2g(blk + kOffA4hi, tKQ, 16384);
             bulk_s2g(blk + kOffA4lo, tKQ + 16384, 16384);
@@ -335,7 +350,7 @@ done:
     if (outstanding >= 0) mbar_wait(mbar, (uint32_t)outstanding, a.err);  // bounded
     if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
     tc_sync();
-    if (warp == 0) tmem_dealloc(*tbase, 256);
+    if (warp == 0 && held) tmem_dealloc(tmem, 256);
 }
 
 // ---- state pass: one CTA per (sequence, head, d_v split), chunks in order -----------
