@@ -238,7 +238,10 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         pendP = false;
         {
             // token row rr, a quarter of the columns per thread: dO (B1) and G scale dO
-            // (B2) rows, MN-major (j, t)
+            // (B2) rows, MN-major (j, t); dO also to the workspace (K-major (r, j)) and
+            // beta (split 0) for k_tc_grad
+            unsigned char* gdo = blk_of(n) + kOffdO;
+            if (sp == 0 && tid < C) reinterpret_cast<float*>(blk_of(n) + kOffBet)[tid] = bcur;
             const bool in = rr < nrows;
             const float gr = gam[rr];
             const float Gr = in ? simt::gate(gr) : 0.f;
@@ -256,7 +259,12 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
                 float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(gs, x[e]);
-                store8_split(sm + L::B1hi, sm + L::B1lo, mn_off(j8 * 8, rr, DVS), x);
+                uint4 hi, lo;
+                split8(x, hi, lo);
+                *reinterpret_cast<uint4*>(sm + L::B1hi + mn_off(j8 * 8, rr, DVS)) = hi;
+                *reinterpret_cast<uint4*>(sm + L::B1lo + mn_off(j8 * 8, rr, DVS)) = lo;
+                *reinterpret_cast<uint4*>(gdo + cm_off(rr, j0 + j8 * 8, D)) = hi;
+                *reinterpret_cast<uint4*>(gdo + 16384 + cm_off(rr, j0 + j8 * 8, D)) = lo;
                 store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(j8 * 8, rr, DVS), y);
             }
         }
@@ -471,7 +479,9 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     auto blk_of = [&](int w) { return a.ws + (size_t)w * kBlockTrain; };   // w = cidx * H + h
     auto issue_in = [&](int w) {
         const unsigned char* blk = blk_of(w);
-        mbar_expect_tx(bar_in, 6 * 16384 + 256 + 16);
+        mbar_expect_tx(bar_in, 8 * 16384 + 2 * 256 + 16);
+        bulk_g2s(Rhi, blk + kOffdO, 16384, bar_in);              // dO rows, split
+        bulk_g2s(Rlo, blk + kOffdO + 16384, 16384, bar_in);
         bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_in);     // Q rows
         bulk_g2s(QK + 16384, blk + kOffKmn, 16384, bar_in);      // K rows
         bulk_g2s(Rhi + 16384, blk + kOffdR, 16384, bar_in);
@@ -480,6 +490,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_in);
         bulk_g2s(gam, blk + kOffGam, 256, bar_in);
         bulk_g2s(red, blk + kOffHdot, 16, bar_in);               // the splits' <dH', H_n>
+        bulk_g2s(bet, blk + kOffBet, 256, bar_in);
     };
     auto issue_hn = [&](int w) {
         mbar_expect_tx(bar_hn, 65536);
@@ -517,23 +528,6 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     const int Lr = nrows - 1;
     const unsigned char* blk = blk_of(w);
     tc_sync();   // the previous item's TMEM reads and shared-memory use are over
-    // dO rows (zero past the chunk's end) split into R rows 0..63
-#pragma unroll 4
-    for (int i = tid; i < 64 * (D / 8); i += 256) {
-        const int rr = i / (D / 8), d8 = i % (D / 8);
-        float x[8];
-        if (rr < nrows) {
-            const float4* src = reinterpret_cast<const float4*>(a.dO + ((size_t)(t0 + rr) * H + h) * D + d8 * 8);
-            const float4 u0 = src[0], u1 = src[1];
-            x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-            x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-        store8_split(Rhi, Rlo, cm_off(rr, d8 * 8, D), x);
-    }
-    if (tid < C) bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     {
         const bool ok = mbar_wait(bar_in, ph, a.err) && mbar_wait(bar_hn, ph, a.err);
         fence_async_smem();

@@ -48,7 +48,9 @@ constexpr size_t kOffDl = kOffHn + 65536;      // Delta, 64 x 128 (s, j): hi, lo
 constexpr size_t kOffdH = kOffDl + 32768;      // dL/dH_{n+1}, 128 x 128 (d, j): hi, lo
 constexpr size_t kOffdR = kOffdH + 65536;      // dL/dR, 64 x 128 (r, j): hi, lo
 constexpr size_t kOffHdot = kOffdR + 32768;    // <dH', H_n> over each d_v split's columns (fp32 x 4)
-constexpr size_t kBlockTrain = kOffHdot + 256;
+constexpr size_t kOffBet = kOffHdot + 256;     // beta of the chunk's rows (fp32 x 64, 0 past the end)
+constexpr size_t kOffdO = kOffBet + 256;       // dO, 64 x 128 (r, j): hi, lo (rows past the end 0)
+constexpr size_t kBlockTrain = kOffdO + 32768;
 
 struct TcArgs {
     const __nv_bfloat16* q;
