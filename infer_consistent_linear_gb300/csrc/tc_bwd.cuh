@@ -269,10 +269,6 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             }
         }
         const float GL = simt::gate(gam[Lr]);
-        if (n > 0) {   // the next chunk's dO slice and beta, a chunk ahead
-            load_dO(n - 1);
-            bcur = beta_of(n - 1);
-        }
         fence_async_smem();
         ok = mbar_wait(bar_KQ + cur, ph_KQ[cur], a.err);
         fence_after();
@@ -292,7 +288,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         mma_out = true;
         {
             // <dH', H_n> over this thread's columns (dH' = dHreg, still chunk n's) while the
-            // MMAs run, then a fixed tree over the warp; the next chunk's H_n follows
+            // MMAs run, then a fixed tree over the warp.  The next chunk's dO slice, beta
+            // and H_n are loaded here, just after a proxy fence: a fence.proxy.async waits
+            // for this thread's global loads in flight, and the next one is a phase away.
             float acc = 0.f;
 #pragma unroll
             for (int j8 = 0; j8 < HALF / 8; ++j8) {
@@ -303,7 +301,11 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             }
             acc = warp_sum_tree(acc);
             if (lane == 0) red[warp] = acc;
-            if (n > 0) load_hn(n - 1);
+            if (n > 0) {
+                load_dO(n - 1);
+                bcur = beta_of(n - 1);
+                load_hn(n - 1);
+            }
         }
         ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();

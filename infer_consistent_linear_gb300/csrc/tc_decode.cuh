@@ -185,13 +185,14 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         gams[p] = __fadd_rn(p > 0 ? cg[p - 1] : 0.f, a.g[sh]);
         bets[p] = a.beta[sh];
     }
-    // this thread's column of the cached T rows (for the T row chain), loaded early
-    float tcol[C];
-#pragma unroll
-    for (int s = 0; s < C; ++s) tcol[s] = (tid < C && s < p) ? ct[s * C + tid] : 0.f;
     cp_async_wait_all();
     fence_async_smem();
     tc_sync();
+    // this thread's column of the cached T rows (for the T row chain), loaded after the
+    // proxy fence (which would wait for them) so that they land while the S1 MMA runs
+    float tcol[C];
+#pragma unroll
+    for (int s = 0; s < C; ++s) tcol[s] = (tid < C && s < p) ? ct[s * C + tid] : 0.f;
     const uint32_t tmem = *tbase;
     uint32_t phase = 0;
     bool ok = true;
