@@ -374,7 +374,8 @@ struct StateSmem {
     static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32, [DVS/4][64] float4
     static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 (bulk copied)
     static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
-    static constexpr size_t Bar = Dec + 256;                 // 5 mbarriers + TMEM base
+    static constexpr size_t Ost = Dec + 256;                 // output rows, 64 x (DVS + 4) fp32
+    static constexpr size_t Bar = Ost + 64 * (DVS + 4) * 4;  // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
     static constexpr uint32_t LoadA = 32768 + 16384 + 256;   // A4 tiles + gam
     static constexpr uint32_t LoadB = 16384 + 64 * DVS * 4;  // K, U
@@ -487,7 +488,24 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         mbar_expect_tx(bar_ldP, L::LoadP);
         bulk_g2s(sm + L::Phi, blk_of(n) + kOffPhi, 16384, bar_ldP);
     };
-    // output rows of chunk m: o_r = G_r (scale qh_r) + (P Delta)_r
+    // output rows of chunk m: o_r = G_r (scale qh_r) + (P Delta)_r, staged in Ost (rows
+    // padded to DVS + 4 floats: conflict-free writes).  o_copy (the 128 threads of lane
+    // quarters 2 and 3, idle while the Delta epilogue runs) stores them, whole rows per
+    // warp instruction.
+    float* ost = reinterpret_cast<float*>(sm + L::Ost);
+    auto o_copy = [&](int m) {
+        if (!a.o) return;
+        constexpr int R4 = DVS / 4;   // float4 per row
+        const int t0 = seq0 + m * C, nrows = min(C, T - m * C);
+        const int lt = ((warp & 3) - 2) * 64 + (warp >> 2) * 32 + lane;  // 0..127 over warps 2, 3, 6, 7
+#pragma unroll
+        for (int i = 0; i < 64 * R4 / 128; ++i) {
+            const int idx = i * 128 + lt, r = idx / R4, c4 = idx % R4;
+            if (r < nrows)
+                *reinterpret_cast<float4*>(a.o + ((size_t)(t0 + r) * H + h) * D + j0 + 4 * c4) =
+                    *reinterpret_cast<const float4*>(ost + r * (DVS + 4) + 4 * c4);
+        }
+    };
     auto o_epilogue = [&](int m) -> bool {
         const bool w = mbar_wait(bar_pd, ph_pd, a.err);
         fence_after();
@@ -499,7 +517,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
             issue_P(m + 1);
         }
         pendP = (m + 1 < nch);
-        const int t0 = seq0 + m * C, nrows = min(C, T - m * C);
+        const int nrows = min(C, T - m * C);
         float v[32];
         if (quarter >= 2) {  // Q H rows (accumulator rows 64..127) -> sQ, scaled by G_r
             tmem_ld32(taddr_of(acc4(m), warp, cb), v);
@@ -517,7 +535,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         tmem_ld32(taddr_of(acc5(m), warp, cb), v);  // M = 64: row 16 quarter + lane, lanes < 16
         const int r = quarter * 16 + lane;
         if (lane < 16 && r < nrows && a.o) {
-            float* orow = a.o + ((size_t)(t0 + r) * H + h) * D + j0 + cb;
+            float* orow = ost + r * (DVS + 4) + cb;
 #pragma unroll
             for (int j4 = 0; j4 < HALF / 4; ++j4) {
                 const float4 q4 = reinterpret_cast<const float4*>(sQ)[(cb / 4 + j4) * 64 + r];
@@ -609,6 +627,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
                     *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
                 }
             }
+        } else if (n > 0) {
+            o_copy(n - 1);   // staged by o_epilogue(n - 1), barriers ago
         }
         if (cstate && last && nrows < C) put_state(cstate);
         fence_async_smem();
@@ -651,6 +671,10 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         tc_sync();
     }
     if (!failed && nch > 0 && !o_epilogue(nch - 1)) failed = true;
+    if (!failed && nch > 0) {
+        __syncthreads();
+        if (quarter >= 2) o_copy(nch - 1);
+    }
     if (!failed && a.final_state) put_state(a.final_state + sh * D * D);
     if (failed) {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
