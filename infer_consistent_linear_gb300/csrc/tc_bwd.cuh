@@ -555,6 +555,41 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         mma_commit(bar_mma);
     }
     mma_out = true;
+    if (tid >= 128) {
+        // dv = b dR and dR . v while the first MMA group runs (dR, beta and the v rows are
+        // all in): a warp per row, 16-byte pieces side by side, the v rows loaded first
+        const int t = tid - 128, w4 = t >> 5, c4 = (t & 31) * 4;
+        uint2 vrow[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int rr = w4 + 4 * k;
+            vrow[k] = (rr < nrows) ? *reinterpret_cast<const uint2*>(a.v + ((size_t)(t0 + rr) * H + h) * D + c4)
+                                   : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int rr = w4 + 4 * k;
+            if (rr >= nrows) break;
+            const uint32_t off = cm_off(rr, c4, D);
+            const uint2 hi = *reinterpret_cast<const uint2*>(Rhi + 16384 + off);
+            const uint2 lo = *reinterpret_cast<const uint2*>(Rlo + 16384 + off);
+            const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&hi);
+            const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&lo);
+            const size_t g = ((size_t)(t0 + rr) * H + h) * D + c4;
+            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vrow[k]);
+            const float brr = bet[rr];
+            float x[4], sdot = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[e] = __fadd_rn(__bfloat162float(hh[e]), __bfloat162float(ll[e]));
+                sdot = __fmaf_rn(x[e], __bfloat162float(vb[e]), sdot);
+            }
+            *reinterpret_cast<float4*>(a.dv + g) =
+                make_float4(__fmul_rn(brr, x[0]), __fmul_rn(brr, x[1]), __fmul_rn(brr, x[2]), __fmul_rn(brr, x[3]));
+            sdot = warp_sum_tree(sdot);
+            if ((t & 31) == 0) dRv[rr] = sdot;
+        }
+    }
     {
         const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
@@ -641,40 +676,6 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         float acc = 0.f;
         for (int rr = s + 1; rr < nrows; ++rr) acc = __fadd_rn(acc, scr[rr * 65 + s]);
         colE[s] = acc;
-    } else if (tid >= 128) {
-        // dv = b dR and dR . v, a warp per row, 16-byte pieces side by side; every
-        // row's v loads are issued before any is used
-        const int t = tid - 128, w4 = t >> 5, c4 = (t & 31) * 4;
-        uint2 vrow[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int rr = w4 + 4 * k;
-            vrow[k] = (rr < nrows) ? *reinterpret_cast<const uint2*>(a.v + ((size_t)(t0 + rr) * H + h) * D + c4)
-                                   : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int rr = w4 + 4 * k;
-            if (rr >= nrows) break;
-            const uint32_t off = cm_off(rr, c4, D);
-            const uint2 hi = *reinterpret_cast<const uint2*>(Rhi + 16384 + off);
-            const uint2 lo = *reinterpret_cast<const uint2*>(Rlo + 16384 + off);
-            const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&hi);
-            const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&lo);
-            const size_t g = ((size_t)(t0 + rr) * H + h) * D + c4;
-            const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(&vrow[k]);
-            const float brr = bet[rr];
-            float x[4], sdot = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[e] = __fadd_rn(__bfloat162float(hh[e]), __bfloat162float(ll[e]));
-                sdot = __fmaf_rn(x[e], __bfloat162float(vb[e]), sdot);
-            }
-            *reinterpret_cast<float4*>(a.dv + g) =
-                make_float4(__fmul_rn(brr, x[0]), __fmul_rn(brr, x[1]), __fmul_rn(brr, x[2]), __fmul_rn(brr, x[3]));
-            sdot = warp_sum_tree(sdot);
-            if ((t & 31) == 0) dRv[rr] = sdot;
-        }
     }
     {
         // dH' has arrived: X2 = [dR; Delta] dH'^T (rows 64.. are Delta dH'^T)
