@@ -808,18 +808,18 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
             tmem_ld32(taddr_of(tmem + tdq, warp, c0), y);
             tmem_ld32(taddr_of(tmem + tX2, warp, c0), z);
             tmem_ld32(taddr_of(tmem + tdk, warp, c0), w2);
-            if (in) {
+            if (in) {   // whole 32-byte sectors: one row per lane
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float o4[4];
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    float o8[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * j4 + e;
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * j8 + e;
                         // bottom: -bg X1 + dec X2 + (s G1)^T Q + G2^T K + G2 K (the last from tdq)
-                        o4[e] = top ? __fmul_rn(scale, __fmaf_rn(gr, x1[j], y[j]))
+                        o8[e] = top ? __fmul_rn(scale, __fmaf_rn(gr, x1[j], y[j]))
                                     : __fadd_rn(__fadd_rn(__fmaf_rn(nb, x1[j], __fmul_rn(dr, z[j])), w2[j]), y[j]);
                     }
-                    *reinterpret_cast<float4*>(out + c0 + 4 * j4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                    st_global_v8(out + c0 + 8 * j8, o8);
                 }
             }
         }

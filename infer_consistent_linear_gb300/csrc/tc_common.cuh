@@ -184,6 +184,12 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src_smem, uint32
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                  :: "l"(dst), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
 }
+// One 32-byte global store (a whole sector): p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float* p, const float (&x)[8]) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                    "f"(x[7]) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
