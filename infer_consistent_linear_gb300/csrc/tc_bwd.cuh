@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
     // loaded into registers one chunk ahead; rows past the end are zero
     constexpr int NJ8 = DVS / 32;                     // 8-column groups per thread
     const int rr = tid & 63, part = tid >> 6;
+    // (the loads read a valid row unconditionally; rows past the end are masked where
+    // the values are used, so that nothing waits on the loads where they are issued)
     float4 dOpre[2 * NJ8];
     auto load_dO = [&](int n) {
         const int t0 = seq0 + n * C;
@@ -181,13 +183,13 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
 #pragma unroll
         for (int q = 0; q < NJ8; ++q) {
             const int j8 = part * NJ8 + q;
-            dOpre[2 * q] = in ? src[2 * j8] : make_float4(0.f, 0.f, 0.f, 0.f);
-            dOpre[2 * q + 1] = in ? src[2 * j8 + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+            dOpre[2 * q] = src[2 * j8];
+            dOpre[2 * q + 1] = src[2 * j8 + 1];
         }
     };
     auto beta_of = [&](int n) {
         const int t0 = seq0 + n * C, nrows = min(C, T - n * C);
-        return (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+        return a.beta[(size_t)(t0 + (tid < nrows ? tid : 0)) * H + h];
     };
 
     // this thread's part of H_n (row d, its columns) for <dH', H_n>, loaded a chunk ahead
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             // (B2) rows, MN-major (j, t); dO also to the workspace (K-major (r, j)) and
             // beta (split 0) for k_tc_grad
             unsigned char* gdo = blk_of(n) + kOffdO;
+            bcur = (tid < nrows) ? bcur : 0.f;
             if (sp == 0 && tid < C) reinterpret_cast<float*>(blk_of(n) + kOffBet)[tid] = bcur;
             const bool in = rr < nrows;
             const float gr = gam[rr];
@@ -255,7 +258,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             for (int q = 0; q < NJ8; ++q) {
                 const int j8 = part * NJ8 + q;
                 const float4 u0 = dOpre[2 * q], u1 = dOpre[2 * q + 1];
-                const float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float x[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = in ? x[e] : 0.f;
                 float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(gs, x[e]);
@@ -555,20 +560,20 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         mma_commit(bar_mma);
     }
     mma_out = true;
-    if (tid >= 128) {
+    {
         // dv = b dR and dR . v while the first MMA group runs (dR, beta and the v rows are
         // all in): a warp per row, 16-byte pieces side by side, the v rows loaded first
-        const int t = tid - 128, w4 = t >> 5, c4 = (t & 31) * 4;
-        uint2 vrow[16];
+        const int w4 = warp, c4 = lane * 4;
+        uint2 vrow[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int rr = w4 + 4 * k;
+        for (int k = 0; k < 8; ++k) {
+            const int rr = w4 + 8 * k;
             vrow[k] = (rr < nrows) ? *reinterpret_cast<const uint2*>(a.v + ((size_t)(t0 + rr) * H + h) * D + c4)
                                    : make_uint2(0u, 0u);
         }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int rr = w4 + 4 * k;
+        for (int k = 0; k < 8; ++k) {
+            const int rr = w4 + 8 * k;
             if (rr >= nrows) break;
             const uint32_t off = cm_off(rr, c4, D);
             const uint2 hi = *reinterpret_cast<const uint2*>(Rhi + 16384 + off);
@@ -587,7 +592,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
             *reinterpret_cast<float4*>(a.dv + g) =
                 make_float4(__fmul_rn(brr, x[0]), __fmul_rn(brr, x[1]), __fmul_rn(brr, x[2]), __fmul_rn(brr, x[3]));
             sdot = warp_sum_tree(sdot);
-            if ((t & 31) == 0) dRv[rr] = sdot;
+            if (lane == 0) dRv[rr] = sdot;
         }
     }
     {
