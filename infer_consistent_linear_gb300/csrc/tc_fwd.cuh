@@ -84,9 +84,11 @@ __device__ __forceinline__ uint4 ld16_or_zero(const __nv_bfloat16* p, bool valid
 // row).  Step t adds a_rt T_tj to every row r > t of column j.  Two threads per column
 // (lanes 2j and 2j + 1) keep the running sums of the even and odd rows in registers; the
 // owner of row t hands its final value to the partner with a shuffle.  At2 holds A
-// transposed with the rows of each parity together: At2[s * 64 + (r & 1) * 32 + r / 2] =
-// a_rs.  Writes T rows < nrows of column j to Tout[r * ldT + j] (rows >= nrows get 0).
-// 128 threads.
+// transposed with the rows of each parity together, the odd half rotated by 16 so that
+// the two halves' float4 groups fall in different banks:
+// At2[s * 64 + at2_pos(r)] = a_rs.  Writes T rows < nrows of column j to Tout[r * ldT + j]
+// (rows >= nrows get 0).  128 threads.
+__device__ __forceinline__ int at2_pos(int r) { return (r & 1) * 32 + (((r >> 1) + (r & 1) * 16) & 31); }
 __device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int ldT, int nrows) {
     const int j = threadIdx.x >> 1, p = threadIdx.x & 1;
     float acc[C / 2];
@@ -103,7 +105,7 @@ __device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int
             const float* arow = At2 + t * C + p * (C / 2);
 #pragma unroll
             for (int i4 = t / 8; i4 < C / 8; ++i4) {   // i >= t / 2 - 1 covers every row > t
-                const float4 a4 = *reinterpret_cast<const float4*>(arow + 4 * i4);
+                const float4 a4 = *reinterpret_cast<const float4*>(arow + 4 * ((i4 + 4 * p) & 7));
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -216,7 +218,7 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {   // a_rs = (b_r E_rs) kk_rs, as a_entry
                     const int s = c0 + j;
-                    At[s * C + (r & 1) * (C / 2) + (r >> 1)] =
+                    At[s * C + at2_pos(r)] =
                         (s < r && r < nrows) ? __fmul_rn(__fmul_rn(bet[r], Tfp[r * 65 + s]), v[j]) : 0.f;
                 }
             } else {
