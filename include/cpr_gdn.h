@@ -178,8 +178,11 @@ typedef struct cpr_cache_layout {
     size_t pos;         /* int32  [n_seq]            tokens in the current chunk   */
     size_t done;        /* uint32 [n_seq]            internal step counter (zero)  */
     size_t state;       /* fp32   [n_seq, H, d_k, d_v] chunk-start state H_n      */
-    size_t k_rows;      /* io     [n_seq, H, C, d_k]                               */
-    size_t v_rows;      /* io     [n_seq, H, C, d_v]                               */
+    size_t k_rows;      /* io     [n_seq, H, C, d_k]; tensor-core contracts keep each
+                           (sequence, head) block as an operand tile: element (r, i) at
+                           byte ((r/8)(d_k/8) + i/8) * 128 + (r%8) * 16 + (i%8) * 2, rows at
+                           or past the position zero                              */
+    size_t v_rows;      /* io     [n_seq, H, C, d_v]; same tile form as k_rows        */
     size_t gam_rows;    /* fp32   [n_seq, H, C]      in-chunk gate prefix          */
     size_t beta_rows;   /* fp32   [n_seq, H, C]                                    */
     size_t t_rows;      /* fp32   [n_seq, H, C, C]   rows of (I + A)^-1            */

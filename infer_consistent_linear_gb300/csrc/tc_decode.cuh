@@ -1,6 +1,6 @@
 // CPR Gated DeltaNet decode step on the tensor cores (policy TC_BF16X3).
 //
-// One CTA per (sequence, head).  For the new row p of the current chunk it
+// Per (sequence, head) unit: for the new row p of the current chunk it
 // re-issues exactly the MMA instructions of the prefill kernels (k_tc_prep,
 // k_tc_state): same shapes, same operand tiles, layouts and row positions,
 // same k-step and hi/lo pass order, with the rows of the chunk that do not
@@ -21,16 +21,17 @@ namespace tc {
 
 struct DecSmem {
     static constexpr size_t Hhi = 0, Hlo = 32768;   // state tiles, per split MN-major DVS (j) x 128 (d)
-    static constexpr size_t Kmn = 65536;             // K, MN-major 128 (d) x 64 (token)
+    static constexpr size_t Kmn = 65536;             // K tile, MN-major 128 (d) x 64 (token)
     static constexpr size_t R1 = 81920;              // 64 KB right after Kmn, reused by phase
-    static constexpr size_t F = R1 + 65536;          // fp32 scratch
+    static constexpr size_t Vt = R1 + 65536;         // V tile, MN-major 128 (d) x 64 (token)
+    static constexpr size_t F = Vt + 16384;          // fp32 scratch
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
                          fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
                          fRow2 = 1088, fEnd = 1216;
-    static constexpr size_t Dt = 153600;             // Delta tiles: hi (16 KB) | lo (16 KB), per split
+    static constexpr size_t Dt = F + 5120;           // Delta tiles: hi (16 KB) | lo (16 KB), per split
                                                      // MN-major DVS (j) x 64 (token); at a commit the
                                                      // fp32 Delta rows
-    static constexpr size_t Bar = Dt + 32768;
+    static constexpr size_t Bar = Dt + 32768;        // 4 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -55,7 +56,9 @@ struct TcDecArgs {
 // chunk's Delta rows (rows >= pos zero) as the decode's hi/lo operand tiles, per split
 // MN-major (split sp at sp * DVS * 256 / 128 bytes, lo tiles 32 KB / 16 KB after hi) --
 // split8 of the fp32 values the state pass left in the cache, so the decode reads the
-// same bits it would compute itself.  One CTA per (sequence, head).
+// same bits it would compute itself.  The K and V rows of the current chunk are kept
+// as operand tiles (row r at cm_off(r, ., D), written by the prefill for r < pos); their
+// rows >= pos are zeroed here.  One CTA per (sequence, head).
 template <int DVS>
 __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff co, const int32_t* chunk_off,
                                                         int n_seq, int H) {
@@ -67,6 +70,13 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
     const float* Dr = reinterpret_cast<const float*>(cache + co.delta_rows) + sh * C * D;
     unsigned char* ct = cache + co.state_tiles + sh * 65536;
     unsigned char* cdt = cache + co.delta_tiles + sh * 32768;
+    unsigned char* ckt = cache + co.k_rows + sh * C * D * 2;
+    unsigned char* cvt = cache + co.v_rows + sh * C * D * 2;
+    for (int i = threadIdx.x; i < (C - p) * (D / 8); i += blockDim.x) {
+        const uint32_t off = cm_off(p + i / (D / 8), (i % (D / 8)) * 8, D);
+        *reinterpret_cast<uint4*>(ckt + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(cvt + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int i = threadIdx.x; i < (D + C) * (D / 8); i += blockDim.x) {
         const bool st = i < D * (D / 8);
         const int rr = (st ? i : i - D * (D / 8)) / (D / 8), j8 = i % (D / 8);
@@ -95,8 +105,13 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
     }
 }
 
+// Persistent: a CTA per SM walks the (sequence, head) units of the step.  While
+// unit u runs, the next unit's operands arrive by bulk copies into buffers u no
+// longer needs: K and V tiles once the X MMA has read them, the state tiles once
+// A4 has, the Delta prefix once P Delta has (after the commit MMA when u commits),
+// and the new token's q, k, v pieces and gate rows into registers.
 template <int DVS>
-__global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
+__global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     using S = DecSmem;
     constexpr int NSPLIT = D / DVS;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -105,33 +120,118 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
           *prow = F + S::fProw, *trow = F + S::fTrow, *decs = F + S::fDec, *Wp = F + S::fWp,
           *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs, *row1 = F + S::fRow,
           *row2 = F + S::fRow2;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);
-    uint64_t* bar_ld = mbar + 1;
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 2);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);   // MMA groups
+    uint64_t* bar_H = mbar + 1;                                   // state tiles
+    uint64_t* bar_D = mbar + 2;                                   // Delta tiles; fp32 Delta rows
+    uint64_t* bar_KV = mbar + 3;                                  // K and V tiles
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 4);
     float* stage = reinterpret_cast<float*>(sm + S::Dt);   // fp32 Delta rows at a commit
+    unsigned char* R1 = sm + S::R1;
     __shared__ int ok_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const int nunit = a.n_seq * H;
     const uint32_t* hdr = reinterpret_cast<const uint32_t*>(a.cache + a.co.header);
     int32_t* pos = reinterpret_cast<int32_t*>(a.cache + a.co.pos);
     uint32_t* done = reinterpret_cast<uint32_t*>(a.cache + a.co.done);
-    if (tid == 0) {
+    if (tid == 0) {  // the cache header and the position of every unit this CTA takes
         bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
         for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
         for (int i = 0; i < 7; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
-        const int p = ok ? pos[b] : -1;
-        if (!(p >= 0 && p < C)) ok = false;
+        for (int u = blockIdx.x; ok && u < nunit; u += gridDim.x) {
+            const int p = pos[u / H];
+            if (!(p >= 0 && p < C)) ok = false;
+        }
         if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
-        ok_s = ok ? 1 + p : 0;
+        ok_s = ok ? 1 : 0;
     }
     __syncthreads();
-    if (!ok_s) return;
-    const int p = ok_s - 1;
-    const size_t sh = (size_t)b * H + h;
-    __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
-    __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
+    if (!ok_s || (int)blockIdx.x >= nunit) return;
+
+    // unit u = sequence u / H, head u % H = row u of every [n_seq, H, ...] section
+    auto k_tile = [&](int u) { return a.cache + a.co.k_rows + (size_t)u * C * D * 2; };
+    auto v_tile = [&](int u) { return a.cache + a.co.v_rows + (size_t)u * C * D * 2; };
+    auto issue_KV = [&](int u) {
+        mbar_expect_tx(bar_KV, 32768);
+        bulk_g2s(sm + S::Kmn, k_tile(u), 16384, bar_KV);
+        bulk_g2s(sm + S::Vt, v_tile(u), 16384, bar_KV);
+    };
+    auto issue_H = [&](int u) {
+        mbar_expect_tx(bar_H, 65536);
+        bulk_g2s(sm + S::Hhi, a.cache + a.co.state_tiles + (size_t)u * 65536, 65536, bar_H);
+    };
+    auto issue_D = [&](int u, int p) {  // each split's Delta tile rows < p (8-row groups)
+        const uint32_t dpre = (uint32_t)((p + 7) / 8) * (DVS / 8) * 128;
+        const unsigned char* cdt = a.cache + a.co.delta_tiles + (size_t)u * 32768;
+        mbar_expect_tx(bar_D, 2u * NSPLIT * dpre);
+        if (dpre) {
+#pragma unroll
+            for (int sp = 0; sp < NSPLIT; ++sp) {
+                const uint32_t t = (uint32_t)sp * DVS * 128;
+                bulk_g2s(sm + S::Dt + t, cdt + t, dpre, bar_D);
+                bulk_g2s(sm + S::Dt + 16384 + t, cdt + 16384 + t, dpre, bar_D);
+            }
+        }
+    };
+    // the new token's q (threads 0..15), k (16..31), v (32..47) pieces and the cached
+    // gate / beta rows, into registers (the n* set is the next unit's, loaded while this
+    // one runs); every load reads valid memory, masks apply at use
+    uint4 rowreg = make_uint4(0u, 0u, 0u, 0u), nrowreg = rowreg;
+    float cgv = 0.f, cbv = 0.f, gprev = 0.f, gnew = 0.f, bnew = 0.f;
+    float ncgv = 0.f, ncbv = 0.f, ngprev = 0.f, ngnew = 0.f, nbnew = 0.f;
+    auto load_rows = [&](int u, int p) {
+        if (tid < 48) {
+            const __nv_bfloat16* src = (tid < 16 ? a.q : tid < 32 ? a.k : a.v) + (size_t)u * D + (tid & 15) * 8;
+            nrowreg = *reinterpret_cast<const uint4*>(src);
+        }
+        const float* cg = reinterpret_cast<const float*>(a.cache + a.co.gam_rows) + (size_t)u * C;
+        const float* cb = reinterpret_cast<const float*>(a.cache + a.co.beta_rows) + (size_t)u * C;
+        ncgv = cg[tid & (C - 1)];
+        ncbv = cb[tid & (C - 1)];
+        ngprev = cg[p > 0 ? p - 1 : 0];
+        ngnew = a.g[u];
+        nbnew = a.beta[u];
+    };
+    auto take_rows = [&]() {
+        rowreg = nrowreg;
+        cgv = ncgv; cbv = ncbv; gprev = ngprev; gnew = ngnew; bnew = nbnew;
+    };
+
+    if (warp == 0) tmem_alloc(tbase, 256);
+    int p = pos[blockIdx.x / H];
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(mbar + i, 1);
+        mbar_init_fence();
+        issue_KV(blockIdx.x);
+        issue_H(blockIdx.x);
+        issue_D(blockIdx.x, p);
+    }
+    load_rows(blockIdx.x, p);
+    take_rows();
+    tc_sync();
+    const uint32_t tmem = *tbase;
+    uint32_t ph_mma = 0, ph_H = 0, ph_D = 0, ph_KV = 0;
+    bool pend_KV = true, pend_H = true, pend_D = true, mma_out = false;
+    bool ok = true;
+    auto mma_wait = [&]() {
+        const bool w = mbar_wait(mbar, ph_mma, a.err);
+        fence_after();
+        if (w) {
+            ph_mma ^= 1u;
+            mma_out = false;
+        }
+        return !__syncthreads_or(!w);
+    };
+
+    for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
+    const int b = u / H;
+    const size_t sh = (size_t)u;
+    const int un = u + (int)gridDim.x;
+    const bool has_next = un < nunit;
+    int pn = 0;   // the next unit's position, read once the S1 MMA is on its way
+    __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(k_tile(u));
+    __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(v_tile(u));
     float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
     float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
     float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
@@ -139,78 +239,46 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     float* Hst = reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D;
     unsigned char* cst = a.cache + a.co.state_tiles + sh * 65536;     // state hi | lo tiles
     unsigned char* cdt = a.cache + a.co.delta_tiles + sh * 32768;     // Delta hi | lo tiles
-    // bytes of each split's Delta tile holding rows < p (8-row core-matrix groups)
-    const uint32_t dpre = (uint32_t)((p + 7) / 8) * (DVS / 8) * 128;
-    const __nv_bfloat16* qt = a.q + sh * D;
-    const __nv_bfloat16* kt = a.k + sh * D;
-    const __nv_bfloat16* vt = a.v + sh * D;
-    unsigned char* R1 = sm + S::R1;
-
-    if (warp == 0) tmem_alloc(tbase, 256);
-    if (tid == 0) {
-        mbar_init(mbar, 1);
-        mbar_init(bar_ld, 1);
-        mbar_init_fence();
-        // the chunk-start state as ready operand tiles, and the Delta rows < p
-        mbar_expect_tx(bar_ld, 65536 + 2u * NSPLIT * dpre);
-        bulk_g2s(sm + S::Hhi, cst, 65536, bar_ld);
-        if (dpre) {
-#pragma unroll
-            for (int sp = 0; sp < NSPLIT; ++sp) {
-                const uint32_t t = (uint32_t)sp * DVS * 128;
-                bulk_g2s(sm + S::Dt + t, cdt + t, dpre, bar_ld);
-                bulk_g2s(sm + S::Dt + 16384 + t, cdt + 16384 + t, dpre, bar_ld);
-            }
+    {
+        // this unit's K and V tiles (rows >= p zero in the cache) have landed: row p from
+        // the new token, and the q row p of the [K; Q] operand (rows 64.. = R1's first
+        // 16 KB; other rows of an A operand reach only accumulator rows never read)
+        const bool w = mbar_wait(bar_KV, ph_KV, a.err);
+        if (w) {
+            ph_KV ^= 1u;
+            pend_KV = false;
         }
+        if (__syncthreads_or(!w)) { ok = false; break; }
     }
-    // K and V rows s <= p as MN-major tiles (Kmn; R1 + 32 KB), later rows zero-filled
-    // by the copies themselves.  The K tile read K-major is the [K; Q] operand's
-    // first 64 rows (the two layouts are byte-identical); its rows 64.. are
-    // R1's first 16 KB, of which only row 64 + p = q_p is written: other rows of
-    // an A operand reach only accumulator rows this step never reads.
-    for (int i = tid; i < 64 * (D / 8); i += 128) {
-        const int r = i / (D / 8), d8 = i % (D / 8);
-        const bool in = r <= p;
-        const __nv_bfloat16* ks = (r < p ? ck + (size_t)r * D : kt) + d8 * 8;
-        const __nv_bfloat16* vs = (r < p ? cv + (size_t)r * D : vt) + d8 * 8;
-        cp_async16(sm + S::Kmn + mn_off(d8 * 8, r, D), ks, in);
-        cp_async16(R1 + 32768 + mn_off(d8 * 8, r, D), vs, in);
-    }
-    if (tid < D / 8) cp_async16(R1 + cm_off(p, tid * 8, D), qt + tid * 8, true);
+    if (tid < 16) *reinterpret_cast<uint4*>(R1 + cm_off(p, tid * 8, D)) = rowreg;
+    else if (tid < 32) *reinterpret_cast<uint4*>(sm + S::Kmn + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+    else if (tid < 48) *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
     if (tid < p) {
-        gams[tid] = cg[tid];
-        bets[tid] = cb[tid];
+        gams[tid] = cgv;
+        bets[tid] = cbv;
     }
     if (tid == 0) {
-        gams[p] = __fadd_rn(p > 0 ? cg[p - 1] : 0.f, a.g[sh]);
-        bets[p] = a.beta[sh];
+        gams[p] = __fadd_rn(p > 0 ? gprev : 0.f, gnew);
+        bets[p] = bnew;
     }
-    cp_async_wait_all();
     fence_async_smem();
     tc_sync();
     // this thread's column of the cached T rows (for the T row chain), loaded after the
-    // proxy fence (which would wait for them) so that they land while the S1 MMA runs
+    // proxy fence (which would wait for them) so that they land while the S1 MMA runs;
+    // rows s >= p are read but never used
     float tcol[C];
+    if (tid < C) {
 #pragma unroll
-    for (int s = 0; s < C; ++s) tcol[s] = (tid < C && s < p) ? ct[s * C + tid] : 0.f;
-    const uint32_t tmem = *tbase;
-    uint32_t phase = 0;
-    bool ok = true;
-    bool ld_pending = true;   // the state copy is in flight from the start
-    uint32_t ld_phase = 0;
-    auto mma_wait = [&]() {
-        const bool w = mbar_wait(mbar, phase, a.err);
-        fence_after();
-        phase ^= 1u;
-        return !__syncthreads_or(!w);
-    };
+        for (int s = 0; s < C; ++s) tcol[s] = ct[s * C + tid];
+    }
+    if (has_next) pn = pos[un / H];
     if (tid == 0) {
         mma_tile<128, 64, D>(tmem, sm + S::Kmn, sm + S::Kmn, false);
         mma_commit(mbar);
     }
+    mma_out = true;
     if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid]);
-    ok = mma_wait();
-    if (!ok) goto cleanup;
+    if (!mma_wait()) { ok = false; break; }
     {
         float v[32];
         for (int c0 = 0; c0 < C; c0 += 32) {
@@ -259,12 +327,17 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     if (tid == 0) {
         mma_tile_mj<64, D, C, false, true>(tmem, R1, sm + S::Kmn, false);
         mma_tile_mj<64, D, C, false, true>(tmem, R1 + 8192, sm + S::Kmn, true);
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 16384, R1 + 32768, false);
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 24576, R1 + 32768, true);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 16384, sm + S::Vt, false);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 24576, sm + S::Vt, true);
         mma_commit(mbar);
     }
-    ok = mma_wait();
-    if (!ok) goto cleanup;
+    mma_out = true;
+    if (!mma_wait()) { ok = false; break; }
+    if (tid == 0 && has_next && p != C - 1) {  // K and V are consumed (a committing unit still
+        fence_async_smem();                    // needs K): the next unit's tiles
+        issue_KV(un);
+    }
+    if (has_next && p != C - 1) pend_KV = true;
     {
         const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
         float v[32];
@@ -281,24 +354,30 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     }
     // A4 tiles (R1: hi at +0, lo at +32 KB): row p = W'_p, row 64 + p = q_p
     __syncthreads();
-    if (tid < 16) {
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = Wp[tid * 8 + e];
-        store8_split(R1, R1 + 32768, cm_off(p, tid * 8, D), x);
+    if (tid < 16) {  // q_p has no lo part: that row of the lo tile is zero, as in the prefill
+        *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, tid * 8, D)) = rowreg;
+        *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(64 + p, tid * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
     } else if (tid < 32) {
         const int d8 = tid - 16;
-        *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, d8 * 8, D)) = *reinterpret_cast<const uint4*>(qt + d8 * 8);
-    } else if (tid < 48) {  // q_p has no lo part: that row of the lo tile is zero, as in the prefill
-        *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(64 + p, (tid - 32) * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = Wp[d8 * 8 + e];
+        store8_split(R1, R1 + 32768, cm_off(p, d8 * 8, D), x);
     }
     {
         // state tiles and the Delta rows < p have landed; rows >= p of every Delta tile are
         // set to zero (row p is written below; rows past it only meet zero P entries)
-        const bool okh = mbar_wait(bar_ld, 0, a.err);
-        if (__syncthreads_or(!okh)) goto cleanup;
-        ld_pending = false;
-        ld_phase = 1;
+        const bool wh = mbar_wait(bar_H, ph_H, a.err);
+        const bool wd = mbar_wait(bar_D, ph_D, a.err);
+        if (wh) {
+            ph_H ^= 1u;
+            pend_H = false;
+        }
+        if (wd) {
+            ph_D ^= 1u;
+            pend_D = false;
+        }
+        if (__syncthreads_or(!(wh && wd))) { ok = false; break; }
         constexpr int CH = DVS / 8;                        // 16-byte chunks per tile row
         for (int i = tid; i < (C - p) * CH * NSPLIT * 2; i += 128) {
             const int sr = p + i / (CH * NSPLIT * 2), rem = i % (CH * NSPLIT * 2);
@@ -321,8 +400,14 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         }
         mma_commit(mbar);
     }
-    ok = mma_wait();
-    if (!ok) goto cleanup;
+    mma_out = true;
+    if (has_next) load_rows(un, pn);   // the next unit's token rows land while A4 runs
+    if (!mma_wait()) { ok = false; break; }
+    if (tid == 0 && has_next) {  // the state tiles are consumed: the next unit's
+        fence_async_smem();
+        issue_H(un);
+    }
+    if (has_next) pend_H = true;
     {
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -378,8 +463,13 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         }
         mma_commit(mbar);
     }
-    ok = mma_wait();
-    if (!ok) goto cleanup;
+    mma_out = true;
+    if (!mma_wait()) { ok = false; break; }
+    if (tid == 0 && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
+        fence_async_smem();                    // (a committing unit stages its rows there first)
+        issue_D(un, pn);
+    }
+    if (has_next && p != C - 1) pend_D = true;
     {
         const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
         float v[32];
@@ -394,9 +484,14 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
     __syncthreads();
     a.o[sh * D + tid] = __fadd_rn(Qs[tid], row1[tid]);
     {
-        // append row p to the cache
-        if (tid < 16) *reinterpret_cast<uint4*>(ck + (size_t)p * D + tid * 8) = *reinterpret_cast<const uint4*>(kt + tid * 8);
-        else if (tid < 32) *reinterpret_cast<uint4*>(cv + (size_t)p * D + (tid - 16) * 8) = *reinterpret_cast<const uint4*>(vt + (tid - 16) * 8);
+        // append row p to the cache (k and v as rows of their operand tiles; a committing
+        // step clears those tiles for the next chunk instead)
+        if (p != C - 1) {
+            if (tid >= 16 && tid < 32)
+                *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(ck) + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+            else if (tid >= 32 && tid < 48)
+                *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(cv) + cm_off(p, (tid - 32) * 8, D)) = rowreg;
+        }
         cd[(size_t)p * D + tid] = Dp[tid];
         if (tid < C) ct[p * C + tid] = trow[tid];
         if (tid == 0) {
@@ -408,15 +503,18 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
         const int Lr = C - 1;
         if (tid == 0) {  // the chunk's other fp32 Delta rows (the Delta tiles are consumed)
             fence_async_smem();
-            mbar_expect_tx(bar_ld, (uint32_t)p * D * 4);
-            bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_ld);
+            mbar_expect_tx(bar_D, (uint32_t)p * D * 4);
+            bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_D);
         }
-        ld_pending = true;
+        pend_D = true;
         if (tid < C) decs[tid] = simt::decay(gams[Lr], gams[tid]);
         {
-            const bool okd = mbar_wait(bar_ld, 1, a.err);
-            if (__syncthreads_or(!okd)) goto cleanup;
-            ld_pending = false;
+            const bool wd = mbar_wait(bar_D, ph_D, a.err);
+            if (wd) {
+                ph_D ^= 1u;
+                pend_D = false;
+            }
+            if (__syncthreads_or(!wd)) { ok = false; break; }
         }
         if (tid < C) {
             const int s = tid;
@@ -453,8 +551,14 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
             }
             mma_commit(mbar);
         }
-        ok = mma_wait();
-        if (!ok) goto cleanup;
+        mma_out = true;
+        if (!mma_wait()) { ok = false; break; }
+        if (tid == 0 && has_next) {  // K and the staged rows are consumed: the next unit's
+            fence_async_smem();      // K, V and Delta tiles
+            issue_KV(un);
+            issue_D(un, pn);
+        }
+        if (has_next) pend_KV = pend_D = true;
         const float GL = simt::gate(gams[Lr]);
         float v[32];
         const int d = tid;
@@ -479,6 +583,10 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
                 *reinterpret_cast<uint4*>(cst + 32768 + off) = lo;
             }
         }
+        for (int i = tid; i < C * D / 8; i += 128) {  // the next chunk starts with no K, V rows
+            reinterpret_cast<uint4*>(ck)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(cv)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     __syncthreads();
     if (tid == 0) {  // advance the position once every head of the sequence is done
@@ -491,8 +599,15 @@ __global__ void __launch_bounds__(128) k_tc_decode(TcDecArgs a) {
             __threadfence();
         }
     }
-cleanup:
-    if (ld_pending) mbar_wait(bar_ld, ld_phase, a.err);  // bounded: let the copy land
+    p = pn;
+    take_rows();
+    }  // units
+    if (!ok) {  // let this CTA's copies and MMAs in flight finish (bounded) before TMEM goes
+        if (pend_KV) mbar_wait(bar_KV, ph_KV, a.err);
+        if (pend_H) mbar_wait(bar_H, ph_H, a.err);
+        if (pend_D) mbar_wait(bar_D, ph_D, a.err);
+        if (mma_out) mbar_wait(mbar, ph_mma, a.err);
+    }
     tc_sync();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }

@@ -278,11 +278,14 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
         __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
         float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
         float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
-        for (int i = tid; i < nrows * (D / 8); i += 128) {
+        for (int i = tid; i < nrows * (D / 8); i += 128) {  // as rows of the decode's operand tiles
             const int r = i / (D / 8), d8 = i % (D / 8);
             const size_t src = ((size_t)(t0 + r) * H + h) * D + d8 * 8;
-            *reinterpret_cast<uint4*>(ck + r * D + d8 * 8) = *reinterpret_cast<const uint4*>(a.k + src);
-            *reinterpret_cast<uint4*>(cv + r * D + d8 * 8) = *reinterpret_cast<const uint4*>(a.v + src);
+            const uint32_t off = cm_off(r, d8 * 8, D);
+            *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(ck) + off) =
+                *reinterpret_cast<const uint4*>(a.k + src);
+            *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(cv) + off) =
+                *reinterpret_cast<const uint4*>(a.v + src);
         }
         if (tid < nrows) {
             cg[tid] = gam[tid];

@@ -44,7 +44,14 @@ cudaError_t decode(const tc::TcDecArgs& a, cudaStream_t st) {
     const size_t sm = tc::DecSmem::Total;
     cudaError_t e = set_smem(kern, sm);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)a.n_seq * a.H;
+    // persistent: one CTA per SM walks the (sequence, head) units
+    int dev = 0, nsm = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.n_seq * a.H;
+    const int64_t grid = units < nsm ? units : nsm;
     if (grid > 0) {
         ProfScope ps("cpr_tc_decode", st);
         kern<<<(unsigned)grid, 128, sm, st>>>(a);
