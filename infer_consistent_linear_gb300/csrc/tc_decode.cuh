@@ -161,18 +161,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         mbar_expect_tx(bar_H, 65536);
         bulk_g2s(sm + S::Hhi, a.cache + a.co.state_tiles + (size_t)u * 65536, 65536, bar_H);
     };
-    auto issue_D = [&](int u, int p) {  // each split's Delta tile rows < p (8-row groups)
-        const uint32_t dpre = (uint32_t)((p + 7) / 8) * (DVS / 8) * 128;
-        const unsigned char* cdt = a.cache + a.co.delta_tiles + (size_t)u * 32768;
-        mbar_expect_tx(bar_D, 2u * NSPLIT * dpre);
-        if (dpre) {
-#pragma unroll
-            for (int sp = 0; sp < NSPLIT; ++sp) {
-                const uint32_t t = (uint32_t)sp * DVS * 128;
-                bulk_g2s(sm + S::Dt + t, cdt + t, dpre, bar_D);
-                bulk_g2s(sm + S::Dt + 16384 + t, cdt + 16384 + t, dpre, bar_D);
-            }
-        }
+    auto issue_D = [&](int u) {  // the Delta tiles (rows >= p are zero in the cache)
+        mbar_expect_tx(bar_D, 32768);
+        bulk_g2s(sm + S::Dt, a.cache + a.co.delta_tiles + (size_t)u * 32768, 32768, bar_D);
     };
     // the new token's q (threads 0..15), k (16..31), v (32..47) pieces and the cached
     // gate / beta rows, into registers (the n* set is the next unit's, loaded while this
@@ -205,7 +196,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         mbar_init_fence();
         issue_KV(blockIdx.x);
         issue_H(blockIdx.x);
-        issue_D(blockIdx.x, p);
+        issue_D(blockIdx.x);
     }
     load_rows(blockIdx.x, p);
     take_rows();
@@ -365,8 +356,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         store8_split(R1, R1 + 32768, cm_off(p, d8 * 8, D), x);
     }
     {
-        // state tiles and the Delta rows < p have landed; rows >= p of every Delta tile are
-        // set to zero (row p is written below; rows past it only meet zero P entries)
+        // the state tiles and the Delta tiles (rows >= p zero; row p is written below, and
+        // rows past it only meet zero P entries) have landed
         const bool wh = mbar_wait(bar_H, ph_H, a.err);
         const bool wd = mbar_wait(bar_D, ph_D, a.err);
         if (wh) {
@@ -378,13 +369,6 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
             pend_D = false;
         }
         if (__syncthreads_or(!(wh && wd))) { ok = false; break; }
-        constexpr int CH = DVS / 8;                        // 16-byte chunks per tile row
-        for (int i = tid; i < (C - p) * CH * NSPLIT * 2; i += 128) {
-            const int sr = p + i / (CH * NSPLIT * 2), rem = i % (CH * NSPLIT * 2);
-            const int sp = (rem / CH) % NSPLIT, lohi = rem / (CH * NSPLIT), c8 = rem % CH;
-            *reinterpret_cast<uint4*>(sm + S::Dt + lohi * 16384 + sp * DVS * 128 + mn_off(c8 * 8, sr, DVS)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
     }
     __syncthreads();
     fence_async_smem();
@@ -467,7 +451,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (!mma_wait()) { ok = false; break; }
     if (tid == 0 && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
         fence_async_smem();                    // (a committing unit stages its rows there first)
-        issue_D(un, pn);
+        issue_D(un);
     }
     if (has_next && p != C - 1) pend_D = true;
     {
@@ -556,7 +540,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         if (tid == 0 && has_next) {  // K and the staged rows are consumed: the next unit's
             fence_async_smem();      // K, V and Delta tiles
             issue_KV(un);
-            issue_D(un, pn);
+            issue_D(un);
         }
         if (has_next) pend_KV = pend_D = true;
         const float GL = simt::gate(gams[Lr]);
@@ -583,10 +567,11 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
                 *reinterpret_cast<uint4*>(cst + 32768 + off) = lo;
             }
         }
-        for (int i = tid; i < C * D / 8; i += 128) {  // the next chunk starts with no K, V rows
+        for (int i = tid; i < C * D / 8; i += 128) {  // the next chunk starts with no K, V, Delta rows
             reinterpret_cast<uint4*>(ck)[i] = make_uint4(0u, 0u, 0u, 0u);
             reinterpret_cast<uint4*>(cv)[i] = make_uint4(0u, 0u, 0u, 0u);
         }
+        for (int i = tid; i < 32768 / 16; i += 128) reinterpret_cast<uint4*>(cdt)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
     if (tid == 0) {  // advance the position once every head of the sequence is done
