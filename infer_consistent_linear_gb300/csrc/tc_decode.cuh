@@ -31,7 +31,8 @@ struct DecSmem {
     static constexpr size_t Dt = F + 5120;           // Delta tiles: hi (16 KB) | lo (16 KB), per split
                                                      // MN-major DVS (j) x 64 (token); at a commit the
                                                      // fp32 Delta rows
-    static constexpr size_t Bar = Dt + 32768;        // 4 mbarriers + TMEM base
+    static constexpr size_t Tt = Dt + 32768;         // the cached T rows, fp32 [C][C] (rows < p valid)
+    static constexpr size_t Bar = Tt + C * C * 4;    // 4 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -152,10 +153,11 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     // unit u = sequence u / H, head u % H = row u of every [n_seq, H, ...] section
     auto k_tile = [&](int u) { return a.cache + a.co.k_rows + (size_t)u * C * D * 2; };
     auto v_tile = [&](int u) { return a.cache + a.co.v_rows + (size_t)u * C * D * 2; };
-    auto issue_KV = [&](int u) {
-        mbar_expect_tx(bar_KV, 32768);
+    auto issue_KV = [&](int u) {   // K and V tiles and the T rows
+        mbar_expect_tx(bar_KV, 32768 + C * C * 4);
         bulk_g2s(sm + S::Kmn, k_tile(u), 16384, bar_KV);
         bulk_g2s(sm + S::Vt, v_tile(u), 16384, bar_KV);
+        bulk_g2s(sm + S::Tt, a.cache + a.co.t_rows + (size_t)u * C * C * 4, C * C * 4, bar_KV);
     };
     auto issue_H = [&](int u) {
         mbar_expect_tx(bar_H, 65536);
@@ -254,14 +256,6 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     fence_async_smem();
     tc_sync();
-    // this thread's column of the cached T rows (for the T row chain), loaded after the
-    // proxy fence (which would wait for them) so that they land while the S1 MMA runs;
-    // rows s >= p are read but never used
-    float tcol[C];
-    if (tid < C) {
-#pragma unroll
-        for (int s = 0; s < C; ++s) tcol[s] = ct[s * C + tid];
-    }
     if (has_next) pn = pos[un / H];
     if (tid == 0) {
         mma_tile<128, 64, D>(tmem, sm + S::Kmn, sm + S::Kmn, false);
@@ -292,12 +286,13 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     // X tiles (R1 + 0 .. 32 KB, row p only) and the T row
     __syncthreads();
-    if (tid < C) {  // T row p: T_pj = -(sum_{s=j}^{p-1} a_ps T_sj), ascending s
+    if (tid < C) {  // T row p: T_pj = -(sum_{s=j}^{p-1} a_ps T_sj), ascending s (cached rows s < p)
         const int j = tid;
+        const float* Tt = reinterpret_cast<const float*>(sm + S::Tt);
         float acc = 0.f;
 #pragma unroll
         for (int s = 0; s < C; ++s)
-            if (s >= j && s < p) acc = __fmaf_rn(arow[s], tcol[s], acc);
+            if (s >= j && s < p) acc = __fmaf_rn(arow[s], Tt[s * C + j], acc);
         trow[j] = (j < p) ? -acc : (j == p ? 1.f : 0.f);
     }
     __syncthreads();
