@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     };
 
     for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
-    const int b = u / H;
     const size_t sh = (size_t)u;
     const int un = u + (int)gridDim.x;
     const bool has_next = un < nunit;
@@ -569,19 +568,20 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         for (int i = tid; i < 32768 / 16; i += 128) reinterpret_cast<uint4*>(cdt)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
-    if (tid == 0) {  // advance the position once every head of the sequence is done
-        // No fence before the count: every CTA of the sequence read pos[b] (and used it)
-        // before its own increment, and the next step is a later launch.
-        const uint32_t prev = atomicAdd(&done[b], 1u);
-        if (prev == (uint32_t)H - 1) {
-            pos[b] = (p + 1) % C;
-            done[b] = 0u;
-            __threadfence();
-        }
-    }
     p = pn;
     take_rows();
     }  // units
+    if (ok && tid == 0) {
+        // every sequence advances one token per step: the last CTA to finish moves all the
+        // positions on.  Every CTA read the positions of its units before its count, and the
+        // next step is a later launch.
+        const uint32_t prev = atomicAdd(&done[0], 1u);
+        if (prev == gridDim.x - 1) {
+            for (int sq = 0; sq < a.n_seq; ++sq) pos[sq] = (pos[sq] + 1) % C;
+            done[0] = 0u;
+            __threadfence();
+        }
+    }
     if (!ok) {  // let this CTA's copies and MMAs in flight finish (bounded) before TMEM goes
         if (pend_KV) mbar_wait(bar_KV, ph_KV, a.err);
         if (pend_H) mbar_wait(bar_H, ph_H, a.err);
