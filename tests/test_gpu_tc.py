@@ -55,6 +55,15 @@ def test_tc_decode_equals_prefill(splits):
                        operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=splits)
 
 
+def test_tc_decode_persistent_mixed_positions():
+    """More (sequence, head) units than SMs and positions all over the chunk in one launch:
+    each persistent CTA walks several units with different positions, some of them
+    committing a chunk while the next unit's tiles are prefetched."""
+    lens = [(17 * i) % 131 for i in range(38)] + [64, 128]
+    _decode_vs_prefill(torch.bfloat16, 128, lens, 66, 8, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
+                       dv_splits=2)
+
+
 def test_tc_chunk_aligned_split_and_batch_invariance():
     c = _tc()
     lens = [300, 77, 1, 128]
