@@ -511,6 +511,21 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
                     *reinterpret_cast<const float4*>(ost + r * (DVS + 4) + 4 * c4);
         }
     };
+    // chunk n's Q H rows (accumulator rows 64..127, lane quarters 2 and 3) -> sQ, scaled
+    // by G_r: taken while quarters 0 and 1 run the Delta epilogue
+    auto qh_to_sq = [&](int n) {
+        float v[32];
+        tmem_ld32(taddr_of(acc4(n), warp, cb), v);
+        const int rr = d - 64;
+        const float gr = Gm[rr];
+#pragma unroll
+        for (int j4 = 0; j4 < HALF / 4; ++j4)
+            reinterpret_cast<float4*>(sQ)[(cb / 4 + j4) * 64 + rr] =
+                make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
+                            __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
+                            __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
+                            __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
+    };
     auto o_epilogue = [&](int m) -> bool {
         const bool w = mbar_wait(bar_pd, ph_pd, a.err);
         fence_after();
@@ -524,19 +539,6 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         pendP = (m + 1 < nch);
         const int nrows = min(C, T - m * C);
         float v[32];
-        if (quarter >= 2) {  // Q H rows (accumulator rows 64..127) -> sQ, scaled by G_r
-            tmem_ld32(taddr_of(acc4(m), warp, cb), v);
-            const int rr = d - 64;
-            const float gr = Gm[rr];
-#pragma unroll
-            for (int j4 = 0; j4 < HALF / 4; ++j4)
-                reinterpret_cast<float4*>(sQ)[(cb / 4 + j4) * 64 + rr] =
-                    make_float4(__fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4])),
-                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 1])),
-                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
-                                __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
-        }
-        __syncthreads();
         tmem_ld32(taddr_of(acc5(m), warp, cb), v);  // M = 64: row 16 quarter + lane, lanes < 16
         const int r = quarter * 16 + lane;
         if (lane < 16 && r < nrows && a.o) {
@@ -632,8 +634,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
                     *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
                 }
             }
-        } else if (n > 0) {
-            o_copy(n - 1);   // staged by o_epilogue(n - 1), barriers ago
+        } else {
+            if (n > 0) o_copy(n - 1);   // staged by o_epilogue(n - 1), barriers ago
+            qh_to_sq(n);
         }
         if (cstate && last && nrows < C) put_state(cstate);
         fence_async_smem();
