@@ -526,10 +526,12 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
                             __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 2])),
                             __fmul_rn(gr, __fmul_rn(a.scale, v[4 * j4 + 3])));
     };
+    // (each thread waits for P Delta itself; a failed wait reaches the other threads at the
+    // next barrier)
     auto o_epilogue = [&](int m) -> bool {
         const bool w = mbar_wait(bar_pd, ph_pd, a.err);
         fence_after();
-        if (__syncthreads_or(!w)) return false;
+        if (!w) return false;
         ph_pd ^= 1u;
         pd_out = false;
         if (tid == 0 && m + 1 < nch) {  // P of chunk m is consumed
@@ -577,16 +579,18 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
             mma_commit(bar_mma);
         }
         mma_out = true;
-        if (n > 0 && !o_epilogue(n - 1)) { failed = true; break; }
+        const bool okpd = n == 0 || o_epilogue(n - 1);
         if (tid < C) {
             Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
             dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
         }
         const float GL = simt::gate(gam[Lr]);
         ok = mbar_wait(bar_ldB, ph_ldB, a.err);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_ldB ^= 1u;
-        pendB = false;
+        if (ok) {
+            ph_ldB ^= 1u;
+            pendB = false;
+        }
+        if (__syncthreads_or(!(ok && okpd))) { failed = true; break; }
         ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
         if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -678,10 +682,10 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         fence_async_smem();
         tc_sync();
     }
-    if (!failed && nch > 0 && !o_epilogue(nch - 1)) failed = true;
-    if (!failed && nch > 0) {
-        __syncthreads();
-        if (quarter >= 2) o_copy(nch - 1);
+    if (!failed && nch > 0) {   // (failed is the same in every thread here)
+        const bool okl = o_epilogue(nch - 1);
+        if (__syncthreads_or(!okl)) failed = true;
+        else if (quarter >= 2) o_copy(nch - 1);
     }
     if (!failed && a.final_state) put_state(a.final_state + sh * D * D);
     if (failed) {
