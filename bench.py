@@ -624,6 +624,106 @@ def secondary(name, dev, world, local, steps, warmup, pk, policy):
     return res
 
 
+# ------------------------------------------------------------ stage-table ablations
+class NativeDecode:
+    """"Native mixed" decode: the Decode workload's chunked (tensor-core) prefill, then
+    token-recurrent steps on its fp32 final states, no resynchronisation."""
+
+    def __init__(self, dev, n_steps):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("decode")
+        H, d = WORKLOADS["decode"]["H"], WORKLOADS["decode"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        full = [L + n_steps for L in self.lens]
+        xd = make_inputs(full, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        cu = xd.cu_seqlens.tolist()
+        n_seq = len(self.lens)
+        sel = torch.cat([torch.arange(cu[b], cu[b] + self.lens[b]) for b in range(n_seq)]).to(dev)
+        cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(self.lens), 0).tolist(), dtype=torch.int32,
+                              device=dev)
+        _, self.state = cpr.cpr_gdn_fwd(xd.q[sel], xd.k[sel], xd.v[sel], xd.g[sel], xd.beta[sel], cu_pre,
+                                        contract=self.c)
+        idx = torch.tensor([[cu[b] + self.lens[b] + t for b in range(n_seq)] for t in range(n_steps)],
+                           device=dev).reshape(-1)
+        self.tok = [t.index_select(0, idx).view(n_steps, n_seq, *t.shape[1:]).contiguous()
+                    for t in (xd.q, xd.k, xd.v, xd.g, xd.beta)]
+        self.o_steps = torch.empty(n_steps, n_seq, H, d, device=dev)
+        o_full, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=self.c,
+                                    want_final=False)
+        self.ref = o_full.index_select(0, idx).view_as(self.o_steps)   # what CPR's decode reproduces
+        self.units = n_seq * H
+        self.t = 0
+        torch.cuda.synchronize()
+
+    def run(self):
+        q, k, v, g, b = (x[self.t] for x in self.tok)
+        self.cpr.cpr_gdn_recurrent_step(q, k, v, g, b, self.state, contract=self.c, out=self.o_steps[self.t])
+        self.t += 1
+
+
+class RecurrentPrefill:
+    """"Recurrent everywhere" on the Prefill workload: the token recurrence over each
+    whole sequence."""
+
+    def __init__(self, dev):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("prefill")
+        H, d = WORKLOADS["prefill"]["H"], WORKLOADS["prefill"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d)
+        self.xd = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        torch.cuda.synchronize()
+
+    def run(self):
+        x = self.xd
+        self.cpr.cpr_gdn_recurrent_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c)
+
+
+def stage_table(dev, world, pk, cpr_prefill_ms, sec):
+    """The pages' stage comparison on this GPU: CPR (every stage bitwise consistent)
+    against "native mixed" (chunked prefill and trainer, token-recurrent decode without
+    resynchronisation) and "recurrent everywhere"."""
+    K, W = 512, 3
+    nd = NativeDecode(dev, K + W)
+    ms_d, prof_d = time_device(nd, K, W, world, profile=True)
+    n_steps = K + W
+    bitwise = bool(torch.equal(nd.ref.view(torch.int32), nd.o_steps.contiguous().view(torch.int32)))
+    us_launch = prof_d["cpr_rec_step"][1] / prof_d["cpr_rec_step"][0] * 1e3
+    d = WORKLOADS["decode"]["d"]
+    byt = nd.units * (2 * d * d * 4 + 3 * d * 2 + 8 + d * 4)   # state read + write, token in, o out
+    native_decode = {"us_per_step": round(ms_d * 1e3, 3), "bitwise_decode_vs_prefill": bitwise,
+                     "roofline": {"kernel": "cpr_rec_step", "bound": "hbm",
+                                  "achieved": round(byt / (us_launch * 1e-6) / 1e9, 1),
+                                  "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(byt / (us_launch * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                                  "algo_bytes_per_launch": byt}}
+    del nd
+    rp = RecurrentPrefill(dev)
+    ms_p, _ = time_device(rp, 3, 2, world, profile=False)
+    tok = sum(rp.lens)
+    del rp
+    torch.cuda.empty_cache()
+    cpr_dec = sec.get("decode", {})
+    cpr_tr = sec.get("trainer", {})
+    return {
+        "cpr": {"prefill_ms": round(cpr_prefill_ms, 4), "trainer_fwd_bwd_ms": cpr_tr.get("ms_per_step"),
+                "decode_us_per_step": cpr_dec.get("value"),
+                "bitwise_decode_vs_prefill": cpr_dec.get("bitwise_decode_vs_prefill")},
+        "native_mixed": {"prefill_ms": round(cpr_prefill_ms, 4), "trainer_fwd_bwd_ms": cpr_tr.get("ms_per_step"),
+                         "decode_us_per_step": native_decode["us_per_step"],
+                         "bitwise_decode_vs_prefill": native_decode["bitwise_decode_vs_prefill"],
+                         "decode_roofline": native_decode["roofline"]},
+        "recurrent_everywhere": {"prefill_ms": round(ms_p, 4),
+                                 "prefill_tokens_per_s": round(tok / (ms_p * 1e-3) * world, 1)},
+        "note": "native mixed shares this build's chunked prefill and trainer kernels (CPR's "
+                "constraints change only how decode reaches its bits); its decode is the token "
+                "recurrence on the prefill's fp32 states",
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -688,6 +788,8 @@ def main():
             if nm != name:
                 sec[nm] = secondary(nm, dev, world, local, s, w, pk, args.policy)
         line["workloads"] = sec
+        if name == "prefill" and args.policy == "tc" and args.n_seq is None:
+            line["stage_table"] = stage_table(dev, world, pk, ms, sec)
     if rank == 0 and world == 1:
         u, dt, desc, cores = cpu_sample(name)
         cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)

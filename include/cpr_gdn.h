@@ -336,6 +336,35 @@ const char* cpr_last_error(void);
  * with cpr_get_device_error. */
 int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed);
 
+/* ---- stage-table ablations (outside the CPR guarantee) -------------------
+ * The gated delta rule run as a plain token recurrence, the engines' native
+ * decode that CPR replaces (page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配",
+ * section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet", stage table:
+ * "native mixed" = chunked prefill + token-recurrent decode without
+ * resynchronisation; "recurrent everywhere").  Per token, with H = S^T:
+ * H_t = a H + k u^T, u = b (v - a H^T k), a = exp(g), o_t = H_t^T (scale q),
+ * every sum an fp32 fma chain in a fixed order, so the two calls below agree
+ * bit for bit with each other; they do not agree bit for bit with the chunked
+ * path (which is the point of the comparison).  No digest: these calls make
+ * no cross-path promise.  The contract gives d_k = d_v (64 or 128), the io
+ * dtype (bf16 or fp32) and scale.  Pointers: device, 16-byte aligned (g and
+ * beta 4-byte); layouts as cpr_gdn_fwd; o is fp32.  Errors: CPR_ERR_INVALID_ARG,
+ * CPR_ERR_ALIGNMENT, CPR_ERR_UNSUPPORTED (d_k != d_v or d not 64/128), and
+ * CPR_ERR_BAD_SEQLENS on the device word for a sequence outside [0, n_tok]. */
+
+/* Token recurrence over whole sequences ("recurrent everywhere"): o for every
+ * token and, if final_state is not NULL, the final state.  h0 may be NULL. */
+int cpr_gdn_recurrent_fwd(const cpr_contract* c, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const int32_t* cu_seqlens,
+                          int n_seq, int64_t n_tok, int H, const float* h0, float* o,
+                          float* final_state, void* stream);
+
+/* One token per sequence on an fp32 state [n_seq, H, d_k, d_v] updated in
+ * place (the native decode step); q_t..beta_t as cpr_gdn_decode_step. */
+int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k_t,
+                           const void* v_t, const float* g_t, const float* beta_t, int n_seq,
+                           int H, float* state, float* o_t, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH):
                             P, SZ, P]),
         "cpr_gdn_fwd_train": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
         "cpr_selftest_wait_timeout": (I, [U32, ctypes.POINTER(U32)]),
+        "cpr_gdn_recurrent_fwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
+        "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -330,6 +332,35 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                            _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),
                            wsb, _stream()))
     return outs
+
+
+def cpr_gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
+                          want_final: bool = True):
+    """Stage-table ablation "recurrent everywhere": the token recurrence over whole
+    sequences (cpr_gdn_recurrent_fwd).  Returns (o fp32, final_state or None)."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
+    fin = (torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
+           if want_final else None)
+    _check(lib.cpr_gdn_recurrent_fwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o), _ptr(fin),
+                                     _stream()))
+    return o, fin
+
+
+def cpr_gdn_recurrent_step(q_t, k_t, v_t, g_t, beta_t, state, contract: Optional[Contract] = None,
+                           out=None):
+    """Stage-table ablation "native" decode: one token per sequence on the fp32 state
+    [n_seq, H, d_k, d_v], updated in place (cpr_gdn_recurrent_step).  Returns o_t fp32."""
+    lib = load_library()
+    c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
+    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
+    o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
+    _check(lib.cpr_gdn_recurrent_step(ctypes.byref(c), _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(g_t),
+                                      _ptr(beta_t), n_seq, H, _ptr(state), _ptr(o), _stream()))
+    return o
 
 
 def selftest_wait_timeout(poll_limit: int = 4096) -> bool:

@@ -12,6 +12,7 @@
 #include "sha256.h"
 #include "simt_launch.cuh"
 #include "tc_decode.cuh"
+#include "rec.h"
 #include "tc_launch.h"
 
 namespace {
@@ -565,6 +566,64 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
     if (e == cudaSuccess) e = cudaMemcpy(completed, d_ok, sizeof(uint32_t), cudaMemcpyDeviceToHost);
     cudaFree(d_ok);
     if (e != cudaSuccess) return cuda_fail(e, "selftest");
+    return CPR_OK;
+}
+
+static int rec_check(const cpr_contract* c) {
+    if (!c) return fail(CPR_ERR_INVALID_ARG, "contract is NULL");
+    if (c->d_k != c->d_v || (c->d_k != 64 && c->d_k != 128))
+        return fail(CPR_ERR_UNSUPPORTED, "recurrent path: d_k = d_v = 64 or 128 only");
+    if (c->io_dtype != CPR_DTYPE_BF16 && c->io_dtype != CPR_DTYPE_F32)
+        return fail(CPR_ERR_UNSUPPORTED, "recurrent path: io dtype bf16 or fp32");
+    return CPR_OK;
+}
+
+int cpr_gdn_recurrent_fwd(const cpr_contract* c, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const int32_t* cu_seqlens,
+                          int n_seq, int64_t n_tok, int H, const float* h0, float* o,
+                          float* final_state, void* stream) {
+    int rc = rec_check(c);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, n_tok, H);
+    if (rc) return rc;
+    REQ_PTR4(cu_seqlens);
+    if (n_tok > 0) {
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta); REQ_PTR(o);
+    }
+    OPT_PTR(h0); OPT_PTR(final_state);
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    cpr::rec::RecArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens; a.n_seq = n_seq;
+    a.n_tok = n_tok; a.H = H; a.scale = c->scale; a.h0 = h0; a.final_state = final_state; a.o = o;
+    a.err = err;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_rec_fwd", st);
+    const cudaError_t e = cpr::rec_launch(a, (int)c->d_k, c->io_dtype == CPR_DTYPE_BF16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent forward launch");
+    return CPR_OK;
+}
+
+int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k_t,
+                           const void* v_t, const float* g_t, const float* beta_t, int n_seq,
+                           int H, float* state, float* o_t, void* stream) {
+    int rc = rec_check(c);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, 0, H);
+    if (rc) return rc;
+    if (n_seq > 0) {
+        REQ_PTR(q_t); REQ_PTR(k_t); REQ_PTR(v_t); REQ_PTR4(g_t); REQ_PTR4(beta_t); REQ_PTR(o_t);
+        REQ_PTR(state);
+    }
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    cpr::rec::RecArgs a{};
+    a.q = q_t; a.k = k_t; a.v = v_t; a.g = g_t; a.beta = beta_t; a.cu = nullptr; a.n_seq = n_seq;
+    a.n_tok = n_seq; a.H = H; a.scale = c->scale; a.state = state; a.o = o_t; a.err = err;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_rec_step", st);
+    const cudaError_t e = cpr::rec_launch(a, (int)c->d_k, c->io_dtype == CPR_DTYPE_BF16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent step launch");
     return CPR_OK;
 }
 

@@ -1,0 +1,151 @@
+// The gated delta rule as a plain token recurrence, for the stage-table ablations:
+// "recurrent everywhere" (cpr_gdn_recurrent_fwd over whole sequences) and the
+// non-resynchronised decode of "native mixed" (cpr_gdn_recurrent_step on an fp32
+// state, after a chunked prefill).  Page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配",
+// section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet" and its stage table:
+// the engines' native path decodes token by token, which is what CPR replaces.
+//
+// Per token, with H = S^T (d_k x d_v) and a = exp(g):
+//   S_t = a S_{t-1} (I - b k k^T) + b v k^T   <=>   H_t = a H + k u^T,  u = b (v - a H^T k)
+//   o_t = S_t q = H_t^T (scale q)
+// One CTA per (sequence, head), 2 d threads: thread (j, part) keeps column j of H for
+// rows part * d/2 .. + d/2 in registers.  Every sum is one fp32 fma chain in ascending
+// row order per half, the two halves added half 0 first, so the prefill and a decode
+// step evaluate the same operations for a token (the two agree bit for bit); neither
+// agrees bit for bit with the chunked form.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "rec.h"
+
+namespace cpr {
+namespace rec {
+
+__device__ __forceinline__ float ld_io(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ld_io(const float* p, size_t i) { return p[i]; }
+
+template <int D>
+struct RecSmem {
+    float kq[2][2][D];   // [buffer][k | scale q][row]
+    float vv[2][D];
+    float ab[2][2];      // [buffer][a | b]
+    float red[2][D];     // H^T k halves
+    float red2[2][D];    // H^T q halves
+};
+
+// One token: H = a H + k u^T, u = b (v - a H^T k); returns the complete o_j (valid after
+// the second barrier).  `stage` runs between the two barriers (the next token's rows).
+template <int D, typename Stage>
+__device__ __forceinline__ float token(float (&h)[D / 2], RecSmem<D>& s, int cur, int j, int part,
+                                       Stage&& stage) {
+    const float* ks = s.kq[cur][0] + part * (D / 2);
+    const float* qs = s.kq[cur][1] + part * (D / 2);
+    float w = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) w = __fmaf_rn(h[i], ks[i], w);
+    s.red[part][j] = w;
+    __syncthreads();
+    const float a = s.ab[cur][0], b = s.ab[cur][1];
+    const float wj = __fadd_rn(s.red[0][j], s.red[1][j]);
+    const float u = __fmul_rn(b, __fsub_rn(s.vv[cur][j], __fmul_rn(a, wj)));
+    float o = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) {
+        h[i] = __fmaf_rn(ks[i], u, __fmul_rn(a, h[i]));
+        o = __fmaf_rn(h[i], qs[i], o);
+    }
+    s.red2[part][j] = o;
+    stage();
+    __syncthreads();
+    return __fadd_rn(s.red2[0][j], s.red2[1][j]);
+}
+
+template <int D, typename IO>
+__global__ void __launch_bounds__(2 * D) k_rec(RecArgs a) {
+    __shared__ RecSmem<D> s;
+    const int tid = threadIdx.x, j = tid % D, part = tid / D;
+    const int H = a.H;
+    const int b = blockIdx.x / H, h = blockIdx.x % H;
+    const size_t sh = (size_t)b * H + h;
+    const IO* q = static_cast<const IO*>(a.q);
+    const IO* k = static_cast<const IO*>(a.k);
+    const IO* v = static_cast<const IO*>(a.v);
+    int t0, t1;
+    if (a.cu) {  // recurrent prefill over the sequence's tokens
+        t0 = a.cu[b];
+        t1 = a.cu[b + 1];
+        if (t0 < 0 || t1 < t0 || (int64_t)t1 > a.n_tok) {
+            if (tid == 0) set_error(a.err, CPR_ERR_BAD_SEQLENS);
+            return;
+        }
+    } else {     // one decode step: token b of the step's batch
+        t0 = b;
+        t1 = b + 1;
+    }
+    // the state: column j, this thread's half of the rows
+    float hr[D / 2];
+    const float* hin = a.cu ? a.h0 : a.state;
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i)
+        hr[i] = hin ? hin[(sh * D + part * (D / 2) + i) * D + j] : 0.f;
+    // token rows into registers (threads < D), then into a shared buffer
+    float rk = 0.f, rq = 0.f, rv = 0.f, ra = 0.f, rb = 0.f;
+    auto load = [&](int t) {
+        if (tid < D) {
+            const size_t row = ((size_t)t * H + h) * D + tid;
+            rk = ld_io(k, row);
+            rq = __fmul_rn(a.scale, ld_io(q, row));
+            rv = ld_io(v, row);
+        }
+        if (tid == 0) {
+            ra = expf(a.g[(size_t)t * H + h]);
+            rb = a.beta[(size_t)t * H + h];
+        }
+    };
+    auto store = [&](int buf) {
+        if (tid < D) {
+            s.kq[buf][0][tid] = rk;
+            s.kq[buf][1][tid] = rq;
+            s.vv[buf][tid] = rv;
+        }
+        if (tid == 0) {
+            s.ab[buf][0] = ra;
+            s.ab[buf][1] = rb;
+        }
+    };
+    if (t0 < t1) {
+        load(t0);
+        store(0);
+    }
+    __syncthreads();
+    for (int t = t0; t < t1; ++t) {
+        const int cur = (t - t0) & 1;
+        const bool more = t + 1 < t1;
+        if (more) load(t + 1);   // lands while this token's sums run
+        const float o = token<D>(hr, s, cur, j, part, [&]() { if (more) store(cur ^ 1); });
+        if (part == 0) a.o[((size_t)t * H + h) * D + j] = o;
+    }
+    float* hout = a.cu ? a.final_state : a.state;
+    if (hout) {
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) hout[(sh * D + part * (D / 2) + i) * D + j] = hr[i];
+    }
+}
+
+template <int D, typename IO>
+static cudaError_t launch(const RecArgs& a, cudaStream_t st) {
+    const int64_t grid = (int64_t)a.n_seq * a.H;
+    if (grid > 0) k_rec<D, IO><<<(unsigned)grid, 2 * D, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace rec
+
+cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st) {
+    if (d == 128) return bf16 ? rec::launch<128, __nv_bfloat16>(a, st) : rec::launch<128, float>(a, st);
+    if (d == 64) return bf16 ? rec::launch<64, __nv_bfloat16>(a, st) : rec::launch<64, float>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace cpr

@@ -1,0 +1,32 @@
+// Token-recurrence kernels for the stage-table ablations (see rec.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cpr {
+namespace rec {
+
+struct RecArgs {
+    const void* q;            // io dtype [n_tok, H, d]
+    const void* k;
+    const void* v;
+    const float* g;           // [n_tok, H]
+    const float* beta;
+    const int32_t* cu;        // sequences for the prefill; null for a decode step
+    int n_seq;
+    int64_t n_tok;
+    int H;
+    float scale;
+    const float* h0;          // prefill: initial state or null (zeros)
+    float* state;             // decode: the state, read and written in place
+    float* final_state;       // prefill: final state or null
+    float* o;                 // fp32 [n_tok, H, d]
+    uint32_t* err;
+};
+
+}  // namespace rec
+
+// d in {64, 128}; io bf16 or fp32.
+cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st);
+
+}  // namespace cpr

@@ -1,0 +1,92 @@
+"""Stage-table ablation paths (the token recurrence): parity with the oracle, bit
+agreement between the recurrent prefill and recurrent decode steps, and the property
+the comparison is about: a chunked prefill followed by recurrent decode steps ("native
+mixed") is close to the oracle but not bit-identical to a one-shot prefill."""
+import pytest
+import torch
+
+import infer_consistent_linear_gb300 as cpr
+import oracle
+from infer_consistent_linear_gb300.synth import make_inputs
+from gpu_helpers import TOL_BF16, TOL_F32, assert_bitwise, assert_close, require_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@pytest.mark.parametrize("io,d,tol", [(torch.bfloat16, 128, TOL_BF16), (torch.float32, 64, TOL_F32)])
+def test_recurrent_fwd_matches_oracle(io, d, tol):
+    lens, H = [200, 64, 1, 0, 130], 2
+    x = make_inputs(lens, H, d, d, io_dtype=io, seed=3, h0_std=0.1)
+    xd = x.to(DEV)
+    c = cpr.default_contract(io, d)
+    o, fin = cpr.cpr_gdn_recurrent_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    o_ref, h_ref = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
+    assert_close("o", o.cpu(), o_ref, tol)
+    assert_close("final", fin.cpu(), h_ref, tol)
+    o2, fin2 = cpr.cpr_gdn_recurrent_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0,
+                                         contract=c)
+    assert_bitwise("o rerun", o2, o)
+    assert_bitwise("final rerun", fin2, fin)
+
+
+def test_recurrent_steps_equal_recurrent_prefill():
+    pre, steps, H, d = [70, 64, 0, 5], 40, 2, 128
+    full = [L + steps for L in pre]
+    x = make_inputs(full, H, d, d, io_dtype=torch.bfloat16, seed=4, h0_std=0.1).to(DEV)
+    c = cpr.default_contract(torch.bfloat16, d)
+    o_full, fin_full = cpr.cpr_gdn_recurrent_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0,
+                                                 contract=c)
+    cu = x.cu_seqlens.tolist()
+    sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(len(pre))]).to(DEV)
+    cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(pre), 0).tolist(), dtype=torch.int32, device=DEV)
+    _, state = cpr.cpr_gdn_recurrent_fwd(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel], cu_pre,
+                                         h0=x.h0, contract=c)
+    for t in range(steps):
+        idx = torch.tensor([cu[b] + pre[b] + t for b in range(len(pre))], device=DEV)
+        ot = cpr.cpr_gdn_recurrent_step(x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx], state,
+                                        contract=c)
+        assert_bitwise(f"step {t}", ot, o_full[idx])
+    assert_bitwise("final state", state, fin_full)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+
+
+def test_native_mixed_is_close_but_not_bitwise():
+    """Chunked (tensor-core) prefill, then recurrent decode from its final state: the
+    outputs stay within tolerance of the oracle, and differ in bits from the one-shot
+    prefill that CPR's decode reproduces exactly."""
+    pre, steps, H, d = [128, 100, 64, 37], 30, 2, 128
+    full = [L + steps for L in pre]
+    x = make_inputs(full, H, d, d, io_dtype=torch.bfloat16, seed=5, h0_std=0.1)
+    xd = x.to(DEV)
+    c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+    o_full, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    cu = x.cu_seqlens.tolist()
+    sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(len(pre))]).to(DEV)
+    cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(pre), 0).tolist(), dtype=torch.int32, device=DEV)
+    _, state = cpr.cpr_gdn_fwd(xd.q[sel], xd.k[sel], xd.v[sel], xd.g[sel], xd.beta[sel], cu_pre,
+                               h0=xd.h0, contract=c)
+    outs, idxs = [], []
+    for t in range(steps):
+        idx = torch.tensor([cu[b] + pre[b] + t for b in range(len(pre))], device=DEV)
+        outs.append(cpr.cpr_gdn_recurrent_step(xd.q[idx], xd.k[idx], xd.v[idx], xd.g[idx], xd.beta[idx],
+                                               state, contract=c))
+        idxs.append(idx)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    o_dec = torch.stack(outs)                       # [steps, n_seq, H, d]
+    o_pre = torch.stack([o_full[i] for i in idxs])
+    differ = int((o_dec.view(torch.int32) != o_pre.view(torch.int32)).sum())
+    assert differ > 0, "native mixed decode unexpectedly reproduced the prefill's bits"
+    o_ref, _ = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
+    o_ref = torch.as_tensor(o_ref)
+    o_ref_steps = torch.stack([o_ref[i.cpu()] for i in idxs])
+    assert_close("native mixed decode vs oracle", o_dec.cpu(), o_ref_steps, TOL_BF16)
