@@ -682,6 +682,67 @@ class RecurrentPrefill:
         self.cpr.cpr_gdn_recurrent_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c)
 
 
+class ContextParallelPrefill:
+    """Context-parallel prefill emulated on one GPU: the Prefill workload's sequences cut
+    into R chunk-aligned segments (one per emulated rank), run one after another with the
+    fp32 state handed on as the next segment's h0."""
+
+    def __init__(self, dev, R):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("prefill")
+        H, d = WORKLOADS["prefill"]["H"], WORKLOADS["prefill"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        x = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        self.o_ref, self.fin_ref = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c)
+        cu = x.cu_seqlens.tolist()
+        n_seq = len(self.lens)
+        self.segs = []
+        for r in range(R):
+            idx, seg_lens = [], []
+            for b, L in enumerate(self.lens):
+                nch = (L + C - 1) // C
+                lo, hi = min(L, C * ((nch * r) // R)), min(L, C * ((nch * (r + 1)) // R))
+                idx.append(torch.arange(cu[b] + lo, cu[b] + hi))
+                seg_lens.append(hi - lo)
+            idx = torch.cat(idx).to(dev)
+            cus = torch.tensor([0] + torch.cumsum(torch.tensor(seg_lens), 0).tolist(), dtype=torch.int32,
+                               device=dev)
+            n_tok = int(idx.numel())
+            self.segs.append(dict(idx=idx, q=x.q[idx], k=x.k[idx], v=x.v[idx], g=x.g[idx], beta=x.beta[idx],
+                                  cu=cus, o=torch.empty(n_tok, H, d, device=dev),
+                                  ws=torch.empty(cpr.workspace_bytes(self.c, cpr.CPR_OP_FWD, n_seq, n_tok, H),
+                                                 dtype=torch.uint8, device=dev)))
+        self.h = [torch.empty(n_seq, H, d, d, device=dev) for _ in range(R)]
+        torch.cuda.synchronize()
+
+    def run(self):
+        h = None
+        for s_, fin in zip(self.segs, self.h):
+            self.cpr.cpr_gdn_fwd(s_["q"], s_["k"], s_["v"], s_["g"], s_["beta"], s_["cu"], h0=h,
+                                 contract=self.c, out=s_["o"], final=fin, workspace=s_["ws"])
+            h = fin
+
+    def bitwise(self):
+        ok = all(torch.equal(s_["o"].view(torch.int32), self.o_ref.index_select(0, s_["idx"]).view(torch.int32))
+                 for s_ in self.segs)
+        return bool(ok and torch.equal(self.h[-1].view(torch.int32), self.fin_ref.view(torch.int32)))
+
+
+def context_parallel(dev, world, unsplit_ms, R=4):
+    cp = ContextParallelPrefill(dev, R)
+    ms, _ = time_device(cp, 10, 3, world, profile=False)
+    res = {"workload": WORKLOADS["prefill"]["desc"] + f", {R} chunk-aligned segments per sequence "
+                                                     "run in turn with the state handed on",
+           "ms_per_step": round(ms, 4), "unsplit_ms_per_step": round(unsplit_ms, 4),
+           "tokens_per_s": round(sum(cp.lens) / (ms * 1e-3) * world, 1),
+           "bitwise_vs_unsplit": cp.bitwise()}
+    del cp
+    torch.cuda.empty_cache()
+    return res
+
+
 def stage_table(dev, world, pk, cpr_prefill_ms, sec):
     """The pages' stage comparison on this GPU: CPR (every stage bitwise consistent)
     against "native mixed" (chunked prefill and trainer, token-recurrent decode without
@@ -790,6 +851,7 @@ def main():
         line["workloads"] = sec
         if name == "prefill" and args.policy == "tc" and args.n_seq is None:
             line["stage_table"] = stage_table(dev, world, pk, ms, sec)
+            line["context_parallel"] = context_parallel(dev, world, ms)
     if rank == 0 and world == 1:
         u, dt, desc, cores = cpu_sample(name)
         cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)

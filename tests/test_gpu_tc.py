@@ -92,6 +92,31 @@ def test_tc_chunk_aligned_split_and_batch_invariance():
     assert_bitwise("split final", f2, fin[0:1])
 
 
+def test_tc_context_parallel_segments_bitwise():
+    """Context-parallel prefill emulated on one GPU: every sequence cut into chunk-aligned
+    segments (one per emulated rank), run one after another with the fp32 state handed
+    on as the next segment's h0; outputs and final states equal the unsplit run bit for
+    bit, whatever the cut points."""
+    c = _tc()
+    lens, H = [1024, 700, 192, 65], 2
+    x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=6, h0_std=0.1).to(DEV)
+    o, fin = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
+    cu = x.cu_seqlens.tolist()
+    for R in (2, 4):
+        for b, L in enumerate(lens):
+            nch = (L + 63) // 64
+            cuts = sorted({min(L, 64 * ((nch * r) // R)) for r in range(R + 1)})
+            h = x.h0[b:b + 1].contiguous()
+            for lo, hi in zip(cuts[:-1], cuts[1:]):
+                sl = slice(cu[b] + lo, cu[b] + hi)
+                cub = torch.tensor([0, hi - lo], dtype=torch.int32, device=DEV)
+                os, h = cpr.cpr_gdn_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl], cub, h0=h, contract=c)
+                assert_bitwise(f"o seq {b} segment [{lo}, {hi}) of {R}", os, o[sl])
+            assert_bitwise(f"final seq {b}, {R} segments", h, fin[b:b + 1])
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+
+
 def test_tc_prefill_cache_refused_by_simt_decode():
     x = make_inputs([70], 1, 128, 128, io_dtype=torch.bfloat16, seed=1).to(DEV)
     cu = torch.tensor([0, 69], dtype=torch.int32, device=DEV)
