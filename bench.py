@@ -743,6 +743,43 @@ def context_parallel(dev, world, unsplit_ms, R=4):
     return res
 
 
+class ProjectionGemm:
+    """The projection in front of the layer on the Prefill workload's tokens: X [16384,
+    2048] bf16 times W [2048, 16 x 128] bf16, K in 4 fixed leaves of 512."""
+
+    def __init__(self, dev, d_model=2048, leaf_k=512):
+        import infer_consistent_linear_gb300 as cpr
+        self.cpr = cpr
+        w = WORKLOADS["prefill"]
+        self.M, self.K, self.N, self.leaf_k = sum(workload_lens("prefill")), d_model, w["H"] * w["d"], leaf_k
+        g = torch.Generator().manual_seed(0)
+        self.x = torch.randn(self.M, self.K, generator=g).to(torch.bfloat16).to(dev)
+        self.w = (torch.randn(self.K, self.N, generator=g) / self.K ** 0.5).to(torch.bfloat16).to(dev)
+        self.y = torch.empty(self.M, self.N, device=dev)
+        torch.cuda.synchronize()
+
+    def run(self):
+        self.cpr.cpr_gemm(self.x, self.w, self.leaf_k, out=self.y)
+
+
+def projection_gemm(dev, world, pk):
+    pg = ProjectionGemm(dev)
+    ms, _ = time_device(pg, 10, 3, world, profile=False)
+    flops = 2.0 * pg.M * pg.N * pg.K
+    tf = flops / (ms * 1e-3) / 1e12
+    sub = pg.cpr.cpr_gemm(pg.x[1000:1777].contiguous(), pg.w, pg.leaf_k)
+    inv = bool(torch.equal(sub.view(torch.int32), pg.y[1000:1777].view(torch.int32)))
+    res = {"shape": f"X [{pg.M}, {pg.K}] x W [{pg.K}, {pg.N}], bf16 in, fp32 out, {pg.K // pg.leaf_k} "
+                    f"leaves of {pg.leaf_k}",
+           "ms": round(ms, 4), "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                            "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                            "frac": round(tf / pk["bf16_tflops"], 4)},
+           "rows_bitwise_in_a_sub_batch": inv}
+    del pg, sub
+    torch.cuda.empty_cache()
+    return res
+
+
 def stage_table(dev, world, pk, cpr_prefill_ms, sec):
     """The pages' stage comparison on this GPU: CPR (every stage bitwise consistent)
     against "native mixed" (chunked prefill and trainer, token-recurrent decode without
@@ -852,6 +889,7 @@ def main():
         if name == "prefill" and args.policy == "tc" and args.n_seq is None:
             line["stage_table"] = stage_table(dev, world, pk, ms, sec)
             line["context_parallel"] = context_parallel(dev, world, ms)
+            line["projection_gemm"] = projection_gemm(dev, world, pk)
     if rank == 0 and world == 1:
         u, dt, desc, cores = cpu_sample(name)
         cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)

@@ -365,6 +365,21 @@ int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k
                            const void* v_t, const float* g_t, const float* beta_t, int n_seq,
                            int H, float* state, float* o_t, void* stream);
 
+/* ---- batch-invariant projection GEMM ------------------------------------
+ * Y = X W for the projections that feed the CPR layer (page "IsoExec: 切换
+ * SkyRL 中的训练器-推理不匹配": batch-invariant kernels for everything around
+ * the layer, so a token's inputs do not change with its batch).  X bf16 [M, K],
+ * W bf16 [K, N], Y fp32 [M, N], all row-major, device, 16-byte aligned.  K is
+ * split into K / leaf_k contiguous leaves (leaf_k a multiple of 64; 1, 2 or 4
+ * leaves); each leaf is accumulated in fp32 by tensor-core MMAs in ascending
+ * k and the leaves are added in the fixed tree (P0 + P1) + (P2 + P3).  A row's
+ * result depends only on that row of X, on W and on leaf_k: it is the same for
+ * any M and any batch the row sits in.  N must be a multiple of 128.  Errors:
+ * CPR_ERR_INVALID_ARG (shapes, leaf_k, NULL), CPR_ERR_ALIGNMENT; a bounded
+ * device wait that runs out records CPR_ERR_DEVICE_TIMEOUT. */
+int cpr_gemm_bf16(const void* X, const void* W, float* Y, int M, int N, int K, int leaf_k,
+                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

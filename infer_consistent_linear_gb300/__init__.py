@@ -97,6 +97,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_selftest_wait_timeout": (I, [U32, ctypes.POINTER(U32)]),
         "cpr_gdn_recurrent_fwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
+        "cpr_gemm_bf16": (I, [P, P, P, I, I, I, I, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -361,6 +362,17 @@ def cpr_gdn_recurrent_step(q_t, k_t, v_t, g_t, beta_t, state, contract: Optional
     _check(lib.cpr_gdn_recurrent_step(ctypes.byref(c), _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(g_t),
                                       _ptr(beta_t), n_seq, H, _ptr(state), _ptr(o), _stream()))
     return o
+
+
+def cpr_gemm(x, w, leaf_k: int, out=None):
+    """Batch-invariant projection GEMM (cpr_gemm_bf16): x bf16 [M, K], w bf16 [K, N] ->
+    fp32 [M, N], K in fixed leaves of leaf_k rows."""
+    lib = load_library()
+    M, K = int(x.shape[0]), int(x.shape[1])
+    N = int(w.shape[1])
+    y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _check(lib.cpr_gemm_bf16(_ptr(x), _ptr(w), _ptr(y), M, N, K, leaf_k, _stream()))
+    return y
 
 
 def selftest_wait_timeout(poll_limit: int = 4096) -> bool:

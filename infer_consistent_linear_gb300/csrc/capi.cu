@@ -13,6 +13,7 @@
 #include "simt_launch.cuh"
 #include "tc_decode.cuh"
 #include "rec.h"
+#include "gemm.h"
 #include "tc_launch.h"
 
 namespace {
@@ -624,6 +625,29 @@ int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k
     cpr::ProfScope ps("cpr_rec_step", st);
     const cudaError_t e = cpr::rec_launch(a, (int)c->d_k, c->io_dtype == CPR_DTYPE_BF16, st);
     if (e != cudaSuccess) return cuda_fail(e, "recurrent step launch");
+    return CPR_OK;
+}
+
+int cpr_gemm_bf16(const void* X, const void* W, float* Y, int M, int N, int K, int leaf_k,
+                  void* stream) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 128 || K % 64 || leaf_k <= 0 || leaf_k % 64 || K % leaf_k)
+        return fail(CPR_ERR_INVALID_ARG, "gemm: N a multiple of 128, leaf_k a multiple of 64 dividing K");
+    const int nleaf = K / leaf_k;
+    if (nleaf != 1 && nleaf != 2 && nleaf != 4)
+        return fail(CPR_ERR_INVALID_ARG, "gemm: K / leaf_k must be 1, 2 or 4");
+    if ((int64_t)M * K > INT32_MAX * 4ll) return fail(CPR_ERR_INVALID_ARG, "gemm: M * K too large");
+    if (M > 0) {
+        REQ_PTR(X); REQ_PTR(W); REQ_PTR(Y);
+    }
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    cpr::gemm::GemmArgs a{};
+    a.X = static_cast<const __nv_bfloat16*>(X); a.W = static_cast<const __nv_bfloat16*>(W); a.Y = Y;
+    a.M = M; a.N = N; a.K = K; a.leaf_k = leaf_k; a.err = err;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_gemm", st);
+    const cudaError_t e = cpr::gemm_launch(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return CPR_OK;
 }
 

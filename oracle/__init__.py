@@ -135,3 +135,10 @@ class OracleBuild:
 
     def gdn_bwd(self, *a, **kw):
         return gdn_bwd(*a, _lib_override=self._lib, **kw)
+
+
+def gemm(x, w):
+    """Projection oracle: Y = X W in fp64 (numpy matmul of the exact inputs), the
+    definition the batch-invariant split-K GEMM is checked against.  Pinned in
+    tests/test_oracle_gemm.py against a brute-force triple loop on small shapes."""
+    return _f64(x) @ _f64(w)
