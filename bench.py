@@ -780,6 +780,49 @@ def projection_gemm(dev, world, pk):
     return res
 
 
+class ReadingB:
+    """Reading B on the Prefill workload: the chunk-form training forward, then every
+    chunk's outputs by the token recurrence from its boundary state."""
+
+    def __init__(self, dev):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("prefill")
+        H, d = WORKLOADS["prefill"]["H"], WORKLOADS["prefill"]["d"]
+        self.H = H
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        self.x_host = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0)
+        self.xd = self.x_host.to(dev)
+        n_tok, n_seq = sum(self.lens), len(self.lens)
+        self.ws = torch.empty(cpr.workspace_bytes(self.c, cpr.CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
+                              device=dev)
+        torch.cuda.synchronize()
+
+    def run(self):
+        x = self.xd
+        self.o, _ = self.cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c,
+                                                   workspace=self.ws)
+
+
+def reading_b(dev, world, reading_a_ms):
+    """Speed of reading B against reading A on the same workload, and how far apart the two
+    readings' outputs are (both are checked against the oracle in the GPU tests)."""
+    rb = ReadingB(dev)
+    ms, _ = time_device(rb, 5, 2, world, profile=False)
+    x = rb.xd
+    oa, _ = rb.cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=rb.c, want_final=False)
+    ob = rb.o
+    diff = float((ob - oa).abs().max()) / float(oa.pow(2).mean().sqrt())
+    res = {"workload": WORKLOADS["prefill"]["desc"], "ms_per_step": round(ms, 4),
+           "reading_a_ms_per_step": round(reading_a_ms, 4),
+           "max_abs_diff_to_reading_a_over_rms": diff,
+           "bitwise_equal_to_reading_a": bool(torch.equal(oa.view(torch.int32), ob.view(torch.int32)))}
+    del rb
+    torch.cuda.empty_cache()
+    return res
+
+
 def stage_table(dev, world, pk, cpr_prefill_ms, sec):
     """The pages' stage comparison on this GPU: CPR (every stage bitwise consistent)
     against "native mixed" (chunked prefill and trainer, token-recurrent decode without
@@ -890,6 +933,7 @@ def main():
             line["stage_table"] = stage_table(dev, world, pk, ms, sec)
             line["context_parallel"] = context_parallel(dev, world, ms)
             line["projection_gemm"] = projection_gemm(dev, world, pk)
+            line["reading_b"] = reading_b(dev, world, ms)
     if rank == 0 and world == 1:
         u, dt, desc, cores = cpu_sample(name)
         cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)

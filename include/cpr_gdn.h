@@ -352,6 +352,20 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed);
  * CPR_ERR_ALIGNMENT, CPR_ERR_UNSUPPORTED (d_k != d_v or d not 64/128), and
  * CPR_ERR_BAD_SEQLENS on the device word for a sequence outside [0, n_tok]. */
 
+/* Reading B of CPR (the pages' literal wording: within a chunk, the token
+ * recurrence from the resynchronised boundary state), tensor-core contracts
+ * only: the training forward of cpr_gdn_fwd_train (same arguments, same
+ * CPR_OP_BWD-sized workspace, the same final state), then every chunk's o
+ * recomputed by the token recurrence above, started at the chunk form's
+ * boundary state H_n as the hi + lo operand tiles the forward leaves in the
+ * workspace -- the bits a decode cache's state tiles hold for that chunk.  o
+ * holds reading B's outputs on return; chunks are independent (parallel). */
+int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                          const void* k, const void* v, const float* g, const float* beta,
+                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                          const float* h0, void* o, float* final_state, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Token recurrence over whole sequences ("recurrent everywhere"): o for every
  * token and, if final_state is not NULL, the final state.  h0 may be NULL. */
 int cpr_gdn_recurrent_fwd(const cpr_contract* c, const void* q, const void* k, const void* v,

@@ -98,6 +98,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_recurrent_fwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gemm_bf16": (I, [P, P, P, I, I, I, I, P]),
+        "cpr_gdn_fwd_reading_b": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -333,6 +334,24 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                            _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),
                            wsb, _stream()))
     return outs
+
+
+def cpr_gdn_fwd_reading_b(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
+                          digest: Optional[bytes] = None, workspace=None):
+    """Reading B (cpr_gdn_fwd_reading_b): chunk-form boundary states, in-chunk token
+    recurrence for the outputs.  Returns (o fp32, final_state)."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(c, CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
+                                device=q.device)
+    o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
+    fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
+    _check(lib.cpr_gdn_fwd_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
+                                     _ptr(fin), _ptr(workspace), workspace.numel(), _stream()))
+    return o, fin
 
 
 def cpr_gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,

@@ -570,6 +570,30 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
     return CPR_OK;
 }
 
+int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                          const void* k, const void* v, const float* g, const float* beta,
+                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                          const float* h0, void* o, float* final_state, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    // the chunk form leaves every chunk's boundary state in the workspace (training forward)
+    const int rc = forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                                final_state, nullptr, workspace, workspace_bytes, stream, true);
+    if (rc) return rc;
+    const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    cpr::rec::RbArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q); a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v); a.g = g; a.beta = beta; a.cu = cu_seqlens;
+    a.chunk_off = reinterpret_cast<const int32_t*>(wsb + w.chunk_off); a.n_seq = n_seq; a.H = H;
+    a.scale = c->scale; a.ws = wsb + w.W; a.blk_bytes = cpr::tc::kBlockTrain;
+    a.off_hn = cpr::tc::kOffHn; a.o = static_cast<float*>(o);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_reading_b", st);
+    const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
+    return CPR_OK;
+}
+
 static int rec_check(const cpr_contract* c) {
     if (!c) return fail(CPR_ERR_INVALID_ARG, "contract is NULL");
     if (c->d_k != c->d_v || (c->d_k != 64 && c->d_k != 128))

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "rec.h"
+#include "tc_common.cuh"
 
 namespace cpr {
 namespace rec {
@@ -61,6 +62,51 @@ __device__ __forceinline__ float token(float (&h)[D / 2], RecSmem<D>& s, int cur
     return __fadd_rn(s.red2[0][j], s.red2[1][j]);
 }
 
+// Tokens t0 .. t1 - 1 of head h from the state in hr: each token's rows are loaded into
+// registers while the previous token's sums run, then staged in a shared buffer.
+template <int D, typename IO>
+__device__ __forceinline__ void token_loop(float (&hr)[D / 2], RecSmem<D>& s, const IO* q, const IO* k,
+                                           const IO* v, const float* g, const float* beta, int H, int h,
+                                           float scale, int t0, int t1, float* out) {
+    const int tid = threadIdx.x, j = tid % D, part = tid / D;
+    float rk = 0.f, rq = 0.f, rv = 0.f, ra = 0.f, rb = 0.f;
+    auto load = [&](int t) {
+        if (tid < D) {
+            const size_t row = ((size_t)t * H + h) * D + tid;
+            rk = ld_io(k, row);
+            rq = __fmul_rn(scale, ld_io(q, row));
+            rv = ld_io(v, row);
+        }
+        if (tid == 0) {
+            ra = expf(g[(size_t)t * H + h]);
+            rb = beta[(size_t)t * H + h];
+        }
+    };
+    auto store = [&](int buf) {
+        if (tid < D) {
+            s.kq[buf][0][tid] = rk;
+            s.kq[buf][1][tid] = rq;
+            s.vv[buf][tid] = rv;
+        }
+        if (tid == 0) {
+            s.ab[buf][0] = ra;
+            s.ab[buf][1] = rb;
+        }
+    };
+    if (t0 < t1) {
+        load(t0);
+        store(0);
+    }
+    __syncthreads();
+    for (int t = t0; t < t1; ++t) {
+        const int cur = (t - t0) & 1;
+        const bool more = t + 1 < t1;
+        if (more) load(t + 1);   // lands while this token's sums run
+        const float o = token<D>(hr, s, cur, j, part, [&]() { if (more) store(cur ^ 1); });
+        if (part == 0) out[((size_t)t * H + h) * D + j] = o;
+    }
+}
+
 template <int D, typename IO>
 __global__ void __launch_bounds__(2 * D) k_rec(RecArgs a) {
     __shared__ RecSmem<D> s;
@@ -89,48 +135,39 @@ __global__ void __launch_bounds__(2 * D) k_rec(RecArgs a) {
 #pragma unroll
     for (int i = 0; i < D / 2; ++i)
         hr[i] = hin ? hin[(sh * D + part * (D / 2) + i) * D + j] : 0.f;
-    // token rows into registers (threads < D), then into a shared buffer
-    float rk = 0.f, rq = 0.f, rv = 0.f, ra = 0.f, rb = 0.f;
-    auto load = [&](int t) {
-        if (tid < D) {
-            const size_t row = ((size_t)t * H + h) * D + tid;
-            rk = ld_io(k, row);
-            rq = __fmul_rn(a.scale, ld_io(q, row));
-            rv = ld_io(v, row);
-        }
-        if (tid == 0) {
-            ra = expf(a.g[(size_t)t * H + h]);
-            rb = a.beta[(size_t)t * H + h];
-        }
-    };
-    auto store = [&](int buf) {
-        if (tid < D) {
-            s.kq[buf][0][tid] = rk;
-            s.kq[buf][1][tid] = rq;
-            s.vv[buf][tid] = rv;
-        }
-        if (tid == 0) {
-            s.ab[buf][0] = ra;
-            s.ab[buf][1] = rb;
-        }
-    };
-    if (t0 < t1) {
-        load(t0);
-        store(0);
-    }
-    __syncthreads();
-    for (int t = t0; t < t1; ++t) {
-        const int cur = (t - t0) & 1;
-        const bool more = t + 1 < t1;
-        if (more) load(t + 1);   // lands while this token's sums run
-        const float o = token<D>(hr, s, cur, j, part, [&]() { if (more) store(cur ^ 1); });
-        if (part == 0) a.o[((size_t)t * H + h) * D + j] = o;
-    }
+    token_loop<D, IO>(hr, s, q, k, v, a.g, a.beta, H, h, a.scale, t0, t1, a.o);
     float* hout = a.cu ? a.final_state : a.state;
     if (hout) {
 #pragma unroll
         for (int i = 0; i < D / 2; ++i) hout[(sh * D + part * (D / 2) + i) * D + j] = hr[i];
     }
+}
+
+// Reading B of the chunk form: each chunk's outputs from the token recurrence started at
+// the chunk form's boundary state H_n.  The training forward leaves H_n in every chunk's
+// workspace block as hi/lo operand tiles (K-major (d, j)); the start state is hi + lo,
+// the same bits a decode cache's state tiles hold for that chunk.  One CTA per (chunk,
+// head), chunks independent.
+__global__ void __launch_bounds__(256) k_rb(RbArgs a) {
+    constexpr int D = 128;
+    __shared__ RecSmem<D> s;
+    const int tid = threadIdx.x, j = tid % D, part = tid / D;
+    const int total = a.chunk_off[a.n_seq];
+    const int cidx = blockIdx.x, h = blockIdx.y, H = a.H;
+    if (total < 0 || cidx >= total) return;
+    const int b = find_seq(a.chunk_off, a.n_seq, cidx);
+    const int n = cidx - a.chunk_off[b];
+    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
+    const int t0 = seq0 + n * kChunk, t1 = t0 + min(kChunk, T - n * kChunk);
+    const unsigned char* hn = a.ws + ((size_t)cidx * H + h) * a.blk_bytes + a.off_hn;
+    float hr[D / 2];
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) {
+        const uint32_t off = tc::cm_off(part * (D / 2) + i, j, D);
+        hr[i] = __fadd_rn(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hn + off)),
+                          __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hn + 32768 + off)));
+    }
+    token_loop<D, __nv_bfloat16>(hr, s, a.q, a.k, a.v, a.g, a.beta, H, h, a.scale, t0, t1, a.o);
 }
 
 template <int D, typename IO>
@@ -141,6 +178,11 @@ static cudaError_t launch(const RecArgs& a, cudaStream_t st) {
 }
 
 }  // namespace rec
+
+cudaError_t rb_launch(const rec::RbArgs& a, int64_t cmax, cudaStream_t st) {
+    if (cmax > 0 && a.H > 0) rec::k_rb<<<dim3((unsigned)cmax, (unsigned)a.H), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st) {
     if (d == 128) return bf16 ? rec::launch<128, __nv_bfloat16>(a, st) : rec::launch<128, float>(a, st);

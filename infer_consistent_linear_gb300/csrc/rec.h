@@ -1,5 +1,6 @@
 // Token-recurrence kernels for the stage-table ablations (see rec.cu).
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,9 +25,28 @@ struct RecArgs {
     uint32_t* err;
 };
 
+struct RbArgs {               // reading B (d = 128, bf16 io)
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    const int32_t* chunk_off;   // the training forward's chunk table
+    int n_seq;
+    int H;
+    float scale;
+    const unsigned char* ws;    // its per-(chunk, head) blocks
+    size_t blk_bytes;
+    size_t off_hn;              // H_n hi/lo tiles within a block
+    float* o;
+};
+
 }  // namespace rec
 
 // d in {64, 128}; io bf16 or fp32.
 cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st);
+// grid (chunk slots, H)
+cudaError_t rb_launch(const rec::RbArgs& a, int64_t cmax, cudaStream_t st);
 
 }  // namespace cpr

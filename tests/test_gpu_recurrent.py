@@ -90,3 +90,46 @@ def test_native_mixed_is_close_but_not_bitwise():
     o_ref = torch.as_tensor(o_ref)
     o_ref_steps = torch.stack([o_ref[i.cpu()] for i in idxs])
     assert_close("native mixed decode vs oracle", o_dec.cpu(), o_ref_steps, TOL_BF16)
+
+
+def _tc():
+    return cpr.default_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+
+
+def test_reading_b_matches_oracle_and_differs_from_reading_a():
+    """Reading B: the chunk form's boundary states, the token recurrence inside each chunk.
+    Within tolerance of the oracle like reading A, with the same final state (the same
+    chunk-form forward), and not the same bits as reading A's outputs."""
+    lens, H = [200, 64, 1, 0, 130], 2
+    x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=8, h0_std=0.1)
+    xd = x.to(DEV)
+    c = _tc()
+    ob, fb = cpr.cpr_gdn_fwd_reading_b(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    oa, fa = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    o_ref, h_ref = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
+    assert_close("o reading B", ob.cpu(), o_ref, TOL_BF16)
+    assert_close("o reading A", oa.cpu(), o_ref, TOL_BF16)
+    assert_bitwise("final state", fb, fa)
+    assert int((ob.view(torch.int32) != oa.view(torch.int32)).sum()) > 0
+    ob2, _ = cpr.cpr_gdn_fwd_reading_b(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    assert_bitwise("reading B rerun", ob2, ob)
+
+
+def test_reading_b_first_chunk_is_the_token_recurrence():
+    """With no initial state every sequence's first boundary state is zero, so reading B's
+    first chunk is exactly the token recurrence from zero (cpr_gdn_recurrent_fwd)."""
+    lens, H = [130, 64, 40], 2
+    x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=9).to(DEV)
+    ob, _ = cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=_tc())
+    cu = x.cu_seqlens.tolist()
+    for b, L in enumerate(lens):
+        n = min(L, 64)
+        sl = slice(cu[b], cu[b] + n)
+        cub = torch.tensor([0, n], dtype=torch.int32, device=DEV)
+        orr, _ = cpr.cpr_gdn_recurrent_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl], cub,
+                                           contract=cpr.default_contract(torch.bfloat16, 128))
+        assert_bitwise(f"first chunk of seq {b}", ob[sl], orr)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
