@@ -135,14 +135,11 @@ __global__ void __launch_bounds__(128, 1) k_gemm(GemmArgs a) {
 }  // namespace gemm
 
 cudaError_t gemm_launch(const gemm::GemmArgs& a, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm::k_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)gemm::kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
     if (a.M == 0) return cudaSuccess;
+    // per call (the attribute belongs to the current device), as the other launchers do
+    const cudaError_t e = cudaFuncSetAttribute(gemm::k_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)gemm::kSmem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(a.N / gemm::BN), (unsigned)((a.M + gemm::BM - 1) / gemm::BM));
     gemm::k_gemm<<<grid, 128, gemm::kSmem, st>>>(a);
     return cudaGetLastError();
