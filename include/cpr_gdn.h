@@ -366,6 +366,26 @@ int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const
                           const float* h0, void* o, float* final_state, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* Reading B with a decode cache: cpr_gdn_fwd_reading_b plus the decode cache of
+ * cpr_gdn_prefill (same cache layout, digest and CPR commits), and `run`, a
+ * caller-owned fp32 [n_seq, H, d_k, d_v] buffer that receives each sequence's
+ * in-chunk state after a partial last chunk. */
+int cpr_gdn_prefill_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                              const void* k, const void* v, const float* g, const float* beta,
+                              const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                              const float* h0, void* o, float* final_state, void* cache,
+                              float* run, void* workspace, size_t workspace_bytes, void* stream);
+
+/* One reading-B decode step: cpr_gdn_decode_step on the same cache (its rows,
+ * positions and chunk commits are unchanged), then one token of the recurrence
+ * on `run`, restarted from hi + lo of the cache's chunk-start state tiles at a
+ * chunk's first row.  o_t holds reading B's output.  Bit-identical to
+ * cpr_gdn_fwd_reading_b over the same tokens. */
+int cpr_gdn_decode_step_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
+                                  const void* k_t, const void* v_t, const float* g_t,
+                                  const float* beta_t, int n_seq, int H, void* cache, float* run,
+                                  void* o_t, void* stream);
+
 /* Token recurrence over whole sequences ("recurrent everywhere"): o for every
  * token and, if final_state is not NULL, the final state.  h0 may be NULL. */
 int cpr_gdn_recurrent_fwd(const cpr_contract* c, const void* q, const void* k, const void* v,

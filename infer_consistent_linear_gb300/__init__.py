@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gemm_bf16": (I, [P, P, P, I, I, I, I, P]),
         "cpr_gdn_fwd_reading_b": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
+        "cpr_gdn_prefill_reading_b": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, SZ, P]),
+        "cpr_gdn_decode_step_reading_b": (I, [CP, P, P, P, P, P, P, I, I, P, P, P, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -352,6 +354,40 @@ def cpr_gdn_fwd_reading_b(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optio
                                      _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
                                      _ptr(fin), _ptr(workspace), workspace.numel(), _stream()))
     return o, fin
+
+
+def cpr_gdn_prefill_reading_b(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
+                              digest: Optional[bytes] = None, workspace=None):
+    """Reading B with a decode cache (cpr_gdn_prefill_reading_b).  Returns (o, final_state,
+    cache, run) where run holds the running in-chunk states for the decode steps."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(c, CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
+                                device=q.device)
+    cache = new_decode_cache(c, n_seq, H, q.device)
+    run = torch.zeros(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
+    o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
+    fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
+    _check(lib.cpr_gdn_prefill_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(g), _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0),
+                                         _ptr(o), _ptr(fin), _ptr(cache.blob), _ptr(run), _ptr(workspace),
+                                         workspace.numel(), _stream()))
+    return o, fin, cache, run
+
+
+def cpr_gdn_decode_step_reading_b(q_t, k_t, v_t, g_t, beta_t, cache, run, contract: Optional[Contract] = None,
+                                  digest: Optional[bytes] = None, out=None):
+    """One reading-B decode step (cpr_gdn_decode_step_reading_b).  Returns o_t fp32."""
+    lib = load_library()
+    c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
+    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
+    o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
+    _check(lib.cpr_gdn_decode_step_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t), _ptr(v_t),
+                                             _ptr(g_t), _ptr(beta_t), n_seq, H, _ptr(cache.blob), _ptr(run),
+                                             _ptr(o), _stream()))
+    return o
 
 
 def cpr_gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,

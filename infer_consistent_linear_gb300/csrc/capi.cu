@@ -570,14 +570,14 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
     return CPR_OK;
 }
 
-int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
-                          const void* k, const void* v, const float* g, const float* beta,
-                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
-                          const float* h0, void* o, float* final_state, void* workspace,
+static int reading_b_impl(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
+                          const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                          int n_seq, int64_t n_tok, int H, const float* h0, void* o,
+                          float* final_state, void* cache, float* run, void* workspace,
                           size_t workspace_bytes, void* stream) {
     // the chunk form leaves every chunk's boundary state in the workspace (training forward)
     const int rc = forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
-                                final_state, nullptr, workspace, workspace_bytes, stream, true);
+                                final_state, cache, workspace, workspace_bytes, stream, true);
     if (rc) return rc;
     const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
     unsigned char* wsb = static_cast<unsigned char*>(workspace);
@@ -586,11 +586,56 @@ int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const
     a.v = static_cast<const __nv_bfloat16*>(v); a.g = g; a.beta = beta; a.cu = cu_seqlens;
     a.chunk_off = reinterpret_cast<const int32_t*>(wsb + w.chunk_off); a.n_seq = n_seq; a.H = H;
     a.scale = c->scale; a.ws = wsb + w.W; a.blk_bytes = cpr::tc::kBlockTrain;
-    a.off_hn = cpr::tc::kOffHn; a.o = static_cast<float*>(o);
+    a.off_hn = cpr::tc::kOffHn; a.o = static_cast<float*>(o); a.run = run;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cpr::ProfScope ps("cpr_reading_b", st);
     const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
+    return CPR_OK;
+}
+
+int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                          const void* k, const void* v, const float* g, const float* beta,
+                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                          const float* h0, void* o, float* final_state, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    return reading_b_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                          final_state, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int cpr_gdn_prefill_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
+                              const void* k, const void* v, const float* g, const float* beta,
+                              const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
+                              const float* h0, void* o, float* final_state, void* cache,
+                              float* run, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!cache) return fail(CPR_ERR_INVALID_ARG, "cache is NULL");
+    REQ_PTR(run);
+    return reading_b_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                          final_state, cache, run, workspace, workspace_bytes, stream);
+}
+
+int cpr_gdn_decode_step_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
+                                  const void* k_t, const void* v_t, const float* g_t,
+                                  const float* beta_t, int n_seq, int H, void* cache, float* run,
+                                  void* o_t, void* stream) {
+    if (c && c->operand_policy != CPR_POLICY_TC_BF16X3)
+        return fail(CPR_ERR_UNSUPPORTED, "reading B: tensor-core operand policy only");
+    // the CPR step keeps the cache (rows, commit) and moves the positions on
+    int rc = cpr_gdn_decode_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+    if (rc) return rc;
+    if (n_seq == 0) return CPR_OK;
+    REQ_PTR(run);
+    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+    cpr::rec::RbStepArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q_t); a.k = static_cast<const __nv_bfloat16*>(k_t);
+    a.v = static_cast<const __nv_bfloat16*>(v_t); a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
+    a.scale = c->scale; a.pos = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(cache) + cl.pos);
+    a.state_tiles = static_cast<const unsigned char*>(cache) + cl.state_tiles;
+    a.dvs = (int)(c->d_v / c->dv_splits); a.run = run; a.o = static_cast<float*>(o_t);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_reading_b_step", st);
+    const cudaError_t e = cpr::rb_step_launch(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B step launch");
     return CPR_OK;
 }
 

@@ -168,6 +168,43 @@ __global__ void __launch_bounds__(256) k_rb(RbArgs a) {
                           __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hn + 32768 + off)));
     }
     token_loop<D, __nv_bfloat16>(hr, s, a.q, a.k, a.v, a.g, a.beta, H, h, a.scale, t0, t1, a.o);
+    if (a.run && t1 == seq0 + T && t1 - t0 < kChunk) {  // a decode continues this partial chunk
+        float* run = a.run + ((size_t)b * H + h) * D * D;
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) run[(part * (D / 2) + i) * D + j] = hr[i];
+    }
+}
+
+// Reading B, one decode step per (sequence, head), after the CPR decode step of the same
+// tokens (which keeps the cache and commits a full chunk): at a chunk's first row the
+// running state restarts from hi + lo of the cache's chunk-start state tiles -- the bits
+// the reading-B prefill starts that chunk from -- otherwise it continues; one token of
+// the recurrence, o from it.
+__global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
+    constexpr int D = 128;
+    __shared__ RecSmem<D> s;
+    const int tid = threadIdx.x, j = tid % D, part = tid / D;
+    const int H = a.H, b = blockIdx.x / H, h = blockIdx.x % H;
+    const size_t sh = (size_t)b * H + h;
+    const int p = (a.pos[b] + kChunk - 1) % kChunk;   // this step's row in its chunk
+    float* run = a.run + sh * D * D;
+    float hr[D / 2];
+    if (p == 0) {
+        const unsigned char* ct = a.state_tiles + sh * 65536;
+        const int sp = j / a.dvs, jl = j - sp * a.dvs;
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) {
+            const uint32_t off = (uint32_t)sp * a.dvs * 256 + tc::mn_off(jl, part * (D / 2) + i, a.dvs);
+            hr[i] = __fadd_rn(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ct + off)),
+                              __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(ct + 32768 + off)));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) hr[i] = run[(part * (D / 2) + i) * D + j];
+    }
+    token_loop<D, __nv_bfloat16>(hr, s, a.q, a.k, a.v, a.g, a.beta, H, h, a.scale, b, b + 1, a.o);
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) run[(part * (D / 2) + i) * D + j] = hr[i];
 }
 
 template <int D, typename IO>
@@ -181,6 +218,12 @@ static cudaError_t launch(const RecArgs& a, cudaStream_t st) {
 
 cudaError_t rb_launch(const rec::RbArgs& a, int64_t cmax, cudaStream_t st) {
     if (cmax > 0 && a.H > 0) rec::k_rb<<<dim3((unsigned)cmax, (unsigned)a.H), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t rb_step_launch(const rec::RbStepArgs& a, cudaStream_t st) {
+    const int64_t grid = (int64_t)a.n_seq * a.H;
+    if (grid > 0) rec::k_rb_step<<<(unsigned)grid, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

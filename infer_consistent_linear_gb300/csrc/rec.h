@@ -40,6 +40,23 @@ struct RbArgs {               // reading B (d = 128, bf16 io)
     size_t blk_bytes;
     size_t off_hn;              // H_n hi/lo tiles within a block
     float* o;
+    float* run;                 // or null: the in-chunk state after a sequence's partial last chunk
+};
+
+struct RbStepArgs {           // reading B decode step (d = 128, bf16 io)
+    const __nv_bfloat16* q;   // [n_seq, H, d]
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    int n_seq;
+    int H;
+    float scale;
+    const int32_t* pos;                 // the cache's positions (already moved on by this step)
+    const unsigned char* state_tiles;   // the cache's chunk-start state tiles (64 KB per unit)
+    int dvs;                            // d_v columns per split of those tiles
+    float* run;                         // [n_seq, H, d, d] running in-chunk states
+    float* o;
 };
 
 }  // namespace rec
@@ -48,5 +65,6 @@ struct RbArgs {               // reading B (d = 128, bf16 io)
 cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st);
 // grid (chunk slots, H)
 cudaError_t rb_launch(const rec::RbArgs& a, int64_t cmax, cudaStream_t st);
+cudaError_t rb_step_launch(const rec::RbStepArgs& a, cudaStream_t st);
 
 }  // namespace cpr

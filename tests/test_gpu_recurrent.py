@@ -133,3 +133,36 @@ def test_reading_b_first_chunk_is_the_token_recurrence():
         assert_bitwise(f"first chunk of seq {b}", ob[sl], orr)
     torch.cuda.synchronize()
     assert cpr.get_device_error() == 0
+
+
+def test_reading_b_decode_equals_reading_b_prefill():
+    """Reading B end to end: a reading-B prefill with a decode cache, then reading-B decode
+    steps (CPR steps keep the cache and commit chunks; the running in-chunk state restarts
+    from the committed state's tiles at each chunk's first row) give the bits of a one-shot
+    reading-B forward over the full sequences, and the committed states are CPR's."""
+    pre, steps, H = [100, 64, 0, 37, 130], 70, 2
+    full = [L + steps for L in pre]
+    x = make_inputs(full, H, 128, 128, io_dtype=torch.bfloat16, seed=10, h0_std=0.1).to(DEV)
+    c = _tc()
+    o_full, _ = cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
+    cu = x.cu_seqlens.tolist()
+    sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(len(pre))]).to(DEV)
+    cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(pre), 0).tolist(), dtype=torch.int32, device=DEV)
+    o_pre, _, cache, run = cpr.cpr_gdn_prefill_reading_b(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel],
+                                                         cu_pre, h0=x.h0, contract=c)
+    assert_bitwise("prefill part", o_pre, o_full[sel])
+    for t in range(steps):
+        idx = torch.tensor([cu[b] + pre[b] + t for b in range(len(pre))], device=DEV)
+        ot = cpr.cpr_gdn_decode_step_reading_b(x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx], cache, run,
+                                               contract=c)
+        assert_bitwise(f"reading-B decode step {t}", ot, o_full[idx])
+        for b in range(len(pre)):
+            n_done = pre[b] + t + 1
+            if n_done % 64 == 0:
+                sl = slice(cu[b], cu[b] + n_done)
+                _, fin = cpr.cpr_gdn_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl],
+                                         torch.tensor([0, n_done], dtype=torch.int32, device=DEV),
+                                         h0=x.h0[b:b + 1], contract=c)
+                assert_bitwise(f"committed state seq {b} at {n_done}", cache.state()[b:b + 1], fin)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
