@@ -440,12 +440,14 @@ def load_traffic():
 
 
 def kernel_src_sha():
-    """Hash of the kernel sources the stored ncu traffic figures belong to."""
+    """Hash of the chunk-form kernels' sources (tc_*, simt_*, common.cuh), which the
+    stored ncu traffic figures belong to; the C-ABI, the token-recurrence and GEMM files
+    do not enter it."""
     import hashlib
     csrc = os.path.join(ROOT, "infer_consistent_linear_gb300", "csrc")
     h = hashlib.sha256()
     for s in sorted(os.listdir(csrc)):
-        if s.endswith((".cu", ".cuh")):
+        if s.endswith((".cu", ".cuh", ".h")) and s.startswith(("tc_", "simt_", "common")):
             with open(os.path.join(csrc, s), "rb") as f:
                 h.update(s.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
