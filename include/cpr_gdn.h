@@ -45,7 +45,9 @@
  *   - Every compute call is asynchronous on `stream` (a cudaStream_t passed
  *     as void*; NULL = legacy default stream).
  *   - Tensor pointers must be 16-byte aligned, except the per-token scalar
- *     tensors (g, beta, dg, dbeta) and cu_seqlens, which need 4 bytes
+ *     tensors (g, beta, dg, dbeta) and cu_seqlens, which need 4 bytes, and
+ *     the outputs written in whole 32-byte sectors, which need 32 bytes: dq
+ *     and dk under CPR_POLICY_TC_BF16X3, and Y of cpr_gemm_bf16
  *     (CPR_ERR_ALIGNMENT).  Token tensors may be NULL when n_tok == 0.
  *   - Host-side checks return an error code immediately and launch nothing.
  *     Checks that need device data (cu_seqlens validity, the digest stored in
@@ -68,7 +70,7 @@ extern "C" {
 #define CPR_OK                     0
 #define CPR_ERR_INVALID_ARG        1  /* null/negative/inconsistent argument  */
 #define CPR_ERR_UNSUPPORTED        2  /* valid contract this build cannot run */
-#define CPR_ERR_ALIGNMENT          3  /* pointer not 16-byte aligned          */
+#define CPR_ERR_ALIGNMENT          3  /* pointer not aligned as required      */
 #define CPR_ERR_CONTRACT_MISMATCH  4  /* digest != SHA-256(contract), or a
                                          decode cache made under another
                                          contract (device-side)              */
@@ -403,9 +405,10 @@ int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k
  * Y = X W for the projections that feed the CPR layer (page "IsoExec: 切换
  * SkyRL 中的训练器-推理不匹配": batch-invariant kernels for everything around
  * the layer, so a token's inputs do not change with its batch).  X bf16 [M, K],
- * W bf16 [K, N], Y fp32 [M, N], all row-major, device, 16-byte aligned.  K is
- * split into K / leaf_k contiguous leaves (leaf_k a multiple of 64; 1, 2 or 4
- * leaves); each leaf is accumulated in fp32 by tensor-core MMAs in ascending
+ * W bf16 [K, N], Y fp32 [M, N], all row-major, device, X and W 16-byte and
+ * Y 32-byte aligned.  K is split into K / leaf_k contiguous leaves (leaf_k a
+ * multiple of 64; 1, 2 or 4 leaves); each leaf is accumulated in fp32 by
+ * tensor-core MMAs in ascending
  * k and the leaves are added in the fixed tree (P0 + P1) + (P2 + P3).  A row's
  * result depends only on that row of X, on W and on leaf_k: it is the same for
  * any M and any batch the row sits in.  N must be a multiple of 128.  Errors:

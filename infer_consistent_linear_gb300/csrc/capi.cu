@@ -217,6 +217,12 @@ int cuda_fail(cudaError_t e, const char* what) {
         if (!(p)) return fail(CPR_ERR_INVALID_ARG, "%s is NULL", #p);          \
         if (reinterpret_cast<uintptr_t>(p) & 3u) return fail(CPR_ERR_ALIGNMENT, "%s not 4-byte aligned", #p); \
     } while (0)
+// Outputs written with whole 32-byte sector stores.
+#define REQ_PTR32(p)                                                           \
+    do {                                                                       \
+        if (reinterpret_cast<uintptr_t>(p) & 31u)                              \
+            return fail(CPR_ERR_ALIGNMENT, "%s not 32-byte aligned", #p);      \
+    } while (0)
 #define OPT_PTR(p)                                                             \
     do {                                                                       \
         if ((p) && !aligned16(p)) return fail(CPR_ERR_ALIGNMENT, "%s not 16-byte aligned", #p); \
@@ -466,6 +472,9 @@ static int backward_impl(const cpr_contract* c, const uint8_t* digest, const voi
     if (n_tok > 0) {
         REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta);
         REQ_PTR(dO); REQ_PTR(dq); REQ_PTR(dk); REQ_PTR(dv); REQ_PTR4(dg); REQ_PTR4(dbeta);
+        if (c->operand_policy == CPR_POLICY_TC_BF16X3) {
+            REQ_PTR32(dq); REQ_PTR32(dk);
+        }
     }
     OPT_PTR(h0); OPT_PTR(dHT);
     const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
@@ -706,7 +715,7 @@ int cpr_gemm_bf16(const void* X, const void* W, float* Y, int M, int N, int K, i
         return fail(CPR_ERR_INVALID_ARG, "gemm: K / leaf_k must be 1, 2 or 4");
     if ((int64_t)M * K > INT32_MAX * 4ll) return fail(CPR_ERR_INVALID_ARG, "gemm: M * K too large");
     if (M > 0) {
-        REQ_PTR(X); REQ_PTR(W); REQ_PTR(Y);
+        REQ_PTR(X); REQ_PTR(W); REQ_PTR(Y); REQ_PTR32(Y);
     }
     uint32_t* err = device_error_ptr();
     if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");

@@ -165,3 +165,20 @@ def test_training_forward_and_saved_backward_need_tc_contract(lib):
     rc = lib.cpr_gdn_fwd_train(ctypes.byref(t), dt, *p[:6], 1, 64, 1, None, p[6], None, p[7],
                                small, None)
     assert rc == 7                                          # a forward-sized workspace is too small
+
+
+def test_sector_store_outputs_need_32_byte_alignment(lib):
+    """dq, dk under the tensor-core policy and the GEMM's Y are written in whole 32-byte
+    sectors: a pointer that is 16- but not 32-byte aligned is refused on the host."""
+    t = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=2)
+    dt = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(t))
+    p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    for which in (0, 1):                                    # dq, then dk
+        grads = [ctypes.c_void_p(0x200000 * (i + 1)) for i in range(6)]
+        grads[which] = ctypes.c_void_p(grads[which].value + 16)
+        rc = lib.cpr_gdn_bwd_saved(ctypes.byref(t), dt, *p[:6], 1, 64, 1, None, p[6], None, *grads, p[7],
+                                   1 << 40, None)
+        assert rc == 3 and "32-byte" in lib.cpr_last_error().decode()
+    x, w = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    assert lib.cpr_gemm_bf16(x, w, ctypes.c_void_p(0x30010), 8, 128, 64, 64, None) == 3
+    assert "32-byte" in lib.cpr_last_error().decode()
