@@ -749,11 +749,12 @@ class ProjectionGemm:
     """The projection in front of the layer on the Prefill workload's tokens: X [16384,
     2048] bf16 times W [2048, 16 x 128] bf16, K in 4 fixed leaves of 512."""
 
-    def __init__(self, dev, d_model=2048, leaf_k=512):
+    def __init__(self, dev, d_model=2048, leaf_k=512, M=None):
         import infer_consistent_linear_gb300 as cpr
         self.cpr = cpr
         w = WORKLOADS["prefill"]
-        self.M, self.K, self.N, self.leaf_k = sum(workload_lens("prefill")), d_model, w["H"] * w["d"], leaf_k
+        self.M = M if M is not None else sum(workload_lens("prefill"))
+        self.K, self.N, self.leaf_k = d_model, w["H"] * w["d"], leaf_k
         g = torch.Generator().manual_seed(0)
         self.x = torch.randn(self.M, self.K, generator=g).to(torch.bfloat16).to(dev)
         self.w = (torch.randn(self.K, self.N, generator=g) / self.K ** 0.5).to(torch.bfloat16).to(dev)
@@ -764,13 +765,15 @@ class ProjectionGemm:
         self.cpr.cpr_gemm(self.x, self.w, self.leaf_k, out=self.y)
 
 
-def projection_gemm(dev, world, pk):
-    pg = ProjectionGemm(dev)
-    ms, _ = time_device(pg, 10, 3, world, profile=False)
+def projection_gemm(dev, world, pk, M=None, steps=10, warmup=3):
+    pg = ProjectionGemm(dev, M=M)
+    ms, _ = time_device(pg, steps, warmup, world, profile=False)
     flops = 2.0 * pg.M * pg.N * pg.K
     tf = flops / (ms * 1e-3) / 1e12
-    sub = pg.cpr.cpr_gemm(pg.x[1000:1777].contiguous(), pg.w, pg.leaf_k)
-    inv = bool(torch.equal(sub.view(torch.int32), pg.y[1000:1777].view(torch.int32)))
+    lo = min(1000, pg.M // 2)
+    hi = min(pg.M, lo + 777)
+    sub = pg.cpr.cpr_gemm(pg.x[lo:hi].contiguous(), pg.w, pg.leaf_k)
+    inv = bool(torch.equal(sub.view(torch.int32), pg.y[lo:hi].view(torch.int32)))
     res = {"shape": f"X [{pg.M}, {pg.K}] x W [{pg.K}, {pg.N}], bf16 in, fp32 out, {pg.K // pg.leaf_k} "
                     f"leaves of {pg.leaf_k}",
            "ms": round(ms, 4), "roofline": {"bound": "tensor", "achieved": round(tf, 1),
@@ -881,6 +884,9 @@ def main():
     ap.add_argument("--n-seq", type=int, default=None,
                     help="run only the first n sequences of the workload (a smaller case for "
                          "profiler captures; the line then does not describe the named workload)")
+    ap.add_argument("--gemm-only", type=int, default=None, metavar="M",
+                    help="time only the projection GEMM, on M rows of its workload, and print its "
+                         "object (a case for profiler captures; no bench line)")
     args = ap.parse_args()
     global N_SEQ_OVERRIDE
     N_SEQ_OVERRIDE = args.n_seq
@@ -895,6 +901,10 @@ def main():
     _build.build()
     cpr.load_library()
     pk = peaks()
+    if args.gemm_only is not None:
+        print(json.dumps(projection_gemm(dev, world, pk, M=args.gemm_only, steps=max(args.steps, 1),
+                                         warmup=max(args.warmup, 1))), flush=True)
+        return
     name = args.workload
     K, W = args.steps, max(args.warmup, 0)
     n_dec = K + W if WORKLOADS[name]["op"] == "decode" else 0

@@ -360,9 +360,23 @@ done:
     if (warp == 0 && held) tmem_dealloc(tmem, 256);
 }
 
+// OR over the predicates of `count` threads meeting at hardware barrier `id` (a
+// __syncthreads_or for a subset of the CTA's warps).
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
 // ---- state pass: one CTA per (sequence, head, d_v split), chunks in order -----------
-// 256 threads: warp w reads TMEM lane quarter w % 4; the two warps of a quarter
-// take one half of the DVS columns each.  Per chunk the dependent chain is
+// 288 threads: warps 0..7 do the operand and epilogue work (warp w reads TMEM lane
+// quarter w % 4; the two warps of a quarter take one half of the DVS columns each);
+// warp 8 only issues the MMA groups, so that issuing (about 56 cycles an instruction
+// at N = 64) and epilogue work do not queue behind each other on one warp.  Barriers:
+// three CTA-wide ones per chunk (chunk start, Delta tiles written, and the next chunk's
+// start), the others only among warps 0..7 (hardware barrier 1).  Per chunk the dependent chain is
 // A4 MMA -> Delta epilogue -> H' MMA -> H' epilogue; the output rows of chunk n
 // (P Delta and the Q H rows) are read while chunk n + 1's A4 MMA runs, from
 // double-buffered accumulators.
@@ -388,8 +402,10 @@ struct StateSmem {
     static constexpr uint32_t TmemCols = 5 * DVS > 256 ? 512 : 256;
 };
 
+constexpr int kStateThreads = 288, kStateIssuer = 256;
+
 template <int DVS>
-__global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
+__global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     using L = StateSmem<DVS>;
     constexpr int NSPLIT = D / DVS;
     constexpr int HALF = DVS / 2;  // columns per thread
@@ -414,7 +430,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
     const int b = blockIdx.x / (NSPLIT * H);
     const int j0 = sp * DVS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const bool epi = warp < 8;                  // warp 8 issues the MMAs
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int cb = half * HALF;                 // this thread's first column (within the split)
     const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
     const int nch = a.chunk_off[b + 1] - a.chunk_off[b];
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         for (int i = 0; i < 5; ++i) mbar_init(bar_mma + i, 1);
         mbar_init_fence();
     }
-    for (int i = tid; i < 1024; i += 256)  // rows 64..127 of the W'_lo operand stay zero
+    for (int i = tid; i < 1024; i += kStateThreads)  // rows 64..127 of the W'_lo operand stay zero
         reinterpret_cast<uint4*>(sm + L::A4lo + 16384)[i] = make_uint4(0u, 0u, 0u, 0u);
     // state row d = 32 quarter + lane, columns j0 + cb .. + HALF, fp32 in registers
     float Hreg[HALF];
@@ -434,7 +451,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
 #pragma unroll
     for (int j4 = 0; j4 < HALF / 4; ++j4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.h0) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + cb + 4 * j4);
+        if (a.h0 && epi) x = *reinterpret_cast<const float4*>(a.h0 + (sh * D + d) * D + j0 + cb + 4 * j4);
         Hreg[4 * j4] = x.x; Hreg[4 * j4 + 1] = x.y; Hreg[4 * j4 + 2] = x.z; Hreg[4 * j4 + 3] = x.w;
     }
     const int coff = a.chunk_off[b];
@@ -465,8 +482,10 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
             *reinterpret_cast<float4*>(dst + (size_t)d * D + j0 + cb + 4 * j4) =
                 make_float4(Hreg[4 * j4], Hreg[4 * j4 + 1], Hreg[4 * j4 + 2], Hreg[4 * j4 + 3]);
     };
-    put_h(0);
-    if (nch == 0 && cstate) put_state(cstate);
+    if (epi) {
+        put_h(0);
+        if (nch == 0 && cstate) put_state(cstate);
+    }
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
@@ -564,92 +583,108 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         pendA = pendB = pendP = true;
     }
 
+    bool carry = true;   // the previous H' epilogue's consensus among warps 0..7
     for (int n = 0; n < nch; ++n) {
         const int nrows = min(C, T - n * C);
         const int Lr = nrows - 1;
         const bool last = (n == nch - 1);
+        // [all] the A4 tiles have landed; the H tiles put_h wrote are visible
         bool ok = mbar_wait(bar_ldA, ph_ldA, a.err);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
+        fence_before();
+        if (__syncthreads_or(!(ok && carry))) { failed = true; break; }
+        fence_after();
         ph_ldA ^= 1u;
         pendA = false;
-        if (tid == 0) {
+        bool okg = true;   // this phase's consensus among warps 0..7
+        float GL = 0.f;    // G_L, read before issue_A(n + 1) replaces gam
+        if (tid == kStateIssuer) {
             mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hhi, false);
             mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hlo, true);
             mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4lo, sm + L::Hhi, true);
             mma_commit(bar_mma);
         }
         mma_out = true;
-        const bool okpd = n == 0 || o_epilogue(n - 1);
-        if (tid < C) {
-            Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
-            dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
-        }
-        const float GL = simt::gate(gam[Lr]);
-        ok = mbar_wait(bar_ldB, ph_ldB, a.err);
+        ok = mbar_wait(bar_ldB, ph_ldB, a.err);   // K and U (every thread tracks the phase)
         if (ok) {
             ph_ldB ^= 1u;
             pendB = false;
         }
-        if (__syncthreads_or(!(ok && okpd))) { failed = true; break; }
-        ok = mbar_wait(bar_mma, ph_mma, a.err);
-        fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_mma ^= 1u;
-        mma_out = false;
-        if (tid == 0 && n + 1 < nch) {  // the A4 operand tiles and gam of chunk n are consumed
-            fence_async_smem();
-            issue_A(n + 1);
-        }
-        pendA = (n + 1 < nch);
-        if (quarter < 2) {
-            // rows 0..63: Delta = U - W'H, columns cb .. cb + HALF
-            const int r = d;
-            float v[32];
-            tmem_ld32(taddr_of(acc4(n), warp, cb), v);
-            const bool in = r < nrows;
-            float* cd = (a.cache && last && nrows < C && in)
-                            ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0 + cb
-                            : nullptr;
-            const float dr = dec[r];
+        if (epi) {
+            const bool okpd = n == 0 || o_epilogue(n - 1);
+            if (tid < C) {
+                Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
+                dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
+            }
+            GL = simt::gate(gam[Lr]);
+            okg = !bar_or(1, 256, !(ok && okpd));
+            if (okg) {
+                ok = mbar_wait(bar_mma, ph_mma, a.err);
+                fence_after();
+                okg = !bar_or(1, 256, !ok);
+            }
+            if (okg) {
+                ph_mma ^= 1u;
+                mma_out = false;
+                if (tid == 0 && n + 1 < nch) {  // the A4 operand tiles and gam of chunk n are consumed
+                    fence_async_smem();
+                    issue_A(n + 1);
+                }
+                pendA = (n + 1 < nch);
+                if (quarter < 2) {
+                    // rows 0..63: Delta = U - W'H, columns cb .. cb + HALF
+                    const int r = d;
+                    float v[32];
+                    tmem_ld32(taddr_of(acc4(n), warp, cb), v);
+                    const bool in = r < nrows;
+                    float* cd = (a.cache && last && nrows < C && in)
+                                    ? reinterpret_cast<float*>(a.cache + a.co.delta_rows) + (sh * C + r) * D + j0 + cb
+                                    : nullptr;
+                    const float dr = dec[r];
 #pragma unroll
-            for (int j8 = 0; j8 < HALF / 8; ++j8) {
-                float x[8], y[8];
-                const int jj = cb + j8 * 8;
-                const float4 u0 = reinterpret_cast<const float4*>(sU)[(jj / 4) * 64 + r];
-                const float4 u1 = reinterpret_cast<const float4*>(sU)[(jj / 4 + 1) * 64 + r];
-                const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    for (int j8 = 0; j8 < HALF / 8; ++j8) {
+                        float x[8], y[8];
+                        const int jj = cb + j8 * 8;
+                        const float4 u0 = reinterpret_cast<const float4*>(sU)[(jj / 4) * 64 + r];
+                        const float4 u1 = reinterpret_cast<const float4*>(sU)[(jj / 4 + 1) * 64 + r];
+                        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
-                    y[e] = __fmul_rn(dr, x[e]);
+                        for (int e = 0; e < 8; ++e) {
+                            x[e] = in ? __fsub_rn(uu[e], v[j8 * 8 + e]) : 0.f;
+                            y[e] = __fmul_rn(dr, x[e]);
+                        }
+                        uint4 hi, lo;
+                        split8(x, hi, lo);
+                        *reinterpret_cast<uint4*>(sm + L::Dhi + mn_off(jj, r, DVS)) = hi;
+                        *reinterpret_cast<uint4*>(sm + L::Dlo + mn_off(jj, r, DVS)) = lo;
+                        if (a.train) {  // Delta rows for the backward, K-major (s, j)
+                            unsigned char* g = blk_of(n) + kOffDl + cm_off(r, j0 + jj, D);
+                            *reinterpret_cast<uint4*>(g) = hi;
+                            *reinterpret_cast<uint4*>(g + 16384) = lo;
+                        }
+                        store8_split(sm + L::Bhi, sm + L::Blo, mn_off(jj, r, DVS), y);
+                        if (cd) {
+                            *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
+                            *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                        }
+                    }
+                } else {
+                    if (n > 0) o_copy(n - 1);   // staged by o_epilogue(n - 1), barriers ago
+                    qh_to_sq(n);
                 }
-                uint4 hi, lo;
-                split8(x, hi, lo);
-                *reinterpret_cast<uint4*>(sm + L::Dhi + mn_off(jj, r, DVS)) = hi;
-                *reinterpret_cast<uint4*>(sm + L::Dlo + mn_off(jj, r, DVS)) = lo;
-                if (a.train) {  // Delta rows for the backward, K-major (s, j)
-                    unsigned char* g = blk_of(n) + kOffDl + cm_off(r, j0 + jj, D);
-                    *reinterpret_cast<uint4*>(g) = hi;
-                    *reinterpret_cast<uint4*>(g + 16384) = lo;
-                }
-                store8_split(sm + L::Bhi, sm + L::Blo, mn_off(jj, r, DVS), y);
-                if (cd) {
-                    *reinterpret_cast<float4*>(cd + j8 * 8) = make_float4(x[0], x[1], x[2], x[3]);
-                    *reinterpret_cast<float4*>(cd + j8 * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
-                }
+                if (cstate && last && nrows < C) put_state(cstate);
             }
         } else {
-            if (n > 0) o_copy(n - 1);   // staged by o_epilogue(n - 1), barriers ago
-            qh_to_sq(n);
+            okg = ok;
         }
-        if (cstate && last && nrows < C) put_state(cstate);
+        // [all] the Delta tiles are written and the P tiles have landed
         fence_async_smem();
-        tc_sync();
-        ok = mbar_wait(bar_ldP, ph_ldP, a.err);
+        ok = okg && mbar_wait(bar_ldP, ph_ldP, a.err);
+        fence_before();
         if (__syncthreads_or(!ok)) { failed = true; break; }
+        fence_after();
         ph_ldP ^= 1u;
         pendP = false;
-        if (tid == 0) {
+        if (tid == kStateIssuer) {
             mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Bhi, false);   // H' part
             mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Blo, true);
             mma_commit(bar_mma);
@@ -660,35 +695,39 @@ __global__ void __launch_bounds__(256, 1) k_tc_state(TcArgs a) {
         }
         mma_out = true;
         pd_out = true;
-        ok = mbar_wait(bar_mma, ph_mma, a.err);
-        fence_after();
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        ph_mma ^= 1u;
-        mma_out = false;
-        if (tid == 0 && n + 1 < nch) {  // K and U of chunk n are consumed
-            fence_async_smem();
-            issue_B(n + 1);
-        }
-        pendB = (n + 1 < nch);
-        {
-            // H' = G_L H + K^T (dec . Delta): row d, columns cb .. cb + HALF
-            float v[32];
-            tmem_ld32(taddr_of(acc6, warp, cb), v);
+        carry = true;
+        if (epi) {
+            ok = mbar_wait(bar_mma, ph_mma, a.err);
+            fence_after();
+            carry = !bar_or(1, 256, !ok);
+            if (carry) {
+                ph_mma ^= 1u;
+                mma_out = false;
+                if (tid == 0 && n + 1 < nch) {  // K and U of chunk n are consumed
+                    fence_async_smem();
+                    issue_B(n + 1);
+                }
+                pendB = (n + 1 < nch);
+                {
+                    // H' = G_L H + K^T (dec . Delta): row d, columns cb .. cb + HALF
+                    float v[32];
+                    tmem_ld32(taddr_of(acc6, warp, cb), v);
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) Hreg[j] = __fadd_rn(__fmul_rn(GL, Hreg[j]), v[j]);
-            put_h(n + 1);
-            if (cstate && last && nrows == C) put_state(cstate);
+                    for (int j = 0; j < HALF; ++j) Hreg[j] = __fadd_rn(__fmul_rn(GL, Hreg[j]), v[j]);
+                    put_h(n + 1);
+                    if (cstate && last && nrows == C) put_state(cstate);
+                }
+            }
         }
         fence_async_smem();
-        tc_sync();
     }
     if (!failed && nch > 0) {   // (failed is the same in every thread here)
-        const bool okl = o_epilogue(nch - 1);
-        if (__syncthreads_or(!okl)) failed = true;
-        else if (quarter >= 2) o_copy(nch - 1);
+        const bool okl = !epi || o_epilogue(nch - 1);
+        if (__syncthreads_or(!(okl && carry))) failed = true;
+        else if (epi && quarter >= 2) o_copy(nch - 1);
     }
-    if (!failed && a.final_state) put_state(a.final_state + sh * D * D);
-    if (failed) {
+    if (!failed && a.final_state && epi) put_state(a.final_state + sh * D * D);
+    if (failed && epi) {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
         if (pendA) mbar_wait(bar_ldA, ph_ldA, a.err);
         if (pendB) mbar_wait(bar_ldB, ph_ldB, a.err);

@@ -23,7 +23,7 @@ cudaError_t state(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
     const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
     if (grid > 0) {
         ProfScope ps("cpr_tc_state", st);
-        kern<<<(unsigned)grid, 256, sm, st>>>(a);
+        kern<<<(unsigned)grid, tc::kStateThreads, sm, st>>>(a);
     }
     return cudaGetLastError();
 }
