@@ -188,6 +188,25 @@ def tc_kernel_flops_per_chunk(name, d, Cc=C):
     return None
 
 
+def tc_kernel_bytes(name, lens, H, d, io_bytes=2, out_bytes=4):
+    """The method's algorithmic bytes (inputs read, results written) each tensor-core
+    kernel is charged with, so that the kernels of a step add up to the path's figure:
+    prep reads q, k, v, g, beta; the state pass writes o and the final states; the
+    reverse state pass reads dO and writes dh0; the gradient kernel reads q, k, v, g,
+    beta again and writes dq, dk, dv, dg, dbeta.  Workspace tiles are not algorithmic."""
+    ht = sum(lens) * H
+    states = len(lens) * H * d * d * 4
+    if name == "cpr_tc_prep":
+        return ht * (3 * d * io_bytes + 8)
+    if name == "cpr_tc_state":
+        return ht * d * out_bytes + states
+    if name == "cpr_tc_state_bwd":
+        return ht * d * 4 + states
+    if name == "cpr_tc_grad":
+        return ht * (3 * d * io_bytes + 8 + 3 * d * out_bytes + 8)
+    return None
+
+
 def chunk_count(lens):
     return sum((L + C - 1) // C for L in lens)
 
@@ -466,12 +485,23 @@ def roofline_for(step, prof, pk):
         traffic = tr.get("bytes_per_launch")
     tfl = tc_kernel_flops_per_chunk(name, step.d)
     if tfl is not None:
+        # the kernel's own roofline: the slower of its algorithmic FLOPs at the bf16 peak
+        # and its algorithmic bytes at the copy bandwidth
         flops = tfl * units
-        ach = flops / avg_s / 1e12
-        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
-                "avg_launch_us": round(avg_s * 1e6, 2), "algo_flops_per_launch": flops,
-                "peak_source": "measured bf16 dense (burst)"}
+        byt = tc_kernel_bytes(name, step.lens, step.H, step.d)
+        t_f = flops / (pk["bf16_tflops"] * 1e12)
+        t_b = byt / (pk["hbm_gbs"] * 1e9)
+        base = {"kernel": name, "traffic": traffic, "avg_launch_us": round(avg_s * 1e6, 2),
+                "algo_flops_per_launch": flops, "algo_bytes_per_launch": byt}
+        if t_f >= t_b:
+            ach = flops / avg_s / 1e12
+            return {**base, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                    "peak_source": "measured bf16 dense (burst)"}
+        ach = byt / avg_s / 1e9
+        return {**base, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": "measured copy bandwidth",
+                "tensor_frac": round(flops / avg_s / 1e12 / pk["bf16_tflops"], 4)}
     if name in ("cpr_decode", "cpr_tc_decode"):
         byt = DECODE_ALGO_BYTES_PER_SEQ_HEAD * units
         ach = byt / avg_s / 1e9
@@ -884,6 +914,8 @@ def main():
     ap.add_argument("--n-seq", type=int, default=None,
                     help="run only the first n sequences of the workload (a smaller case for "
                          "profiler captures; the line then does not describe the named workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="leave out the oracle's timed CPU sample (for profiler runs)")
     ap.add_argument("--gemm-only", type=int, default=None, metavar="M",
                     help="time only the projection GEMM, on M rows of its workload, and print its "
                          "object (a case for profiler captures; no bench line)")
@@ -946,7 +978,7 @@ def main():
             line["context_parallel"] = context_parallel(dev, world, ms)
             line["projection_gemm"] = projection_gemm(dev, world, pk)
             line["reading_b"] = reading_b(dev, world, ms)
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         u, dt, desc, cores = cpu_sample(name)
         cv = round(dt * 1e6, 3) if WORKLOADS[name]["op"] == "decode" else round(u / dt, 1)
         line["cpu_baseline"] = {"value": cv, "unit": unit, "cores": cores, "kind": "oracle",
