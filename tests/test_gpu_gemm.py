@@ -57,3 +57,18 @@ def test_gemm_rejects_bad_shapes():
     x2, w2 = _inputs(8, 128, 96, 5)
     with pytest.raises(cpr.CprError):
         cpr.cpr_gemm(x2.to(DEV), w2.to(DEV), 128)    # N not a multiple of 128
+
+
+def test_gemm_many_tiles_per_cta_sampled_rows():
+    """More 128 x 256 output tiles than SMs, so every persistent CTA walks several tiles
+    (and the TMEM hand-off between a tile's epilogue and the next tile's MMAs repeats):
+    sampled rows against the oracle, and a ragged last row tile."""
+    m, k, n = 40000 + 37, 512, 2048
+    x, w = _inputs(m, k, n, 6)
+    y = cpr.cpr_gemm(x.to(DEV), w.to(DEV), 128).cpu()
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    rows = torch.cat([torch.arange(0, 8), torch.randint(8, m - 8, (56,), generator=torch.Generator().manual_seed(7)),
+                      torch.arange(m - 8, m)])
+    ref = oracle.gemm(x[rows].float().numpy(), w.float().numpy())
+    assert_close("Y sampled rows", y[rows], ref, TOL_F32)
