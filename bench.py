@@ -826,27 +826,31 @@ class ReadingB:
         self.lens = workload_lens("prefill")
         H, d = WORKLOADS["prefill"]["H"], WORKLOADS["prefill"]["d"]
         self.H = H
-        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
+                                      intra_order=cpr.CPR_ORDER_TOKENREC_V1)
         self.x_host = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0)
         self.xd = self.x_host.to(dev)
         n_tok, n_seq = sum(self.lens), len(self.lens)
-        self.ws = torch.empty(cpr.workspace_bytes(self.c, cpr.CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
+        self.ws = torch.empty(cpr.workspace_bytes(self.c, cpr.CPR_OP_FWD, n_seq, n_tok, H), dtype=torch.uint8,
                               device=dev)
         torch.cuda.synchronize()
 
     def run(self):
         x = self.xd
-        self.o, _ = self.cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c,
-                                                   workspace=self.ws)
+        self.o, _ = self.cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c,
+                                         workspace=self.ws)
 
 
 def reading_b(dev, world, reading_a_ms):
-    """Speed of reading B against reading A on the same workload, and how far apart the two
-    readings' outputs are (both are checked against the oracle in the GPU tests)."""
+    """Speed of reading B (contract intra_order TOKENREC_V1) against reading A on the same
+    workload, and how far apart the two readings' outputs are (both are checked against the
+    oracle in the GPU tests)."""
     rb = ReadingB(dev)
     ms, _ = time_device(rb, 5, 2, world, profile=False)
     x = rb.xd
-    oa, _ = rb.cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=rb.c, want_final=False)
+    ca = rb.cpr.Contract.from_buffer_copy(rb.c)      # the same contract under reading A
+    ca.intra_order = rb.cpr.CPR_ORDER_ROWSEQ_V1
+    oa, _ = rb.cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=ca, want_final=False)
     ob = rb.o
     diff = float((ob - oa).abs().max()) / float(oa.pow(2).mean().sqrt())
     res = {"workload": WORKLOADS["prefill"]["desc"], "ms_per_step": round(ms, 4),

@@ -108,6 +108,17 @@ extern "C" {
  * an fma chain in ascending index order from +0; triangular solve by rows
  * with the inner sums ascending.                                           */
 #define CPR_ORDER_ROWSEQ_V1 1u
+/* TOKENREC_V1 (reading B of the pages' CPR wording): chunk-boundary states as
+ * ROWSEQ_V1 computes them; every output of a chunk comes from the plain token
+ * recurrence (H = a H + k u^T, u = b (v - a H^T k), o = H^T (scale q); fp32
+ * fma chains in ascending row order per half of the rows, halves added in
+ * order) started from hi + lo of the chunk's boundary-state operand tiles.
+ * TC_BF16X3 only; forward, prefill and decode (no training ops).  Its decode
+ * cache adds the running in-chunk state (cpr_cache_layout.run).  Page "IsoExec:
+ * 切换 SkyRL 中的训练器-推理不匹配", section "Chunkwise-Parallel Recurrent (CPR)
+ * Gated DeltaNet": the recurrence is primary and the state is resynchronised
+ * every C tokens. */
+#define CPR_ORDER_TOKENREC_V1 2u
 
 /* state_schedule: how chunk states are produced.
  * SEQ_CHUNKS: H_{n+1} = f(H_n, chunk n) strictly in chunk order; d_v may be
@@ -192,6 +203,8 @@ typedef struct cpr_cache_layout {
     size_t state_tiles; /* bf16   [n_seq, H] x 64 KB: H_n as hi/lo tensor-core operand
                            tiles (tensor-core contracts; the fp32 copy stays authoritative) */
     size_t delta_tiles; /* bf16   [n_seq, H] x 32 KB: the Delta rows as hi/lo operand tiles */
+    size_t run;         /* fp32   [n_seq, H, d_k, d_v] running in-chunk state (TOKENREC_V1
+                           contracts; 0 and absent otherwise)                     */
 } cpr_cache_layout;
 
 int cpr_decode_cache_layout(const cpr_contract* c, int n_seq, int H, cpr_cache_layout* out);
@@ -201,7 +214,11 @@ int cpr_decode_cache_bytes(const cpr_contract* c, int n_seq, int H, size_t* byte
 
 /* Trainer forward (case trainer_fwd).  h0 and final_state may be NULL (h0 =
  * zeros; final state not written).  o is required.  workspace: at least
- * cpr_gdn_workspace_size(c, CPR_OP_FWD, ...) bytes, 256-byte aligned. */
+ * cpr_gdn_workspace_size(c, CPR_OP_FWD, ...) bytes, 256-byte aligned.
+ * Under intra_order TOKENREC_V1 (reading B) the chunk-form forward keeps every
+ * chunk's boundary state in the workspace and each chunk's o is then the
+ * token recurrence from it (chunks independent); the final state is the chunk
+ * form's. */
 int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32],
                 const void* q, const void* k, const void* v, const float* g, const float* beta,
                 const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
@@ -214,7 +231,9 @@ int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32],
  * sequence's last chunk and that chunk's rows), so decoding continues exactly
  * where the prefill stopped.  Every sequence starts on a chunk boundary (h0
  * is the state at that boundary); a caller that continues a sequence from a
- * cache whose position is not 0 must decode up to the boundary first. */
+ * cache whose position is not 0 must decode up to the boundary first.  Under
+ * TOKENREC_V1 the cache also receives the in-chunk state after each
+ * sequence's partial last chunk (cpr_cache_layout.run). */
 int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32],
                     const void* q, const void* k, const void* v, const float* g,
                     const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
@@ -228,7 +247,11 @@ int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32],
  * chunk-boundary state equal a one-shot prefill's bits.  When a chunk fills,
  * the step commits H_{n+1} into the cache (the resynchronisation every C
  * tokens).  The cache's stored digest is checked on the device; on mismatch
- * nothing is written and CPR_ERR_CONTRACT_MISMATCH is recorded. */
+ * nothing is written and CPR_ERR_CONTRACT_MISMATCH is recorded.  Under
+ * TOKENREC_V1 the same step keeps the cache, then one token of the recurrence
+ * advances the running in-chunk state (restarted at a chunk's first row from
+ * hi + lo of the cache's chunk-start state tiles) and gives o_t: bit-identical
+ * to cpr_gdn_fwd over the same tokens under that contract. */
 int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32],
                         const void* q_t, const void* k_t, const void* v_t, const float* g_t,
                         const float* beta_t, int n_seq, int H, void* cache, void* o_t,
@@ -254,7 +277,8 @@ int cpr_gdn_bwd(const cpr_contract* c, const uint8_t digest[32],
  * DeltaNet", "Trainer Fwd+Bwd").  workspace: cpr_gdn_workspace_size(c,
  * CPR_OP_BWD, ...) bytes, 256-byte aligned, owned by the caller until the
  * matching cpr_gdn_bwd_saved has run.  CPR_POLICY_TC_BF16X3 contracts only
- * (CPR_ERR_UNSUPPORTED otherwise). */
+ * (CPR_ERR_UNSUPPORTED otherwise).  The training ops (this one, cpr_gdn_bwd,
+ * cpr_gdn_bwd_saved) refuse intra_order TOKENREC_V1 with CPR_ERR_UNSUPPORTED. */
 int cpr_gdn_fwd_train(const cpr_contract* c, const uint8_t digest[32],
                       const void* q, const void* k, const void* v, const float* g,
                       const float* beta, const int32_t* cu_seqlens, int n_seq, int64_t n_tok,
@@ -353,40 +377,6 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed);
  * beta 4-byte); layouts as cpr_gdn_fwd; o is fp32.  Errors: CPR_ERR_INVALID_ARG,
  * CPR_ERR_ALIGNMENT, CPR_ERR_UNSUPPORTED (d_k != d_v or d not 64/128), and
  * CPR_ERR_BAD_SEQLENS on the device word for a sequence outside [0, n_tok]. */
-
-/* Reading B of CPR (the pages' literal wording: within a chunk, the token
- * recurrence from the resynchronised boundary state), tensor-core contracts
- * only: the training forward of cpr_gdn_fwd_train (same arguments, same
- * CPR_OP_BWD-sized workspace, the same final state), then every chunk's o
- * recomputed by the token recurrence above, started at the chunk form's
- * boundary state H_n as the hi + lo operand tiles the forward leaves in the
- * workspace -- the bits a decode cache's state tiles hold for that chunk.  o
- * holds reading B's outputs on return; chunks are independent (parallel). */
-int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
-                          const void* k, const void* v, const float* g, const float* beta,
-                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
-                          const float* h0, void* o, float* final_state, void* workspace,
-                          size_t workspace_bytes, void* stream);
-
-/* Reading B with a decode cache: cpr_gdn_fwd_reading_b plus the decode cache of
- * cpr_gdn_prefill (same cache layout, digest and CPR commits), and `run`, a
- * caller-owned fp32 [n_seq, H, d_k, d_v] buffer that receives each sequence's
- * in-chunk state after a partial last chunk. */
-int cpr_gdn_prefill_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
-                              const void* k, const void* v, const float* g, const float* beta,
-                              const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
-                              const float* h0, void* o, float* final_state, void* cache,
-                              float* run, void* workspace, size_t workspace_bytes, void* stream);
-
-/* One reading-B decode step: cpr_gdn_decode_step on the same cache (its rows,
- * positions and chunk commits are unchanged), then one token of the recurrence
- * on `run`, restarted from hi + lo of the cache's chunk-start state tiles at a
- * chunk's first row.  o_t holds reading B's output.  Bit-identical to
- * cpr_gdn_fwd_reading_b over the same tokens. */
-int cpr_gdn_decode_step_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
-                                  const void* k_t, const void* v_t, const float* g_t,
-                                  const float* beta_t, int n_seq, int H, void* cache, float* run,
-                                  void* o_t, void* stream);
 
 /* Token recurrence over whole sequences ("recurrent everywhere"): o for every
  * token and, if final_state is not NULL, the final state.  h0 may be NULL. */

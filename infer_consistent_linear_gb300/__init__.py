@@ -32,6 +32,7 @@ CPR_DTYPE_BF16 = 2
 CPR_POLICY_SIMT_F32 = 1
 CPR_POLICY_TC_BF16X3 = 2
 CPR_ORDER_ROWSEQ_V1 = 1
+CPR_ORDER_TOKENREC_V1 = 2   # reading B: token recurrence inside each chunk
 CPR_SCHED_SEQ_CHUNKS = 1
 CPR_OP_FWD = 1
 CPR_OP_BWD = 2
@@ -56,7 +57,7 @@ class Contract(ctypes.Structure):
 class CacheLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "total_bytes", "header", "pos", "done", "state", "k_rows", "v_rows", "gam_rows",
-        "beta_rows", "t_rows", "delta_rows", "state_tiles", "delta_tiles")]
+        "beta_rows", "t_rows", "delta_rows", "state_tiles", "delta_tiles", "run")]
 
 
 class KernelTime(ctypes.Structure):
@@ -98,9 +99,6 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_recurrent_fwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gemm_bf16": (I, [P, P, P, I, I, I, I, P]),
-        "cpr_gdn_fwd_reading_b": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
-        "cpr_gdn_prefill_reading_b": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, SZ, P]),
-        "cpr_gdn_decode_step_reading_b": (I, [CP, P, P, P, P, P, P, I, I, P, P, P, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -336,58 +334,6 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
                            _ptr(outs["dg"]), _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(ws),
                            wsb, _stream()))
     return outs
-
-
-def cpr_gdn_fwd_reading_b(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
-                          digest: Optional[bytes] = None, workspace=None):
-    """Reading B (cpr_gdn_fwd_reading_b): chunk-form boundary states, in-chunk token
-    recurrence for the outputs.  Returns (o fp32, final_state)."""
-    lib = load_library()
-    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
-    if workspace is None:
-        workspace = torch.empty(workspace_bytes(c, CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
-                                device=q.device)
-    o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
-    fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
-    _check(lib.cpr_gdn_fwd_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                     _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(o),
-                                     _ptr(fin), _ptr(workspace), workspace.numel(), _stream()))
-    return o, fin
-
-
-def cpr_gdn_prefill_reading_b(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,
-                              digest: Optional[bytes] = None, workspace=None):
-    """Reading B with a decode cache (cpr_gdn_prefill_reading_b).  Returns (o, final_state,
-    cache, run) where run holds the running in-chunk states for the decode steps."""
-    lib = load_library()
-    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
-    if workspace is None:
-        workspace = torch.empty(workspace_bytes(c, CPR_OP_BWD, n_seq, n_tok, H), dtype=torch.uint8,
-                                device=q.device)
-    cache = new_decode_cache(c, n_seq, H, q.device)
-    run = torch.zeros(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
-    o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
-    fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
-    _check(lib.cpr_gdn_prefill_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q), _ptr(k), _ptr(v),
-                                         _ptr(g), _ptr(beta), _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0),
-                                         _ptr(o), _ptr(fin), _ptr(cache.blob), _ptr(run), _ptr(workspace),
-                                         workspace.numel(), _stream()))
-    return o, fin, cache, run
-
-
-def cpr_gdn_decode_step_reading_b(q_t, k_t, v_t, g_t, beta_t, cache, run, contract: Optional[Contract] = None,
-                                  digest: Optional[bytes] = None, out=None):
-    """One reading-B decode step (cpr_gdn_decode_step_reading_b).  Returns o_t fp32."""
-    lib = load_library()
-    c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
-    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
-    o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
-    _check(lib.cpr_gdn_decode_step_reading_b(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t), _ptr(v_t),
-                                             _ptr(g_t), _ptr(beta_t), n_seq, H, _ptr(cache.blob), _ptr(run),
-                                             _ptr(o), _stream()))
-    return o
 
 
 def cpr_gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contract] = None,

@@ -106,7 +106,12 @@ int check_contract(const cpr_contract* c) {
     } else if (c->operand_policy != CPR_POLICY_SIMT_F32) {
         return fail(CPR_ERR_UNSUPPORTED, "operand_policy %u", c->operand_policy);
     }
-    if (c->intra_order != CPR_ORDER_ROWSEQ_V1) return fail(CPR_ERR_UNSUPPORTED, "intra_order %u", c->intra_order);
+    if (c->intra_order == CPR_ORDER_TOKENREC_V1) {
+        if (c->operand_policy != CPR_POLICY_TC_BF16X3)
+            return fail(CPR_ERR_UNSUPPORTED, "intra_order TOKENREC_V1 needs the TC_BF16X3 policy");
+    } else if (c->intra_order != CPR_ORDER_ROWSEQ_V1) {
+        return fail(CPR_ERR_UNSUPPORTED, "intra_order %u", c->intra_order);
+    }
     if (c->state_schedule != CPR_SCHED_SEQ_CHUNKS) return fail(CPR_ERR_UNSUPPORTED, "state_schedule %u", c->state_schedule);
     if (c->dv_splits != 1 && c->dv_splits != 2 && c->dv_splits != 4)
         return fail(CPR_ERR_UNSUPPORTED, "dv_splits %u (1, 2 or 4)", c->dv_splits);
@@ -142,7 +147,9 @@ WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int 
     auto add = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
     add(w.chunk_off, sizeof(int32_t) * (n_seq + 1));
     if (c.operand_policy == CPR_POLICY_TC_BF16X3) {  // per (chunk, head) operand blocks
-        add(w.W, ch * (op == CPR_OP_BWD ? cpr::tc::kBlockTrain : cpr::tc::kBlock));
+        // (reading B's forward keeps every chunk's boundary state: the training block)
+        const bool keep = op == CPR_OP_BWD || c.intra_order == CPR_ORDER_TOKENREC_V1;
+        add(w.W, ch * (keep ? cpr::tc::kBlockTrain : cpr::tc::kBlock));
         w.total = off;
         return w;
     }
@@ -178,6 +185,7 @@ cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
     add(l.delta_rows, sh * C * dv * 4);
     add(l.state_tiles, sh * dk * dv * 4);   // bf16 hi + lo operand tiles of the state
     add(l.delta_tiles, sh * C * dv * 4);    // bf16 hi + lo operand tiles of the Delta rows
+    if (c.intra_order == CPR_ORDER_TOKENREC_V1) add(l.run, sh * dk * dv * 4);   // running in-chunk state
     l.total_bytes = off;
     return l;
 }
@@ -305,6 +313,67 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
     return CPR_OK;
 }
 
+bool reading_b(const cpr_contract* c) { return c && c->intra_order == CPR_ORDER_TOKENREC_V1; }
+
+// TOKENREC_V1 (reading B): the chunk-form forward keeps every chunk's boundary state in
+// the workspace (training blocks); then each chunk's outputs by the token recurrence from
+// hi + lo of that state.  `run` (with a cache) receives the in-chunk state after each
+// sequence's partial last chunk.
+int reading_b_forward(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
+                      const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
+                      int n_seq, int64_t n_tok, int H, const float* h0, void* o, float* final_state,
+                      void* cache, void* workspace, size_t workspace_bytes, void* stream) {
+    const int rc = forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                                final_state, cache, workspace, workspace_bytes, stream, true);
+    if (rc) return rc;
+    const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    cpr::rec::RbArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q); a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v); a.g = g; a.beta = beta; a.cu = cu_seqlens;
+    a.chunk_off = reinterpret_cast<const int32_t*>(wsb + w.chunk_off); a.n_seq = n_seq; a.H = H;
+    a.scale = c->scale; a.ws = wsb + w.W; a.blk_bytes = cpr::tc::kBlockTrain;
+    a.off_hn = cpr::tc::kOffHn; a.o = static_cast<float*>(o);
+    a.run = cache ? reinterpret_cast<float*>(static_cast<uint8_t*>(cache) + cache_layout(*c, n_seq, H).run)
+                  : nullptr;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_reading_b", st);
+    const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
+    return CPR_OK;
+}
+
+// After the CPR decode step (which keeps the cache, commits full chunks and moves the
+// positions on): one token of the recurrence per (sequence, head) on the running state,
+// restarted at a chunk's first row from hi + lo of the cache's chunk-start state tiles.
+int reading_b_step(const cpr_contract* c, const uint8_t* digest, const void* q_t, const void* k_t,
+                   const void* v_t, const float* g_t, const float* beta_t, int n_seq, int H,
+                   void* cache, void* o_t, void* stream) {
+    if (n_seq == 0) return CPR_OK;
+    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+    uint8_t* cb = static_cast<uint8_t*>(cache);
+    cpr::rec::RbStepArgs a{};
+    a.header = reinterpret_cast<const uint32_t*>(cb + cl.header);
+    std::memcpy(a.digest, digest, 32);
+    header_words(*c, n_seq, H, a.hdr);
+    a.q = static_cast<const __nv_bfloat16*>(q_t); a.k = static_cast<const __nv_bfloat16*>(k_t);
+    a.v = static_cast<const __nv_bfloat16*>(v_t); a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
+    a.scale = c->scale; a.pos = reinterpret_cast<const int32_t*>(cb + cl.pos);
+    a.state_tiles = cb + cl.state_tiles;
+    a.dvs = (int)(c->d_v / c->dv_splits); a.run = reinterpret_cast<float*>(cb + cl.run);
+    a.o = static_cast<float*>(o_t);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_reading_b_step", st);
+    const cudaError_t e = cpr::rb_step_launch(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B step launch");
+    return CPR_OK;
+}
+
+int no_training(const cpr_contract* c) {
+    return reading_b(c) ? fail(CPR_ERR_UNSUPPORTED, "intra_order TOKENREC_V1 (reading B) has no training ops")
+                        : CPR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +464,9 @@ int cpr_gdn_fwd(const cpr_contract* c, const uint8_t digest[32], const void* q, 
                 const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
                 int n_seq, int64_t n_tok, int H, const float* h0, void* o, float* final_state,
                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (reading_b(c))
+        return reading_b_forward(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                                 final_state, nullptr, workspace, workspace_bytes, stream);
     return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
                         final_state, nullptr, workspace, workspace_bytes, stream);
 }
@@ -404,6 +476,8 @@ int cpr_gdn_fwd_train(const cpr_contract* c, const uint8_t digest[32], const voi
                       const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
                       const float* h0, void* o, float* final_state, void* workspace,
                       size_t workspace_bytes, void* stream) {
+    const int rc = no_training(c);
+    if (rc) return rc;
     return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
                         final_state, nullptr, workspace, workspace_bytes, stream, true);
 }
@@ -414,13 +488,16 @@ int cpr_gdn_prefill(const cpr_contract* c, const uint8_t digest[32], const void*
                     void* o, float* final_state, void* cache, void* workspace,
                     size_t workspace_bytes, void* stream) {
     if (!cache) return fail(CPR_ERR_INVALID_ARG, "cache is NULL (use cpr_gdn_fwd without a cache)");
+    if (reading_b(c))
+        return reading_b_forward(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
+                                 final_state, cache, workspace, workspace_bytes, stream);
     return forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
                         final_state, cache, workspace, workspace_bytes, stream);
 }
 
-int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
-                        const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
-                        int n_seq, int H, void* cache, void* o_t, void* stream) {
+static int decode_impl(const cpr_contract* c, const uint8_t* digest, const void* q_t,
+                       const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
+                       int n_seq, int H, void* cache, void* o_t, void* stream) {
     int rc = check_digest(c, digest);
     if (rc) return rc;
     rc = check_sizes(n_seq, 0, H);
@@ -462,6 +539,8 @@ static int backward_impl(const cpr_contract* c, const uint8_t* digest, const voi
                   const float* dHT, void* dq, void* dk, void* dv, float* dg, float* dbeta,
                   float* dh0, void* workspace, size_t workspace_bytes, void* stream, bool saved) {
     int rc = check_digest(c, digest);
+    if (rc) return rc;
+    rc = no_training(c);
     if (rc) return rc;
     if (saved && c->operand_policy != CPR_POLICY_TC_BF16X3)
         return fail(CPR_ERR_UNSUPPORTED, "backward from saved tiles: tensor-core operand policy only");
@@ -579,73 +658,12 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
     return CPR_OK;
 }
 
-static int reading_b_impl(const cpr_contract* c, const uint8_t* digest, const void* q, const void* k,
-                          const void* v, const float* g, const float* beta, const int32_t* cu_seqlens,
-                          int n_seq, int64_t n_tok, int H, const float* h0, void* o,
-                          float* final_state, void* cache, float* run, void* workspace,
-                          size_t workspace_bytes, void* stream) {
-    // the chunk form leaves every chunk's boundary state in the workspace (training forward)
-    const int rc = forward_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
-                                final_state, cache, workspace, workspace_bytes, stream, true);
-    if (rc) return rc;
-    const WsLayout w = ws_layout(*c, CPR_OP_BWD, n_seq, n_tok, H);
-    unsigned char* wsb = static_cast<unsigned char*>(workspace);
-    cpr::rec::RbArgs a{};
-    a.q = static_cast<const __nv_bfloat16*>(q); a.k = static_cast<const __nv_bfloat16*>(k);
-    a.v = static_cast<const __nv_bfloat16*>(v); a.g = g; a.beta = beta; a.cu = cu_seqlens;
-    a.chunk_off = reinterpret_cast<const int32_t*>(wsb + w.chunk_off); a.n_seq = n_seq; a.H = H;
-    a.scale = c->scale; a.ws = wsb + w.W; a.blk_bytes = cpr::tc::kBlockTrain;
-    a.off_hn = cpr::tc::kOffHn; a.o = static_cast<float*>(o); a.run = run;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cpr::ProfScope ps("cpr_reading_b", st);
-    const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
-    return CPR_OK;
-}
-
-int cpr_gdn_fwd_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
-                          const void* k, const void* v, const float* g, const float* beta,
-                          const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
-                          const float* h0, void* o, float* final_state, void* workspace,
-                          size_t workspace_bytes, void* stream) {
-    return reading_b_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
-                          final_state, nullptr, nullptr, workspace, workspace_bytes, stream);
-}
-
-int cpr_gdn_prefill_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q,
-                              const void* k, const void* v, const float* g, const float* beta,
-                              const int32_t* cu_seqlens, int n_seq, int64_t n_tok, int H,
-                              const float* h0, void* o, float* final_state, void* cache,
-                              float* run, void* workspace, size_t workspace_bytes, void* stream) {
-    if (!cache) return fail(CPR_ERR_INVALID_ARG, "cache is NULL");
-    REQ_PTR(run);
-    return reading_b_impl(c, digest, q, k, v, g, beta, cu_seqlens, n_seq, n_tok, H, h0, o,
-                          final_state, cache, run, workspace, workspace_bytes, stream);
-}
-
-int cpr_gdn_decode_step_reading_b(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
-                                  const void* k_t, const void* v_t, const float* g_t,
-                                  const float* beta_t, int n_seq, int H, void* cache, float* run,
-                                  void* o_t, void* stream) {
-    if (c && c->operand_policy != CPR_POLICY_TC_BF16X3)
-        return fail(CPR_ERR_UNSUPPORTED, "reading B: tensor-core operand policy only");
-    // the CPR step keeps the cache (rows, commit) and moves the positions on
-    int rc = cpr_gdn_decode_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
-    if (rc) return rc;
-    if (n_seq == 0) return CPR_OK;
-    REQ_PTR(run);
-    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
-    cpr::rec::RbStepArgs a{};
-    a.q = static_cast<const __nv_bfloat16*>(q_t); a.k = static_cast<const __nv_bfloat16*>(k_t);
-    a.v = static_cast<const __nv_bfloat16*>(v_t); a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
-    a.scale = c->scale; a.pos = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(cache) + cl.pos);
-    a.state_tiles = static_cast<const unsigned char*>(cache) + cl.state_tiles;
-    a.dvs = (int)(c->d_v / c->dv_splits); a.run = run; a.o = static_cast<float*>(o_t);
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cpr::ProfScope ps("cpr_reading_b_step", st);
-    const cudaError_t e = cpr::rb_step_launch(a, st);
-    if (e != cudaSuccess) return cuda_fail(e, "reading-B step launch");
-    return CPR_OK;
+int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
+                        const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
+                        int n_seq, int H, void* cache, void* o_t, void* stream) {
+    const int rc = decode_impl(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+    if (rc || !reading_b(c)) return rc;
+    return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
 }
 
 static int rec_check(const cpr_contract* c) {

@@ -179,11 +179,22 @@ __global__ void __launch_bounds__(256) k_rb(RbArgs a) {
 // tokens (which keeps the cache and commits a full chunk): at a chunk's first row the
 // running state restarts from hi + lo of the cache's chunk-start state tiles -- the bits
 // the reading-B prefill starts that chunk from -- otherwise it continues; one token of
-// the recurrence, o from it.
+// the recurrence, o from it.  A cache whose header is not this contract's (another
+// digest, another shape; the CPR step has recorded the mismatch) is left untouched: its
+// blob need not have the running-state section at all.
 __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
     constexpr int D = 128;
     __shared__ RecSmem<D> s;
+    __shared__ int ok_s;
     const int tid = threadIdx.x, j = tid % D, part = tid / D;
+    if (tid == 0) {
+        bool ok = a.header[0] == kCacheMagic && a.header[1] == CPR_CONTRACT_VERSION;
+        for (int i = 0; i < 8; ++i) ok = ok && a.header[2 + i] == a.digest[i];
+        for (int i = 0; i < 7; ++i) ok = ok && a.header[10 + i] == a.hdr[i];
+        ok_s = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!ok_s) return;
     const int H = a.H, b = blockIdx.x / H, h = blockIdx.x % H;
     const size_t sh = (size_t)b * H + h;
     const int p = (a.pos[b] + kChunk - 1) % kChunk;   // this step's row in its chunk

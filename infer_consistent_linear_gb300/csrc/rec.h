@@ -44,6 +44,9 @@ struct RbArgs {               // reading B (d = 128, bf16 io)
 };
 
 struct RbStepArgs {           // reading B decode step (d = 128, bf16 io)
+    const uint32_t* header;   // the cache's header words
+    uint32_t digest[8];       // the contract's digest and header words the cache must carry
+    uint32_t hdr[7];
     const __nv_bfloat16* q;   // [n_seq, H, d]
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;

@@ -182,3 +182,37 @@ def test_sector_store_outputs_need_32_byte_alignment(lib):
     x, w = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
     assert lib.cpr_gemm_bf16(x, w, ctypes.c_void_p(0x30010), 8, 128, 64, 64, None) == 3
     assert "32-byte" in lib.cpr_last_error().decode()
+
+
+def test_reading_b_is_its_own_contract(lib):
+    """intra_order TOKENREC_V1 (reading B): accepted on the tensor-core policy only, a digest
+    of its own, a decode cache with the running in-chunk state appended, the training
+    forward's workspace, and no training ops (refused on the host)."""
+    a = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=2)
+    b = cpr.Contract.from_buffer_copy(a)
+    b.intra_order = cpr.CPR_ORDER_TOKENREC_V1
+    assert lib.cpr_contract_check(ctypes.byref(b)) == 0
+    assert cpr.contract_digest(a) != cpr.contract_digest(b)
+    s = cpr.default_contract(torch.bfloat16, 128)                  # SIMT policy
+    s.intra_order = cpr.CPR_ORDER_TOKENREC_V1
+    assert lib.cpr_contract_check(ctypes.byref(s)) == 2
+    x = cpr.Contract.from_buffer_copy(a)
+    x.intra_order = 3
+    assert lib.cpr_contract_check(ctypes.byref(x)) == 2
+    n_seq, H, d = 3, 4, 128
+    la, lb = cpr.cache_layout(a, n_seq, H), cpr.cache_layout(b, n_seq, H)
+    assert la.run == 0
+    assert lb.run >= la.total_bytes and lb.run % 256 == 0
+    assert lb.total_bytes >= lb.run + n_seq * H * d * d * 4
+    for f in ("header", "pos", "state", "k_rows", "t_rows", "state_tiles", "delta_tiles"):
+        assert getattr(la, f) == getattr(lb, f), f
+    assert cpr.workspace_bytes(b, cpr.CPR_OP_FWD, n_seq, 4096, H) == cpr.workspace_bytes(a, cpr.CPR_OP_BWD, n_seq, 4096, H)
+    db = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(b))
+    p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    grads = [ctypes.c_void_p(0x200000 * (i + 1)) for i in range(6)]
+    rc = lib.cpr_gdn_fwd_train(ctypes.byref(b), db, *p[:6], 1, 64, 1, None, p[6], None, p[7], 1 << 40, None)
+    assert rc == 2 and "TOKENREC" in lib.cpr_last_error().decode()
+    rc = lib.cpr_gdn_bwd_saved(ctypes.byref(b), db, *p[:6], 1, 64, 1, None, p[6], None, *grads, p[7], 1 << 40, None)
+    assert rc == 2 and "TOKENREC" in lib.cpr_last_error().decode()
+    rc = lib.cpr_gdn_bwd(ctypes.byref(b), db, *p[:6], 1, 64, 1, None, p[6], None, *grads, p[7], 1 << 40, None)
+    assert rc == 2

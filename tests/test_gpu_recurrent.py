@@ -96,24 +96,30 @@ def _tc():
     return cpr.default_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
 
 
+def _rb():
+    """Reading B as its own contract: intra_order TOKENREC_V1 on the tensor-core policy."""
+    return cpr.default_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
+                                intra_order=cpr.CPR_ORDER_TOKENREC_V1)
+
+
 def test_reading_b_matches_oracle_and_differs_from_reading_a():
     """Reading B: the chunk form's boundary states, the token recurrence inside each chunk.
     Within tolerance of the oracle like reading A, with the same final state (the same
-    chunk-form forward), and not the same bits as reading A's outputs."""
+    chunk-form forward), not the same bits as reading A's outputs, and another digest."""
     lens, H = [200, 64, 1, 0, 130], 2
     x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=8, h0_std=0.1)
     xd = x.to(DEV)
-    c = _tc()
-    ob, fb = cpr.cpr_gdn_fwd_reading_b(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
-    oa, fa = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    ob, fb = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=_rb())
+    oa, fa = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=_tc())
     torch.cuda.synchronize()
     assert cpr.get_device_error() == 0
+    assert cpr.contract_digest(_rb()) != cpr.contract_digest(_tc())
     o_ref, h_ref = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0)
     assert_close("o reading B", ob.cpu(), o_ref, TOL_BF16)
     assert_close("o reading A", oa.cpu(), o_ref, TOL_BF16)
     assert_bitwise("final state", fb, fa)
     assert int((ob.view(torch.int32) != oa.view(torch.int32)).sum()) > 0
-    ob2, _ = cpr.cpr_gdn_fwd_reading_b(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
+    ob2, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=_rb())
     assert_bitwise("reading B rerun", ob2, ob)
 
 
@@ -122,7 +128,7 @@ def test_reading_b_first_chunk_is_the_token_recurrence():
     first chunk is exactly the token recurrence from zero (cpr_gdn_recurrent_fwd)."""
     lens, H = [130, 64, 40], 2
     x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=9).to(DEV)
-    ob, _ = cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=_tc())
+    ob, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=_rb())
     cu = x.cu_seqlens.tolist()
     for b, L in enumerate(lens):
         n = min(L, 64)
@@ -136,25 +142,25 @@ def test_reading_b_first_chunk_is_the_token_recurrence():
 
 
 def test_reading_b_decode_equals_reading_b_prefill():
-    """Reading B end to end: a reading-B prefill with a decode cache, then reading-B decode
-    steps (CPR steps keep the cache and commit chunks; the running in-chunk state restarts
-    from the committed state's tiles at each chunk's first row) give the bits of a one-shot
-    reading-B forward over the full sequences, and the committed states are CPR's."""
+    """Reading B end to end under its contract: a prefill (the decode cache also keeps the
+    running in-chunk state), then decode steps (the chunk-form step keeps the cache and
+    commits chunks; the running state restarts from the committed state's tiles at each
+    chunk's first row) give the bits of a one-shot forward over the full sequences, and
+    the committed states are the chunk form's."""
     pre, steps, H = [100, 64, 0, 37, 130], 70, 2
     full = [L + steps for L in pre]
     x = make_inputs(full, H, 128, 128, io_dtype=torch.bfloat16, seed=10, h0_std=0.1).to(DEV)
-    c = _tc()
-    o_full, _ = cpr.cpr_gdn_fwd_reading_b(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
+    cb = _rb()
+    o_full, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=cb)
     cu = x.cu_seqlens.tolist()
     sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(len(pre))]).to(DEV)
     cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(pre), 0).tolist(), dtype=torch.int32, device=DEV)
-    o_pre, _, cache, run = cpr.cpr_gdn_prefill_reading_b(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel],
-                                                         cu_pre, h0=x.h0, contract=c)
+    o_pre, _, cache = cpr.cpr_gdn_prefill(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel], cu_pre,
+                                          h0=x.h0, contract=cb)
     assert_bitwise("prefill part", o_pre, o_full[sel])
     for t in range(steps):
         idx = torch.tensor([cu[b] + pre[b] + t for b in range(len(pre))], device=DEV)
-        ot = cpr.cpr_gdn_decode_step_reading_b(x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx], cache, run,
-                                               contract=c)
+        ot = cpr.cpr_gdn_decode_step(x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx], cache, contract=cb)
         assert_bitwise(f"reading-B decode step {t}", ot, o_full[idx])
         for b in range(len(pre)):
             n_done = pre[b] + t + 1
@@ -162,7 +168,20 @@ def test_reading_b_decode_equals_reading_b_prefill():
                 sl = slice(cu[b], cu[b] + n_done)
                 _, fin = cpr.cpr_gdn_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl],
                                          torch.tensor([0, n_done], dtype=torch.int32, device=DEV),
-                                         h0=x.h0[b:b + 1], contract=c)
+                                         h0=x.h0[b:b + 1], contract=_tc())
                 assert_bitwise(f"committed state seq {b} at {n_done}", cache.state()[b:b + 1], fin)
     torch.cuda.synchronize()
     assert cpr.get_device_error() == 0
+
+
+def test_reading_a_cache_refused_by_reading_b_decode():
+    """A decode cache made under reading A carries reading A's digest: a reading-B decode
+    step on it writes nothing and records CPR_ERR_CONTRACT_MISMATCH on the device."""
+    x = make_inputs([100], 2, 128, 128, io_dtype=torch.bfloat16, seed=11).to(DEV)
+    _, _, cache = cpr.cpr_gdn_prefill(x.q[:99], x.k[:99], x.v[:99], x.g[:99], x.beta[:99],
+                                      torch.tensor([0, 99], dtype=torch.int32, device=DEV), contract=_tc())
+    assert cpr.get_device_error(clear=True) == 0
+    before = cache.blob.clone()
+    cpr.cpr_gdn_decode_step(x.q[99:], x.k[99:], x.v[99:], x.g[99:], x.beta[99:], cache, contract=_rb())
+    assert cpr.get_device_error(clear=True) == 4      # CPR_ERR_CONTRACT_MISMATCH
+    assert torch.equal(cache.blob, before)
