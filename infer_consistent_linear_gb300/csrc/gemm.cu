@@ -248,6 +248,7 @@ bool encode(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) 
 
 cudaError_t gemm_launch(const gemm::GemmArgs& a, cudaStream_t st) {
     if (a.M == 0) return cudaSuccess;
+    if (!gemm::encode_fn()) return cudaErrorNotSupported;   // the driver has no tensor-map encoder
     CUtensorMap mx, mw;
     if (!gemm::encode(&mx, a.X, a.M, a.K, gemm::BM) || !gemm::encode(&mw, a.W, a.K, a.N, gemm::BK))
         return cudaErrorInvalidValue;
