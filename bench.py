@@ -841,6 +841,38 @@ class ReadingB:
                                          workspace=self.ws)
 
 
+class ReadingBDecode:
+    """Reading B's decode on the Decode workload: a reading-B prefill of every sequence
+    (the decode cache also keeps the running in-chunk state), then decode steps under the
+    same contract (the chunk-form step, then one token of the recurrence)."""
+
+    def __init__(self, dev, n_steps):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("decode")
+        H, d = WORKLOADS["decode"]["H"], WORKLOADS["decode"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
+                                      intra_order=cpr.CPR_ORDER_TOKENREC_V1)
+        n_seq = len(self.lens)
+        xd = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        _, _, self.cache = cpr.cpr_gdn_prefill(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=self.c,
+                                               want_final=False)
+        del xd
+        tok = make_inputs([n_steps] * n_seq, H, d, d, io_dtype=torch.bfloat16, seed=1).to(dev)
+        # token t of sequence b is row b * n_steps + t
+        self.tok = [x.view(n_seq, n_steps, *x.shape[1:]).transpose(0, 1).contiguous()
+                    for x in (tok.q, tok.k, tok.v, tok.g, tok.beta)]
+        self.o = torch.empty(n_seq, H, d, device=dev)
+        self.t = 0
+        torch.cuda.synchronize()
+
+    def run(self):
+        q, k, v, g, b = (x[self.t] for x in self.tok)
+        self.cpr.cpr_gdn_decode_step(q, k, v, g, b, self.cache, contract=self.c, out=self.o)
+        self.t += 1
+
+
 def reading_b(dev, world, reading_a_ms):
     """Speed of reading B (contract intra_order TOKENREC_V1) against reading A on the same
     workload, and how far apart the two readings' outputs are (both are checked against the
@@ -857,9 +889,23 @@ def reading_b(dev, world, reading_a_ms):
            "reading_a_ms_per_step": round(reading_a_ms, 4),
            "max_abs_diff_to_reading_a_over_rms": diff,
            "bitwise_equal_to_reading_a": bool(torch.equal(oa.view(torch.int32), ob.view(torch.int32)))}
-    del rb
+    del rb, oa, ob
+    torch.cuda.empty_cache()
+    try:   # reading B's decode step on the Decode workload (its bits are checked in the GPU tests)
+        K, W = 64, 3
+        rd = ReadingBDecode(dev, K + W)
+        ms_d, _ = time_device(rd, K, W, world, profile=False)
+        res["decode"] = {"workload": WORKLOADS["decode"]["desc"], "us_per_step": round(ms_d * 1e3, 3),
+                         "steps": K, "error_word": rb_err(rd.cpr)}
+        del rd
+    except Exception as e:   # reported, not fatal to the bench line
+        res["decode"] = {"error": f"{type(e).__name__}: {e}"}
     torch.cuda.empty_cache()
     return res
+
+
+def rb_err(cpr):
+    return cpr.get_device_error(clear=True)
 
 
 def stage_table(dev, world, pk, cpr_prefill_ms, sec):
