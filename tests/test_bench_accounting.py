@@ -39,3 +39,20 @@ def test_prefill_kernels_are_hbm_bound_by_the_rule():
     t_f = bench.tc_kernel_flops_per_chunk("cpr_tc_prep", d) * units / (pk["bf16_tflops"] * 1e12)
     t_b = bench.tc_kernel_bytes("cpr_tc_prep", lens, H, d) / (pk["hbm_gbs"] * 1e9)
     assert t_b > 3 * t_f
+
+
+def test_reference_arm_prints_its_line():
+    """`bench.py --impl reference` times the oracle on the host (no GPU) and prints one
+    JSON line with the keys the launch contract names."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
