@@ -2,7 +2,7 @@
 //
 // Plain, slow, fp64 reference for the gated delta rule.  It is used by the
 // test suite, by the smoke check and by the benchmark's CPU-baseline leg to
-// judge the CUDA library; the library never calls it, links it or shares
+// check the CUDA library; the library never calls it, links it or shares
 // code with it.
 //
 // What it computes (page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配",
