@@ -216,6 +216,8 @@ def _dig(c: Contract, digest: Optional[bytes]):
 
 def _ws(c, op, n_seq, n_tok, H, device, workspace):
     need = workspace_bytes(c, op, n_seq, n_tok, H)
+    if workspace is not None:
+        _validate([_blob("workspace", workspace)])
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     return workspace, workspace.numel()
@@ -248,6 +250,61 @@ def new_decode_cache(c: Contract, n_seq: int, H: int, device) -> DecodeCache:
     return DecodeCache(blob, lay, n_seq, H, c.d_k, c.d_v)
 
 
+def _validate(specs):
+    """Refuses, before anything is launched, tensors the kernels would not read as the C
+    ABI describes them.  specs: (name, tensor or None, dtype, shape); None passes
+    (optional arguments).  Every tensor is checked for its dtype, shape and contiguity
+    first, then all must sit on one CUDA device (a host tensor would hand a kernel a host
+    address)."""
+    for name, t, dtype, shape in specs:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+        if t.dtype != dtype:
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: dtype {t.dtype}, expected {dtype}")
+        if tuple(t.shape) != tuple(shape):
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if not t.is_contiguous():
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: not contiguous")
+    dev = None
+    for name, t, _, _ in specs:
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: on {t.device}, expected a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise CprError(CPR_ERR_INVALID_ARG, f"{name}: on {t.device}, the other tensors on {dev}")
+
+
+def _io_dtype(c: Contract):
+    return torch.bfloat16 if c.io_dtype == CPR_DTYPE_BF16 else torch.float32
+
+
+def _tok_specs(c: Contract, q, k, v, g, beta, cu_seqlens=None, h0=None, sfx=""):
+    """Specs of one call's token tensors ([n, H, d]: n tokens, or n sequences for a decode
+    step) under the contract; returns (specs, n, H)."""
+    if not isinstance(q, torch.Tensor) or q.dim() != 3:
+        raise CprError(CPR_ERR_INVALID_ARG, f"q{sfx}: expected a [n, H, d_k] tensor")
+    n, H = int(q.shape[0]), int(q.shape[1])
+    io = _io_dtype(c)
+    specs = [("q" + sfx, q, io, (n, H, c.d_k)), ("k" + sfx, k, io, (n, H, c.d_k)),
+             ("v" + sfx, v, io, (n, H, c.d_v)), ("g" + sfx, g, torch.float32, (n, H)),
+             ("beta" + sfx, beta, torch.float32, (n, H))]
+    if cu_seqlens is not None:
+        if not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise CprError(CPR_ERR_INVALID_ARG, "cu_seqlens: expected an int32 [n_seq + 1] tensor")
+        specs += [("cu_seqlens", cu_seqlens, torch.int32, (cu_seqlens.numel(),)),
+                  ("h0", h0, torch.float32, (cu_seqlens.numel() - 1, H, c.d_k, c.d_v))]
+    return specs, n, H
+
+
+def _blob(name, t):
+    return (name, t, torch.uint8, (t.numel(),) if isinstance(t, torch.Tensor) else ())
+
+
 def _shape_args(q, v, cu_seqlens):
     n_tok, H, _ = q.shape
     return int(n_tok), int(H), int(cu_seqlens.numel() - 1)
@@ -261,7 +318,11 @@ def cpr_gdn_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Contra
     keeps the tiles cpr_gdn_bwd(..., saved=True) reads instead of recomputing the forward."""
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
+    n_seq = int(cu_seqlens.numel() - 1)
+    _validate(specs + [("out", out, torch.float32, (n_tok, H, c.d_v)),
+                       ("final", final, torch.float32, (n_seq, H, c.d_k, c.d_v)),
+                       _blob("workspace", workspace) if workspace is not None else ("workspace", None, None, None)])
     o = out if out is not None else torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
     fin = final if final is not None else (
         torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device) if want_final else None)
@@ -282,7 +343,11 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Co
     """Rollout prefill.  Returns (o, final or None, DecodeCache)."""
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
+    n_seq = int(cu_seqlens.numel() - 1)
+    _validate(specs + [("out", out, torch.float32, (n_tok, H, c.d_v)),
+                       _blob("cache.blob", cache.blob) if cache is not None else ("cache", None, None, None),
+                       _blob("workspace", workspace) if workspace is not None else ("workspace", None, None, None)])
     o = out if out is not None else torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
     fin = torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device) if want_final else None
     cache = cache or new_decode_cache(c, n_seq, H, q.device)
@@ -299,7 +364,8 @@ def cpr_gdn_decode_step(q_t, k_t, v_t, g_t, beta_t, cache: DecodeCache,
     """One decode step; tokens [n_seq, H, d].  Returns o_t [n_seq, H, d_v] fp32."""
     lib = load_library()
     c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
-    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
+    specs, n_seq, H = _tok_specs(c, q_t, k_t, v_t, g_t, beta_t, sfx="_t")
+    _validate(specs + [("out", out, torch.float32, (n_seq, H, c.d_v)), _blob("cache.blob", cache.blob)])
     o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
     _check(lib.cpr_gdn_decode_step(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t),
                                    _ptr(v_t), _ptr(g_t), _ptr(beta_t), n_seq, H,
@@ -317,8 +383,19 @@ def cpr_gdn_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
         raise CprError(CPR_ERR_INVALID_ARG, "saved=True needs the training forward's workspace")
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
+    n_seq = int(cu_seqlens.numel() - 1)
     dev = q.device
+    if dO is None:
+        raise CprError(CPR_ERR_INVALID_ARG, "dO is required")
+    specs += [("dO", dO, torch.float32, (n_tok, H, c.d_v)), ("dHT", dHT, torch.float32, (n_seq, H, c.d_k, c.d_v))]
+    if outs is not None:
+        specs += [(name, outs.get(name), torch.float32, shape) for name, shape in (
+            ("dq", (n_tok, H, c.d_k)), ("dk", (n_tok, H, c.d_k)), ("dv", (n_tok, H, c.d_v)),
+            ("dg", (n_tok, H)), ("dbeta", (n_tok, H)), ("dh0", (n_seq, H, c.d_k, c.d_v)))]
+    if workspace is not None:
+        specs.append(_blob("workspace", workspace))
+    _validate(specs)
     if outs is None:
         outs = dict(dq=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
                     dk=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
@@ -342,7 +419,9 @@ def cpr_gdn_recurrent_fwd(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optio
     sequences (cpr_gdn_recurrent_fwd).  Returns (o fp32, final_state or None)."""
     lib = load_library()
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
-    n_tok, H, n_seq = _shape_args(q, v, cu_seqlens)
+    specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
+    _validate(specs)
+    n_seq = int(cu_seqlens.numel() - 1)
     o = torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=q.device)
     fin = (torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=q.device)
            if want_final else None)
@@ -358,7 +437,11 @@ def cpr_gdn_recurrent_step(q_t, k_t, v_t, g_t, beta_t, state, contract: Optional
     [n_seq, H, d_k, d_v], updated in place (cpr_gdn_recurrent_step).  Returns o_t fp32."""
     lib = load_library()
     c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
-    n_seq, H = int(q_t.shape[0]), int(q_t.shape[1])
+    specs, n_seq, H = _tok_specs(c, q_t, k_t, v_t, g_t, beta_t, sfx="_t")
+    if state is None:
+        raise CprError(CPR_ERR_INVALID_ARG, "state is required")
+    _validate(specs + [("state", state, torch.float32, (n_seq, H, c.d_k, c.d_v)),
+                       ("out", out, torch.float32, (n_seq, H, c.d_v))])
     o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
     _check(lib.cpr_gdn_recurrent_step(ctypes.byref(c), _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(g_t),
                                       _ptr(beta_t), n_seq, H, _ptr(state), _ptr(o), _stream()))
@@ -369,8 +452,12 @@ def cpr_gemm(x, w, leaf_k: int, out=None):
     """Batch-invariant projection GEMM (cpr_gemm_bf16): x bf16 [M, K], w bf16 [K, N] ->
     fp32 [M, N], K in fixed leaves of leaf_k rows."""
     lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or not isinstance(w, torch.Tensor) or w.dim() != 2:
+        raise CprError(CPR_ERR_INVALID_ARG, "cpr_gemm: x [M, K] and w [K, N] matrices expected")
     M, K = int(x.shape[0]), int(x.shape[1])
     N = int(w.shape[1])
+    _validate([("x", x, torch.bfloat16, (M, K)), ("w", w, torch.bfloat16, (K, N)),
+               ("out", out, torch.float32, (M, N))])
     y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
     _check(lib.cpr_gemm_bf16(_ptr(x), _ptr(w), _ptr(y), M, N, K, leaf_k, _stream()))
     return y
