@@ -228,7 +228,7 @@ class OurStep:
             self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2,
                                           operand_policy=cpr.CPR_POLICY_TC_BF16X3)
         else:
-            self.c = cpr.default_contract(torch.bfloat16, d)
+            self.c = cpr.simt_contract(torch.bfloat16, d)
         self.dig = cpr.contract_digest(self.c)
         self.saved = policy == "tc"
         self.dev = dev

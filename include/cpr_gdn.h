@@ -148,8 +148,10 @@ typedef struct cpr_contract {
 uint32_t cpr_kernel_build_id(void);
 
 /* Fill *c with this build's default contract for the given io dtype and head
- * dims (C = 64, fp32 out/state/accumulation, SIMT_F32, ROWSEQ_V1,
- * SEQ_CHUNKS, dv_splits = 4 for d_v = 128 else 2, scale = 1). */
+ * dims: C = 64, fp32 out/state/accumulation, ROWSEQ_V1, SEQ_CHUNKS, scale = 1;
+ * operand policy TC_BF16X3 with dv_splits = 2 for bf16 io at d_k = d_v = 128
+ * (the shape the tensor-core kernels cover), else SIMT_F32 with dv_splits = 4
+ * for d_v = 128 and 2 below. */
 int cpr_contract_init_default(cpr_contract* c, uint32_t io_dtype, uint32_t d_k, uint32_t d_v);
 
 /* Canonical serialisation: the 16-byte tag "CPR-GDN-CONTRACT" followed by
@@ -196,7 +198,7 @@ typedef struct cpr_cache_layout {
                            byte ((r/8)(d_k/8) + i/8) * 128 + (r%8) * 16 + (i%8) * 2, rows at
                            or past the position zero                              */
     size_t v_rows;      /* io     [n_seq, H, C, d_v]; same tile form as k_rows        */
-    size_t gam_rows;    /* fp32   [n_seq, H, C]      in-chunk gate prefix          */
+    size_t gam_rows;    /* fp32   [n_seq, H, 2, C]   in-chunk gate prefix hi, lo   */
     size_t beta_rows;   /* fp32   [n_seq, H, C]                                    */
     size_t t_rows;      /* fp32   [n_seq, H, C, C]   rows of (I + A)^-1            */
     size_t delta_rows;  /* fp32   [n_seq, H, C, d_v] rows of Delta                 */
@@ -311,7 +313,10 @@ int cpr_gdn_bwd_saved(const cpr_contract* c, const uint8_t digest[32],
  * CPR_OP_FWD) exceeds that size is rejected with CPR_ERR_WORKSPACE before
  * anything is launched.  The first call on a device looks up the array's
  * device address with that device current; make that first call before any
- * stream capture.  All calls share the one array and it keeps the last
+ * stream capture.  The address is kept per device and looked up again when the
+ * device's context has changed since (cudaDeviceReset destroys the context and
+ * the module that holds the array), so the first call after a reset is again a
+ * first call in this sense.  All calls share the one array and it keeps the last
  * call's contents (the forward writes every scratch word before reading it,
  * so nothing needs clearing); calls that overlap on the GPU -- on two streams,
  * or from two host threads -- race on it and must be serialised by the

@@ -138,6 +138,15 @@ def default_contract(io_dtype=torch.bfloat16, d_k: int = 128, d_v: Optional[int]
     return c
 
 
+def simt_contract(io_dtype=torch.bfloat16, d_k: int = 128, d_v: Optional[int] = None,
+                  **overrides) -> Contract:
+    """The CUDA-core contract (operand policy SIMT_F32: fp32 fma chains) for shapes where
+    the default is the tensor-core policy; d_v split count 4 at d_v >= 128, else 2."""
+    kw = dict(operand_policy=CPR_POLICY_SIMT_F32, dv_splits=4 if (d_v or d_k) >= 128 else 2)
+    kw.update(overrides)
+    return default_contract(io_dtype, d_k, d_v, **kw)
+
+
 def contract_bytes(c: Contract) -> bytes:
     lib = load_library()
     n = ctypes.c_size_t(76)
@@ -277,6 +286,42 @@ def _validate(specs):
             dev = t.device
         elif t.device != dev:
             raise CprError(CPR_ERR_INVALID_ARG, f"{name}: on {t.device}, the other tensors on {dev}")
+    if dev is not None:
+        _require_current(dev, torch.cuda.current_device())
+
+
+def _require_current(dev: torch.device, current: int):
+    """The kernels run on the current device's stream (and its workspace and cache are
+    allocated there), so the tensors must live on the current device: addresses of another
+    GPU's memory would be handed to this GPU's kernels."""
+    idx = dev.index if dev.index is not None else current
+    if idx != current:
+        raise CprError(CPR_ERR_INVALID_ARG, f"tensors on cuda:{idx} but the current device is "
+                                            f"cuda:{current} (use torch.cuda.device({idx}))")
+
+
+def _check_cache(c: Contract, cache, n_seq: int, H: int):
+    """A decode cache must have been made for this contract and batch shape: the kernels
+    address it by the layout of (contract, n_seq, H), and the C ABI takes no size, so a
+    cache made for fewer sequences or heads, another head size, or another reading (the
+    reading-B layout appends a section) would be written past its end."""
+    if not isinstance(cache, DecodeCache):
+        raise CprError(CPR_ERR_INVALID_ARG, f"cache: expected a DecodeCache, got {type(cache).__name__}")
+    if (cache.n_seq, cache.H, cache.d_k, cache.d_v) != (n_seq, H, c.d_k, c.d_v):
+        raise CprError(CPR_ERR_INVALID_ARG,
+                       f"cache: made for n_seq={cache.n_seq}, H={cache.H}, d_k={cache.d_k}, d_v={cache.d_v}; "
+                       f"this call has n_seq={n_seq}, H={H}, d_k={c.d_k}, d_v={c.d_v}")
+    need = cache_layout(c, n_seq, H)
+    blob = cache.blob
+    if not isinstance(blob, torch.Tensor) or blob.dtype != torch.uint8 or blob.dim() != 1:
+        raise CprError(CPR_ERR_INVALID_ARG, "cache.blob: expected a 1-D uint8 tensor")
+    if blob.numel() < need.total_bytes:
+        raise CprError(CPR_ERR_INVALID_ARG, f"cache.blob: {blob.numel()} bytes, this contract's layout "
+                                            f"needs {need.total_bytes}")
+    diff = [f for f, _ in CacheLayout._fields_ if getattr(cache.layout, f) != getattr(need, f)]
+    if diff:
+        raise CprError(CPR_ERR_INVALID_ARG, f"cache: its layout differs from this contract's in {diff} "
+                                            "(made under another contract)")
 
 
 def _io_dtype(c: Contract):
@@ -345,6 +390,8 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Co
     c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
     specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
     n_seq = int(cu_seqlens.numel() - 1)
+    if cache is not None:
+        _check_cache(c, cache, n_seq, H)
     _validate(specs + [("out", out, torch.float32, (n_tok, H, c.d_v)),
                        _blob("cache.blob", cache.blob) if cache is not None else ("cache", None, None, None),
                        _blob("workspace", workspace) if workspace is not None else ("workspace", None, None, None)])
@@ -365,6 +412,7 @@ def cpr_gdn_decode_step(q_t, k_t, v_t, g_t, beta_t, cache: DecodeCache,
     lib = load_library()
     c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
     specs, n_seq, H = _tok_specs(c, q_t, k_t, v_t, g_t, beta_t, sfx="_t")
+    _check_cache(c, cache, n_seq, H)
     _validate(specs + [("out", out, torch.float32, (n_seq, H, c.d_v)), _blob("cache.blob", cache.blob)])
     o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
     _check(lib.cpr_gdn_decode_step(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t),

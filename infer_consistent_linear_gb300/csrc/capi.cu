@@ -19,7 +19,7 @@
 namespace {
 
 // Bumped whenever any rounding-relevant detail of a kernel changes.
-constexpr uint32_t kKernelBuildId = 2u;
+constexpr uint32_t kKernelBuildId = 3u;
 
 thread_local char g_msg[512] = "";
 
@@ -156,7 +156,7 @@ WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int 
     add(w.W, ch * C * dk * 4);
     add(w.U, ch * C * dv * 4);
     add(w.P, ch * C * C * 4);
-    add(w.gam, ch * C * 4);
+    add(w.gam, ch * 2 * C * 4);   // gate prefix hi, lo
     if (op == CPR_OP_BWD) {
         add(w.T, ch * C * C * 4);
         add(w.Kd, ch * C * C * 4);
@@ -179,7 +179,7 @@ cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
     add(l.state, sh * dk * dv * 4);
     add(l.k_rows, sh * C * dk * io);
     add(l.v_rows, sh * C * dv * io);
-    add(l.gam_rows, sh * C * 4);
+    add(l.gam_rows, sh * 2 * C * 4);   // gate prefix hi, lo
     add(l.beta_rows, sh * C * 4);
     add(l.t_rows, sh * C * C * 4);
     add(l.delta_rows, sh * C * dv * 4);
@@ -392,10 +392,13 @@ int cpr_contract_init_default(cpr_contract* c, uint32_t io_dtype, uint32_t d_k, 
     c->gate_dtype = CPR_DTYPE_F32;
     c->accum_dtype = CPR_DTYPE_F32;
     c->state_dtype = CPR_DTYPE_F32;
-    c->operand_policy = CPR_POLICY_SIMT_F32;
+    // the tensor-core policy wherever this build has it (bf16 io, d_k = d_v = 128), the
+    // CUDA-core policy for the other shapes
+    const bool tc = io_dtype == CPR_DTYPE_BF16 && d_k == 128 && d_v == 128;
+    c->operand_policy = tc ? CPR_POLICY_TC_BF16X3 : CPR_POLICY_SIMT_F32;
     c->intra_order = CPR_ORDER_ROWSEQ_V1;
     c->state_schedule = CPR_SCHED_SEQ_CHUNKS;
-    c->dv_splits = d_v >= 128 ? 4 : 2;
+    c->dv_splits = tc ? 2 : (d_v >= 128 ? 4 : 2);
     c->scale = 1.0f;
     c->kernel_build_id = kKernelBuildId;
     return check_contract(c);

@@ -5,7 +5,10 @@
 // deadlock), or embedders with fixed memory pools.  This entry point gives
 // them the forward with its scratch in a file-scope device array instead of a
 // caller workspace, and then runs the ordinary cpr_gdn_fwd path unchanged.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <mutex>
+#include <utility>
 
 #include "cpr_gdn.h"
 
@@ -21,11 +24,39 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[CPR_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the scratch for the current device, looked up once per
-// device (with that device current).  Returns nullptr on failure.
+// Unique id of the calling thread's current CUDA context (0 when the driver does
+// not offer the query).  A device reset destroys the context, and with it the
+// module holding the scratch; the next context on that device gets another id.
+unsigned long long current_context_id() {
+    static const auto fns = [] {
+        void* get = nullptr;
+        void* id = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &get, 4000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            get = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            id = nullptr;
+        return std::make_pair(reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(get),
+                              reinterpret_cast<PFN_cuCtxGetId_v12000>(id));
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long cid = 0;
+    if (!fns.first || !fns.second || fns.first(&ctx) != CUDA_SUCCESS || !ctx ||
+        fns.second(ctx, &cid) != CUDA_SUCCESS)
+        return 0;
+    return cid;
+}
+
+// Device address of the scratch for the current device.  It is looked up with
+// cudaGetSymbolAddress once per device -- with that device current -- and again
+// whenever the device's context has changed since (after cudaDeviceReset the old
+// address would point into a destroyed module).  Returns nullptr on failure.
 void* scratch_for_current_device(cudaError_t* why) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {nullptr};
+    static unsigned long long ctx_of[kMaxDevices] = {0};
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -33,14 +64,27 @@ void* scratch_for_current_device(cudaError_t* why) {
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
+    // (the query makes the runtime create the device's context if it has none yet)
+    void* p = nullptr;
+    const bool fresh = addr[dev] == nullptr;
+    if (fresh) {
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) {
             *why = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
             return nullptr;
         }
+    }
+    const unsigned long long cid = current_context_id();
+    if (!fresh && cid != ctx_of[dev]) {   // a new context since the set-up: look up again
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            *why = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            return nullptr;
+        }
+    }
+    if (p) {
         addr[dev] = p;
+        ctx_of[dev] = cid;
     }
     return addr[dev];
 }

@@ -133,12 +133,12 @@ __global__ void __launch_bounds__(256) k_state_bwd(BwdArgs a) {
             store8(Qs + r * LKI + c8, qv);
         }
         if (tid < C) {
-            const float* gw = a.wsGam + ch * C;
+            const float* gw = a.wsGam + ch * 2 * C;   // gate prefix hi | lo
             const bool in = tid < nrows;
-            const float gr = gw[tid];
-            Gm[tid] = in ? gate(gr) : 0.f;
-            bg[tid] = in ? bg_entry(a.beta[(size_t)(t0 + tid) * H + h], gr) : 0.f;
-            dec[tid] = in ? decay(gw[L], gr) : 0.f;
+            const float gr = gw[tid], lr = gw[C + tid];
+            Gm[tid] = in ? gate(gr, lr) : 0.f;
+            bg[tid] = in ? bg_entry(a.beta[(size_t)(t0 + tid) * H + h], gr, lr) : 0.f;
+            dec[tid] = in ? decay(gw[L], gw[C + L], gr, lr) : 0.f;
         }
         __syncthreads();
         // dD = P^T dO + kt dH'
@@ -208,8 +208,9 @@ __global__ void __launch_bounds__(256) k_grad_chunk(BwdArgs a) {
     float* G2 = G1 + C * LC;                          // [C][LC]  dA, then b E dA
     float* part1 = G2 + C * LC;                       // [C][NJT]
     float* part2 = part1 + C * NJT;                   // [C][NJT]
-    float* gam = part2 + C * NJT;                     // [C]
-    float* Gm = gam + C;
+    float* gam = part2 + C * NJT;                     // [C] gate prefix, hi
+    float* gml = gam + C;                             // [C] gate prefix, lo
+    float* Gm = gml + C;
     float* bet = Gm + C;
     float* bg = bet + C;
     float* decL = bg + C;
@@ -277,13 +278,15 @@ __global__ void __launch_bounds__(256) k_grad_chunk(BwdArgs a) {
     }
     if (tid < C) {
         const bool in = tid < nrows;
-        const float gr = a.wsGam[ch * C + tid];
+        const float* gw = a.wsGam + ch * 2 * C;   // gate prefix hi | lo
+        const float gr = gw[tid], lr = gw[C + tid];
         const float br = in ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
         gam[tid] = gr;
-        Gm[tid] = in ? gate(gr) : 0.f;
+        gml[tid] = lr;
+        Gm[tid] = in ? gate(gr, lr) : 0.f;
         bet[tid] = br;
-        bg[tid] = in ? bg_entry(br, gr) : 0.f;
-        decL[tid] = in ? decay(a.wsGam[ch * C + L], gr) : 0.f;
+        bg[tid] = in ? bg_entry(br, gr, lr) : 0.f;
+        decL[tid] = in ? decay(gw[L], gw[C + L], gr, lr) : 0.f;
     }
     __syncthreads();
     // ---- P2: Delta = U - W' H (the forward's chains)
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(256) k_grad_chunk(BwdArgs a) {
     for (int i = tid; i < C * C; i += blockDim.x) {
         const int r = i / C, s = i % C;
         if (r < nrows && s <= r) {
-            const float e = decay(gam[r], gam[s]);
+            const float e = decay(gam[r], gml[r], gam[s], gml[s]);
             G1[r * LC + s] = __fmul_rn(e, G1[r * LC + s]);
             G2[r * LC + s] = (s < r) ? __fmul_rn(__fmul_rn(bet[r], e), G2[r * LC + s]) : 0.f;
         }

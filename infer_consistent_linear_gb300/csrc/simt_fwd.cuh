@@ -8,7 +8,8 @@
 // decode re-synchronises the state every C tokens.  The chunk form is derived
 // from the recurrence (the pages name it, they do not write it).  For a
 // chunk of n <= C rows with start state H (d_k x d_v):
-//   gam_r = gam_{r-1} + g_r  (gam_{-1} = 0),  G_r = exp(gam_r)
+//   gam_r = gam_{r-1} + g_r  (gam_{-1} = 0; kept as a compensated pair, gam_add),
+//   G_r = exp(gam_r)
 //   a_rs  = (b_r exp(gam_r - gam_s)) (k_r . k_s)            s < r
 //   T     = (I + A)^-1   (unit lower triangular)
 //   W'_r  = sum_{s<=r} T_rs (b_s G_s) k_s,   U_r = sum_{s<=r} T_rs b_s v_s
@@ -38,15 +39,40 @@ namespace cpr {
 namespace simt {
 
 // ---- scalar arithmetic shared by every path --------------------------------
-__device__ __forceinline__ float decay(float gr, float gs) { return expf(__fsub_rn(gr, gs)); }
-__device__ __forceinline__ float gate(float gr) { return expf(gr); }
-__device__ __forceinline__ float a_entry(float beta_r, float gr, float gs, float kk) {
-    return __fmul_rn(__fmul_rn(beta_r, decay(gr, gs)), kk);
+// In-chunk gate prefix gam_r = sum_{s<=r} g_s, in token order, carried as the
+// unevaluated pair hi + lo: hi is the plain fp32 running sum and lo collects the
+// exact rounding error of each of its additions (Knuth's TwoSum).  Reason: after a
+// strong gate (g << 0, e.g. a reset with alpha ~ 0) |gam| is large, and a single
+// fp32 running sum rounds every later log-gate to the spacing of |gam| (about 1e-3
+// at |gam| = 1e4), so exp(gam_r - gam_s) between two later tokens would be off by
+// a relative 1e-3.  With the pair, hi_r - hi_s is exact whenever the two are
+// within a factor of two (Sterbenz), and the exponent below is accurate to a few
+// units in the last place of its own size.  (hi, lo) start at (0, 0) in every
+// chunk; every path advances them with this one function.
+__device__ __forceinline__ void gam_add(float& hi, float& lo, float g) {
+    const float s = __fadd_rn(hi, g);
+    const float bp = __fsub_rn(s, hi);
+    const float ap = __fsub_rn(s, bp);
+    const float err = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(g, bp));
+    hi = s;
+    lo = __fadd_rn(lo, err);
 }
-__device__ __forceinline__ float p_entry(float gr, float gs, float qk) {
-    return __fmul_rn(decay(gr, gs), qk);
+// gam_r - gam_s from the two pairs.
+__device__ __forceinline__ float gam_diff(float hr, float lr, float hs, float ls) {
+    return __fadd_rn(__fsub_rn(hr, hs), __fsub_rn(lr, ls));
 }
-__device__ __forceinline__ float bg_entry(float beta, float gam) { return __fmul_rn(beta, gate(gam)); }
+// exp(gam_r - gam_s) (s <= r: <= 1) and exp(gam_r).
+__device__ __forceinline__ float decay(float hr, float lr, float hs, float ls) {
+    return expf(gam_diff(hr, lr, hs, ls));
+}
+__device__ __forceinline__ float gate(float hr, float lr) { return expf(__fadd_rn(hr, lr)); }
+__device__ __forceinline__ float a_entry(float beta_r, float hr, float lr, float hs, float ls, float kk) {
+    return __fmul_rn(__fmul_rn(beta_r, decay(hr, lr, hs, ls)), kk);
+}
+__device__ __forceinline__ float p_entry(float hr, float lr, float hs, float ls, float qk) {
+    return __fmul_rn(decay(hr, lr, hs, ls), qk);
+}
+__device__ __forceinline__ float bg_entry(float beta, float hr, float lr) { return __fmul_rn(beta, gate(hr, lr)); }
 __device__ __forceinline__ float qhat(float scale, float q) { return __fmul_rn(scale, q); }
 
 // ---- tiled fma chains over shared-memory operands ----------------------------
@@ -173,8 +199,9 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
     IO* Vs = Qs + C * LK;
     float* A = reinterpret_cast<float*>(Vs + C * LV);
     float* Tm = A + C * LC;
-    float* gam = Tm + C * LC;
-    float* bet = gam + C;
+    float* gam = Tm + C * LC;   // gate prefix, hi
+    float* gml = gam + C;       // gate prefix, lo
+    float* bet = gml + C;
     float* bg = bet + C;
 
     const int total = a.chunk_off[a.n_seq];
@@ -218,18 +245,20 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
     }
     if (tid < C) {
         gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
+        gml[tid] = 0.f;
         bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     }
     __syncthreads();
-    if (tid == 0) {  // gate prefix: serial fp32 sum in token order
-        float acc = 0.f;
+    if (tid == 0) {  // gate prefix: serial compensated sum in token order
+        float hi = 0.f, lo = 0.f;
         for (int r = 0; r < nrows; ++r) {
-            acc = __fadd_rn(acc, gam[r]);
-            gam[r] = acc;
+            gam_add(hi, lo, gam[r]);
+            gam[r] = hi;
+            gml[r] = lo;
         }
     }
     __syncthreads();
-    if (tid < C) bg[tid] = (tid < nrows) ? bg_entry(bet[tid], gam[tid]) : 0.f;
+    if (tid < C) bg[tid] = (tid < nrows) ? bg_entry(bet[tid], gam[tid], gml[tid]) : 0.f;
 
     // A = strict_lower(b_r decay kk) (and Kd), P = lower(decay qk) -> workspace
     const size_t ch = (size_t)cidx * H + h;
@@ -248,8 +277,8 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
                 for (int j = 0; j < 4; ++j) {
                     const int r = m0 + i, s = n0 + j;
                     const bool in = (s < r && r < nrows);
-                    A[r * LC + s] = in ? a_entry(bet[r], gam[r], gam[s], acc[i][j]) : 0.f;
-                    if (Kd) Kd[r * C + s] = in ? __fmul_rn(decay(gam[r], gam[s]), acc[i][j]) : 0.f;
+                    A[r * LC + s] = in ? a_entry(bet[r], gam[r], gml[r], gam[s], gml[s], acc[i][j]) : 0.f;
+                    if (Kd) Kd[r * C + s] = in ? __fmul_rn(decay(gam[r], gml[r], gam[s], gml[s]), acc[i][j]) : 0.f;
                 }
         });
     tile_mm<4, 4>(C, C, Zero{},
@@ -263,7 +292,7 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int r = m0 + i, s = n0 + j;
-                    out[j] = (s <= r && r < nrows) ? p_entry(gam[r], gam[s], acc[i][j]) : 0.f;
+                    out[j] = (s <= r && r < nrows) ? p_entry(gam[r], gml[r], gam[s], gml[s], acc[i][j]) : 0.f;
                 }
                 *reinterpret_cast<float4*>(P + (m0 + i) * C + n0) = make_float4(out[0], out[1], out[2], out[3]);
             }
@@ -306,7 +335,10 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
                 *reinterpret_cast<float4*>(U + (m0 + i) * DV + n0) =
                     make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         });
-    if (tid < C) a.wsGam[ch * C + tid] = gam[tid];
+    if (tid < C) {
+        a.wsGam[ch * 2 * C + tid] = gam[tid];
+        a.wsGam[ch * 2 * C + C + tid] = gml[tid];
+    }
     if (a.wsT) {
         float* Tw = a.wsT + ch * C * C;
         for (int i = tid; i < C * C; i += blockDim.x) Tw[i] = Tm[(i / C) * LC + (i % C)];
@@ -316,7 +348,7 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
         const size_t sh = (size_t)b * H + h;
         IO* ck = reinterpret_cast<IO*>(a.cache + a.co.k_rows) + sh * C * DK;
         IO* cv = reinterpret_cast<IO*>(a.cache + a.co.v_rows) + sh * C * DV;
-        float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
+        float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * 2 * C;
         float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
         float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
         for (int i = tid; i < nrows * DK; i += blockDim.x)
@@ -325,6 +357,7 @@ __global__ void __launch_bounds__(256) k_prep(FwdArgs a) {
             cv[i] = v[((size_t)(t0 + i / DV) * H + h) * DV + i % DV];
         if (tid < nrows) {
             cg[tid] = gam[tid];
+            cg[C + tid] = gml[tid];
             cb[tid] = bet[tid];
         }
         for (int i = tid; i < nrows * C; i += blockDim.x) ct[i] = Tm[(i / C) * LC + (i % C)];
@@ -343,8 +376,9 @@ __global__ void __launch_bounds__(256) k_state_fwd(FwdArgs a) {
     float* Hs = Ps + C * LC;                          // [DK][LS]  state columns
     float* Ds = Hs + DK * LS;                         // [C][LS]   U, then Delta
     float* QH = Ds + C * LS;                          // [C][LS]
-    float* gam = QH + C * LS;                         // [C]
-    float* dec = gam + C;                             // [C]
+    float* gam = QH + C * LS;                         // [C] gate prefix, hi
+    float* gml = gam + C;                             // [C] gate prefix, lo
+    float* dec = gml + C;                             // [C]
     IO* Qs = reinterpret_cast<IO*>(dec + C);          // [C][LKI]
     IO* Ks = Qs + C * LKI;                            // [C][LKI]
 
@@ -410,7 +444,10 @@ __global__ void __launch_bounds__(256) k_state_fwd(FwdArgs a) {
             store8(Ks + r * LKI + c8, kv);
             store8(Qs + r * LKI + c8, qv);
         }
-        if (tid < C) gam[tid] = a.wsGam[ch * C + tid];
+        if (tid < C) {
+            gam[tid] = a.wsGam[ch * 2 * C + tid];
+            gml[tid] = a.wsGam[ch * 2 * C + C + tid];
+        }
         if (a.wsHn) {  // chunk-start state (backward)
             float* Hn = a.wsHn + ch * DK * DV;
             for (int i = tid; i < DK * DVS; i += blockDim.x)
@@ -444,7 +481,7 @@ __global__ void __launch_bounds__(256) k_state_fwd(FwdArgs a) {
         if (want_o) {
             // o_r = G_r QH_r + sum_{s<=r} p_rs D_s
             tile_mm<2, 4>(C, DVS,
-                [&](int r, int j) { return __fmul_rn(gate(gam[r]), QH[r * LS + j]); },
+                [&](int r, int j) { return __fmul_rn(gate(gam[r], gml[r]), QH[r * LS + j]); },
                 [&](int r, int s) { return Ps[r * LC + s]; },
                 [&](int s, int j) { return Ds[s * LS + j]; },
                 [&](int m0, int& k0, int& k1) { k0 = 0; k1 = min(m0 + 2, nrows); },
@@ -460,9 +497,9 @@ __global__ void __launch_bounds__(256) k_state_fwd(FwdArgs a) {
         }
         // commit: H' = G_L H + sum_{s<=L} (decay(L, s) k_s) D_s^T
         const int L = nrows - 1;
-        if (tid < C) dec[tid] = (tid < nrows) ? decay(gam[L], gam[tid]) : 0.f;
+        if (tid < C) dec[tid] = (tid < nrows) ? decay(gam[L], gml[L], gam[tid], gml[tid]) : 0.f;
         __syncthreads();
-        const float GL = gate(gam[L]);
+        const float GL = gate(gam[L], gml[L]);
         tile_mm<4, 4>(DK, DVS,
             [&](int d, int j) { return __fmul_rn(GL, Hs[d * LS + j]); },
             [&](int d, int s) { return __fmul_rn(dec[s], cvt(Ks[s * LKI + d])); },
@@ -490,13 +527,13 @@ __global__ void __launch_bounds__(256) k_state_fwd(FwdArgs a) {
 template <class IO, int DK, int DV, int DVS>
 constexpr size_t state_fwd_smem() {
     return sizeof(float) * ((size_t)kChunk * (DK + 4) + kChunk * (kChunk + 4) + DK * (DVS + 4) +
-                            2 * kChunk * (DVS + 4) + 2 * kChunk) +
+                            2 * kChunk * (DVS + 4) + 3 * kChunk) +
            sizeof(IO) * 2 * kChunk * (DK + 8);
 }
 template <class IO, int DK, int DV>
 constexpr size_t prep_smem() {
     return sizeof(IO) * ((size_t)2 * kChunk * (DK + 8) + kChunk * (DV + 8)) +
-           sizeof(float) * (2 * kChunk * (kChunk + 1) + 3 * kChunk);
+           sizeof(float) * (2 * kChunk * (kChunk + 1) + 4 * kChunk);
 }
 
 // ---- decode: one token per sequence, one CTA per (sequence, head) ---------------
@@ -521,7 +558,7 @@ template <class IO, int DK, int DV>
 __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     constexpr int C = kChunk;
     __shared__ float kp[DK], qp[DK], vp[DV], Wp[DK], Up[DV], Dp[DV];
-    __shared__ float arow[C], prow[C], trow[C], gams[C], bets[C], bgs[C];
+    __shared__ float arow[C], prow[C], trow[C], gams[C], gmls[C], bets[C], bgs[C];
     __shared__ int ok_s;
     const int tid = threadIdx.x;
     const int H = a.H;
@@ -544,7 +581,7 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     const size_t sh = (size_t)b * H + h;
     const IO* ck = reinterpret_cast<const IO*>(a.cache + a.co.k_rows) + sh * C * DK;
     const IO* cv = reinterpret_cast<const IO*>(a.cache + a.co.v_rows) + sh * C * DV;
-    float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
+    float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * 2 * C;   // hi | lo
     float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
     float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
     float* cd = reinterpret_cast<float*>(a.cache + a.co.delta_rows) + sh * C * DV;
@@ -560,23 +597,26 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     for (int j = tid; j < DV; j += blockDim.x) vp[j] = cvt(v[j]);
     if (tid < p) {
         gams[tid] = cg[tid];
+        gmls[tid] = cg[C + tid];
         bets[tid] = cb[tid];
     }
     if (tid == 0) {
-        const float gp = a.g[sh];
-        gams[p] = __fadd_rn(p > 0 ? cg[p - 1] : 0.f, gp);
+        float hi = p > 0 ? cg[p - 1] : 0.f, lo = p > 0 ? cg[C + p - 1] : 0.f;
+        gam_add(hi, lo, a.g[sh]);
+        gams[p] = hi;
+        gmls[p] = lo;
         bets[p] = a.beta[sh];
     }
     __syncthreads();
-    if (tid <= p) bgs[tid] = bg_entry(bets[tid], gams[tid]);
-    const float gp = gams[p], bp = bets[p];
+    if (tid <= p) bgs[tid] = bg_entry(bets[tid], gams[tid], gmls[tid]);
+    const float gp = gams[p], lp = gmls[p], bp = bets[p];
     // a_ps (s < p) and p_ps (s <= p): dot chains over d ascending
     if (tid < C) {
         const int s = tid;
         if (s < p) {
             float acc = 0.f;
             for (int d = 0; d < DK; ++d) acc = __fmaf_rn(kp[d], cvt(ck[s * DK + d]), acc);
-            arow[s] = a_entry(bp, gp, gams[s], acc);
+            arow[s] = a_entry(bp, gp, lp, gams[s], gmls[s], acc);
         } else {
             arow[s] = 0.f;
         }
@@ -586,7 +626,7 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
             float acc = 0.f;
             for (int d = 0; d < DK; ++d)
                 acc = __fmaf_rn(qp[d], s == p ? kp[d] : cvt(ck[s * DK + d]), acc);
-            prow[s] = p_entry(gp, gams[s], acc);
+            prow[s] = p_entry(gp, lp, gams[s], gmls[s], acc);
         }
     }
     __syncthreads();
@@ -628,7 +668,7 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
         }
         const float dp = __fsub_rn(Up[j], wh);
         Dp[j] = dp;
-        float acc = __fmul_rn(gate(gp), qh);
+        float acc = __fmul_rn(gate(gp, lp), qh);
         for (int s = 0; s <= p; ++s) acc = __fmaf_rn(prow[s], s == p ? dp : cd[s * DV + j], acc);
         a.o[sh * DV + j] = acc;
     }
@@ -644,14 +684,15 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     if (tid < C) ct[p * C + tid] = trow[tid];
     if (tid == 0) {
         cg[p] = gp;
+        cg[C + p] = lp;
         cb[p] = bp;
     }
     if (p == C - 1) {  // resynchronise: commit H_{n+1}
         __syncthreads();
         const int L = C - 1;
-        if (tid < C) arow[tid] = decay(gams[L], gams[tid]);
+        if (tid < C) arow[tid] = decay(gams[L], gmls[L], gams[tid], gmls[tid]);
         __syncthreads();
-        const float GL = gate(gams[L]);
+        const float GL = gate(gams[L], gmls[L]);
         for (int i = tid; i < DK * DV; i += blockDim.x) {
             const int d = i / DV, j = i % DV;
             float acc = __fmul_rn(GL, Hst[d * DV + j]);

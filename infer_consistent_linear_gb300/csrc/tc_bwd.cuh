@@ -78,9 +78,9 @@ struct SbSmem {
     static constexpr size_t B1lo = B1hi + DVS * 64 * 2;
     static constexpr size_t B2hi = B1lo + DVS * 64 * 2;      // G scale dO, then -bg dR
     static constexpr size_t B2lo = B2hi + DVS * 64 * 2;
-    static constexpr size_t Vec = B2lo + DVS * 64 * 2;      // gam, Gm, dec, bg (64 fp32 each),
-                                                             // 8 warp sums
-    static constexpr size_t Bar = Vec + 5 * 256;             // 5 mbarriers + TMEM base
+    static constexpr size_t Vec = B2lo + DVS * 64 * 2;      // gam (hi, lo), Gm, dec, bg (64 fp32
+                                                             // each), 8 warp sums
+    static constexpr size_t Bar = Vec + 6 * 256;             // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
 };
 
@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
     constexpr int NSPLIT = D / DVS;
     constexpr int HALF = DVS / 2;
     extern __shared__ __align__(1024) unsigned char sm[];
-    float* gam = reinterpret_cast<float*>(sm + L::Vec);
-    float* Gm = gam + 64;
+    float* gam = reinterpret_cast<float*>(sm + L::Vec);   // gate prefix hi, then lo
+    float* gml = gam + 64;
+    float* Gm = gml + 64;
     float* dec = Gm + 64;
     float* bgv = dec + 64;
     float* red = bgv + 64;
@@ -153,9 +154,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
     };
     auto issue_P = [&](int n) {
         const unsigned char* blk = blk_of(n);
-        mbar_expect_tx(bar_P, 16384 + 256);
+        mbar_expect_tx(bar_P, 16384 + 512);
         bulk_g2s(sm + L::Phi, blk + kOffPhi, 16384, bar_P);
-        bulk_g2s(gam, blk + kOffGam, 256, bar_P);
+        bulk_g2s(gam, blk + kOffGam, 512, bar_P);
     };
     auto issue_T = [&](int n) {
         mbar_expect_tx(bar_T, 16384);
@@ -246,12 +247,12 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
             bcur = (tid < nrows) ? bcur : 0.f;
             if (sp == 0 && tid < C) reinterpret_cast<float*>(blk_of(n) + kOffBet)[tid] = bcur;
             const bool in = rr < nrows;
-            const float gr = gam[rr];
-            const float Gr = in ? simt::gate(gr) : 0.f;
+            const float gr = gam[rr], lr = gml[rr];
+            const float Gr = in ? simt::gate(gr, lr) : 0.f;
             if (part == 0) {
                 Gm[rr] = Gr;
-                dec[rr] = in ? simt::decay(gam[Lr], gr) : 0.f;
-                bgv[rr] = in ? simt::bg_entry(bcur, gr) : 0.f;
+                dec[rr] = in ? simt::decay(gam[Lr], gml[Lr], gr, lr) : 0.f;
+                bgv[rr] = in ? simt::bg_entry(bcur, gr, lr) : 0.f;
             }
             const float gs = __fmul_rn(Gr, scale);
 #pragma unroll
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
                 store8_split(sm + L::B2hi, sm + L::B2lo, mn_off(j8 * 8, rr, DVS), y);
             }
         }
-        const float GL = simt::gate(gam[Lr]);
+        const float GL = simt::gate(gam[Lr], gml[Lr]);
         fence_async_smem();
         ok = mbar_wait(bar_KQ + cur, ph_KQ[cur], a.err);
         fence_after();
@@ -466,7 +467,8 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     float *gam = vec, *Gm = vec + 64, *bet = vec + 128, *bgv = vec + 192, *dec = vec + 256,
           *qh = vec + 320, *kh = vec + 448, *rowA = vec + 576, *rowB = vec + 704, *dbA = vec + 832,
           *dRv = vec + 960, *colE = vec + 1024, *eL = vec + 1088, *dgam = vec + 1216,
-          *red = vec + 1280;   // red: the d_v splits' shares of <dH', H_n>; 1284 floats in all
+          *red = vec + 1280,   // red: the d_v splits' shares of <dH', H_n>
+          *gml = vec + 1288;   // gate prefix, lo; 1352 floats in all
     uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + L::Bar);   // Q, K, dR, Delta, gam
     uint64_t* bar_hn = bar_in + 1;                                   // H_n
     uint64_t* bar_dh = bar_in + 2;                                   // dH'
@@ -486,7 +488,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     auto blk_of = [&](int w) { return a.ws + (size_t)w * kBlockTrain; };   // w = cidx * H + h
     auto issue_in = [&](int w) {
         const unsigned char* blk = blk_of(w);
-        mbar_expect_tx(bar_in, 8 * 16384 + 2 * 256 + 16);
+        mbar_expect_tx(bar_in, 8 * 16384 + 3 * 256 + 16);
         bulk_g2s(Rhi, blk + kOffdO, 16384, bar_in);              // dO rows, split
         bulk_g2s(Rlo, blk + kOffdO + 16384, 16384, bar_in);
         bulk_g2s(QK, blk + kOffA4hi + 16384, 16384, bar_in);     // Q rows
@@ -495,7 +497,8 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         bulk_g2s(Rlo + 16384, blk + kOffdR + 16384, 16384, bar_in);
         bulk_g2s(Rhi + 32768, blk + kOffDl, 16384, bar_in);
         bulk_g2s(Rlo + 32768, blk + kOffDl + 16384, 16384, bar_in);
-        bulk_g2s(gam, blk + kOffGam, 256, bar_in);
+        bulk_g2s(gam, blk + kOffGam, 256, bar_in);               // gate prefix hi, lo
+        bulk_g2s(gml, blk + kOffGam + 256, 256, bar_in);
         bulk_g2s(red, blk + kOffHdot, 16, bar_in);               // the splits' <dH', H_n>
         bulk_g2s(bet, blk + kOffBet, 256, bar_in);
     };
@@ -544,10 +547,10 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     pend_in = pend_hn = false;
     if (tid < C) {
         const bool in = tid < nrows;
-        const float gr = gam[tid];
-        Gm[tid] = in ? simt::gate(gr) : 0.f;
-        dec[tid] = in ? simt::decay(gam[Lr], gr) : 0.f;
-        bgv[tid] = in ? simt::bg_entry(bet[tid], gr) : 0.f;
+        const float gr = gam[tid], lr = gml[tid];
+        Gm[tid] = in ? simt::gate(gr, lr) : 0.f;
+        dec[tid] = in ? simt::decay(gam[Lr], gml[Lr], gr, lr) : 0.f;
+        bgv[tid] = in ? simt::bg_entry(bet[tid], gr, lr) : 0.f;
     }
     if (tid == 0) {
         mma_tile<128, 64, D>(tmem + tS1, QK, QK + 16384, false);            // [Q; K] K^T
@@ -611,7 +614,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     {
         // ---- phase A: one pass over this thread's 32 columns s of the row
         const int s0 = hf * 32;
-        const float gr = gam[r], br = bet[r];
+        const float gr = gam[r], lr = gml[r], br = bet[r];
         float v1[32], v2[32];
         tmem_ld32(taddr_of(tmem + tS1, warp, s0), v1);
         tmem_ld32(taddr_of(tmem + tG, warp, s0), v2);
@@ -624,7 +627,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
                 const int s = s0 + j8 * 8 + e, j = j8 * 8 + e;
                 if (top) {
                     const bool in = s <= r && r < nrows;
-                    const float E = in ? simt::decay(gr, gam[s]) : 0.f;
+                    const float E = in ? simt::decay(gr, lr, gam[s], gml[s]) : 0.f;
                     const float P = __fmul_rn(E, __fmul_rn(scale, v1[j]));
                     const float dP = in ? v2[j] : 0.f;
                     const float t = (s < r) ? __fmul_rn(dP, P) : 0.f;
@@ -633,7 +636,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
                     x[e] = __fmul_rn(E, dP);                        // G1 = E . dP
                 } else {
                     const bool in = s < r && r < nrows;
-                    const float E = in ? simt::decay(gr, gam[s]) : 0.f;
+                    const float E = in ? simt::decay(gr, lr, gam[s], gml[s]) : 0.f;
                     const float Kd = __fmul_rn(E, v1[j]);
                     const float dA = in ? -v2[j] : 0.f;
                     sa = __fmaf_rn(dA, Kd, sa);                      // dbA part

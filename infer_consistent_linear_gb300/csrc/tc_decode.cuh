@@ -27,7 +27,7 @@ struct DecSmem {
     static constexpr size_t F = Vt + 16384;          // fp32 scratch
     static constexpr int fGam = 0, fBet = 64, fBg = 128, fArow = 192, fProw = 256, fTrow = 320,
                          fDec = 384, fWp = 448, fUp = 576, fDp = 704, fQs = 832, fRow = 960,
-                         fRow2 = 1088, fEnd = 1216;
+                         fRow2 = 1088, fGml = 1216, fEnd = 1280;
     static constexpr size_t Dt = F + 5120;           // Delta tiles: hi (16 KB) | lo (16 KB), per split
                                                      // MN-major DVS (j) x 64 (token); at a commit the
                                                      // fp32 Delta rows
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     float *gams = F + S::fGam, *bets = F + S::fBet, *bgs = F + S::fBg, *arow = F + S::fArow,
           *prow = F + S::fProw, *trow = F + S::fTrow, *decs = F + S::fDec, *Wp = F + S::fWp,
           *Up = F + S::fUp, *Dp = F + S::fDp, *Qs = F + S::fQs, *row1 = F + S::fRow,
-          *row2 = F + S::fRow2;
+          *row2 = F + S::fRow2, *gmls = F + S::fGml;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + S::Bar);   // MMA groups
     uint64_t* bar_H = mbar + 1;                                   // state tiles
     uint64_t* bar_D = mbar + 2;                                   // Delta tiles; fp32 Delta rows
@@ -171,24 +171,26 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     // gate / beta rows, into registers (the n* set is the next unit's, loaded while this
     // one runs); every load reads valid memory, masks apply at use
     uint4 rowreg = make_uint4(0u, 0u, 0u, 0u), nrowreg = rowreg;
-    float cgv = 0.f, cbv = 0.f, gprev = 0.f, gnew = 0.f, bnew = 0.f;
-    float ncgv = 0.f, ncbv = 0.f, ngprev = 0.f, ngnew = 0.f, nbnew = 0.f;
+    float cgv = 0.f, clv = 0.f, cbv = 0.f, gprev = 0.f, lprev = 0.f, gnew = 0.f, bnew = 0.f;
+    float ncgv = 0.f, nclv = 0.f, ncbv = 0.f, ngprev = 0.f, nlprev = 0.f, ngnew = 0.f, nbnew = 0.f;
     auto load_rows = [&](int u, int p) {
         if (tid < 48) {
             const __nv_bfloat16* src = (tid < 16 ? a.q : tid < 32 ? a.k : a.v) + (size_t)u * D + (tid & 15) * 8;
             nrowreg = *reinterpret_cast<const uint4*>(src);
         }
-        const float* cg = reinterpret_cast<const float*>(a.cache + a.co.gam_rows) + (size_t)u * C;
+        const float* cg = reinterpret_cast<const float*>(a.cache + a.co.gam_rows) + (size_t)u * 2 * C;
         const float* cb = reinterpret_cast<const float*>(a.cache + a.co.beta_rows) + (size_t)u * C;
         ncgv = cg[tid & (C - 1)];
+        nclv = cg[C + (tid & (C - 1))];
         ncbv = cb[tid & (C - 1)];
         ngprev = cg[p > 0 ? p - 1 : 0];
+        nlprev = cg[C + (p > 0 ? p - 1 : 0)];
         ngnew = a.g[u];
         nbnew = a.beta[u];
     };
     auto take_rows = [&]() {
         rowreg = nrowreg;
-        cgv = ncgv; cbv = ncbv; gprev = ngprev; gnew = ngnew; bnew = nbnew;
+        cgv = ncgv; clv = nclv; cbv = ncbv; gprev = ngprev; lprev = nlprev; gnew = ngnew; bnew = nbnew;
     };
 
     if (warp == 0) tmem_alloc(tbase, 256);
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     int pn = 0;   // the next unit's position, read once the S1 MMA is on its way
     __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(k_tile(u));
     __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(v_tile(u));
-    float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
+    float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * 2 * C;   // hi | lo
     float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
     float* ct = reinterpret_cast<float*>(a.cache + a.co.t_rows) + sh * C * C;
     float* cd = reinterpret_cast<float*>(a.cache + a.co.delta_rows) + sh * C * D;
@@ -247,10 +249,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     else if (tid < 48) *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
     if (tid < p) {
         gams[tid] = cgv;
+        gmls[tid] = clv;
         bets[tid] = cbv;
     }
     if (tid == 0) {
-        gams[p] = __fadd_rn(p > 0 ? gprev : 0.f, gnew);
+        float hi = p > 0 ? gprev : 0.f, lo = p > 0 ? lprev : 0.f;
+        simt::gam_add(hi, lo, gnew);
+        gams[p] = hi;
+        gmls[p] = lo;
         bets[p] = bnew;
     }
     fence_async_smem();
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         mma_commit(mbar);
     }
     mma_out = true;
-    if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid]);
+    if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid], gmls[tid]);
     if (!mma_wait()) { ok = false; break; }
     {
         float v[32];
@@ -279,9 +285,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     __syncthreads();
     if (tid < C) {
         const int s = tid;
-        const float gp = gams[p], bp = bets[p];
-        arow[s] = (s < p) ? simt::a_entry(bp, gp, gams[s], row1[s]) : 0.f;
-        prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, gams[s]), __fmul_rn(a.scale, row2[s])) : 0.f;
+        const float gp = gams[p], lp = gmls[p], bp = bets[p];
+        arow[s] = (s < p) ? simt::a_entry(bp, gp, lp, gams[s], gmls[s], row1[s]) : 0.f;
+        prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, lp, gams[s], gmls[s]), __fmul_rn(a.scale, row2[s])) : 0.f;
     }
     // X tiles (R1 + 0 .. 32 KB, row p only) and the T row
     __syncthreads();
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     __syncthreads();
     {
-        const float Gp = simt::gate(gams[p]);
+        const float Gp = simt::gate(gams[p], gmls[p]);
         const int j = tid;  // D == 128 == blockDim
         Dp[j] = __fsub_rn(Up[j], row1[j]);
         Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
@@ -474,6 +480,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         if (tid < C) ct[p * C + tid] = trow[tid];
         if (tid == 0) {
             cg[p] = gams[p];
+            cg[C + p] = gmls[p];
             cb[p] = bets[p];
         }
     }
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
             bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_D);
         }
         pend_D = true;
-        if (tid < C) decs[tid] = simt::decay(gams[Lr], gams[tid]);
+        if (tid < C) decs[tid] = simt::decay(gams[Lr], gmls[Lr], gams[tid], gmls[tid]);
         {
             const bool wd = mbar_wait(bar_D, ph_D, a.err);
             if (wd) {
@@ -537,7 +544,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
             issue_D(un);
         }
         if (has_next) pend_KV = pend_D = true;
-        const float GL = simt::gate(gams[Lr]);
+        const float GL = simt::gate(gams[Lr], gmls[Lr]);
         float v[32];
         const int d = tid;
         for (int c0 = 0; c0 < D; c0 += 32) {

@@ -5,6 +5,7 @@
 // 推理不匹配", section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet";
 // the form is derived from the gated delta rule):
 //   S1   = [K; Q] K^T                      (exact bf16 inputs, one MMA group)
+//   gam  = in-chunk prefix of g (compensated pair, simt::gam_add)
 //   a_rs = (b_r exp(gam_r - gam_s)) kk_rs       s < r
 //   p_rs = exp(gam_r - gam_s) (scale qk_rs)     s <= r
 //   T    = (I + A)^-1                       (fp32, T_rj = -sum_{s=j}^{r-1} a_rs T_sj, ascending s)
@@ -38,8 +39,8 @@ constexpr size_t kOffKmn = 49152;     // K as an MN-major 128 (d) x 64 (token) t
 constexpr size_t kOffPhi = 65536;     // 64 x 64 bf16 K-major
 constexpr size_t kOffPlo = 73728;     // 64 x 64 bf16 K-major
 constexpr size_t kOffU = 81920;       // 64 x 128 fp32, [split][DVS/4][64 rows] float4 groups
-constexpr size_t kOffGam = 114688;    // 64 fp32
-constexpr size_t kBlock = 114944;
+constexpr size_t kOffGam = 114688;    // gate prefix: 64 fp32 hi, then 64 fp32 lo
+constexpr size_t kBlock = 115200;
 // Training blocks (the backward) append, all as hi/lo bf16 tile pairs in the
 // K-major core-matrix layout the backward kernels read with bulk copies:
 constexpr size_t kOffT = kBlock;               // T, 64 x 64 (r, j): hi, lo (8 KB each)
@@ -125,7 +126,7 @@ __device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int
 // TMEM columns are allocated once the copies are in flight: with three CTAs per SM
 // the third one's allocation waits for another CTA to finish, but its loads do not.
 constexpr size_t kPrepOffVmn = 32768, kPrepOffT = 49152, kPrepOffVec = kPrepOffT + 64 * 65 * 4;
-constexpr size_t kPrepSmem = kPrepOffVec + 3 * 64 * 4 + 64;
+constexpr size_t kPrepSmem = kPrepOffVec + 4 * 64 * 4 + 64;
 
 static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -134,8 +135,9 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     unsigned char* tVmn = sm + kPrepOffVmn;        // V, MN-major
     float* At = reinterpret_cast<float*>(sm + 16384);        // [64][64], a_rs at s * 64 + (r & 1) * 32 + r / 2
     float* Tfp = reinterpret_cast<float*>(sm + kPrepOffT);   // [64][65]
-    float* gam = reinterpret_cast<float*>(sm + kPrepOffVec);
-    float* bet = gam + 64;
+    float* gam = reinterpret_cast<float*>(sm + kPrepOffVec);   // gate prefix hi, then lo (gml)
+    float* gml = gam + 64;
+    float* bet = gml + 64;
     float* bg = bet + 64;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(bg + 64);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
@@ -168,16 +170,18 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     }
     if (tid < C) {
         gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
+        gml[tid] = 0.f;
         bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     }
     if (warp == 0) tmem_alloc(tbase, 256);   // while the copies land
     cp_async_wait_all();
     __syncthreads();
-    if (tid == 0) {  // gate prefix: serial fp32 sum in token order
-        float acc = 0.f;
+    if (tid == 0) {  // gate prefix: serial compensated sum in token order
+        float hi = 0.f, lo = 0.f;
         for (int r = 0; r < nrows; ++r) {
-            acc = __fadd_rn(acc, gam[r]);
-            gam[r] = acc;
+            simt::gam_add(hi, lo, gam[r]);
+            gam[r] = hi;
+            gml[r] = lo;
         }
     }
     fence_async_smem();
@@ -193,13 +197,13 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
         bulk_s2g(blk + kOffKmn, tKmn, 16384);
         bulk_commit();
     }
-    if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid]) : 0.f;
+    if (tid < C) bg[tid] = (tid < nrows) ? simt::bg_entry(bet[tid], gam[tid], gml[tid]) : 0.f;
     // E_rs = exp(gam_r - gam_s), s <= r, once per pair, spread evenly over the threads while
     // the S1 MMA runs (rows p and 63 - p together hold 65 entries), into the T buffer
     for (int i = tid; i < 32 * (C + 1); i += 128) {
         const int pr = i / (C + 1), k = i % (C + 1);
         const int r = (k <= pr) ? pr : C - 1 - pr, s_ = (k <= pr) ? k : k - pr - 1;
-        Tfp[r * 65 + s_] = simt::decay(gam[r], gam[s_]);
+        Tfp[r * 65 + s_] = simt::decay(gam[r], gml[r], gam[s_], gml[s_]);
     }
     {
         const bool ok1 = mbar_wait(mbar, 0, a.err);
@@ -276,7 +280,7 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
         const size_t sh = (size_t)b * H + h;
         __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.k_rows) + sh * C * D;
         __nv_bfloat16* cv = reinterpret_cast<__nv_bfloat16*>(a.cache + a.co.v_rows) + sh * C * D;
-        float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * C;
+        float* cg = reinterpret_cast<float*>(a.cache + a.co.gam_rows) + sh * 2 * C;   // hi | lo
         float* cb = reinterpret_cast<float*>(a.cache + a.co.beta_rows) + sh * C;
         for (int i = tid; i < nrows * (D / 8); i += 128) {  // as rows of the decode's operand tiles
             const int r = i / (D / 8), d8 = i % (D / 8);
@@ -289,6 +293,7 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
         }
         if (tid < nrows) {
             cg[tid] = gam[tid];
+            cg[C + tid] = gml[tid];
             cb[tid] = bet[tid];
         }
     }
@@ -349,7 +354,7 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
             bulk_s2g(blk + kOffA4hi, tKQ, 16384);
             bulk_s2g(blk + kOffA4lo, tKQ + 16384, 16384);
             bulk_s2g(blk + kOffU, tVmn, 32768);
-            bulk_s2g(blk + kOffGam, gam, 256);
+            bulk_s2g(blk + kOffGam, gam, 512);
             bulk_commit();
         }
     }
@@ -391,12 +396,12 @@ struct StateSmem {
     static constexpr size_t Bhi = Dlo + DVS * 64 * 2;        // decay * Delta, same layout
     static constexpr size_t Blo = Bhi + DVS * 64 * 2;
     static constexpr size_t Q = Blo + DVS * 64 * 2;          // 64 x DVS fp32, [DVS/4][64] float4
-    static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 (bulk copied)
-    static constexpr size_t Gm = Gam + 256, Dec = Gm + 256;
+    static constexpr size_t Gam = Q + 64 * DVS * 4;          // 64 fp32 hi, 64 lo (bulk copied)
+    static constexpr size_t Gm = Gam + 512, Dec = Gm + 256;
     static constexpr size_t Ost = Dec + 256;                 // output rows, 64 x (DVS + 4) fp32
     static constexpr size_t Bar = Ost + 64 * (DVS + 4) * 4;  // 5 mbarriers + TMEM base
     static constexpr size_t Total = Bar + 64;
-    static constexpr uint32_t LoadA = 32768 + 16384 + 256;   // A4 tiles + gam
+    static constexpr uint32_t LoadA = 32768 + 16384 + 512;   // A4 tiles + gam
     static constexpr uint32_t LoadB = 16384 + 64 * DVS * 4;  // K, U
     static constexpr uint32_t LoadP = 16384;                 // P hi, lo
     static constexpr uint32_t TmemCols = 5 * DVS > 256 ? 512 : 256;
@@ -412,7 +417,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     float* sU = reinterpret_cast<float*>(sm + L::U);
     float* sQ = reinterpret_cast<float*>(sm + L::Q);
-    float* gam = reinterpret_cast<float*>(sm + L::Gam);
+    float* gam = reinterpret_cast<float*>(sm + L::Gam);   // gate prefix hi, then lo
+    float* gml = gam + 64;
     float* Gm = reinterpret_cast<float*>(sm + L::Gm);
     float* dec = reinterpret_cast<float*>(sm + L::Dec);
     uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + L::Bar);   // A4 and H' groups
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         mbar_expect_tx(bar_ldA, L::LoadA);
         bulk_g2s(sm + L::A4hi, blk + kOffA4hi, 32768, bar_ldA);
         bulk_g2s(sm + L::A4lo, blk + kOffA4lo, 16384, bar_ldA);
-        bulk_g2s(sm + L::Gam, blk + kOffGam, 256, bar_ldA);
+        bulk_g2s(sm + L::Gam, blk + kOffGam, 512, bar_ldA);
     };
     auto issue_B = [&](int n) {
         const unsigned char* blk = blk_of(n);
@@ -612,10 +618,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         if (epi) {
             const bool okpd = n == 0 || o_epilogue(n - 1);
             if (tid < C) {
-                Gm[tid] = (tid < nrows) ? simt::gate(gam[tid]) : 0.f;
-                dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gam[tid]) : 0.f;
+                Gm[tid] = (tid < nrows) ? simt::gate(gam[tid], gml[tid]) : 0.f;
+                dec[tid] = (tid < nrows) ? simt::decay(gam[Lr], gml[Lr], gam[tid], gml[tid]) : 0.f;
             }
-            GL = simt::gate(gam[Lr]);
+            GL = simt::gate(gam[Lr], gml[Lr]);
             okg = !bar_or(1, 256, !(ok && okpd));
             if (okg) {
                 ok = mbar_wait(bar_mma, ph_mma, a.err);

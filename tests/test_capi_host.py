@@ -85,7 +85,7 @@ def test_tensor_core_contract_rules(lib):
     c = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
                              dv_splits=2)
     assert lib.cpr_contract_check(ctypes.byref(c)) == 0
-    assert cpr.contract_digest(c) != cpr.contract_digest(cpr.default_contract(torch.bfloat16, 128, dv_splits=2))
+    assert cpr.contract_digest(c) != cpr.contract_digest(cpr.simt_contract(torch.bfloat16, 128, dv_splits=2))
     for field, val in [("dv_splits", 1), ("d_k", 64), ("io_dtype", cpr.CPR_DTYPE_F32)]:
         x = cpr.Contract.from_buffer_copy(c)
         setattr(x, field, val)
@@ -149,7 +149,7 @@ def test_host_argument_errors(lib):
 
 
 def test_training_forward_and_saved_backward_need_tc_contract(lib):
-    c = cpr.default_contract(torch.bfloat16, 128)          # SIMT policy
+    c = cpr.simt_contract(torch.bfloat16, 128)
     dig = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(c))
     p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
     rc = lib.cpr_gdn_fwd_train(ctypes.byref(c), dig, *p[:6], 1, 64, 1, None, p[6], None, p[7],
@@ -193,7 +193,7 @@ def test_reading_b_is_its_own_contract(lib):
     b.intra_order = cpr.CPR_ORDER_TOKENREC_V1
     assert lib.cpr_contract_check(ctypes.byref(b)) == 0
     assert cpr.contract_digest(a) != cpr.contract_digest(b)
-    s = cpr.default_contract(torch.bfloat16, 128)                  # SIMT policy
+    s = cpr.simt_contract(torch.bfloat16, 128)
     s.intra_order = cpr.CPR_ORDER_TOKENREC_V1
     assert lib.cpr_contract_check(ctypes.byref(s)) == 2
     x = cpr.Contract.from_buffer_copy(a)

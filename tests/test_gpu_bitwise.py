@@ -25,7 +25,7 @@ def _decode_vs_prefill(io, d, pre_lens, n_steps, H, check_oracle_tol=None, **con
     n_seq = len(pre_lens)
     full_lens = [L + n_steps for L in pre_lens]
     x = make_inputs(full_lens, H, d, d, io_dtype=io, seed=7, h0_std=0.1).to(DEV)
-    c = cpr.default_contract(io, d, **contract_overrides)
+    c = cpr.simt_contract(io, d, **contract_overrides)
     o_full, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
     cu = x.cu_seqlens.tolist()
     sel = torch.cat([torch.arange(cu[b], cu[b] + pre_lens[b]) for b in range(n_seq)]).to(DEV)
@@ -69,7 +69,7 @@ def test_decode_bf16_d64():
 
 
 def test_chunk_aligned_split():
-    c = cpr.default_contract(torch.bfloat16, 128)
+    c = cpr.simt_contract(torch.bfloat16, 128)
     x = make_inputs([300], 2, 128, 128, io_dtype=torch.bfloat16, seed=2, h0_std=0.1).to(DEV)
     o_all, fin_all = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
     for T1 in (64, 128, 256):
@@ -89,7 +89,7 @@ def test_chunk_aligned_split():
 def test_batch_invariance_fwd_bwd():
     lens = [77, 200, 1, 0, 128, 64]
     H, d = 2, 128
-    c = cpr.default_contract(torch.bfloat16, d)
+    c = cpr.simt_contract(torch.bfloat16, d)
     x = make_inputs(lens, H, d, d, io_dtype=torch.bfloat16, seed=11, h0_std=0.1,
                     with_grad=True).to(DEV)
     o, fin = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
@@ -114,7 +114,7 @@ def test_dv_split_count_does_not_change_bits():
     x = make_inputs([150, 33], 2, 128, 128, io_dtype=torch.bfloat16, seed=12, h0_std=0.1).to(DEV)
     outs = []
     for s in (1, 2, 4):
-        c = cpr.default_contract(torch.bfloat16, 128, dv_splits=s)
+        c = cpr.simt_contract(torch.bfloat16, 128, dv_splits=s)
         outs.append(cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c))
     for o, f in outs[1:]:
         assert_bitwise("o", o, outs[0][0])
@@ -122,7 +122,7 @@ def test_dv_split_count_does_not_change_bits():
 
 
 def test_run_to_run_determinism():
-    c = cpr.default_contract(torch.bfloat16, 128)
+    c = cpr.simt_contract(torch.bfloat16, 128)
     x = make_inputs([333, 64], 2, 128, 128, io_dtype=torch.bfloat16, seed=13, h0_std=0.1,
                     with_grad=True).to(DEV)
     r1 = cpr.cpr_gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, contract=c)
@@ -132,7 +132,7 @@ def test_run_to_run_determinism():
 
 
 def test_device_error_bad_seqlens():
-    c = cpr.default_contract(torch.bfloat16, 64)
+    c = cpr.simt_contract(torch.bfloat16, 64)
     x = make_inputs([10, 10], 1, 64, 64, io_dtype=torch.bfloat16, seed=1).to(DEV)
     cpr.get_device_error(clear=True)
     o = torch.full((20, 1, 64), 7.0, device=DEV)
@@ -147,8 +147,8 @@ def test_device_error_bad_seqlens():
 
 def test_decode_rejects_cache_of_another_contract():
     x = make_inputs([70], 1, 64, 64, io_dtype=torch.bfloat16, seed=1).to(DEV)
-    ca = cpr.default_contract(torch.bfloat16, 64, dv_splits=1)
-    cb = cpr.default_contract(torch.bfloat16, 64, dv_splits=2)
+    ca = cpr.simt_contract(torch.bfloat16, 64, dv_splits=1)
+    cb = cpr.simt_contract(torch.bfloat16, 64, dv_splits=2)
     cu = torch.tensor([0, 69], dtype=torch.int32, device=DEV)
     _, _, cache = cpr.cpr_gdn_prefill(x.q[:69], x.k[:69], x.v[:69], x.g[:69], x.beta[:69], cu,
                                       contract=ca)
@@ -170,7 +170,7 @@ def test_bounded_wait_expires_with_device_timeout_and_context_stays_usable():
     cpr.get_device_error(clear=True)
     assert cpr.selftest_wait_timeout(4096)                 # the wait ran out
     assert cpr.get_device_error(clear=True) == 9           # CPR_ERR_DEVICE_TIMEOUT recorded
-    c = cpr.default_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+    c = cpr.simt_contract(torch.bfloat16, 128, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
     x = make_inputs([100], 2, 128, 128, io_dtype=torch.bfloat16, seed=3)
     o, _ = cpr.cpr_gdn_fwd(*(t.to(DEV) for t in (x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)), contract=c)
     torch.cuda.synchronize()

@@ -21,7 +21,7 @@ def _gpu():
 def _fwd_case(lens, H, d, io, tol, h0_std, splits=None):
     x = make_inputs(lens, H, d, d, io_dtype=io, seed=3, h0_std=h0_std)
     xd = x.to(DEV)
-    c = cpr.default_contract(io, d, **({"dv_splits": splits} if splits else {}))
+    c = cpr.simt_contract(io, d, **({"dv_splits": splits} if splits else {}))
     o, fin = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c)
     torch.cuda.synchronize()
     assert cpr.get_device_error() == 0
@@ -54,7 +54,7 @@ def _bwd_case(lens, H, d, io, tol, with_dHT=True):
     gen = torch.Generator().manual_seed(9)
     dHT = torch.randn(len(lens), H, d, d, generator=gen) if with_dHT else None
     xd = x.to(DEV)
-    c = cpr.default_contract(io, d)
+    c = cpr.simt_contract(io, d)
     got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0,
                           dHT=None if dHT is None else dHT.to(DEV), contract=c)
     torch.cuda.synchronize()
@@ -79,7 +79,7 @@ def test_bwd_without_dHT():
 def test_scale_parameter():
     x = make_inputs([90, 40], 2, 64, 64, io_dtype=torch.bfloat16, seed=4, with_grad=True)
     xd = x.to(DEV)
-    c = cpr.default_contract(torch.bfloat16, 64, scale=0.125)
+    c = cpr.simt_contract(torch.bfloat16, 64, scale=0.125)
     o, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=c)
     gr = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, contract=c)
     o_ref, _ = oracle.gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, scale=0.125)
@@ -90,7 +90,7 @@ def test_scale_parameter():
 
 
 def test_zero_token_batch_passes_state_through():
-    c = cpr.default_contract(torch.bfloat16, 128)
+    c = cpr.simt_contract(torch.bfloat16, 128)
     x = make_inputs([0, 0], 2, 128, 128, io_dtype=torch.bfloat16, seed=1, h0_std=0.5).to(DEV)
     o, fin = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
     torch.cuda.synchronize()

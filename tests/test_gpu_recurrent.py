@@ -175,13 +175,28 @@ def test_reading_b_decode_equals_reading_b_prefill():
 
 
 def test_reading_a_cache_refused_by_reading_b_decode():
-    """A decode cache made under reading A carries reading A's digest: a reading-B decode
-    step on it writes nothing and records CPR_ERR_CONTRACT_MISMATCH on the device."""
+    """A decode cache made under reading A carries reading A's digest and layout.  The
+    binding refuses it for a reading-B decode step on the host (its layout is not reading
+    B's).  Through the C ABI, in a blob of reading B's size, the device-side header check
+    refuses it: nothing is written and CPR_ERR_CONTRACT_MISMATCH is recorded."""
+    import ctypes
     x = make_inputs([100], 2, 128, 128, io_dtype=torch.bfloat16, seed=11).to(DEV)
     _, _, cache = cpr.cpr_gdn_prefill(x.q[:99], x.k[:99], x.v[:99], x.g[:99], x.beta[:99],
                                       torch.tensor([0, 99], dtype=torch.int32, device=DEV), contract=_tc())
     assert cpr.get_device_error(clear=True) == 0
-    before = cache.blob.clone()
-    cpr.cpr_gdn_decode_step(x.q[99:], x.k[99:], x.v[99:], x.g[99:], x.beta[99:], cache, contract=_rb())
+    tok = (x.q[99:], x.k[99:], x.v[99:], x.g[99:], x.beta[99:])
+    with pytest.raises(cpr.CprError, match="needs|layout"):
+        cpr.cpr_gdn_decode_step(*tok, cache, contract=_rb())
+    rb = _rb()
+    blob = torch.zeros(cpr.cache_layout(rb, 1, 2).total_bytes, dtype=torch.uint8, device=DEV)
+    blob[:cache.blob.numel()] = cache.blob
+    before = blob.clone()
+    o = torch.empty(1, 2, 128, dtype=torch.float32, device=DEV)
+    lib = cpr.load_library()
+    dig = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(rb))
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = lib.cpr_gdn_decode_step(ctypes.byref(rb), dig, *[p(t) for t in tok], 1, 2, p(blob), p(o),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, lib.cpr_last_error().decode()
     assert cpr.get_device_error(clear=True) == 4      # CPR_ERR_CONTRACT_MISMATCH
-    assert torch.equal(cache.blob, before)
+    assert torch.equal(blob, before)

@@ -96,11 +96,16 @@ def test_tc_context_parallel_segments_bitwise():
     """Context-parallel prefill emulated on one GPU: every sequence cut into chunk-aligned
     segments (one per emulated rank), run one after another with the fp32 state handed
     on as the next segment's h0; outputs and final states equal the unsplit run bit for
-    bit, whatever the cut points."""
+    bit, whatever the cut points, and that run is within tolerance of the oracle."""
     c = _tc()
     lens, H = [1024, 700, 192, 65], 2
-    x = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=6, h0_std=0.1).to(DEV)
+    xc = make_inputs(lens, H, 128, 128, io_dtype=torch.bfloat16, seed=6, h0_std=0.1)
+    x = xc.to(DEV)
     o, fin = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=c)
+    # the unsplit run, and so every segmented one, against the fp64 oracle on these inputs
+    o_ref, h_ref = oracle.gdn_fwd(xc.q, xc.k, xc.v, xc.g, xc.beta, xc.cu_seqlens, h0=xc.h0)
+    assert_close("o", o, o_ref, TOL_BF16)
+    assert_close("final_state", fin, h_ref, TOL_BF16)
     cu = x.cu_seqlens.tolist()
     for R in (2, 4):
         for b, L in enumerate(lens):
@@ -123,7 +128,7 @@ def test_tc_prefill_cache_refused_by_simt_decode():
     _, _, cache = cpr.cpr_gdn_prefill(x.q[:69], x.k[:69], x.v[:69], x.g[:69], x.beta[:69], cu,
                                       contract=_tc())
     cpr.get_device_error(clear=True)
-    simt = cpr.default_contract(torch.bfloat16, 128, dv_splits=2)
+    simt = cpr.simt_contract(torch.bfloat16, 128, dv_splits=2)
     cpr.cpr_gdn_decode_step(x.q[69:], x.k[69:], x.v[69:], x.g[69:], x.beta[69:], cache, contract=simt)
     assert cpr.get_device_error(clear=True) == 4
 
