@@ -139,8 +139,9 @@ def algo_fwd_bytes_per_head_token(d, io_bytes=2, out_bytes=4):
 
 
 def algo_bwd_bytes_per_head_token(d, io_bytes=2, out_bytes=4):
-    # reads q, k, v, g, beta, dO (fp32); writes dq, dk, dv (fp32), dg, dbeta
-    return 3 * d * io_bytes + 8 + d * 4 + 3 * d * out_bytes + 8
+    # reads q, k, v, g, beta, dO; writes dq, dk, dv, dg, dbeta (dO and the three gradients
+    # at out_bytes: 1,808 B with bf16, 2,832 B with the fp32 this build reads and writes)
+    return 3 * d * io_bytes + 8 + d * out_bytes + 3 * d * out_bytes + 8
 
 
 def algo_fwd_flops_per_chunk(d, Cc=C):
@@ -277,7 +278,9 @@ class OurStep:
                               dh0=torch.empty(n_seq, H, d, d, device=dev))
         torch.cuda.synchronize()
 
-    def run(self, xd=None):
+    def run(self, xd=None, outs=None):
+        """One step; `xd` / `outs` replace the step's own device inputs / outputs (outs: o,
+        final, then dq, dk, dv, dg, dbeta, dh0 for the trainer)."""
         cpr = self.cpr
         if self.op == "decode":
             t = self.t
@@ -287,15 +290,18 @@ class OurStep:
             self.t += 1
             return
         x = xd if xd is not None else self.xd
+        o, fin = (outs[0], outs[1]) if outs is not None else (self.o, self.fin)
+        gouts = (dict(zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), outs[2:]))
+                 if outs is not None and self.op == "fwdbwd" else getattr(self, "gouts", None))
         # the trainer step: a training forward that keeps its tiles for the backward
         # (tensor-core contract), or forward + backward-with-recompute (SIMT contract)
         train = self.op == "fwdbwd" and self.saved
         cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c, digest=self.dig,
-                        out=self.o, final=self.fin, workspace=self.wsb if train else self.ws,
+                        out=o, final=fin, workspace=self.wsb if train else self.ws,
                         train=train)
         if self.op == "fwdbwd":
             cpr.cpr_gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, contract=self.c,
-                            digest=self.dig, workspace=self.wsb, outs=self.gouts, saved=train)
+                            digest=self.dig, workspace=self.wsb, outs=gouts, saved=train)
 
     def tokens_per_step(self):
         return len(self.lens) if self.op == "decode" else sum(self.lens)
@@ -382,70 +388,82 @@ def time_device(step, K, W, world, profile=False):
 
 
 def time_e2e(step, K, W, world):
-    """Same step through the public API with pinned host buffers: every step
-    copies its inputs host->device and its results device->host inside the
-    timed region.  Returns (ms_per_step, h2d_bytes, d2h_bytes)."""
-    dev_bufs, host_in, host_out, dev_out = [], [], [], []
+    """Same step through the public API with pinned host buffers: every step copies its
+    inputs host->device and its results device->host inside the timed region.  The copies
+    run on their own streams with two sets of device buffers, so that step i + 1's upload
+    and step i - 1's download overlap step i's kernels, as a serving loop would run them.
+    Returns (ms_per_step, h2d_bytes, d2h_bytes)."""
+    cs = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     if step.op == "decode":
-        n = len(step.tok[0])
-        ins = [t for t in step.tok]                       # [n_steps, n_seq, ...]
-        host_in = [t.cpu().pin_memory() for t in ins]
-        dev_bufs = [torch.empty_like(t[0]) for t in ins]
-        out_host = torch.empty_like(step.o_steps[0], device="cpu").pin_memory()
-        total = min(n, W + K)
+        n_steps = len(step.tok[0])
+        host_in = [t.cpu().pin_memory() for t in step.tok]          # [n_steps, n_seq, ...]
+        dev_in = [[torch.empty_like(t[0]) for t in step.tok] for _ in range(2)]
+        dev_out = [[torch.empty_like(step.o_steps[0])] for _ in range(2)]
+        host_in_of = lambda i: [t[i] for t in host_in]
+        total = min(n_steps, W + K)
     else:
-        x = step.xd
         names = ["q", "k", "v", "g", "beta", "cu_seqlens"] + (["dO"] if step.op == "fwdbwd" else [])
-        srcs = [getattr(step.x_host, nm) for nm in names]
-        host_in = [t.contiguous().pin_memory() for t in srcs]
-        dev_bufs = [torch.empty_like(getattr(x, nm)) for nm in names]
-        dev_out = [step.o, step.fin] + ([step.gouts[k] for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0")]
-                                        if step.op == "fwdbwd" else [])
-        host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in dev_out]
-    h2d = sum(t[0].numel() * t.element_size() if step.op == "decode" else t.numel() * t.element_size()
-              for t in host_in)
-    stream = torch.cuda.current_stream()
+        srcs = [getattr(step.x_host, nm).contiguous().pin_memory() for nm in names]
+        dev_in = [[torch.empty_like(getattr(step.xd, nm)) for nm in names] for _ in range(2)]
+        outs0 = [step.o, step.fin] + ([step.gouts[k] for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0")]
+                                      if step.op == "fwdbwd" else [])
+        dev_out = [outs0] + [[torch.empty_like(t) for t in outs0]]
+        host_in_of = lambda i: srcs
+        total = W + K
+    host_out = [[torch.empty_like(t, device="cpu").pin_memory() for t in dev_out[0]] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in_of(0))
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    ev_up = [torch.cuda.Event() for _ in range(2)]     # buffer b's inputs have landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # the kernels reading/writing buffer b are done
+    ev_down = [torch.cuda.Event() for _ in range(2)]   # buffer b's results have left
 
     def one(i):
-        if step.op == "decode":
-            for hb, db in zip(host_in, dev_bufs):
-                db.copy_(hb[i], non_blocking=True)
-            q, k, v, g, b = dev_bufs
-            step.cpr.cpr_gdn_decode_step(q, k, v, g, b, step.cache, contract=step.c,
-                                         digest=step.dig, out=step.o_steps[i])
-            out_host.copy_(step.o_steps[i], non_blocking=True)
-        else:
-            for hb, db in zip(host_in, dev_bufs):
+        b = i % 2
+        with torch.cuda.stream(up):
+            up.wait_event(ev_done[b])          # step i - 2 no longer reads these inputs
+            for hb, db in zip(host_in_of(i), dev_in[b]):
                 db.copy_(hb, non_blocking=True)
+            ev_up[b].record(up)
+        cs.wait_event(ev_up[b])
+        cs.wait_event(ev_down[b])              # step i - 2's results are on the host
+        if step.op == "decode":
+            q, k, v, g, bt = dev_in[b]
+            step.cpr.cpr_gdn_decode_step(q, k, v, g, bt, step.cache, contract=step.c, digest=step.dig,
+                                         out=dev_out[b][0])
+        else:
             from infer_consistent_linear_gb300.synth import GdnInputs
-            d = dict(zip(["q", "k", "v", "g", "beta", "cu_seqlens", "dO"], dev_bufs))
-            xin = GdnInputs(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], None, d.get("dO"))
-            step.run(xin)
-            for ho, do in zip(host_out, dev_out):
+            d = dict(zip(["q", "k", "v", "g", "beta", "cu_seqlens", "dO"], dev_in[b]))
+            step.run(GdnInputs(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], None, d.get("dO")),
+                     outs=dev_out[b])
+        ev_done[b].record(cs)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            for ho, do in zip(host_out[b], dev_out[b]):
                 ho.copy_(do, non_blocking=True)
+            ev_down[b].record(down)
 
     if step.op == "decode":
-        # replay the same token sequence from the post-prefill cache
-        step.cache.blob.copy_(step.blob0)
-        for i in range(min(W, total)):
-            one(i)
-        start = min(W, total)
-        K = min(K, total - start)
+        step.cache.blob.copy_(step.blob0)      # replay the same tokens from the post-prefill cache
+        Wd = min(W, total)
+        K = min(K, total - Wd)
     else:
-        for i in range(W):
-            one(i)
-        start = 0
+        Wd = W
+    for i in range(Wd):
+        one(i)
     torch.cuda.synchronize()
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
+    s.record(cs)
+    up.wait_event(s)
+    down.wait_event(s)
     for i in range(K):
-        one(start + i)
-    e.record(stream)
+        one(Wd + i)
+    cs.wait_event(ev_down[0])
+    cs.wait_event(ev_down[1])
+    e.record(cs)
     torch.cuda.synchronize()
     barrier(world)
-    d2h = (out_host.numel() * out_host.element_size() if step.op == "decode"
-           else sum(t.numel() * t.element_size() for t in host_out))
     return max_over_ranks(s.elapsed_time(e) / K, world), int(h2d), int(d2h)
 
 
@@ -472,8 +490,26 @@ def kernel_src_sha():
     return h.hexdigest()[:16]
 
 
+def step_bytes(step, out_bytes):
+    """The method's algorithmic bytes of one step, with o (and for the backward dq, dk, dv)
+    counted at `out_bytes` per element: q, k, v, g, beta in, o out, the final states; the
+    backward reads them and dO again and writes the gradients and dh0."""
+    d, H = step.d, step.H
+    ht = sum(step.lens) * H
+    states = len(step.lens) * H * d * d * 4
+    byt = ht * algo_fwd_bytes_per_head_token(d, out_bytes=out_bytes) + states
+    if step.op == "fwdbwd":
+        byt += ht * algo_bwd_bytes_per_head_token(d, out_bytes=out_bytes) + states
+    return byt
+
+
 def roofline_for(step, prof, pk):
-    """Roofline of the dominant kernel (largest share of device time)."""
+    """Roofline of the dominant kernel (largest share of device time).  `achieved` and
+    `frac` charge the launch with ALL of the step's algorithmic bytes (the method's
+    per-head-token figure with a bf16 o, times the head-tokens one launch covers, plus the
+    states) over the kernel's average launch time; `frac_fp32_out` is the same with the
+    fp32 o (and gradients) this build writes; `frac_kernel_share` charges the kernel only
+    its own share of those bytes (what it reads or writes of the method's tensors)."""
     if not prof:
         return None
     name, (launches, total_ms) = max(prof.items(), key=lambda kv: kv[1][1])
@@ -485,23 +521,22 @@ def roofline_for(step, prof, pk):
         traffic = tr.get("bytes_per_launch")
     tfl = tc_kernel_flops_per_chunk(name, step.d)
     if tfl is not None:
-        # the kernel's own roofline: the slower of its algorithmic FLOPs at the bf16 peak
-        # and its algorithmic bytes at the copy bandwidth
         flops = tfl * units
-        byt = tc_kernel_bytes(name, step.lens, step.H, step.d)
-        t_f = flops / (pk["bf16_tflops"] * 1e12)
-        t_b = byt / (pk["hbm_gbs"] * 1e9)
-        base = {"kernel": name, "traffic": traffic, "avg_launch_us": round(avg_s * 1e6, 2),
-                "algo_flops_per_launch": flops, "algo_bytes_per_launch": byt}
-        if t_f >= t_b:
-            ach = flops / avg_s / 1e12
-            return {**base, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
-                    "peak_source": "measured bf16 dense (burst)"}
-        ach = byt / avg_s / 1e9
-        return {**base, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": "measured copy bandwidth",
-                "tensor_frac": round(flops / avg_s / 1e12 / pk["bf16_tflops"], 4)}
+        share = tc_kernel_bytes(name, step.lens, step.H, step.d)
+        byt16, byt32 = step_bytes(step, 2), step_bytes(step, 4)
+        ach = byt16 / avg_s / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "avg_launch_us": round(avg_s * 1e6, 2), "algo_bytes_per_launch": byt16,
+                "bytes_rule": "all of the step's algorithmic bytes, o counted in bf16 (1,032 B per "
+                              "head-token forward) plus the states, over this kernel's launch time",
+                "frac_fp32_out": round(byt32 / avg_s / 1e9 / pk["hbm_gbs"], 4),
+                "algo_bytes_fp32_out": byt32,
+                "frac_kernel_share": round(share / avg_s / 1e9 / pk["hbm_gbs"], 4),
+                "kernel_share_bytes": share,
+                "tensor_frac": round(flops / avg_s / 1e12 / pk["bf16_tflops"], 4),
+                "algo_flops_per_launch": flops,
+                "peak_source": "measured copy bandwidth (of measured)"}
     if name in ("cpr_decode", "cpr_tc_decode"):
         byt = DECODE_ALGO_BYTES_PER_SEQ_HEAD * units
         ach = byt / avg_s / 1e9
@@ -522,14 +557,22 @@ def roofline_for(step, prof, pk):
 
 def path_roofline(step, ms, pk):
     """The method's roofline for the whole step: the slower of its bytes at
-    HBM bandwidth and its dense-contraction FLOPs at the bf16 tensor peak."""
+    HBM bandwidth and its dense-contraction FLOPs at the bf16 tensor peak.  `frac`
+    counts o in bf16 (the method's byte figure), `frac_fp32_out` in fp32."""
     byt, fl = step.algo()
-    t_hbm = byt / (pk["hbm_gbs"] * 1e9)
     t_mma = fl / (pk["bf16_tflops"] * 1e12)
-    t = max(t_hbm, t_mma)
-    return {"bound": "hbm" if t_hbm >= t_mma else "tensor", "roofline_us": round(t * 1e6, 2),
-            "measured_us": round(ms * 1e3, 2), "frac": round(t / (ms / 1e3), 4),
-            "algo_bytes": int(byt), "algo_flops": int(fl), "peaks": pk["source"]}
+    res = {"measured_us": round(ms * 1e3, 2), "algo_flops": int(fl), "peaks": pk["source"]}
+    if step.op == "decode":
+        t_hbm = byt / (pk["hbm_gbs"] * 1e9)
+        t = max(t_hbm, t_mma)
+        return {**res, "bound": "hbm", "roofline_us": round(t * 1e6, 2), "frac": round(t / (ms / 1e3), 4),
+                "algo_bytes": int(byt)}
+    b16, b32 = step_bytes(step, 2), step_bytes(step, 4)
+    t16, t32 = max(b16 / (pk["hbm_gbs"] * 1e9), t_mma), max(b32 / (pk["hbm_gbs"] * 1e9), t_mma)
+    return {**res, "bound": "hbm" if b16 / (pk["hbm_gbs"] * 1e9) >= t_mma else "tensor",
+            "roofline_us": round(t16 * 1e6, 2), "frac": round(t16 / (ms / 1e3), 4), "algo_bytes": int(b16),
+            "roofline_us_fp32_out": round(t32 * 1e6, 2), "frac_fp32_out": round(t32 / (ms / 1e3), 4),
+            "algo_bytes_fp32_out": int(b32)}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -695,6 +738,131 @@ class NativeDecode:
         self.t += 1
 
 
+class ChunkwiseDecode:
+    """"Chunkwise everywhere" decode on the Decode workload: every step re-runs the chunk
+    forward (cpr_gdn_fwd) over the current chunk's tokens so far, for every sequence, from
+    the committed chunk-start state, and the chunk's last step commits the next state.  One
+    chunk of 64 steps after the 2048-token prefill; each step's packed batch of (p + 1) rows
+    per sequence is laid out before timing."""
+
+    def __init__(self, dev):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("decode")
+        H, d = WORKLOADS["decode"]["H"], WORKLOADS["decode"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3)
+        n_seq = len(self.lens)
+        full = [L + C for L in self.lens]
+        xd = make_inputs(full, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        cu = xd.cu_seqlens.tolist()
+        pre = torch.cat([torch.arange(cu[b], cu[b] + self.lens[b]) for b in range(n_seq)]).to(dev)
+        cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(self.lens), 0).tolist(), dtype=torch.int32,
+                              device=dev)
+        _, self.h0 = cpr.cpr_gdn_fwd(xd.q[pre], xd.k[pre], xd.v[pre], xd.g[pre], xd.beta[pre], cu_pre,
+                                     contract=self.c)
+        o_full, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=self.c,
+                                    want_final=False)
+        self.batches, self.ref = [], []
+        for p in range(C):
+            idx = torch.cat([torch.arange(cu[b] + self.lens[b], cu[b] + self.lens[b] + p + 1)
+                             for b in range(n_seq)]).to(dev)
+            cub = torch.arange(0, n_seq + 1, dtype=torch.int32, device=dev) * (p + 1)
+            n_tok = n_seq * (p + 1)
+            last = torch.tensor([cu[b] + self.lens[b] + p for b in range(n_seq)], device=dev)
+            self.batches.append(dict(q=xd.q[idx], k=xd.k[idx], v=xd.v[idx], g=xd.g[idx], beta=xd.beta[idx],
+                                     cu=cub, o=torch.empty(n_tok, H, d, device=dev),
+                                     last=cub[1:].long() - 1))
+            self.ref.append(o_full.index_select(0, last))
+        self.ws = torch.empty(cpr.workspace_bytes(self.c, cpr.CPR_OP_FWD, n_seq, n_seq * C, H),
+                              dtype=torch.uint8, device=dev)
+        self.fin = torch.empty_like(self.h0)
+        del o_full
+        self.t = 0
+        torch.cuda.synchronize()
+
+    def run(self):
+        p = self.t % C
+        bt = self.batches[p]
+        self.cpr.cpr_gdn_fwd(bt["q"], bt["k"], bt["v"], bt["g"], bt["beta"], bt["cu"], h0=self.h0,
+                             contract=self.c, out=bt["o"], final=self.fin if p == C - 1 else None,
+                             want_final=p == C - 1, workspace=self.ws)
+        self.t += 1
+
+    def bitwise(self):
+        """Each step's output row (the last row of every sequence's packed chunk) against the
+        one-shot forward over the full sequences."""
+        return bool(all(torch.equal(bt["o"].index_select(0, bt["last"]).view(torch.int32), r.view(torch.int32))
+                        for bt, r in zip(self.batches, self.ref)))
+
+
+class RecurrentDecode:
+    """"Recurrent everywhere" decode on the Decode workload: a token-recurrent prefill of the
+    2048 tokens, then token-recurrent steps on its state; compared bit for bit with the
+    token recurrence over the full sequences."""
+
+    def __init__(self, dev, n_steps):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("decode")
+        H, d = WORKLOADS["decode"]["H"], WORKLOADS["decode"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d)
+        full = [L + n_steps for L in self.lens]
+        xd = make_inputs(full, H, d, d, io_dtype=torch.bfloat16, seed=0).to(dev)
+        cu = xd.cu_seqlens.tolist()
+        n_seq = len(self.lens)
+        sel = torch.cat([torch.arange(cu[b], cu[b] + self.lens[b]) for b in range(n_seq)]).to(dev)
+        cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(self.lens), 0).tolist(), dtype=torch.int32,
+                              device=dev)
+        _, self.state = cpr.cpr_gdn_recurrent_fwd(xd.q[sel], xd.k[sel], xd.v[sel], xd.g[sel], xd.beta[sel],
+                                                  cu_pre, contract=self.c)
+        idx = torch.tensor([[cu[b] + self.lens[b] + t for b in range(n_seq)] for t in range(n_steps)],
+                           device=dev).reshape(-1)
+        self.tok = [t.index_select(0, idx).view(n_steps, n_seq, *t.shape[1:]).contiguous()
+                    for t in (xd.q, xd.k, xd.v, xd.g, xd.beta)]
+        self.o_steps = torch.empty(n_steps, n_seq, H, d, device=dev)
+        o_full, _ = cpr.cpr_gdn_recurrent_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=self.c,
+                                              want_final=False)
+        self.ref = o_full.index_select(0, idx).view_as(self.o_steps)
+        self.t = 0
+        torch.cuda.synchronize()
+
+    def run(self):
+        q, k, v, g, b = (x[self.t] for x in self.tok)
+        self.cpr.cpr_gdn_recurrent_step(q, k, v, g, b, self.state, contract=self.c, out=self.o_steps[self.t])
+        self.t += 1
+
+
+class RecurrentTrainer:
+    """"Recurrent everywhere" training on the Trainer workload: the token recurrence
+    forward (outputs) and its reverse recurrence (every gradient), per (sequence, head)."""
+
+    def __init__(self, dev):
+        import infer_consistent_linear_gb300 as cpr
+        from infer_consistent_linear_gb300.synth import make_inputs
+        self.cpr = cpr
+        self.lens = workload_lens("trainer")
+        H, d = WORKLOADS["trainer"]["H"], WORKLOADS["trainer"]["d"]
+        self.c = cpr.default_contract(torch.bfloat16, d)
+        self.xd = make_inputs(self.lens, H, d, d, io_dtype=torch.bfloat16, seed=0, with_grad=True).to(dev)
+        n_tok, n_seq = sum(self.lens), len(self.lens)
+        self.ws = torch.empty(cpr.recurrent_bwd_workspace_bytes(self.c, n_seq, n_tok, H), dtype=torch.uint8,
+                              device=dev)
+        self.o = torch.empty(n_tok, H, d, device=dev)
+        self.outs = dict(dq=torch.empty(n_tok, H, d, device=dev), dk=torch.empty(n_tok, H, d, device=dev),
+                         dv=torch.empty(n_tok, H, d, device=dev), dg=torch.empty(n_tok, H, device=dev),
+                         dbeta=torch.empty(n_tok, H, device=dev), dh0=torch.empty(n_seq, H, d, d, device=dev))
+        torch.cuda.synchronize()
+
+    def run(self):
+        x = self.xd
+        self.cpr.cpr_gdn_recurrent_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=self.c,
+                                       want_final=False)
+        self.cpr.cpr_gdn_recurrent_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, contract=self.c,
+                                       workspace=self.ws, outs=self.outs)
+
+
 class RecurrentPrefill:
     """"Recurrent everywhere" on the Prefill workload: the token recurrence over each
     whole sequence."""
@@ -844,7 +1012,8 @@ class ReadingB:
 class ReadingBDecode:
     """Reading B's decode on the Decode workload: a reading-B prefill of every sequence
     (the decode cache also keeps the running in-chunk state), then decode steps under the
-    same contract (the chunk-form step, then one token of the recurrence)."""
+    same contract (one token of the recurrence; the chunk form commits each completed
+    chunk)."""
 
     def __init__(self, dev, n_steps):
         import infer_consistent_linear_gb300 as cpr
@@ -894,9 +1063,9 @@ def reading_b(dev, world, reading_a_ms):
     try:   # reading B's decode step on the Decode workload (its bits are checked in the GPU tests)
         K, W = 64, 3
         rd = ReadingBDecode(dev, K + W)
-        ms_d, _ = time_device(rd, K, W, world, profile=False)
+        ms_d, prof_d = time_device(rd, K, W, world, profile=True)
         res["decode"] = {"workload": WORKLOADS["decode"]["desc"], "us_per_step": round(ms_d * 1e3, 3),
-                         "steps": K, "error_word": rb_err(rd.cpr)}
+                         "steps": K, "error_word": rb_err(rd.cpr), "kernels": kernel_table(prof_d, ms_d)}
         del rd
     except Exception as e:   # reported, not fatal to the bench line
         res["decode"] = {"error": f"{type(e).__name__}: {e}"}
@@ -927,10 +1096,29 @@ def stage_table(dev, world, pk, cpr_prefill_ms, sec):
                                   "frac": round(byt / (us_launch * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                                   "algo_bytes_per_launch": byt}}
     del nd
+    torch.cuda.empty_cache()
+    cw = ChunkwiseDecode(dev)
+    ms_cw, prof_cw = time_device(cw, C - 3, 3, world, profile=True)
+    chunkwise_decode = {"us_per_step": round(ms_cw * 1e3, 3), "bitwise_decode_vs_prefill": cw.bitwise(),
+                        "steps": C - 3, "kernels": kernel_table(prof_cw, ms_cw)}
+    del cw
+    torch.cuda.empty_cache()
+    rd = RecurrentDecode(dev, K + W)
+    ms_rd, _ = time_device(rd, K, W, world, profile=False)
+    rec_decode = {"us_per_step": round(ms_rd * 1e3, 3),
+                  "bitwise_decode_vs_prefill": bool(torch.equal(rd.ref.view(torch.int32),
+                                                                rd.o_steps.contiguous().view(torch.int32)))}
+    del rd
+    torch.cuda.empty_cache()
     rp = RecurrentPrefill(dev)
     ms_p, _ = time_device(rp, 3, 2, world, profile=False)
     tok = sum(rp.lens)
     del rp
+    torch.cuda.empty_cache()
+    rt = RecurrentTrainer(dev)
+    ms_t, prof_t = time_device(rt, 2, 1, world, profile=True)
+    tok_t = sum(rt.lens)
+    del rt
     torch.cuda.empty_cache()
     cpr_dec = sec.get("decode", {})
     cpr_tr = sec.get("trainer", {})
@@ -942,11 +1130,23 @@ def stage_table(dev, world, pk, cpr_prefill_ms, sec):
                          "decode_us_per_step": native_decode["us_per_step"],
                          "bitwise_decode_vs_prefill": native_decode["bitwise_decode_vs_prefill"],
                          "decode_roofline": native_decode["roofline"]},
+        "chunkwise_everywhere": {"prefill_ms": round(cpr_prefill_ms, 4),
+                                 "trainer_fwd_bwd_ms": cpr_tr.get("ms_per_step"),
+                                 "decode_us_per_step": chunkwise_decode["us_per_step"],
+                                 "bitwise_decode_vs_prefill": chunkwise_decode["bitwise_decode_vs_prefill"],
+                                 "decode_kernels": chunkwise_decode["kernels"]},
         "recurrent_everywhere": {"prefill_ms": round(ms_p, 4),
-                                 "prefill_tokens_per_s": round(tok / (ms_p * 1e-3) * world, 1)},
-        "note": "native mixed shares this build's chunked prefill and trainer kernels (CPR's "
-                "constraints change only how decode reaches its bits); its decode is the token "
-                "recurrence on the prefill's fp32 states",
+                                 "prefill_tokens_per_s": round(tok / (ms_p * 1e-3) * world, 1),
+                                 "trainer_fwd_bwd_ms": round(ms_t, 4),
+                                 "trainer_tokens_per_s": round(tok_t / (ms_t * 1e-3) * world, 1),
+                                 "trainer_kernels": kernel_table(prof_t, ms_t),
+                                 "decode_us_per_step": rec_decode["us_per_step"],
+                                 "bitwise_decode_vs_prefill": rec_decode["bitwise_decode_vs_prefill"]},
+        "note": "native mixed and chunkwise everywhere share this build's chunked prefill and "
+                "trainer kernels; native mixed decodes with the token recurrence on the prefill's "
+                "fp32 states (no resynchronisation), chunkwise everywhere re-runs the chunk forward "
+                "over the current chunk every step, recurrent everywhere runs the token recurrence "
+                "in every stage",
     }
 
 

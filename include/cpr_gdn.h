@@ -172,6 +172,20 @@ int cpr_contract_check(const cpr_contract* c);
  * implementation against other SHA-256 implementations). */
 int cpr_sha256(const void* data, size_t len, uint8_t out[32]);
 
+/* Deployment identity (page "IsoExec: 切换 SkyRL 中的训练器-推理不匹配", section
+ * "合约结构与强制执行": the contract's identities are SHA-256 digests, one of them over
+ * the deployment the numerical policy runs on).  SHA-256 of the canonical text
+ *   CPR-GDN-DEPLOYMENT;arch=sm_103a;cc=<major>.<minor>;gpu=<device name>;
+ *   cudart=<runtime version>;driver=<driver version>;kernel_build_id=<id>
+ * (one line, no spaces added) for the CURRENT device.  A decode cache carries the
+ * deployment digest of the process that wrote it (header words 17..24); a decode
+ * step on another deployment -- another build of this library, GPU model, CUDA
+ * runtime or driver -- refuses it on the device like a foreign contract
+ * (CPR_ERR_CONTRACT_MISMATCH recorded, nothing written).  Writes the digest to out
+ * and, when text != NULL, the canonical text (truncated to text_len - 1 bytes,
+ * NUL-terminated).  CPR_ERR_CUDA when no CUDA device is usable. */
+int cpr_deployment_digest(uint8_t out[32], char* text, size_t text_len);
+
 /* ---- workspace and decode cache sizes --------------------------------- */
 #define CPR_OP_FWD 1   /* cpr_gdn_fwd and cpr_gdn_prefill */
 #define CPR_OP_BWD 2   /* cpr_gdn_bwd, cpr_gdn_fwd_train, cpr_gdn_bwd_saved */
@@ -207,6 +221,15 @@ typedef struct cpr_cache_layout {
     size_t delta_tiles; /* bf16   [n_seq, H] x 32 KB: the Delta rows as hi/lo operand tiles */
     size_t run;         /* fp32   [n_seq, H, d_k, d_v] running in-chunk state (TOKENREC_V1
                            contracts; 0 and absent otherwise)                     */
+    /* TOKENREC_V1 contracts only (0 and absent otherwise): the current chunk's token rows,
+       token-major (row b * C + r of sequence b), which the decode step appends to and the
+       chunk commit reads, and the commit's own scratch: */
+    size_t rb_k;        /* io     [n_seq * C, H, d_k]                              */
+    size_t rb_v;        /* io     [n_seq * C, H, d_v]                              */
+    size_t rb_g;        /* fp32   [n_seq * C, H]                                   */
+    size_t rb_beta;     /* fp32   [n_seq * C, H]                                   */
+    size_t rb_cu;       /* int32  [n_seq + 1]  b * C                               */
+    size_t rb_ws;       /* the forward workspace of a batch of n_seq full chunks   */
 } cpr_cache_layout;
 
 int cpr_decode_cache_layout(const cpr_contract* c, int n_seq, int H, cpr_cache_layout* out);
@@ -395,6 +418,25 @@ int cpr_gdn_recurrent_fwd(const cpr_contract* c, const void* q, const void* k, c
 int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k_t,
                            const void* v_t, const float* g_t, const float* beta_t, int n_seq,
                            int H, float* state, float* o_t, void* stream);
+
+/* Backward of cpr_gdn_recurrent_fwd ("recurrent everywhere" training): the adjoint
+ * of each token update, walked from the last token back (the reverse recurrence:
+ * Shat += do q^T, dq = scale S_t^T do, e = v - a S_{t-1} k, sk = Shat k, dv = b sk,
+ * dbeta = e . sk, dk = b Shat^T e - a b S_{t-1}^T sk, dg = a (<Shat, S_{t-1}> - b sk .
+ * S_{t-1} k), Shat = a (Shat - b sk k^T); dh0 = the final Shat^T).  S_{t-1} and S_t are
+ * the recurrent forward's states bit for bit, recomputed from checkpoints the call
+ * keeps every 16 tokens in `workspace` (cpr_gdn_recurrent_bwd_workspace_size bytes,
+ * 256-byte aligned, caller-owned).  h0, dHT may be NULL (zeros).  dO and every
+ * gradient are fp32 in the layouts of cpr_gdn_bwd; deterministic, one CTA per
+ * (sequence, head).  Errors as cpr_gdn_recurrent_fwd, plus CPR_ERR_WORKSPACE. */
+int cpr_gdn_recurrent_bwd_workspace_size(const cpr_contract* c, int n_seq, int64_t n_tok, int H,
+                                         size_t* bytes);
+int cpr_gdn_recurrent_bwd(const cpr_contract* c, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const int32_t* cu_seqlens,
+                          int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
+                          const float* dHT, float* dq, float* dk, float* dv, float* dg,
+                          float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* ---- batch-invariant projection GEMM ------------------------------------
  * Y = X W for the projections that feed the CPR layer (page "IsoExec: 切换

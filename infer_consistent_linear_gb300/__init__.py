@@ -57,7 +57,8 @@ class Contract(ctypes.Structure):
 class CacheLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "total_bytes", "header", "pos", "done", "state", "k_rows", "v_rows", "gam_rows",
-        "beta_rows", "t_rows", "delta_rows", "state_tiles", "delta_tiles", "run")]
+        "beta_rows", "t_rows", "delta_rows", "state_tiles", "delta_tiles", "run", "rb_k", "rb_v",
+        "rb_g", "rb_beta", "rb_cu", "rb_ws")]
 
 
 class KernelTime(ctypes.Structure):
@@ -86,6 +87,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_contract_digest": (I, [CP, P]),
         "cpr_contract_check": (I, [CP]),
         "cpr_sha256": (I, [P, SZ, P]),
+        "cpr_deployment_digest": (I, [P, ctypes.c_char_p, SZ]),
         "cpr_gdn_workspace_size": (I, [CP, I, I, I64, I, ctypes.POINTER(SZ)]),
         "cpr_decode_cache_layout": (I, [CP, I, I, ctypes.POINTER(CacheLayout)]),
         "cpr_decode_cache_bytes": (I, [CP, I, I, ctypes.POINTER(SZ)]),
@@ -99,6 +101,9 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_recurrent_fwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
         "cpr_gdn_recurrent_step": (I, [CP, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gemm_bf16": (I, [P, P, P, I, I, I, I, P]),
+        "cpr_gdn_recurrent_bwd_workspace_size": (I, [CP, I, I64, I, ctypes.POINTER(SZ)]),
+        "cpr_gdn_recurrent_bwd": (I, [CP, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
+                                      P, SZ, P]),
         "cpr_gdn_bwd_saved": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                                   P, SZ, P]),
         "cpr_gdn_fwd_noalloc": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P]),
@@ -168,6 +173,16 @@ def sha256(data: bytes) -> bytes:
     buf = ctypes.create_string_buffer(data, len(data))
     _check(lib.cpr_sha256(buf, len(data), out))
     return bytes(out)
+
+
+def deployment_digest():
+    """(digest, canonical text) of the current device's deployment identity: the compiled
+    arch, the GPU, the CUDA runtime and driver and this library's kernel build."""
+    lib = load_library()
+    out = (ctypes.c_uint8 * 32)()
+    text = ctypes.create_string_buffer(256)
+    _check(lib.cpr_deployment_digest(out, text, 256))
+    return bytes(out), text.value.decode()
 
 
 def workspace_bytes(c: Contract, op: int, n_seq: int, n_tok: int, H: int) -> int:
@@ -494,6 +509,51 @@ def cpr_gdn_recurrent_step(q_t, k_t, v_t, g_t, beta_t, state, contract: Optional
     _check(lib.cpr_gdn_recurrent_step(ctypes.byref(c), _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(g_t),
                                       _ptr(beta_t), n_seq, H, _ptr(state), _ptr(o), _stream()))
     return o
+
+
+def recurrent_bwd_workspace_bytes(c: Contract, n_seq: int, n_tok: int, H: int) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib.cpr_gdn_recurrent_bwd_workspace_size(ctypes.byref(c), n_seq, n_tok, H, ctypes.byref(n)))
+    return n.value
+
+
+def cpr_gdn_recurrent_bwd(q, k, v, g, beta, cu_seqlens, dO, h0=None, dHT=None,
+                          contract: Optional[Contract] = None, workspace=None, outs=None):
+    """Stage-table ablation "recurrent everywhere", training: the backward of
+    cpr_gdn_recurrent_fwd by the reverse token recurrence (cpr_gdn_recurrent_bwd).  Returns
+    dict dq, dk, dv, dg, dbeta, dh0 (fp32)."""
+    lib = load_library()
+    c = contract or default_contract(q.dtype, q.shape[-1], v.shape[-1])
+    specs, n_tok, H = _tok_specs(c, q, k, v, g, beta, cu_seqlens, h0)
+    n_seq = int(cu_seqlens.numel() - 1)
+    if dO is None:
+        raise CprError(CPR_ERR_INVALID_ARG, "dO is required")
+    specs += [("dO", dO, torch.float32, (n_tok, H, c.d_v)), ("dHT", dHT, torch.float32, (n_seq, H, c.d_k, c.d_v))]
+    if outs is not None:
+        specs += [(name, outs.get(name), torch.float32, shape) for name, shape in (
+            ("dq", (n_tok, H, c.d_k)), ("dk", (n_tok, H, c.d_k)), ("dv", (n_tok, H, c.d_v)),
+            ("dg", (n_tok, H)), ("dbeta", (n_tok, H)), ("dh0", (n_seq, H, c.d_k, c.d_v)))]
+    if workspace is not None:
+        specs.append(_blob("workspace", workspace))
+    _validate(specs)
+    need = recurrent_bwd_workspace_bytes(c, n_seq, n_tok, H)
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    if outs is None:
+        outs = dict(dq=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
+                    dk=torch.empty(n_tok, H, c.d_k, dtype=torch.float32, device=dev),
+                    dv=torch.empty(n_tok, H, c.d_v, dtype=torch.float32, device=dev),
+                    dg=torch.empty(n_tok, H, dtype=torch.float32, device=dev),
+                    dbeta=torch.empty(n_tok, H, dtype=torch.float32, device=dev),
+                    dh0=torch.empty(n_seq, H, c.d_k, c.d_v, dtype=torch.float32, device=dev))
+    _check(lib.cpr_gdn_recurrent_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                     _ptr(cu_seqlens), n_seq, n_tok, H, _ptr(h0), _ptr(dO), _ptr(dHT),
+                                     _ptr(outs["dq"]), _ptr(outs["dk"]), _ptr(outs["dv"]), _ptr(outs["dg"]),
+                                     _ptr(outs["dbeta"]), _ptr(outs["dh0"]), _ptr(workspace),
+                                     workspace.numel(), _stream()))
+    return outs
 
 
 def cpr_gemm(x, w, leaf_k: int, out=None):

@@ -167,6 +167,14 @@ WsLayout ws_layout(const cpr_contract& c, int op, int n_seq, int64_t n_tok, int 
     return w;
 }
 
+// Workspace of a reading-B decode commit: a forward of n_seq full chunks under the chunk
+// form's own contract (ROWSEQ_V1).
+WsLayout commit_ws(const cpr_contract& c, int n_seq, int H) {
+    cpr_contract a = c;
+    a.intra_order = CPR_ORDER_ROWSEQ_V1;
+    return ws_layout(a, CPR_OP_FWD, n_seq, (int64_t)n_seq * (int64_t)c.chunk_size, H);
+}
+
 cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
     cpr_cache_layout l{};
     const size_t C = c.chunk_size, dk = c.d_k, dv = c.d_v, io = io_size(c.io_dtype);
@@ -185,7 +193,17 @@ cpr_cache_layout cache_layout(const cpr_contract& c, int n_seq, int H) {
     add(l.delta_rows, sh * C * dv * 4);
     add(l.state_tiles, sh * dk * dv * 4);   // bf16 hi + lo operand tiles of the state
     add(l.delta_tiles, sh * C * dv * 4);    // bf16 hi + lo operand tiles of the Delta rows
-    if (c.intra_order == CPR_ORDER_TOKENREC_V1) add(l.run, sh * dk * dv * 4);   // running in-chunk state
+    if (c.intra_order == CPR_ORDER_TOKENREC_V1) {
+        add(l.run, sh * dk * dv * 4);   // running in-chunk state
+        // the current chunk's token rows and the chunk commit's workspace (a forward of
+        // n_seq full chunks under the chunk form's own contract)
+        add(l.rb_k, sh * C * dk * io);
+        add(l.rb_v, sh * C * dv * io);
+        add(l.rb_g, sh * C * 4);
+        add(l.rb_beta, sh * C * 4);
+        add(l.rb_cu, 4 * ((size_t)n_seq + 1));
+        add(l.rb_ws, commit_ws(c, n_seq, H).total);
+    }
     l.total_bytes = off;
     return l;
 }
@@ -206,13 +224,58 @@ cpr::Digest digest_words(const uint8_t* d) {
     return w;
 }
 
-void header_words(const cpr_contract& c, int n_seq, int H, uint32_t out[7]) {
-    out[0] = (uint32_t)n_seq; out[1] = (uint32_t)H; out[2] = c.chunk_size; out[3] = c.d_k;
-    out[4] = c.d_v; out[5] = c.operand_policy; out[6] = c.io_dtype;
-}
-
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(CPR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// The one -gencode target this library is compiled for (the build passes only it).
+constexpr const char* kBuildArch = "sm_103a";
+
+// Deployment identity of the current device: SHA-256 of a canonical text naming what the
+// numerical policy runs on (the compiled arch, the device's compute capability and name,
+// the CUDA runtime and driver versions, the kernel build).  Worked out once per device.
+struct Deployment {
+    bool ok = false;
+    uint8_t digest[32];
+    char text[256];
+};
+
+int deployment_of_current_device(const Deployment** out) {
+    static std::mutex mu;
+    static Deployment dep[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "deployment identity: no CUDA device");
+    if (dev < 0 || dev >= 64) return fail(CPR_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    Deployment& d = dep[dev];
+    if (!d.ok) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "deployment identity: device properties");
+        int rt = 0, drv = 0;
+        e = cudaRuntimeGetVersion(&rt);
+        if (e == cudaSuccess) e = cudaDriverGetVersion(&drv);
+        if (e != cudaSuccess) return cuda_fail(e, "deployment identity: versions");
+        snprintf(d.text, sizeof(d.text),
+                 "CPR-GDN-DEPLOYMENT;arch=%s;cc=%d.%d;gpu=%s;cudart=%d;driver=%d;kernel_build_id=%u",
+                 kBuildArch, prop.major, prop.minor, prop.name, rt, drv, kKernelBuildId);
+        cpr::sha256(d.text, std::strlen(d.text), d.digest);
+        d.ok = true;
+    }
+    *out = &d;
+    return CPR_OK;
+}
+
+// Header words 10..24 of a decode cache for this contract and batch on the current device.
+int header_words(const cpr_contract& c, int n_seq, int H, uint32_t out[cpr::kHdrWords]) {
+    out[0] = (uint32_t)n_seq; out[1] = (uint32_t)H; out[2] = c.chunk_size; out[3] = c.d_k;
+    out[4] = c.d_v; out[5] = c.operand_policy; out[6] = c.io_dtype;
+    const Deployment* d = nullptr;
+    const int rc = deployment_of_current_device(&d);
+    if (rc) return rc;
+    std::memcpy(out + 7, d->digest, 32);
+    return CPR_OK;
 }
 
 #define REQ_PTR(p)                                                             \
@@ -281,7 +344,11 @@ int forward_impl(const cpr_contract* c, const uint8_t* digest, const void* q, co
     sa.cu = cu; sa.n_seq = n_seq; sa.n_tok = n_tok;
     sa.chunk_off = reinterpret_cast<int32_t*>(wsb + w.chunk_off);
     sa.cache = static_cast<uint8_t*>(cache); sa.co = to_off(cl);
-    sa.digest = digest_words(digest); header_words(*c, n_seq, H, sa.hdr); sa.err = err;
+    sa.digest = digest_words(digest); sa.err = err;
+    if (cache) {
+        rc = header_words(*c, n_seq, H, sa.hdr);
+        if (rc) return rc;
+    }
     cudaError_t e = launch_setup(sa, st);
     if (e != cudaSuccess) return cuda_fail(e, "setup launch");
 
@@ -337,35 +404,97 @@ int reading_b_forward(const cpr_contract* c, const uint8_t* digest, const void* 
     a.run = cache ? reinterpret_cast<float*>(static_cast<uint8_t*>(cache) + cache_layout(*c, n_seq, H).run)
                   : nullptr;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cpr::ProfScope ps("cpr_reading_b", st);
-    const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
+    {
+        cpr::ProfScope ps("cpr_reading_b", st);
+        const cudaError_t e = cpr::rb_launch(a, n_tok > 0 ? w.cmax : 0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "reading-B launch");
+    }
+    if (!cache) return CPR_OK;
+    // the decode steps continue from the cache: the partial last chunk's token rows, and
+    // the chunk table of the commit batch (n_seq full chunks)
+    const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
+    uint8_t* cb = static_cast<uint8_t*>(cache);
+    cpr::rec::RbFillArgs f{};
+    f.k = a.k; f.v = a.v; f.g = g; f.beta = beta; f.cu = cu_seqlens; f.n_seq = n_seq; f.H = H;
+    f.rk = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_k); f.rv = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_v);
+    f.rg = reinterpret_cast<float*>(cb + cl.rb_g); f.rbeta = reinterpret_cast<float*>(cb + cl.rb_beta);
+    f.rcu = reinterpret_cast<int32_t*>(cb + cl.rb_cu);
+    cudaError_t e;
+    {
+        cpr::ProfScope ps("cpr_reading_b_fill", st);
+        e = cpr::rb_fill_launch(f, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B fill launch");
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    cpr::simt::SetupArgs sa{};
+    sa.cu = f.rcu; sa.n_seq = n_seq; sa.n_tok = (int64_t)n_seq * c->chunk_size;
+    sa.chunk_off = reinterpret_cast<int32_t*>(cb + cl.rb_ws + commit_ws(*c, n_seq, H).chunk_off);
+    sa.err = err;
+    e = launch_setup(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "setup launch");
     return CPR_OK;
 }
 
-// After the CPR decode step (which keeps the cache, commits full chunks and moves the
-// positions on): one token of the recurrence per (sequence, head) on the running state,
-// restarted at a chunk's first row from hi + lo of the cache's chunk-start state tiles.
+// Reading B's decode step: the token recurrence on the running state (k_rb_step, which
+// also appends the token's rows to the cache and moves the positions on), then the chunk
+// commit -- the chunk form's prep and state pass over the buffered rows of every sequence
+// whose chunk this token completed, from its fp32 chunk-start state to the next one (the
+// prefill's kernels and inputs, so the prefill's bits).  The commit kernels run every step
+// and return at once for the other sequences; a cache with another header is refused by
+// every kernel before it reads past the header.
 int reading_b_step(const cpr_contract* c, const uint8_t* digest, const void* q_t, const void* k_t,
                    const void* v_t, const float* g_t, const float* beta_t, int n_seq, int H,
                    void* cache, void* o_t, void* stream) {
+    int rc = check_digest(c, digest);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, 0, H);
+    if (rc) return rc;
+    REQ_PTR(cache);
     if (n_seq == 0) return CPR_OK;
+    REQ_PTR(q_t); REQ_PTR(k_t); REQ_PTR(v_t); REQ_PTR4(g_t); REQ_PTR4(beta_t); REQ_PTR(o_t);
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
     const cpr_cache_layout cl = cache_layout(*c, n_seq, H);
     uint8_t* cb = static_cast<uint8_t*>(cache);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cpr::rec::RbStepArgs a{};
     a.header = reinterpret_cast<const uint32_t*>(cb + cl.header);
     std::memcpy(a.digest, digest, 32);
-    header_words(*c, n_seq, H, a.hdr);
+    rc = header_words(*c, n_seq, H, a.hdr);
+    if (rc) return rc;
+    static_assert(sizeof(a.hdr) == sizeof(uint32_t) * cpr::kHdrWords, "header words");
     a.q = static_cast<const __nv_bfloat16*>(q_t); a.k = static_cast<const __nv_bfloat16*>(k_t);
     a.v = static_cast<const __nv_bfloat16*>(v_t); a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
-    a.scale = c->scale; a.pos = reinterpret_cast<const int32_t*>(cb + cl.pos);
-    a.state_tiles = cb + cl.state_tiles;
-    a.dvs = (int)(c->d_v / c->dv_splits); a.run = reinterpret_cast<float*>(cb + cl.run);
-    a.o = static_cast<float*>(o_t);
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cpr::ProfScope ps("cpr_reading_b_step", st);
-    const cudaError_t e = cpr::rb_step_launch(a, st);
+    a.scale = c->scale; a.pos = reinterpret_cast<int32_t*>(cb + cl.pos);
+    a.done = reinterpret_cast<uint32_t*>(cb + cl.done);
+    a.state = reinterpret_cast<const float*>(cb + cl.state); a.run = reinterpret_cast<float*>(cb + cl.run);
+    a.rk = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_k); a.rv = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_v);
+    a.rg = reinterpret_cast<float*>(cb + cl.rb_g); a.rbeta = reinterpret_cast<float*>(cb + cl.rb_beta);
+    a.o = static_cast<float*>(o_t); a.err = err;
+    cudaError_t e;
+    {
+        cpr::ProfScope ps("cpr_reading_b_step", st);
+        e = cpr::rb_step_launch(a, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "reading-B step launch");
+    // the commit: n_seq full chunks from the token rows; only completed ones run
+    const WsLayout w = commit_ws(*c, n_seq, H);
+    cpr::tc::TcArgs t{};
+    t.q = a.rk;   // (q is not needed for the state: these rows are finite, P goes unused)
+    t.k = a.rk; t.v = a.rv; t.g = a.rg; t.beta = a.rbeta;
+    t.cu = reinterpret_cast<const int32_t*>(cb + cl.rb_cu);
+    t.chunk_off = reinterpret_cast<const int32_t*>(cb + cl.rb_ws + w.chunk_off);
+    t.n_seq = n_seq; t.H = H; t.dvs = (int)(c->d_v / c->dv_splits); t.scale = c->scale;
+    t.ws = cb + cl.rb_ws + w.W; t.blk_bytes = cpr::tc::kBlock; t.train = false;
+    t.h0 = reinterpret_cast<const float*>(cb + cl.state);
+    t.final_state = reinterpret_cast<float*>(cb + cl.state);   // in place (each thread its own entries)
+    t.o = nullptr; t.cache = nullptr; t.err = err;
+    t.commit_pos = a.pos; t.commit_header = a.header;
+    std::memcpy(t.commit_words, a.digest, 32);
+    std::memcpy(t.commit_words + 8, a.hdr, sizeof(a.hdr));
+    e = cpr::tc_forward(t, n_seq, n_seq, H, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading-B commit launch");
     return CPR_OK;
 }
 
@@ -425,6 +554,19 @@ int cpr_contract_digest(const cpr_contract* c, uint8_t out[32]) {
 }
 
 int cpr_contract_check(const cpr_contract* c) { return check_contract(c); }
+
+int cpr_deployment_digest(uint8_t out[32], char* text, size_t text_len) {
+    if (!out) return fail(CPR_ERR_INVALID_ARG, "out is NULL");
+    const Deployment* d = nullptr;
+    const int rc = deployment_of_current_device(&d);
+    if (rc) return rc;
+    std::memcpy(out, d->digest, 32);
+    if (text && text_len) {
+        std::strncpy(text, d->text, text_len - 1);
+        text[text_len - 1] = '\0';
+    }
+    return CPR_OK;
+}
 
 int cpr_sha256(const void* data, size_t len, uint8_t out[32]) {
     if ((!data && len) || !out) return fail(CPR_ERR_INVALID_ARG, "NULL argument");
@@ -517,7 +659,9 @@ static int decode_impl(const cpr_contract* c, const uint8_t* digest, const void*
         t.q = static_cast<const __nv_bfloat16*>(q_t); t.k = static_cast<const __nv_bfloat16*>(k_t);
         t.v = static_cast<const __nv_bfloat16*>(v_t); t.g = g_t; t.beta = beta_t;
         t.n_seq = n_seq; t.H = H; t.scale = c->scale; t.cache = static_cast<uint8_t*>(cache);
-        t.co = to_off(cl); t.digest = digest_words(digest); header_words(*c, n_seq, H, t.hdr);
+        t.co = to_off(cl); t.digest = digest_words(digest);
+        rc = header_words(*c, n_seq, H, t.hdr);
+        if (rc) return rc;
         t.o = static_cast<float*>(o_t); t.err = err;
         const cudaError_t e = cpr::tc_decode_step(t, (int)(c->d_v / c->dv_splits),
                                                   static_cast<cudaStream_t>(stream));
@@ -527,7 +671,9 @@ static int decode_impl(const cpr_contract* c, const uint8_t* digest, const void*
     cpr::simt::DecArgs a{};
     a.q = q_t; a.k = k_t; a.v = v_t; a.g = g_t; a.beta = beta_t; a.n_seq = n_seq; a.H = H;
     a.scale = c->scale; a.cache = static_cast<uint8_t*>(cache); a.co = to_off(cl);
-    a.digest = digest_words(digest); header_words(*c, n_seq, H, a.hdr);
+    a.digest = digest_words(digest);
+    rc = header_words(*c, n_seq, H, a.hdr);
+    if (rc) return rc;
     a.o = static_cast<float*>(o_t); a.err = err;
     cpr::LaunchCfg L{0, n_seq, H, (int)c->dv_splits, static_cast<cudaStream_t>(stream)};
     const cudaError_t e = ops_for(*c)->decode(a, L);
@@ -664,9 +810,9 @@ int cpr_selftest_wait_timeout(uint32_t poll_limit, uint32_t* completed) {
 int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
                         const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
                         int n_seq, int H, void* cache, void* o_t, void* stream) {
-    const int rc = decode_impl(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
-    if (rc || !reading_b(c)) return rc;
-    return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+    if (reading_b(c))
+        return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+    return decode_impl(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
 }
 
 static int rec_check(const cpr_contract* c) {
@@ -724,6 +870,57 @@ int cpr_gdn_recurrent_step(const cpr_contract* c, const void* q_t, const void* k
     cpr::ProfScope ps("cpr_rec_step", st);
     const cudaError_t e = cpr::rec_launch(a, (int)c->d_k, c->io_dtype == CPR_DTYPE_BF16, st);
     if (e != cudaSuccess) return cuda_fail(e, "recurrent step launch");
+    return CPR_OK;
+}
+
+static size_t rec_bwd_ckpt_bytes(const cpr_contract* c, int n_seq, int64_t n_tok, int H) {
+    return (size_t)(n_tok / cpr::rec::kRecSeg + n_seq) * (size_t)H * c->d_k * c->d_v * 4;
+}
+
+int cpr_gdn_recurrent_bwd_workspace_size(const cpr_contract* c, int n_seq, int64_t n_tok, int H,
+                                         size_t* bytes) {
+    int rc = rec_check(c);
+    if (rc) return rc;
+    rc = check_sizes(n_seq, n_tok, H);
+    if (rc) return rc;
+    if (!bytes) return fail(CPR_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = align256(rec_bwd_ckpt_bytes(c, n_seq, n_tok, H)) +
+             (size_t)n_seq * H * cpr::rec::kRecSeg * c->d_k * c->d_v * 4;
+    return CPR_OK;
+}
+
+int cpr_gdn_recurrent_bwd(const cpr_contract* c, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const int32_t* cu_seqlens,
+                          int n_seq, int64_t n_tok, int H, const float* h0, const float* dO,
+                          const float* dHT, float* dq, float* dk, float* dv, float* dg,
+                          float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    size_t need = 0;
+    int rc = cpr_gdn_recurrent_bwd_workspace_size(c, n_seq, n_tok, H, &need);
+    if (rc) return rc;
+    REQ_PTR4(cu_seqlens);
+    if (n_seq > 0) REQ_PTR(dh0);
+    if (n_tok > 0) {
+        REQ_PTR(q); REQ_PTR(k); REQ_PTR(v); REQ_PTR4(g); REQ_PTR4(beta); REQ_PTR(dO);
+        REQ_PTR(dq); REQ_PTR(dk); REQ_PTR(dv); REQ_PTR4(dg); REQ_PTR4(dbeta);
+    }
+    OPT_PTR(h0); OPT_PTR(dHT);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(CPR_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+    uint32_t* err = device_error_ptr();
+    if (!err) return fail(CPR_ERR_CUDA, "device error word unavailable");
+    cpr::rec::RecBwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens; a.n_seq = n_seq;
+    a.n_tok = n_tok; a.H = H; a.scale = c->scale; a.h0 = h0; a.dO = dO; a.dHT = dHT;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.ckpt = reinterpret_cast<float*>(ws);
+    a.seg = reinterpret_cast<float*>(ws + align256(rec_bwd_ckpt_bytes(c, n_seq, n_tok, H)));
+    a.err = err;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cpr::ProfScope ps("cpr_rec_bwd", st);
+    const cudaError_t e = cpr::rec_bwd_launch(a, (int)c->d_k, c->io_dtype == CPR_DTYPE_BF16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent backward launch");
     return CPR_OK;
 }
 

@@ -74,8 +74,10 @@ struct Digest {
     uint32_t w[8];
 };
 
-// Header words (uint32): [0] magic, [1] version, [2..9] digest, [10] n_seq,
-// [11] H, [12] C, [13] d_k, [14] d_v, [15] operand policy, [16] io dtype.
+// Header words (uint32): [0] magic, [1] version, [2..9] contract digest, [10] n_seq,
+// [11] H, [12] C, [13] d_k, [14] d_v, [15] operand policy, [16] io dtype, [17..24] the
+// deployment digest of the process that wrote the cache (cpr_deployment_digest).
 constexpr uint32_t kCacheMagic = 0x43505243u;
+constexpr int kHdrWords = 15;   // header words 10..24, after the contract digest
 
 }  // namespace cpr

@@ -25,6 +25,36 @@ struct RecArgs {
     uint32_t* err;
 };
 
+// Backward of the token recurrence (cpr_gdn_recurrent_bwd).  States are recomputed from
+// checkpoints every kRecSeg tokens; each segment's states go to a per-(sequence, head)
+// scratch before the segment is walked back.
+constexpr int kRecSeg = 16;
+
+struct RecBwdArgs {
+    const void* q;            // io dtype [n_tok, H, d]
+    const void* k;
+    const void* v;
+    const float* g;           // [n_tok, H]
+    const float* beta;
+    const int32_t* cu;
+    int n_seq;
+    int64_t n_tok;
+    int H;
+    float scale;
+    const float* h0;          // or null (zeros)
+    const float* dO;          // fp32 [n_tok, H, d]
+    const float* dHT;         // or null (zeros)
+    float* dq;                // fp32 [n_tok, H, d]
+    float* dk;
+    float* dv;
+    float* dg;                // fp32 [n_tok, H]
+    float* dbeta;
+    float* dh0;               // fp32 [n_seq, H, d, d]
+    float* ckpt;              // [(n_tok / kRecSeg + n_seq) * H] states of d * d fp32
+    float* seg;               // [n_seq * H * kRecSeg] states of d * d fp32
+    uint32_t* err;
+};
+
 struct RbArgs {               // reading B (d = 128, bf16 io)
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
@@ -46,7 +76,7 @@ struct RbArgs {               // reading B (d = 128, bf16 io)
 struct RbStepArgs {           // reading B decode step (d = 128, bf16 io)
     const uint32_t* header;   // the cache's header words
     uint32_t digest[8];       // the contract's digest and header words the cache must carry
-    uint32_t hdr[7];
+    uint32_t hdr[15];         // (kHdrWords of common.cuh)
     const __nv_bfloat16* q;   // [n_seq, H, d]
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -55,19 +85,41 @@ struct RbStepArgs {           // reading B decode step (d = 128, bf16 io)
     int n_seq;
     int H;
     float scale;
-    const int32_t* pos;                 // the cache's positions (already moved on by this step)
-    const unsigned char* state_tiles;   // the cache's chunk-start state tiles (64 KB per unit)
-    int dvs;                            // d_v columns per split of those tiles
-    float* run;                         // [n_seq, H, d, d] running in-chunk states
+    int32_t* pos;             // the cache's positions (moved on by this step)
+    uint32_t* done;           // the cache's step counter (one word)
+    const float* state;       // the cache's chunk-start states, fp32 [n_seq, H, d, d]
+    float* run;               // [n_seq, H, d, d] running in-chunk states
+    __nv_bfloat16* rk;        // the current chunk's token rows, token-major [n_seq * C, H, d]
+    __nv_bfloat16* rv;
+    float* rg;                // [n_seq * C, H]
+    float* rbeta;
     float* o;
+    uint32_t* err;
+};
+
+struct RbFillArgs {           // reading B prefill: the partial last chunk's rows into a cache
+    const __nv_bfloat16* k;   // the prefill's token tensors
+    const __nv_bfloat16* v;
+    const float* g;
+    const float* beta;
+    const int32_t* cu;
+    int n_seq;
+    int H;
+    __nv_bfloat16* rk;        // as RbStepArgs
+    __nv_bfloat16* rv;
+    float* rg;
+    float* rbeta;
+    int32_t* rcu;             // [n_seq + 1]: b * C, the commit batch's sequence offsets
 };
 
 }  // namespace rec
 
 // d in {64, 128}; io bf16 or fp32.
 cudaError_t rec_launch(const rec::RecArgs& a, int d, bool bf16, cudaStream_t st);
+cudaError_t rec_bwd_launch(const rec::RecBwdArgs& a, int d, bool bf16, cudaStream_t st);
 // grid (chunk slots, H)
 cudaError_t rb_launch(const rec::RbArgs& a, int64_t cmax, cudaStream_t st);
 cudaError_t rb_step_launch(const rec::RbStepArgs& a, cudaStream_t st);
+cudaError_t rb_fill_launch(const rec::RbFillArgs& a, cudaStream_t st);
 
 }  // namespace cpr

@@ -149,7 +149,7 @@ struct SetupArgs {
     uint8_t* cache;
     CacheOff co;
     Digest digest;
-    uint32_t hdr[7];   // n_seq, H, C, d_k, d_v, policy, io dtype
+    uint32_t hdr[kHdrWords];   // n_seq, H, C, d_k, d_v, policy, io dtype, deployment digest
     uint32_t* err;
 };
 
@@ -175,7 +175,7 @@ static __global__ void k_setup(SetupArgs a) {
         hdr[0] = kCacheMagic;
         hdr[1] = CPR_CONTRACT_VERSION;
         for (int i = 0; i < 8; ++i) hdr[2 + i] = a.digest.w[i];
-        for (int i = 0; i < 7; ++i) hdr[10 + i] = a.hdr[i];
+        for (int i = 0; i < kHdrWords; ++i) hdr[10 + i] = a.hdr[i];
     }
     int32_t* pos = reinterpret_cast<int32_t*>(a.cache + a.co.pos);
     uint32_t* done = reinterpret_cast<uint32_t*>(a.cache + a.co.done);
@@ -549,7 +549,7 @@ struct DecArgs {
     uint8_t* cache;
     CacheOff co;
     Digest digest;
-    uint32_t hdr[7];
+    uint32_t hdr[kHdrWords];
     float* o;
     uint32_t* err;
 };
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     if (tid == 0) {
         bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
         for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
-        for (int i = 0; i < 7; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
+        for (int i = 0; i < kHdrWords; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
         const int p = ok ? pos[b] : -1;
         if (!(p >= 0 && p < C)) ok = false;
         if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);

@@ -48,7 +48,7 @@ struct TcDecArgs {
     uint8_t* cache;
     CacheOff co;
     Digest digest;
-    uint32_t hdr[7];
+    uint32_t hdr[kHdrWords];
     float* o;
     uint32_t* err;
 };
@@ -93,13 +93,12 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
         }
         uint4 hi, lo;
         split8(x, hi, lo);
-        const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
         if (st) {
-            const uint32_t off = (uint32_t)sp * DVS * 256 + mn_off(jl, rr, DVS);
+            const uint32_t off = mn_off(j8 * 8, rr, D);
             *reinterpret_cast<uint4*>(ct + off) = hi;
             *reinterpret_cast<uint4*>(ct + 32768 + off) = lo;
         } else {
-            const uint32_t off = (uint32_t)sp * DVS * 128 + mn_off(jl, rr, DVS);
+            const uint32_t off = mn_off(j8 * 8, rr, D);
             *reinterpret_cast<uint4*>(cdt + off) = hi;
             *reinterpret_cast<uint4*>(cdt + 16384 + off) = lo;
         }
@@ -114,7 +113,6 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
 template <int DVS>
 __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     using S = DecSmem;
-    constexpr int NSPLIT = D / DVS;
     extern __shared__ __align__(1024) unsigned char sm[];
     float* F = reinterpret_cast<float*>(sm + S::F);
     float *gams = F + S::fGam, *bets = F + S::fBet, *bgs = F + S::fBg, *arow = F + S::fArow,
@@ -139,7 +137,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (tid == 0) {  // the cache header and the position of every unit this CTA takes
         bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
         for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
-        for (int i = 0; i < 7; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
+        for (int i = 0; i < kHdrWords; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
         for (int u = blockIdx.x; ok && u < nunit; u += gridDim.x) {
             const int p = pos[u / H];
             if (!(p >= 0 && p < C)) ok = false;
@@ -374,14 +372,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-#pragma unroll
-        for (int sp = 0; sp < NSPLIT; ++sp) {
-            const uint32_t acc = tmem + sp * DVS;
-            const size_t tile = (size_t)sp * DVS * 128 * 2;
-            mma_tile_mj<128, DVS, D, false, true>(acc, R1, sm + S::Hhi + tile, false);
-            mma_tile_mj<128, DVS, D, false, true>(acc, R1, sm + S::Hlo + tile, true);
-            mma_tile_mj<128, DVS, D, false, true>(acc, R1 + 32768, sm + S::Hhi + tile, true);
-        }
+        mma_tile_mj<128, D, D, false, true>(tmem, R1, sm + S::Hhi, false);
+        mma_tile_mj<128, D, D, false, true>(tmem, R1, sm + S::Hlo, true);
+        mma_tile_mj<128, D, D, false, true>(tmem, R1 + 32768, sm + S::Hhi, true);
         mma_commit(mbar);
     }
     mma_out = true;
@@ -421,8 +414,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         for (int e = 0; e < 8; ++e) x[e] = Dp[j8 * 8 + e];
         uint4 hi, lo;
         split8(x, hi, lo);
-        const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
-        const uint32_t off = (uint32_t)sp * DVS * 128 + mn_off(jl, p, DVS);
+        const uint32_t off = mn_off(j8 * 8, p, D);
         *reinterpret_cast<uint4*>(sm + S::Dt + off) = hi;
         *reinterpret_cast<uint4*>(sm + S::Dt + 16384 + off) = lo;
         *reinterpret_cast<uint4*>(cdt + off) = hi;
@@ -437,14 +429,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-#pragma unroll
-        for (int sp = 0; sp < NSPLIT; ++sp) {
-            const uint32_t acc = tmem + 128 + sp * DVS;
-            const size_t tile = (size_t)sp * DVS * 64 * 2;
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1, sm + S::Dt + tile, false);
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1, sm + S::Dt + 16384 + tile, true);
-            mma_tile_mj<64, DVS, C, false, true>(acc, R1 + 8192, sm + S::Dt + tile, true);
-        }
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt, false);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt + 16384, true);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 8192, sm + S::Dt, true);
         mma_commit(mbar);
     }
     mma_out = true;
@@ -519,21 +506,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(ds, x[e]);
-                const int sp = (j8 * 8) / DVS, jl = j8 * 8 - sp * DVS;
-                const size_t tile = (size_t)sp * DVS * 64 * 2;
-                store8_split(R1 + 16384 + tile, R1 + 32768 + tile, mn_off(jl, s, DVS), x);
+                store8_split(R1 + 16384, R1 + 32768, mn_off(j8 * 8, s, D), x);
             }
         }
         fence_async_smem();
         tc_sync();
         if (tid == 0) {
-#pragma unroll
-            for (int sp = 0; sp < NSPLIT; ++sp) {
-                const uint32_t acc = tmem + sp * DVS;
-                const size_t tile = (size_t)sp * DVS * 64 * 2;
-                mma_tile_mj<128, DVS, C, true, true>(acc, sm + S::Kmn, R1 + 16384 + tile, false);
-                mma_tile_mj<128, DVS, C, true, true>(acc, sm + S::Kmn, R1 + 32768 + tile, true);
-            }
+            mma_tile_mj<128, D, C, true, true>(tmem, sm + S::Kmn, R1 + 16384, false);
+            mma_tile_mj<128, D, C, true, true>(tmem, sm + S::Kmn, R1 + 32768, true);
             mma_commit(mbar);
         }
         mma_out = true;
@@ -562,8 +542,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
                 // and the operand tiles the next steps load
                 uint4 hi, lo;
                 split8(x, hi, lo);
-                const int jc = c0 + 8 * j8, sp = jc / DVS, jl = jc - sp * DVS;
-                const uint32_t off = (uint32_t)sp * DVS * 256 + mn_off(jl, d, DVS);
+                const uint32_t off = mn_off(c0 + 8 * j8, d, D);
                 *reinterpret_cast<uint4*>(cst + off) = hi;
                 *reinterpret_cast<uint4*>(cst + 32768 + off) = lo;
             }

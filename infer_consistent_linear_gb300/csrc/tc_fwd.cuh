@@ -74,7 +74,26 @@ struct TcArgs {
     uint8_t* cache;
     CacheOff co;
     uint32_t* err;
+    // Reading-B decode commit (null otherwise): the batch is one full chunk per sequence
+    // (chunk b = sequence b), buffered in a decode cache; only the chunks of sequences
+    // whose position `commit_pos[b]` is 0 after this step's token (the chunk is complete)
+    // run, and only when the cache header carries the magic, version and these words
+    // (contract digest, then n_seq, H, C, d_k, d_v, policy, io dtype, deployment digest).
+    // The header is checked before anything else of the cache is read.
+    const int32_t* commit_pos;
+    const uint32_t* commit_header;
+    uint32_t commit_words[8 + kHdrWords];
 };
+
+// True when a commit-mode CTA of sequence b has nothing to do (see TcArgs).  Uniform over
+// the CTA: every thread reads the same words.
+__device__ __forceinline__ bool commit_skip(const TcArgs& a, int b) {
+    const uint32_t* hdr = a.commit_header;
+    bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
+#pragma unroll
+    for (int i = 0; i < 8 + kHdrWords; ++i) ok = ok && hdr[2 + i] == a.commit_words[i];
+    return !(ok && a.commit_pos[b] == 0);
+}
 
 __device__ __forceinline__ uint4 ld16_or_zero(const __nv_bfloat16* p, bool valid) {
     return valid ? *reinterpret_cast<const uint4*>(p) : make_uint4(0u, 0u, 0u, 0u);
@@ -142,6 +161,7 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     uint64_t* mbar = reinterpret_cast<uint64_t*>(bg + 64);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
 
+    if (a.commit_pos && commit_skip(a, blockIdx.x)) return;
     const int total = a.chunk_off[a.n_seq];
     const int cidx = blockIdx.x, h = blockIdx.y, H = a.H;
     if (total < 0 || cidx >= total) return;
@@ -168,22 +188,25 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
         cp_async16(tKQ + cm_off(64 + tr, d8 * 8, D), a.q + src, in);
         cp_async16(tVmn + mn_off(d8 * 8, tr, D), a.v + src, in);
     }
-    if (tid < C) {
-        gam[tid] = (tid < nrows) ? a.g[(size_t)(t0 + tid) * H + h] : 0.f;
-        gml[tid] = 0.f;
-        bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (tid < C) bet[tid] = (tid < nrows) ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (warp == 3) {  // gate prefix while the copies land: serial compensated sum in token order
+        for (int r = lane; r < C; r += 32) {
+            gam[r] = (r < nrows) ? a.g[(size_t)(t0 + r) * H + h] : 0.f;
+            gml[r] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            float hi = 0.f, lo = 0.f;
+            for (int r = 0; r < nrows; ++r) {
+                simt::gam_add(hi, lo, gam[r]);
+                gam[r] = hi;
+                gml[r] = lo;
+            }
+        }
     }
     if (warp == 0) tmem_alloc(tbase, 256);   // while the copies land
     cp_async_wait_all();
     __syncthreads();
-    if (tid == 0) {  // gate prefix: serial compensated sum in token order
-        float hi = 0.f, lo = 0.f;
-        for (int r = 0; r < nrows; ++r) {
-            simt::gam_add(hi, lo, gam[r]);
-            gam[r] = hi;
-            gml[r] = lo;
-        }
-    }
     fence_async_smem();
     tc_sync();
     const uint32_t tmem = *tbase;
@@ -428,6 +451,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     uint64_t* bar_ldP = bar_mma + 4;
     uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 5);
 
+    if (a.commit_pos && commit_skip(a, blockIdx.x / (NSPLIT * a.H))) return;
     const int total = a.chunk_off[a.n_seq];
     if (total < 0) return;
     const int H = a.H;

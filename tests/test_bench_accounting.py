@@ -56,3 +56,19 @@ def test_reference_arm_prints_its_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_step_bytes_follow_the_methods_per_head_token_figures():
+    """The roofline's byte rule: 1,032 B per head-token forward (bf16 o) plus the final
+    states; the trainer adds 1,808 B per head-token backward plus dh0.  With fp32 outputs
+    (what the kernels write) 1,288 and 2,832."""
+    class S:
+        d, H = 128, 16
+    p = S()
+    p.lens, p.op = [4096] * 4, "fwd"
+    assert bench.step_bytes(p, 2) == 262144 * 1032 + 4 * 16 * 128 * 128 * 4 == 274_726_912
+    assert bench.step_bytes(p, 4) == 262144 * 1288 + 4 * 16 * 128 * 128 * 4
+    t = S()
+    t.lens, t.op = [4096] * 8, "fwdbwd"
+    assert bench.step_bytes(t, 2) == 524288 * (1032 + 1808) + 2 * 8 * 16 * 128 * 128 * 4
+    assert bench.step_bytes(t, 4) == 524288 * (1288 + 2832) + 2 * 8 * 16 * 128 * 128 * 4

@@ -216,3 +216,14 @@ def test_reading_b_is_its_own_contract(lib):
     assert rc == 2 and "TOKENREC" in lib.cpr_last_error().decode()
     rc = lib.cpr_gdn_bwd(ctypes.byref(b), db, *p[:6], 1, 64, 1, None, p[6], None, *grads, p[7], 1 << 40, None)
     assert rc == 2
+
+
+def test_deployment_digest_needs_a_device(lib):
+    """Without a usable CUDA device the deployment identity cannot be formed: CPR_ERR_CUDA
+    and a message, never a made-up digest.  (With a GPU it is checked in the GPU tests.)"""
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    out = (ctypes.c_uint8 * 32)()
+    assert lib.cpr_deployment_digest(out, None, 0) == 6
+    assert "device" in lib.cpr_last_error().decode()
+    assert lib.cpr_deployment_digest(None, None, 0) == 1

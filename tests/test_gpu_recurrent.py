@@ -143,10 +143,11 @@ def test_reading_b_first_chunk_is_the_token_recurrence():
 
 def test_reading_b_decode_equals_reading_b_prefill():
     """Reading B end to end under its contract: a prefill (the decode cache also keeps the
-    running in-chunk state), then decode steps (the chunk-form step keeps the cache and
-    commits chunks; the running state restarts from the committed state's tiles at each
-    chunk's first row) give the bits of a one-shot forward over the full sequences, and
-    the committed states are the chunk form's."""
+    running in-chunk state and the partial chunk's token rows), then decode steps (one
+    token of the recurrence each, restarting from hi + lo of the committed state at each
+    chunk's first row; a completed chunk is committed by the chunk form's prep and state
+    pass over its buffered rows) give the bits of a one-shot forward over the full
+    sequences, and the committed states are the chunk form's."""
     pre, steps, H = [100, 64, 0, 37, 130], 70, 2
     full = [L + steps for L in pre]
     x = make_inputs(full, H, 128, 128, io_dtype=torch.bfloat16, seed=10, h0_std=0.1).to(DEV)
@@ -200,3 +201,44 @@ def test_reading_a_cache_refused_by_reading_b_decode():
     assert rc == 0, lib.cpr_last_error().decode()
     assert cpr.get_device_error(clear=True) == 4      # CPR_ERR_CONTRACT_MISMATCH
     assert torch.equal(blob, before)
+
+
+@pytest.mark.parametrize("io,d,tol", [(torch.bfloat16, 128, TOL_BF16), (torch.float32, 64, TOL_F32)])
+def test_recurrent_bwd_matches_oracle(io, d, tol):
+    """"Recurrent everywhere" training: the reverse token recurrence on the GPU against the
+    oracle's hand-derived adjoint, ragged sequences (segment boundaries at 16 tokens
+    crossed, an empty and a one-token sequence), h0 and dHT given."""
+    lens, H = [70, 16, 1, 0, 40], 2
+    x = make_inputs(lens, H, d, d, io_dtype=io, seed=12, h0_std=0.1, with_grad=True)
+    gen = torch.Generator().manual_seed(13)
+    dHT = torch.randn(len(lens), H, d, d, generator=gen)
+    xd = x.to(DEV)
+    c = cpr.default_contract(io, d)
+    got = cpr.cpr_gdn_recurrent_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0,
+                                    dHT=dHT.to(DEV), contract=c)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    ref = oracle.gdn_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, dHT=dHT)
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        assert_close(n, got[n], ref[n], tol)
+
+
+def test_recurrent_bwd_deterministic_and_batch_invariant():
+    lens, H, d = [50, 33, 17], 2, 128
+    x = make_inputs(lens, H, d, d, io_dtype=torch.bfloat16, seed=14, h0_std=0.1, with_grad=True).to(DEV)
+    c = cpr.default_contract(torch.bfloat16, d)
+    a = cpr.cpr_gdn_recurrent_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, contract=c)
+    b = cpr.cpr_gdn_recurrent_bwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, x.dO, h0=x.h0, contract=c)
+    for n in a:
+        assert_bitwise(n, a[n], b[n])
+    cu = x.cu_seqlens.tolist()
+    for i, L in enumerate(lens):
+        sl = slice(cu[i], cu[i + 1])
+        one = cpr.cpr_gdn_recurrent_bwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl],
+                                        torch.tensor([0, L], dtype=torch.int32, device=DEV),
+                                        x.dO[sl].contiguous(), h0=x.h0[i:i + 1].contiguous(), contract=c)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            assert_bitwise(f"{n}[seq {i}]", one[n], a[n][sl])
+        assert_bitwise(f"dh0[seq {i}]", one["dh0"], a["dh0"][i:i + 1])
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
