@@ -493,7 +493,7 @@ int reading_b_step(const cpr_contract* c, const uint8_t* digest, const void* q_t
     t.commit_pos = a.pos; t.commit_header = a.header;
     std::memcpy(t.commit_words, a.digest, 32);
     std::memcpy(t.commit_words + 8, a.hdr, sizeof(a.hdr));
-    e = cpr::tc_forward(t, n_seq, n_seq, H, st);
+    e = cpr::tc_commit(t, n_seq, H, st);
     if (e != cudaSuccess) return cuda_fail(e, "reading-B commit launch");
     return CPR_OK;
 }

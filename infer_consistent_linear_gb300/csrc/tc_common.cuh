@@ -56,6 +56,11 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
                  :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+// As tmem_alloc, keeping the permit: for a CTA that allocates once per work unit.
+__device__ __forceinline__ void tmem_alloc_keep(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+}
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
 }
@@ -132,6 +137,25 @@ __device__ __forceinline__ void mma_tile_mj(uint32_t d_tmem, const void* a_tile,
         const uint64_t db = BMN ? smem_desc_mn(b0 + ks * 2 * (N / 8) * 128, N) : smem_desc(b0 + ks * 256, K);
         mma_bf16(d_tmem, da, db, idesc, (accumulate || ks > 0) ? 1u : 0u);
     }
+}
+
+// Descriptor of the k-step-0 sub-tile of an operand tile: K-major (smem_desc) or
+// MN-major (smem_desc_mn).  The k-steps of mma_tile_d add a constant to its address field.
+template <int MN, int K, bool MJ>
+__device__ __forceinline__ uint64_t tile_desc(const void* tile) {
+    return MJ ? smem_desc_mn(smem_u32(tile), MN) : smem_desc(smem_u32(tile), K);
+}
+
+// As mma_tile_mj, from precomputed k-step-0 descriptors (tile_desc): the same
+// instructions with the same operands, for an issuing thread that reuses its tiles.
+template <int M, int N, int K, bool AMN, bool BMN>
+__device__ __forceinline__ void mma_tile_d(uint32_t d_tmem, uint64_t da, uint64_t db, bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16_major(M, N, AMN, BMN);
+    constexpr uint64_t astep = AMN ? (2 * (M / 8) * 128) >> 4 : 256 >> 4;
+    constexpr uint64_t bstep = BMN ? (2 * (N / 8) * 128) >> 4 : 256 >> 4;
+#pragma unroll
+    for (int ks = 0; ks < K / 16; ++ks)
+        mma_bf16(d_tmem, da + ks * astep, db + ks * bstep, idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 // Arrives on `mbar` once every MMA issued so far by this thread has completed.

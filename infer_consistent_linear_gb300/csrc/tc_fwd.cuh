@@ -85,14 +85,22 @@ struct TcArgs {
     uint32_t commit_words[8 + kHdrWords];
 };
 
-// True when a commit-mode CTA of sequence b has nothing to do (see TcArgs).  Uniform over
-// the CTA: every thread reads the same words.
-__device__ __forceinline__ bool commit_skip(const TcArgs& a, int b) {
-    const uint32_t* hdr = a.commit_header;
-    bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
-#pragma unroll
-    for (int i = 0; i < 8 + kHdrWords; ++i) ok = ok && hdr[2 + i] == a.commit_words[i];
-    return !(ok && a.commit_pos[b] == 0);
+// True when a commit-mode CTA's cache header is not the one TcArgs names (nothing of the
+// cache past its header may then be read).  Warp 0 compares a word per lane; the verdict
+// reaches every thread of the CTA through shared memory (a CTA barrier inside).
+__device__ __forceinline__ bool commit_header_bad(const TcArgs& a) {
+    __shared__ int bad_s;
+    if (threadIdx.x < 32) {
+        const int i = threadIdx.x;
+        bool ok = true;
+        if (i == 0) ok = a.commit_header[0] == kCacheMagic;
+        else if (i == 1) ok = a.commit_header[1] == CPR_CONTRACT_VERSION;
+        else if (i < 2 + 8 + kHdrWords) ok = a.commit_header[i] == a.commit_words[i - 2];
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (i == 0) bad_s = all_ok ? 0 : 1;
+    }
+    __syncthreads();
+    return bad_s != 0;
 }
 
 __device__ __forceinline__ uint4 ld16_or_zero(const __nv_bfloat16* p, bool valid) {
@@ -144,10 +152,16 @@ __device__ __forceinline__ void t_solve_pairs(const float* At2, float* Tout, int
 // and then the X1 tiles take the Q rows' space once the S1 MMA has read it.  The 256
 // TMEM columns are allocated once the copies are in flight: with three CTAs per SM
 // the third one's allocation waits for another CTA to finish, but its loads do not.
+// (W' and then U in the same 128 columns, so that all three hold theirs at once,
+// measured slower: 224 -> 231 us on the Prefill workload.)
 constexpr size_t kPrepOffVmn = 32768, kPrepOffT = 49152, kPrepOffVec = kPrepOffT + 64 * 65 * 4;
 constexpr size_t kPrepSmem = kPrepOffVec + 4 * 64 * 4 + 64;
 
-static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
+// PERSIST (the reading-B decode commit): a CTA walks the (chunk, head) units blockIdx.x,
+// + gridDim.x, ... and runs only the chunks of sequences that completed one
+// (TcArgs::commit_pos); otherwise a CTA runs chunk blockIdx.x of head blockIdx.y.
+template <bool PERSIST>
+__global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     unsigned char* tKQ = sm;                       // [K; Q] 128 x 128 K-major; Q rows later A^T, X1
     unsigned char* tKmn = sm;                      // the K rows read as an MN-major 128 (d) x 64 tile
@@ -161,10 +175,33 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
     uint64_t* mbar = reinterpret_cast<uint64_t*>(bg + 64);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(mbar + 1);
 
-    if (a.commit_pos && commit_skip(a, blockIdx.x)) return;
+    if (PERSIST && commit_header_bad(a)) return;
     const int total = a.chunk_off[a.n_seq];
-    const int cidx = blockIdx.x, h = blockIdx.y, H = a.H;
-    if (total < 0 || cidx >= total) return;
+    const int H = a.H;
+    if (total < 0) return;
+    const int nunits = PERSIST ? a.n_seq * H : 0;
+    if (PERSIST) {   // most steps commit nothing: leave at once
+        bool any = false;
+        for (int u = blockIdx.x + (int)threadIdx.x * (int)gridDim.x; u < nunits; u += 128 * (int)gridDim.x)
+            any = any || (u / H < total && a.commit_pos[u / H] == 0);
+        if (!__syncthreads_or(any)) return;
+    }
+    __shared__ uint32_t act[4];   // PERSIST: which of a round of 128 units run, a bit each
+    for (int unit = blockIdx.x, k = 0; PERSIST ? unit < nunits : unit == (int)blockIdx.x;
+         unit += gridDim.x, ++k) {
+    if (PERSIST) {   // commit batch: chunk b is sequence b
+        if ((k & 127) == 0) {   // one thread looks up each position of the next round
+            const int u = unit + (int)threadIdx.x * (int)gridDim.x;
+            const bool on = u < nunits && u / H < total && a.commit_pos[u / H] == 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, on);
+            __syncthreads();   // the previous round's bits are read
+            if ((threadIdx.x & 31) == 0) act[threadIdx.x >> 5] = m;
+            __syncthreads();
+        }
+        if (!((act[(k & 127) >> 5] >> (k & 31)) & 1u)) continue;
+    }
+    const int cidx = PERSIST ? unit / H : (int)blockIdx.x, h = PERSIST ? unit % H : (int)blockIdx.y;
+    if (cidx >= total) break;
     const int b = find_seq(a.chunk_off, a.n_seq, cidx);
     const int n = cidx - a.chunk_off[b];
     const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
@@ -204,7 +241,10 @@ static __global__ void __launch_bounds__(128, 3) k_tc_prep(TcArgs a) {
             }
         }
     }
-    if (warp == 0) tmem_alloc(tbase, 256);   // while the copies land
+    if (warp == 0) {   // while the copies land
+        if (PERSIST) tmem_alloc_keep(tbase, 256);
+        else tmem_alloc(tbase, 256);
+    }
     cp_async_wait_all();
     __syncthreads();
     fence_async_smem();
@@ -386,6 +426,7 @@ done:
     if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
     tc_sync();
     if (warp == 0 && held) tmem_dealloc(tmem, 256);
+    }  // units
 }
 
 // OR over the predicates of `count` threads meeting at hardware barrier `id` (a
@@ -432,7 +473,11 @@ struct StateSmem {
 
 constexpr int kStateThreads = 288, kStateIssuer = 256;
 
-template <int DVS>
+// PERSIST (the reading-B decode commit): a CTA walks the units blockIdx.x, + gridDim.x,
+// ... and runs only those whose sequence completed a chunk (TcArgs::commit_pos); TMEM,
+// the mbarriers and their phases carry over from unit to unit.  Otherwise a CTA runs
+// unit blockIdx.x, the (sequence, head, d_v split) it is launched for.
+template <int DVS, bool PERSIST>
 __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     using L = StateSmem<DVS>;
     constexpr int NSPLIT = D / DVS;
@@ -451,22 +496,21 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     uint64_t* bar_ldP = bar_mma + 4;
     uint32_t* tbase = reinterpret_cast<uint32_t*>(bar_mma + 5);
 
-    if (a.commit_pos && commit_skip(a, blockIdx.x / (NSPLIT * a.H))) return;
+    if (PERSIST && commit_header_bad(a)) return;
     const int total = a.chunk_off[a.n_seq];
     if (total < 0) return;
     const int H = a.H;
-    const int sp = blockIdx.x % NSPLIT;
-    const int h = (blockIdx.x / NSPLIT) % H;
-    const int b = blockIdx.x / (NSPLIT * H);
-    const int j0 = sp * DVS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool epi = warp < 8;                  // warp 8 issues the MMAs
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int cb = half * HALF;                 // this thread's first column (within the split)
-    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
-    const int nch = a.chunk_off[b + 1] - a.chunk_off[b];
-    const size_t sh = (size_t)b * H + h;
-    float* cstate = a.cache ? reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D : nullptr;
+    const int d = quarter * 32 + lane;          // this thread's state row
+    if (PERSIST) {   // most steps commit nothing: leave before taking TMEM
+        bool any = false;
+        for (int u = blockIdx.x + tid * (int)gridDim.x; u < a.n_seq * H * NSPLIT; u += kStateThreads * (int)gridDim.x)
+            any = any || a.commit_pos[u / (NSPLIT * H)] == 0;
+        if (!__syncthreads_or(any)) return;
+    }
 
     if (warp == 0) tmem_alloc(tbase, L::TmemCols);
     if (tid == 0) {
@@ -475,9 +519,27 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     }
     for (int i = tid; i < 1024; i += kStateThreads)  // rows 64..127 of the W'_lo operand stay zero
         reinterpret_cast<uint4*>(sm + L::A4lo + 16384)[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t ph_mma = 0, ph_pd = 0, ph_ldA = 0, ph_ldB = 0, ph_ldP = 0;
+    bool pendA = false, pendB = false, pendP = false, failed = false, mma_out = false, pd_out = false;
+    // the issuing thread's operand descriptors (k-step 0), once: its tiles never move
+    const uint64_t dA4hi = tile_desc<128, D, false>(sm + L::A4hi), dA4lo = tile_desc<128, D, false>(sm + L::A4lo);
+    const uint64_t dHhi = tile_desc<DVS, D, true>(sm + L::Hhi), dHlo = tile_desc<DVS, D, true>(sm + L::Hlo);
+    const uint64_t dKmn = tile_desc<128, C, true>(sm + L::Kmn);
+    const uint64_t dBhi = tile_desc<DVS, C, true>(sm + L::Bhi), dBlo = tile_desc<DVS, C, true>(sm + L::Blo);
+    const uint64_t dPhi = tile_desc<64, C, false>(sm + L::Phi), dPlo = tile_desc<64, C, false>(sm + L::Plo);
+    const uint64_t dDhi = tile_desc<DVS, C, true>(sm + L::Dhi), dDlo = tile_desc<DVS, C, true>(sm + L::Dlo);
+    auto run_unit = [&](int unit) {
+    const int b = unit / (NSPLIT * H);
+    const int sp = unit % NSPLIT;
+    const int h = (unit / NSPLIT) % H;
+    const int j0 = sp * DVS;
+    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
+    const int nch = a.chunk_off[b + 1] - a.chunk_off[b];
+    const size_t sh = (size_t)b * H + h;
+    float* cstate = a.cache ? reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D : nullptr;
+
     // state row d = 32 quarter + lane, columns j0 + cb .. + HALF, fp32 in registers
     float Hreg[HALF];
-    const int d = quarter * 32 + lane;
 #pragma unroll
     for (int j4 = 0; j4 < HALF / 4; ++j4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -522,8 +584,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
     auto acc4 = [&](int n) { return tmem + (uint32_t)((n & 1) * DVS); };
     auto acc5 = [&](int n) { return tmem + (uint32_t)((2 + (n & 1)) * DVS); };
     const uint32_t acc6 = tmem + 4 * DVS;
-    uint32_t ph_mma = 0, ph_pd = 0, ph_ldA = 0, ph_ldB = 0, ph_ldP = 0;
-    bool pendA = false, pendB = false, pendP = false, failed = false, mma_out = false, pd_out = false;
 
     auto issue_A = [&](int n) {
         const unsigned char* blk = blk_of(n);
@@ -628,9 +688,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         bool okg = true;   // this phase's consensus among warps 0..7
         float GL = 0.f;    // G_L, read before issue_A(n + 1) replaces gam
         if (tid == kStateIssuer) {
-            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hhi, false);
-            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4hi, sm + L::Hlo, true);
-            mma_tile_mj<128, DVS, D, false, true>(acc4(n), sm + L::A4lo, sm + L::Hhi, true);
+            mma_tile_d<128, DVS, D, false, true>(acc4(n), dA4hi, dHhi, false);
+            mma_tile_d<128, DVS, D, false, true>(acc4(n), dA4hi, dHlo, true);
+            mma_tile_d<128, DVS, D, false, true>(acc4(n), dA4lo, dHhi, true);
             mma_commit(bar_mma);
         }
         mma_out = true;
@@ -715,12 +775,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         ph_ldP ^= 1u;
         pendP = false;
         if (tid == kStateIssuer) {
-            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Bhi, false);   // H' part
-            mma_tile_mj<128, DVS, C, true, true>(acc6, sm + L::Kmn, sm + L::Blo, true);
+            mma_tile_d<128, DVS, C, true, true>(acc6, dKmn, dBhi, false);   // H' part
+            mma_tile_d<128, DVS, C, true, true>(acc6, dKmn, dBlo, true);
             mma_commit(bar_mma);
-            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Phi, sm + L::Dhi, false);  // P Delta
-            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Phi, sm + L::Dlo, true);
-            mma_tile_mj<64, DVS, C, false, true>(acc5(n), sm + L::Plo, sm + L::Dhi, true);
+            mma_tile_d<64, DVS, C, false, true>(acc5(n), dPhi, dDhi, false);  // P Delta
+            mma_tile_d<64, DVS, C, false, true>(acc5(n), dPhi, dDlo, true);
+            mma_tile_d<64, DVS, C, false, true>(acc5(n), dPlo, dDhi, true);
             mma_commit(bar_pd);
         }
         mma_out = true;
@@ -757,6 +817,25 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         else if (epi && quarter >= 2) o_copy(nch - 1);
     }
     if (!failed && a.final_state && epi) put_state(a.final_state + sh * D * D);
+    };  // run_unit
+    if (PERSIST) {
+        // rounds of kStateThreads units of this CTA: one thread looks up each unit's
+        // position, a bit per unit says which run
+        __shared__ uint32_t act[kStateThreads / 32];
+        const int nunits = a.n_seq * H * NSPLIT;
+        for (int r0 = blockIdx.x; r0 < nunits && !failed; r0 += kStateThreads * gridDim.x) {
+            const int u = r0 + tid * (int)gridDim.x;
+            const bool on = u < nunits && a.commit_pos[u / (NSPLIT * H)] == 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, on);
+            if (lane == 0) act[warp] = m;
+            __syncthreads();
+            for (int t = 0; t < kStateThreads && !failed; ++t)
+                if ((act[t >> 5] >> (t & 31)) & 1u) run_unit(r0 + t * (int)gridDim.x);
+            __syncthreads();   // act is rewritten for the next round
+        }
+    } else {
+        run_unit(blockIdx.x);
+    }
     if (failed && epi) {
         // let in-flight copies and MMAs finish (bounded) before TMEM is released
         if (pendA) mbar_wait(bar_ldA, ph_ldA, a.err);
@@ -766,7 +845,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) k_tc_state(TcArgs a) {
         if (pd_out) mbar_wait(bar_pd, ph_pd, a.err);
     }
     tc_sync();
-    if (warp == 0) tmem_dealloc(tmem, L::TmemCols);
+    if (warp == 0) tmem_dealloc(*tbase, L::TmemCols);
 }
 
 }  // namespace tc

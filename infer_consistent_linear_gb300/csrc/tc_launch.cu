@@ -14,15 +14,28 @@ cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int DVS>
+int sm_count() {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return nsm;
+}
+
+// PERSIST: the reading-B commit, one CTA per SM walking the units.
+template <int DVS, bool PERSIST>
 cudaError_t state(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
-    auto kern = tc::k_tc_state<DVS>;
+    auto kern = tc::k_tc_state<DVS, PERSIST>;
     const size_t sm = tc::StateSmem<DVS>::Total;
     cudaError_t e = set_smem(kern, sm);
     if (e != cudaSuccess) return e;
-    const int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
+    int64_t grid = (int64_t)n_seq * H * (tc::D / DVS);
+    if (PERSIST) {
+        const int nsm = sm_count();
+        if (nsm <= 0) return cudaErrorInvalidDevice;
+        grid = grid < nsm ? grid : nsm;
+    }
     if (grid > 0) {
-        ProfScope ps("cpr_tc_state", st);
+        ProfScope ps(PERSIST ? "cpr_tc_commit_state" : "cpr_tc_state", st);
         kern<<<(unsigned)grid, tc::kStateThreads, sm, st>>>(a);
     }
     return cudaGetLastError();
@@ -93,21 +106,42 @@ cudaError_t tc_wait_timeout_selftest(uint32_t* err, uint32_t limit, uint32_t* ok
 }
 
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st) {
-    cudaError_t e = set_smem(tc::k_tc_prep, tc::kPrepSmem);
+    cudaError_t e = set_smem(tc::k_tc_prep<false>, tc::kPrepSmem);
     if (e != cudaSuccess) return e;
     if (cmax > 0) {
         ProfScope ps("cpr_tc_prep", st);
-        tc::k_tc_prep<<<dim3((unsigned)cmax, H), 128, tc::kPrepSmem, st>>>(a);
+        tc::k_tc_prep<false><<<dim3((unsigned)cmax, H), 128, tc::kPrepSmem, st>>>(a);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (a.dvs) {
-        case 64: e = state<64>(a, n_seq, H, st); break;
-        case 32: e = state<32>(a, n_seq, H, st); break;
+        case 64: e = state<64, false>(a, n_seq, H, st); break;
+        case 32: e = state<32, false>(a, n_seq, H, st); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess || !a.cache) return e;
     return a.dvs == 64 ? cache_tiles<64>(a, n_seq, H, st) : cache_tiles<32>(a, n_seq, H, st);
+}
+
+cudaError_t tc_commit(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st) {
+    if (!a.commit_pos || !a.commit_header) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem(tc::k_tc_prep<true>, tc::kPrepSmem);
+    if (e != cudaSuccess) return e;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    const int64_t units = (int64_t)n_seq * H;
+    const int64_t grid = units < nsm ? units : nsm;
+    if (grid > 0) {
+        ProfScope ps("cpr_tc_commit_prep", st);
+        tc::k_tc_prep<true><<<(unsigned)grid, 128, tc::kPrepSmem, st>>>(a);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (a.dvs) {
+        case 64: return state<64, true>(a, n_seq, H, st);
+        case 32: return state<32, true>(a, n_seq, H, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st) {

@@ -11,6 +11,11 @@ struct TcDecArgs;
 // setup must already have run on `st`; a.dvs selects the state-pass split width.
 cudaError_t tc_forward(const tc::TcArgs& a, int64_t cmax, int n_seq, int H, cudaStream_t st);
 cudaError_t tc_decode_step(const tc::TcDecArgs& a, int dvs, cudaStream_t st);
+// Reading-B decode commit: prep and state pass over a batch of one full chunk per
+// sequence, run only for the sequences whose position is 0 (a.commit_pos, a.commit_header
+// set); persistent grids of one CTA per SM, each leaving at once when none of its
+// units commits.
+cudaError_t tc_commit(const tc::TcArgs& a, int n_seq, int H, cudaStream_t st);
 // Test support: a bounded mbarrier wait that cannot complete (see cpr_selftest_wait_timeout).
 cudaError_t tc_wait_timeout_selftest(uint32_t* err, uint32_t limit, uint32_t* ok_out, cudaStream_t st);
 // Training forward (prep + state pass writing the backward's tiles), reverse
