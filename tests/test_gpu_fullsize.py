@@ -52,27 +52,39 @@ def test_prefill_workload_sampled_heads():
         assert_close(f"final[{b},{h}]", fin[b:b + 1, h:h + 1], h_ref, TOL_BF16)
 
 
-def test_trainer_workload_sampled_heads():
+@pytest.mark.parametrize("with_states", [False, True])
+def test_trainer_workload_sampled_heads(with_states):
+    """The Trainer configuration as timed (h0 = 0, no dHT) and with an initial state and an
+    upstream gradient of the final state, which the timed runs leave out."""
     lens, H = [4096] * 8, 16
-    x = make_inputs(lens, H, D, D, io_dtype=torch.bfloat16, seed=0, with_grad=True)
+    x = make_inputs(lens, H, D, D, io_dtype=torch.bfloat16, seed=0, with_grad=True,
+                    h0_std=0.1 if with_states else 0.0)
+    dHT = None
+    if with_states:
+        gen = torch.Generator().manual_seed(5)
+        dHT = torch.randn(len(lens), H, D, D, generator=gen)
     xd = x.to(DEV)
     c = _contract()
     ws = torch.empty(cpr.workspace_bytes(c, cpr.CPR_OP_BWD, len(lens), sum(lens), H),
                      dtype=torch.uint8, device=DEV)
-    o, _ = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, contract=c,
-                           workspace=ws, train=True)
-    got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, contract=c,
-                          workspace=ws, saved=True)
+    o, fin = cpr.cpr_gdn_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, h0=xd.h0, contract=c,
+                             workspace=ws, train=True)
+    got = cpr.cpr_gdn_bwd(xd.q, xd.k, xd.v, xd.g, xd.beta, xd.cu_seqlens, xd.dO, h0=xd.h0,
+                          dHT=None if dHT is None else dHT.to(DEV), contract=c, workspace=ws, saved=True)
     torch.cuda.synchronize()
     assert cpr.get_device_error() == 0
     got = {k: v.cpu() for k, v in got.items()}
-    o, cu = o.cpu(), x.cu_seqlens.tolist()
+    o, fin, cu = o.cpu(), fin.cpu(), x.cu_seqlens.tolist()
     for b, h in [(1, 3), (6, 12)]:
         one = _one(x, cu, b, h, with_grad=True)
-        o_ref, _ = oracle.gdn_fwd(one["q"], one["k"], one["v"], one["g"], one["beta"], one["cu"])
-        ref = oracle.gdn_bwd(one["q"], one["k"], one["v"], one["g"], one["beta"], one["cu"], one["dO"])
+        h0 = None if x.h0 is None else x.h0[b:b + 1, h:h + 1].contiguous()
+        dht = None if dHT is None else dHT[b:b + 1, h:h + 1].contiguous()
+        o_ref, h_ref = oracle.gdn_fwd(one["q"], one["k"], one["v"], one["g"], one["beta"], one["cu"], h0=h0)
+        ref = oracle.gdn_bwd(one["q"], one["k"], one["v"], one["g"], one["beta"], one["cu"], one["dO"],
+                             h0=h0, dHT=dht)
         sl = slice(cu[b], cu[b + 1])
         assert_close(f"o[{b},{h}]", o[sl, h:h + 1], o_ref, TOL_BF16)
+        assert_close(f"final[{b},{h}]", fin[b:b + 1, h:h + 1], h_ref, TOL_BF16)
         for n in GRADS:
             assert_close(f"{n}[{b},{h}]", got[n][sl, h:h + 1], ref[n], TOL_BF16)
         assert_close(f"dh0[{b},{h}]", got["dh0"][b:b + 1, h:h + 1], ref["dh0"], TOL_BF16)
