@@ -476,17 +476,22 @@ def load_traffic():
         return {}
 
 
-def kernel_src_sha():
-    """Hash of the chunk-form kernels' sources (tc_*, simt_*, common.cuh), which the
-    stored ncu traffic figures belong to; the C-ABI, the token-recurrence and GEMM files
-    do not enter it."""
+# the sources each tensor-core kernel's DRAM traffic depends on: the shared forward
+# headers and launchers, plus its own header
+_TC_SRC_BASE = ("common.cuh", "simt_fwd.cuh", "tc_common.cuh", "tc_fwd.cuh", "tc_launch.cu", "tc_launch.h")
+_TC_SRC_OWN = {"cpr_tc_decode": ("tc_decode.cuh",), "cpr_tc_state_bwd": ("tc_bwd.cuh",),
+               "cpr_tc_grad": ("tc_bwd.cuh",)}
+
+
+def kernel_src_sha(name):
+    """Hash of the sources kernel `name` is built from, which its stored ncu traffic
+    figures belong to: a change to another kernel's header leaves them valid."""
     import hashlib
     csrc = os.path.join(ROOT, "infer_consistent_linear_gb300", "csrc")
     h = hashlib.sha256()
-    for s in sorted(os.listdir(csrc)):
-        if s.endswith((".cu", ".cuh", ".h")) and s.startswith(("tc_", "simt_", "common")):
-            with open(os.path.join(csrc, s), "rb") as f:
-                h.update(s.encode() + b"\0" + f.read())
+    for s in sorted(_TC_SRC_BASE + _TC_SRC_OWN.get(name, ())):
+        with open(os.path.join(csrc, s), "rb") as f:
+            h.update(s.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -517,7 +522,7 @@ def roofline_for(step, prof, pk):
     units = step.kernel_units(name)
     traffic = None
     tr = load_traffic().get(f"{name}/{step.name}")
-    if tr and tr.get("kernel_src_sha") == kernel_src_sha():
+    if tr and tr.get("kernel_src_sha") == kernel_src_sha(name):
         traffic = tr.get("bytes_per_launch")
     tfl = tc_kernel_flops_per_chunk(name, step.d)
     if tfl is not None:

@@ -237,7 +237,7 @@ constexpr const char* kBuildArch = "sm_103a";
 struct Deployment {
     bool ok = false;
     uint8_t digest[32];
-    char text[256];
+    char text[512];   // the prefix, a device name of up to 255 bytes and the numbers fit
 };
 
 int deployment_of_current_device(const Deployment** out) {

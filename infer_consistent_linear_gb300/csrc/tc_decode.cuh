@@ -53,6 +53,10 @@ struct TcDecArgs {
     uint32_t* err;
 };
 
+// 16 KB of zeros (never written) that fill the rows of a decode operand tile past the
+// unit's position: a bulk copy of it hits L2, where the cache's own zero rows cost HBM reads.
+static __device__ __align__(128) unsigned char kZeroTile[16384];
+
 // After a prefill that writes a decode cache: the chunk-start state and the current
 // chunk's Delta rows (rows >= pos zero) as the decode's hi/lo operand tiles, per split
 // MN-major (split sp at sp * DVS * 256 / 128 bytes, lo tiles 32 KB / 16 KB after hi) --
@@ -151,19 +155,31 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     // unit u = sequence u / H, head u % H = row u of every [n_seq, H, ...] section
     auto k_tile = [&](int u) { return a.cache + a.co.k_rows + (size_t)u * C * D * 2; };
     auto v_tile = [&](int u) { return a.cache + a.co.v_rows + (size_t)u * C * D * 2; };
-    auto issue_KV = [&](int u) {   // K and V tiles and the T rows
-        mbar_expect_tx(bar_KV, 32768 + C * C * 4);
-        bulk_g2s(sm + S::Kmn, k_tile(u), 16384, bar_KV);
-        bulk_g2s(sm + S::Vt, v_tile(u), 16384, bar_KV);
-        bulk_g2s(sm + S::Tt, a.cache + a.co.t_rows + (size_t)u * C * C * 4, C * C * 4, bar_KV);
+    // Of the K, V and Delta tiles and the T rows only the rows below the unit's position pu
+    // hold data: the copies take the 8-row groups that contain them (2 KB each in every
+    // tile) and the T rows below pu.  The rest of each tile, zero in the cache, is copied
+    // from kZeroTile instead, which every CTA reads and so stays in L2.
+    auto tile_g2s = [&](unsigned char* dst, const unsigned char* src, uint32_t head, uint64_t* bar) {
+        if (head) bulk_g2s(dst, src, head, bar);
+        if (head < 16384u) bulk_g2s(dst + head, kZeroTile, 16384u - head, bar);
+    };
+    auto issue_KV = [&](int u, int pu) {   // K and V tiles and the T rows
+        const uint32_t kv = (uint32_t)((pu + 7) >> 3) * 2048u, tr = (uint32_t)pu * C * 4;
+        mbar_expect_tx(bar_KV, 2 * 16384u + tr);
+        tile_g2s(sm + S::Kmn, k_tile(u), kv, bar_KV);
+        tile_g2s(sm + S::Vt, v_tile(u), kv, bar_KV);
+        if (tr) bulk_g2s(sm + S::Tt, a.cache + a.co.t_rows + (size_t)u * C * C * 4, tr, bar_KV);
     };
     auto issue_H = [&](int u) {
         mbar_expect_tx(bar_H, 65536);
         bulk_g2s(sm + S::Hhi, a.cache + a.co.state_tiles + (size_t)u * 65536, 65536, bar_H);
     };
-    auto issue_D = [&](int u) {  // the Delta tiles (rows >= p are zero in the cache)
-        mbar_expect_tx(bar_D, 32768);
-        bulk_g2s(sm + S::Dt, a.cache + a.co.delta_tiles + (size_t)u * 32768, 32768, bar_D);
+    auto issue_D = [&](int u, int pu) {  // the Delta hi and lo tiles
+        const uint32_t dt = (uint32_t)((pu + 7) >> 3) * 2048u;
+        const unsigned char* src = a.cache + a.co.delta_tiles + (size_t)u * 32768;
+        mbar_expect_tx(bar_D, 2 * 16384u);
+        tile_g2s(sm + S::Dt, src, dt, bar_D);
+        tile_g2s(sm + S::Dt + 16384, src + 16384, dt, bar_D);
     };
     // the new token's q (threads 0..15), k (16..31), v (32..47) pieces and the cached
     // gate / beta rows, into registers (the n* set is the next unit's, loaded while this
@@ -196,9 +212,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(mbar + i, 1);
         mbar_init_fence();
-        issue_KV(blockIdx.x);
+        issue_KV(blockIdx.x, p);
         issue_H(blockIdx.x);
-        issue_D(blockIdx.x);
+        issue_D(blockIdx.x, p);
     }
     load_rows(blockIdx.x, p);
     take_rows();
@@ -232,9 +248,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     unsigned char* cst = a.cache + a.co.state_tiles + sh * 65536;     // state hi | lo tiles
     unsigned char* cdt = a.cache + a.co.delta_tiles + sh * 32768;     // Delta hi | lo tiles
     {
-        // this unit's K and V tiles (rows >= p zero in the cache) have landed: row p from
-        // the new token, and the q row p of the [K; Q] operand (rows 64.. = R1's first
-        // 16 KB; other rows of an A operand reach only accumulator rows never read)
+        // this unit's K and V tiles have landed: row p from the new token, and the q row p of
+        // the [K; Q] operand (rows 64.. = R1's first 16 KB; other rows of an A operand
+        // reach only accumulator rows never read)
         const bool w = mbar_wait(bar_KV, ph_KV, a.err);
         if (w) {
             ph_KV ^= 1u;
@@ -324,7 +340,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (!mma_wait()) { ok = false; break; }
     if (tid == 0 && has_next && p != C - 1) {  // K and V are consumed (a committing unit still
         fence_async_smem();                    // needs K): the next unit's tiles
-        issue_KV(un);
+        issue_KV(un, pn);
     }
     if (has_next && p != C - 1) pend_KV = true;
     {
@@ -354,8 +370,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         store8_split(R1, R1 + 32768, cm_off(p, d8 * 8, D), x);
     }
     {
-        // the state tiles and the Delta tiles (rows >= p zero; row p is written below, and
-        // rows past it only meet zero P entries) have landed
+        // the state tiles and the Delta tiles have landed (row p is written below, and rows
+        // past it only meet zero P entries)
         const bool wh = mbar_wait(bar_H, ph_H, a.err);
         const bool wd = mbar_wait(bar_D, ph_D, a.err);
         if (wh) {
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (!mma_wait()) { ok = false; break; }
     if (tid == 0 && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
         fence_async_smem();                    // (a committing unit stages its rows there first)
-        issue_D(un);
+        issue_D(un, pn);
     }
     if (has_next && p != C - 1) pend_D = true;
     {
@@ -520,8 +536,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         if (!mma_wait()) { ok = false; break; }
         if (tid == 0 && has_next) {  // K and the staged rows are consumed: the next unit's
             fence_async_smem();      // K, V and Delta tiles
-            issue_KV(un);
-            issue_D(un);
+            issue_KV(un, pn);
+            issue_D(un, pn);
         }
         if (has_next) pend_KV = pend_D = true;
         const float GL = simt::gate(gams[Lr], gmls[Lr]);
