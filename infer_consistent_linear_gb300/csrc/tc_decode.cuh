@@ -114,6 +114,10 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
 // longer needs: K and V tiles once the X MMA has read them, the state tiles once
 // A4 has, the Delta prefix once P Delta has (after the commit MMA when u commits),
 // and the new token's q, k, v pieces and gate rows into registers.
+// A unit needs one row of each chunk-form product (row p, and the q row p), so the
+// products the prefill takes as M = 128 groups ([K; Q] K^T and [W'; Q] H) run here as
+// M = 64 groups over an A tile that holds just the two rows (p and p ^ 32): an output
+// element's bits do not depend on the instruction's M or N, nor on which row it sits in.
 template <int DVS>
 __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     using S = DecSmem;
@@ -248,9 +252,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     unsigned char* cst = a.cache + a.co.state_tiles + sh * 65536;     // state hi | lo tiles
     unsigned char* cdt = a.cache + a.co.delta_tiles + sh * 32768;     // Delta hi | lo tiles
     {
-        // this unit's K and V tiles have landed: row p from the new token, and the q row p of
-        // the [K; Q] operand (rows 64.. = R1's first 16 KB; other rows of an A operand
-        // reach only accumulator rows never read)
+        // this unit's K and V tiles have landed: row p from the new token; the S1 operand
+        // (R1's first 16 KB) takes k_p as row p and q_p as row p ^ 32 (its other rows reach
+        // only accumulator rows never read)
         const bool w = mbar_wait(bar_KV, ph_KV, a.err);
         if (w) {
             ph_KV ^= 1u;
@@ -258,9 +262,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         }
         if (__syncthreads_or(!w)) { ok = false; break; }
     }
-    if (tid < 16) *reinterpret_cast<uint4*>(R1 + cm_off(p, tid * 8, D)) = rowreg;
-    else if (tid < 32) *reinterpret_cast<uint4*>(sm + S::Kmn + cm_off(p, (tid - 16) * 8, D)) = rowreg;
-    else if (tid < 48) *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
+    if (tid < 16) {
+        *reinterpret_cast<uint4*>(R1 + cm_off(p ^ 32, tid * 8, D)) = rowreg;
+    } else if (tid < 32) {
+        *reinterpret_cast<uint4*>(sm + S::Kmn + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+        *reinterpret_cast<uint4*>(R1 + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+    } else if (tid < 48) {
+        *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
+    }
     if (tid < p) {
         gams[tid] = cgv;
         gmls[tid] = clv;
@@ -277,20 +286,20 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     tc_sync();
     if (has_next) pn = pos[un / H];
     if (tid == 0) {
-        mma_tile<128, 64, D>(tmem, sm + S::Kmn, sm + S::Kmn, false);
+        mma_tile<64, 64, D>(tmem, R1, sm + S::Kmn, false);
         mma_commit(mbar);
     }
     mma_out = true;
     if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid], gmls[tid]);
     if (!mma_wait()) { ok = false; break; }
-    {
+    if (warp == (p >> 4) || warp == ((p ^ 32) >> 4)) {   // the lane quarters of rows p, p ^ 32
         float v[32];
         for (int c0 = 0; c0 < C; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
-            if (tid == p) {
+            if (tid == lane_m64(p)) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
-            } else if (tid == 64 + p) {
+            } else if (tid == lane_m64(p ^ 32)) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
             }
@@ -309,9 +318,20 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         const int j = tid;
         const float* Tt = reinterpret_cast<const float*>(sm + S::Tt);
         float acc = 0.f;
+        for (int s0 = 0; s0 < p; s0 += 16) {   // 16 rows' loads first, then their fma chain
+            float tv[16], av[16];
 #pragma unroll
-        for (int s = 0; s < C; ++s)
-            if (s >= j && s < p) acc = __fmaf_rn(arow[s], Tt[s * C + j], acc);
+            for (int e = 0; e < 16; ++e) {      // (rows >= p hold stale values, never selected)
+                tv[e] = Tt[(s0 + e) * C + j];
+                av[e] = arow[s0 + e];
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int s = s0 + e;
+                const float f = __fmaf_rn(av[e], tv[e], acc);
+                if (s >= j && s < p) acc = f;
+            }
+        }
         trow[j] = (j < p) ? -acc : (j == p ? 1.f : 0.f);
     }
     __syncthreads();
@@ -343,8 +363,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         issue_KV(un, pn);
     }
     if (has_next && p != C - 1) pend_KV = true;
-    {
-        const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
+    if (warp == (p >> 4)) {   // M = 64: row p is lane p % 16 of lane quarter p / 16
+        const bool mine = lane == (p & 15);
         float v[32];
         for (int c0 = 0; c0 < 2 * D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
@@ -357,11 +377,11 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
             }
         }
     }
-    // A4 tiles (R1: hi at +0, lo at +32 KB): row p = W'_p, row 64 + p = q_p
+    // A4 tiles, M = 64 (R1: hi at +0, lo at +32 KB): row p = W'_p, row p ^ 32 = q_p
     __syncthreads();
     if (tid < 16) {  // q_p has no lo part: that row of the lo tile is zero, as in the prefill
-        *reinterpret_cast<uint4*>(R1 + cm_off(64 + p, tid * 8, D)) = rowreg;
-        *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(64 + p, tid * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(R1 + cm_off(p ^ 32, tid * 8, D)) = rowreg;
+        *reinterpret_cast<uint4*>(R1 + 32768 + cm_off(p ^ 32, tid * 8, D)) = make_uint4(0u, 0u, 0u, 0u);
     } else if (tid < 32) {
         const int d8 = tid - 16;
         float x[8];
@@ -388,9 +408,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     fence_async_smem();
     tc_sync();
     if (tid == 0) {
-        mma_tile_mj<128, D, D, false, true>(tmem, R1, sm + S::Hhi, false);
-        mma_tile_mj<128, D, D, false, true>(tmem, R1, sm + S::Hlo, true);
-        mma_tile_mj<128, D, D, false, true>(tmem, R1 + 32768, sm + S::Hhi, true);
+        mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hhi, false);
+        mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hlo, true);
+        mma_tile_mj<64, D, D, false, true>(tmem, R1 + 32768, sm + S::Hhi, true);
         mma_commit(mbar);
     }
     mma_out = true;
@@ -401,14 +421,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         issue_H(un);
     }
     if (has_next) pend_H = true;
-    {
+    if (warp == (p >> 4) || warp == ((p ^ 32) >> 4)) {   // the lane quarters of rows p, p ^ 32
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
-            if (tid == p) {
+            if (tid == lane_m64(p)) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
-            } else if (tid == 64 + p) {
+            } else if (tid == lane_m64(p ^ 32)) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
             }
@@ -457,8 +477,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         issue_D(un, pn);
     }
     if (has_next && p != C - 1) pend_D = true;
-    {
-        const bool mine = (warp == (p >> 4)) && (lane == (p & 15));
+    if (warp == (p >> 4)) {
+        const bool mine = lane == (p & 15);
         float v[32];
         for (int c0 = 0; c0 < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, 128 + c0), v);
