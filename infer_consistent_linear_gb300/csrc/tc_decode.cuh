@@ -109,6 +109,13 @@ __global__ void __launch_bounds__(256) k_tc_cache_tiles(uint8_t* cache, CacheOff
     }
 }
 
+// One thread's 128 loaded columns into a 16-byte aligned row of shared memory.
+__device__ __forceinline__ void store_row128(float* dst, const float (&v)[128]) {
+#pragma unroll
+    for (int j = 0; j < 128; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+
 // Persistent: a CTA per SM walks the (sequence, head) units of the step.  While
 // unit u runs, the next unit's operands arrive by bulk copies into buffers u no
 // longer needs: K and V tiles once the X MMA has read them, the state tiles once
@@ -365,17 +372,11 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (has_next && p != C - 1) pend_KV = true;
     if (warp == (p >> 4)) {   // M = 64: row p is lane p % 16 of lane quarter p / 16
         const bool mine = lane == (p & 15);
-        float v[32];
-        for (int c0 = 0; c0 < 2 * D; c0 += 32) {
-            tmem_ld32(taddr_of(tmem, warp, c0), v);
-            if (mine) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (c0 < D) Wp[c0 + j] = v[j];
-                    else Up[c0 - D + j] = v[j];
-                }
-            }
-        }
+        float v[128];
+        tmem_ld128(taddr_of(tmem, warp, 0), v);
+        if (mine) store_row128(Wp, v);
+        tmem_ld128(taddr_of(tmem, warp, D), v);
+        if (mine) store_row128(Up, v);
     }
     // A4 tiles, M = 64 (R1: hi at +0, lo at +32 KB): row p = W'_p, row p ^ 32 = q_p
     __syncthreads();
@@ -422,17 +423,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     if (has_next) pend_H = true;
     if (warp == (p >> 4) || warp == ((p ^ 32) >> 4)) {   // the lane quarters of rows p, p ^ 32
-        float v[32];
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            tmem_ld32(taddr_of(tmem, warp, c0), v);
-            if (tid == lane_m64(p)) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
-            } else if (tid == lane_m64(p ^ 32)) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
-            }
-        }
+        float v[128];
+        tmem_ld128(taddr_of(tmem, warp, 0), v);
+        if (tid == lane_m64(p)) store_row128(row1, v);
+        else if (tid == lane_m64(p ^ 32)) store_row128(row2, v);
     }
     __syncthreads();
     {
@@ -478,15 +472,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     if (has_next && p != C - 1) pend_D = true;
     if (warp == (p >> 4)) {
-        const bool mine = lane == (p & 15);
-        float v[32];
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            tmem_ld32(taddr_of(tmem, warp, 128 + c0), v);
-            if (mine) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
-            }
-        }
+        float v[128];
+        tmem_ld128(taddr_of(tmem, warp, 128), v);
+        if (lane == (p & 15)) store_row128(row1, v);
     }
     __syncthreads();
     a.o[sh * D + tid] = __fadd_rn(Qs[tid], row1[tid]);
