@@ -326,8 +326,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_state_bwd(TcBwdArgs a) {
         {
             // dDelta = P^T dO + dec . (K dH') -> B1 (MN-major (j, t)), this thread's columns
             float v1[32], v2[32];
-            tmem_ld32(taddr_of(tD1, warp, cb), v1);
-            tmem_ld32(taddr_of(tD2, warp, cb), v2);
+            tmem_ld32x2(taddr_of(tD1, warp, cb), v1, taddr_of(tD2, warp, cb), v2);
             if (lane < 16) {
                 const float dr = dec[r64];
 #pragma unroll
@@ -616,8 +615,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         const int s0 = hf * 32;
         const float gr = gam[r], lr = gml[r], br = bet[r];
         float v1[32], v2[32];
-        tmem_ld32(taddr_of(tmem + tS1, warp, s0), v1);
-        tmem_ld32(taddr_of(tmem + tG, warp, s0), v2);
+        tmem_ld32x2(taddr_of(tmem + tS1, warp, s0), v1, taddr_of(tmem + tG, warp, s0), v2);
         float sa = 0.f, sb = 0.f;
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
@@ -812,10 +810,8 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         const float gr = Gm[r], nb = -bgv[r], dr = dec[r];
         for (int c = 0; c < 2; ++c) {
             const int c0 = hf * 64 + c * 32;
-            tmem_ld32(taddr_of(tmem + tX1, warp, c0), x1);
-            tmem_ld32(taddr_of(tmem + tdq, warp, c0), y);
-            tmem_ld32(taddr_of(tmem + tX2, warp, c0), z);
-            tmem_ld32(taddr_of(tmem + tdk, warp, c0), w2);
+            tmem_ld32x4(taddr_of(tmem + tX1, warp, c0), x1, taddr_of(tmem + tdq, warp, c0), y,
+                        taddr_of(tmem + tX2, warp, c0), z, taddr_of(tmem + tdk, warp, c0), w2);
             if (in) {   // whole 32-byte sectors: one row per lane
 #pragma unroll
                 for (int j8 = 0; j8 < 4; ++j8) {

@@ -286,6 +286,85 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
     for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Several 32-column loads (any lanes' quarter, any columns) under one wait: as tmem_ld32
+// each, without a wait between them.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t t0, float (&v0)[32], uint32_t t1, float (&v1)[32]) {
+    uint32_t r0[32], r1[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+                 "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]),
+                   "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]),
+                   "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]),
+                   "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]),
+                   "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]),
+                   "=r"(r0[30]), "=r"(r0[31]), "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]),
+                   "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]),
+                   "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]),
+                   "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]),
+                   "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]),
+                   "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+                 : "r"(t0), "r"(t1)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v1[i] = __uint_as_float(r1[i]);
+}
+__device__ __forceinline__ void tmem_ld32x4(uint32_t t0, float (&v0)[32], uint32_t t1, float (&v1)[32],
+                                            uint32_t t2, float (&v2)[32], uint32_t t3, float (&v3)[32]) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+                 "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+                 "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+                 "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+                 "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]),
+                   "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]),
+                   "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]),
+                   "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]),
+                   "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]),
+                   "=r"(r0[30]), "=r"(r0[31]), "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]),
+                   "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]),
+                   "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]),
+                   "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]),
+                   "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]),
+                   "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31]), "=r"(r2[0]), "=r"(r2[1]),
+                   "=r"(r2[2]), "=r"(r2[3]), "=r"(r2[4]), "=r"(r2[5]), "=r"(r2[6]), "=r"(r2[7]),
+                   "=r"(r2[8]), "=r"(r2[9]), "=r"(r2[10]), "=r"(r2[11]), "=r"(r2[12]), "=r"(r2[13]),
+                   "=r"(r2[14]), "=r"(r2[15]), "=r"(r2[16]), "=r"(r2[17]), "=r"(r2[18]), "=r"(r2[19]),
+                   "=r"(r2[20]), "=r"(r2[21]), "=r"(r2[22]), "=r"(r2[23]), "=r"(r2[24]), "=r"(r2[25]),
+                   "=r"(r2[26]), "=r"(r2[27]), "=r"(r2[28]), "=r"(r2[29]), "=r"(r2[30]), "=r"(r2[31]),
+                   "=r"(r3[0]), "=r"(r3[1]), "=r"(r3[2]), "=r"(r3[3]), "=r"(r3[4]), "=r"(r3[5]),
+                   "=r"(r3[6]), "=r"(r3[7]), "=r"(r3[8]), "=r"(r3[9]), "=r"(r3[10]), "=r"(r3[11]),
+                   "=r"(r3[12]), "=r"(r3[13]), "=r"(r3[14]), "=r"(r3[15]), "=r"(r3[16]), "=r"(r3[17]),
+                   "=r"(r3[18]), "=r"(r3[19]), "=r"(r3[20]), "=r"(r3[21]), "=r"(r3[22]), "=r"(r3[23]),
+                   "=r"(r3[24]), "=r"(r3[25]), "=r"(r3[26]), "=r"(r3[27]), "=r"(r3[28]), "=r"(r3[29]),
+                   "=r"(r3[30]), "=r"(r3[31])
+                 : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v1[i] = __uint_as_float(r1[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v2[i] = __uint_as_float(r2[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v3[i] = __uint_as_float(r3[i]);
+}
+
 // TMEM address of (warp's lane quarter, column c).
 __device__ __forceinline__ uint32_t taddr_of(uint32_t base, int warp, int col) {
     return base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)col;
