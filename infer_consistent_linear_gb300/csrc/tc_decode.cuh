@@ -300,15 +300,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid], gmls[tid]);
     if (!mma_wait()) { ok = false; break; }
     if (warp == (p >> 4) || warp == ((p ^ 32) >> 4)) {   // the lane quarters of rows p, p ^ 32
-        float v[32];
-        for (int c0 = 0; c0 < C; c0 += 32) {
-            tmem_ld32(taddr_of(tmem, warp, c0), v);
-            if (tid == lane_m64(p)) {
+        float v0[32], v1[32];
+        tmem_ld32x2(taddr_of(tmem, warp, 0), v0, taddr_of(tmem, warp, 32), v1);
+        float* dst = tid == lane_m64(p) ? row1 : tid == lane_m64(p ^ 32) ? row2 : nullptr;
+        if (dst) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) row1[c0 + j] = v[j];
-            } else if (tid == lane_m64(p ^ 32)) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) row2[c0 + j] = v[j];
+            for (int j = 0; j < 32; j += 4) {
+                *reinterpret_cast<float4*>(dst + j) = make_float4(v0[j], v0[j + 1], v0[j + 2], v0[j + 3]);
+                *reinterpret_cast<float4*>(dst + 32 + j) = make_float4(v1[j], v1[j + 1], v1[j + 2], v1[j + 3]);
             }
         }
     }
