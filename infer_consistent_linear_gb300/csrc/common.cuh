@@ -80,4 +80,18 @@ struct Digest {
 constexpr uint32_t kCacheMagic = 0x43505243u;
 constexpr int kHdrWords = 15;   // header words 10..24, after the contract digest
 
+// Whether a decode cache's header words 0 .. 9 + kHdrWords are the expected ones: the
+// magic, the contract version, `digest` and then `words`.  Called by all 32 lanes of a
+// warp, a word per lane (the loads are independent); every lane gets the verdict.
+__device__ __forceinline__ bool cache_header_ok(const uint32_t* hdr, const uint32_t* digest,
+                                                const uint32_t* words) {
+    const int lane = threadIdx.x & 31;
+    bool ok = true;
+    if (lane == 0) ok = hdr[0] == kCacheMagic;
+    else if (lane == 1) ok = hdr[1] == CPR_CONTRACT_VERSION;
+    else if (lane < 10) ok = hdr[lane] == digest[lane - 2];
+    else if (lane < 10 + kHdrWords) ok = hdr[lane] == words[lane - 10];
+    return __all_sync(0xffffffffu, ok);
+}
+
 }  // namespace cpr

@@ -197,14 +197,14 @@ __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
     __shared__ int ok_s;
     const int tid = threadIdx.x, j = tid % D, part = tid / D;
     const int H = a.H, b = blockIdx.x / H, h = blockIdx.x % H;
-    if (tid == 0) {
-        bool ok = a.header[0] == kCacheMagic && a.header[1] == CPR_CONTRACT_VERSION;
-        for (int i = 0; i < 8; ++i) ok = ok && a.header[2 + i] == a.digest[i];
-        for (int i = 0; i < kHdrWords; ++i) ok = ok && a.header[10 + i] == a.hdr[i];
-        int p = ok ? a.pos[b] : -1;
-        if (!(p >= 0 && p < kChunk)) ok = false;
-        if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
-        ok_s = ok ? 1 + p : 0;
+    if (tid < 32) {   // the header (a word per lane), then the position once it is right
+        bool ok = cache_header_ok(a.header, a.digest, a.hdr);
+        if (tid == 0) {
+            const int p = ok ? a.pos[b] : -1;
+            if (!(p >= 0 && p < kChunk)) ok = false;
+            if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
+            ok_s = ok ? 1 + p : 0;
+        }
     }
     __syncthreads();
     if (!ok_s) return;

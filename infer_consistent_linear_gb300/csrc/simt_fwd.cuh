@@ -566,14 +566,14 @@ __global__ void __launch_bounds__(128) k_decode(DecArgs a) {
     const uint32_t* hdr = reinterpret_cast<const uint32_t*>(a.cache + a.co.header);
     int32_t* pos = reinterpret_cast<int32_t*>(a.cache + a.co.pos);
     uint32_t* done = reinterpret_cast<uint32_t*>(a.cache + a.co.done);
-    if (tid == 0) {
-        bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
-        for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
-        for (int i = 0; i < kHdrWords; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
-        const int p = ok ? pos[b] : -1;
-        if (!(p >= 0 && p < C)) ok = false;
-        if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
-        ok_s = ok ? 1 + p : 0;
+    if (tid < 32) {   // the header (a word per lane), then the position once it is right
+        bool ok = cache_header_ok(hdr, a.digest.w, a.hdr);
+        if (tid == 0) {
+            const int p = ok ? pos[b] : -1;
+            if (!(p >= 0 && p < C)) ok = false;
+            if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
+            ok_s = ok ? 1 + p : 0;
+        }
     }
     __syncthreads();
     if (!ok_s) return;

@@ -149,16 +149,22 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     const uint32_t* hdr = reinterpret_cast<const uint32_t*>(a.cache + a.co.header);
     int32_t* pos = reinterpret_cast<int32_t*>(a.cache + a.co.pos);
     uint32_t* done = reinterpret_cast<uint32_t*>(a.cache + a.co.done);
-    if (tid == 0) {  // the cache header and the position of every unit this CTA takes
-        bool ok = hdr[0] == kCacheMagic && hdr[1] == CPR_CONTRACT_VERSION;
-        for (int i = 0; i < 8; ++i) ok = ok && hdr[2 + i] == a.digest.w[i];
-        for (int i = 0; i < kHdrWords; ++i) ok = ok && hdr[10 + i] == a.hdr[i];
-        for (int u = blockIdx.x; ok && u < nunit; u += gridDim.x) {
-            const int p = pos[u / H];
-            if (!(p >= 0 && p < C)) ok = false;
+    if (warp == 0) {
+        // the cache header, a word per lane (words 0..9 + kHdrWords), and only once it is
+        // the expected one the position of every unit this CTA takes, a unit per lane
+        bool ok = cache_header_ok(hdr, a.digest.w, a.hdr);
+        if (ok) {
+            bool okp = true;
+            for (int u = blockIdx.x + lane * (int)gridDim.x; u < nunit; u += 32 * (int)gridDim.x) {
+                const int p = pos[u / H];
+                okp = okp & (p >= 0) & (p < C);
+            }
+            ok = __all_sync(0xffffffffu, okp);
         }
-        if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
-        ok_s = ok ? 1 : 0;
+        if (lane == 0) {
+            if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
+            ok_s = ok ? 1 : 0;
+        }
     }
     __syncthreads();
     if (!ok_s || (int)blockIdx.x >= nunit) return;
@@ -580,14 +586,17 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     p = pn;
     take_rows();
     }  // units
-    if (ok && tid == 0) {
+    if (ok && warp == 0) {
         // every sequence advances one token per step: the last CTA to finish moves all the
-        // positions on.  Every CTA read the positions of its units before its count, and the
-        // next step is a later launch.
-        const uint32_t prev = atomicAdd(&done[0], 1u);
+        // positions on (warp 0, a sequence per lane).  Every CTA read the positions of its
+        // units before its count, and the next step is a later launch.
+        uint32_t prev = 0;
+        if (lane == 0) prev = atomicAdd(&done[0], 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == gridDim.x - 1) {
-            for (int sq = 0; sq < a.n_seq; ++sq) pos[sq] = (pos[sq] + 1) % C;
-            done[0] = 0u;
+            for (int sq = lane; sq < a.n_seq; sq += 32) pos[sq] = (pos[sq] + 1) % C;
+            __syncwarp();
+            if (lane == 0) done[0] = 0u;
             __threadfence();
         }
     }
