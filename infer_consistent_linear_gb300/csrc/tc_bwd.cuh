@@ -525,13 +525,23 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     int it = 0;                    // this CTA's item count: the load barriers' phase parity
     float bloc[32];                // bottom rows: b_r dA_rs Kd_rs for this thread's columns
 
+    // an item's sequence, its chunk within it, the sequence's first token and length: a
+    // chain of dependent loads, taken for the next item while this one's first MMA group runs
+    int nx_b = -1, nx_n = 0, nx_seq0 = 0, nx_T = 0;
+    auto locate = [&](int w) {
+        const int cidx = w / H;
+        nx_b = find_seq(a.chunk_off, a.n_seq, cidx);
+        nx_n = cidx - a.chunk_off[nx_b];
+        nx_seq0 = a.cu[nx_b];
+        nx_T = a.cu[nx_b + 1] - nx_seq0;
+    };
     for (int w = blockIdx.x; w < nwork; w += gridDim.x, ++it) {
     const uint32_t ph = (uint32_t)(it & 1);
     const int wn = w + (int)gridDim.x;         // the next item of this CTA
-    const int cidx = w / H, h = w % H;
-    const int b = find_seq(a.chunk_off, a.n_seq, cidx);
-    const int n = cidx - a.chunk_off[b];
-    const int seq0 = a.cu[b], T = a.cu[b + 1] - seq0;
+    const int h = w % H;
+    if (nx_b < 0) locate(w);                   // the CTA's first item
+    const int b = nx_b, n = nx_n, seq0 = nx_seq0, T = nx_T;
+    nx_b = -1;
     const int t0 = seq0 + n * C;
     const int nrows = min(C, T - n * C);
     const int Lr = nrows - 1;
@@ -597,6 +607,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
             if (lane == 0) dRv[rr] = sdot;
         }
     }
+    if (wn < nwork) locate(wn);
     {
         const bool ok = mbar_wait(bar_mma, ph_mma, a.err);
         fence_after();
