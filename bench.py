@@ -78,19 +78,71 @@ def workload_lens(name):
 
 
 # ---------------------------------------------------------------- clocks
+class _Nvml:
+    """Read-only NVML queries through the driver's library (ctypes): the SM clock, its
+    maximum and the active clock-event (throttle) reasons of one device."""
+    SM = 1   # NVML_CLOCK_SM
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, index):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        rc = -1
+        try:   # the same physical GPU as torch's device `index` (NVML may number GPUs otherwise)
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(index).uuid)
+            rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        except Exception:
+            rc = -1
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(mx)) == 0 \
+            else None
+
+    def sample(self):
+        c = self.c
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(mhz)) != 0:
+            return None
+        bits = rs.value if self.reasons_fn(self.h, c.byref(rs)) == 0 else 0
+        return float(mhz.value), [n for n, b in self.BITS.items() if bits & b]
+
+
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons while running: NVML every millisecond when the
+    driver's library loads (a timed region can be a few milliseconds), else nvidia-smi every
+    200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
         self.dev = device_index
-        self.rows = []
+        self.rows = []       # nvidia-smi rows
+        self.fast = []       # (mhz, [reasons]) from NVML
+        self.nvml = None
         self.proc = None
         self.thread = None
+        self.running = False
 
     def start(self):
+        try:
+            self.nvml = _Nvml(self.dev)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.running = True
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
@@ -102,6 +154,13 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self):
+        while self.running:
+            s = self.nvml.sample()
+            if s is not None:
+                self.fast.append(s)
+            time.sleep(0.001)
+
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
@@ -109,6 +168,7 @@ class ClockSampler:
                 self.rows.append(parts)
 
     def stop(self):
+        self.running = False
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -119,6 +179,12 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
+        if self.fast:
+            sm = [m for m, _ in self.fast]
+            reasons = sorted({r for _, rs in self.fast for r in rs})
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.nvml.max_mhz, "reasons": reasons,
+                    "samples": len(self.fast), "source": "NVML, 1 ms"}
+
         def num(x):
             try:
                 return float(x)
@@ -129,7 +195,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows),
+                "source": "nvidia-smi, 200 ms"}
 
 
 # ------------------------------------------------------- algorithmic work
