@@ -1087,11 +1087,16 @@ class ReadingBDecode:
     same contract (one token of the recurrence; the chunk form commits each completed
     chunk)."""
 
-    def __init__(self, dev, n_steps):
+    def __init__(self, dev, n_steps, claim=True):
         import infer_consistent_linear_gb300 as cpr
         from infer_consistent_linear_gb300.synth import make_inputs
         self.cpr = cpr
         self.lens = workload_lens("decode")
+        # the positions the caller knows from its lengths: a step that completes no chunk
+        # runs as cpr_gdn_decode_step_nocommit (no commit launch) when `claim` is set
+        self.claim = claim
+        self.pos = [L % 64 for L in self.lens]
+        self.claims = []
         H, d = WORKLOADS["decode"]["H"], WORKLOADS["decode"]["d"]
         self.c = cpr.default_contract(torch.bfloat16, d, dv_splits=2, operand_policy=cpr.CPR_POLICY_TC_BF16X3,
                                       intra_order=cpr.CPR_ORDER_TOKENREC_V1)
@@ -1110,7 +1115,10 @@ class ReadingBDecode:
 
     def run(self):
         q, k, v, g, b = (x[self.t] for x in self.tok)
-        self.cpr.cpr_gdn_decode_step(q, k, v, g, b, self.cache, contract=self.c, out=self.o)
+        free = self.claim and all(p != 63 for p in self.pos)
+        self.claims.append(free)
+        self.cpr.cpr_gdn_decode_step(q, k, v, g, b, self.cache, contract=self.c, out=self.o, no_commit=free)
+        self.pos = [(p + 1) % 64 for p in self.pos]
         self.t += 1
 
 
@@ -1133,12 +1141,25 @@ def reading_b(dev, world, reading_a_ms):
     del rb, oa, ob
     torch.cuda.empty_cache()
     try:   # reading B's decode step on the Decode workload (its bits are checked in the GPU tests)
+        # Step times without per-kernel events (one event pair per launch would add a few µs
+        # to each of a step's launches); the kernel table from a separate profiled run
         K, W = 64, 3
+        out = {"workload": WORKLOADS["decode"]["desc"], "steps": K}
+        for claim, key in ((True, "us_per_step"), (False, "us_per_step_commit_every_step")):
+            rd = ReadingBDecode(dev, K + W, claim=claim)
+            ms_d, _ = time_device(rd, K, W, world, profile=False)
+            out[key] = round(ms_d * 1e3, 3)
+            if claim:
+                out["timed_steps_without_commit_launch"] = int(sum(rd.claims[-K:]))
+            out["error_word" if claim else "error_word_commit_every_step"] = rb_err(rd.cpr)
+            del rd
+            torch.cuda.empty_cache()
         rd = ReadingBDecode(dev, K + W)
-        ms_d, prof_d = time_device(rd, K, W, world, profile=True)
-        res["decode"] = {"workload": WORKLOADS["decode"]["desc"], "us_per_step": round(ms_d * 1e3, 3),
-                         "steps": K, "error_word": rb_err(rd.cpr), "kernels": kernel_table(prof_d, ms_d)}
+        ms_p, prof_d = time_device(rd, K, W, world, profile=True)
+        out["kernels"] = kernel_table(prof_d, ms_p)
+        out["us_per_step_profiled"] = round(ms_p * 1e3, 3)
         del rd
+        res["decode"] = out
     except Exception as e:   # reported, not fatal to the bench line
         res["decode"] = {"error": f"{type(e).__name__}: {e}"}
     torch.cuda.empty_cache()

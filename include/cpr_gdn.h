@@ -81,6 +81,9 @@ extern "C" {
 #define CPR_ERR_BAD_SEQLENS        8  /* cu_seqlens invalid (device-side)     */
 #define CPR_ERR_DEVICE_TIMEOUT     9  /* a bounded device-side wait expired;
                                          the kernel gave up (device-side)     */
+#define CPR_ERR_COMMIT_DUE        10  /* a no-commit decode step while some
+                                         sequence completes its chunk
+                                         (device-side; nothing written)       */
 
 /* ---- contract --------------------------------------------------------- */
 #define CPR_CONTRACT_VERSION 1u
@@ -281,6 +284,21 @@ int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32],
                         const void* q_t, const void* k_t, const void* v_t, const float* g_t,
                         const float* beta_t, int n_seq, int H, void* cache, void* o_t,
                         void* stream);
+
+/* cpr_gdn_decode_step for a step in which the caller knows that no sequence
+ * completes its chunk (no sequence's position is C - 1 before the step; the
+ * caller knows its sequences' lengths).  Under TOKENREC_V1 the chunk-form
+ * commit is then not launched at all, which leaves the token recurrence's step
+ * alone in C - 1 of every C steps.  The claim is checked on the device against
+ * every sequence's position: if some sequence would complete its chunk, nothing
+ * is written, no position moves, and CPR_ERR_COMMIT_DUE is recorded.  Under
+ * reading A (whose step commits inside its own kernel) it is
+ * cpr_gdn_decode_step.  Same arguments, results and bits as
+ * cpr_gdn_decode_step. */
+int cpr_gdn_decode_step_nocommit(const cpr_contract* c, const uint8_t digest[32],
+                                 const void* q_t, const void* k_t, const void* v_t,
+                                 const float* g_t, const float* beta_t, int n_seq, int H,
+                                 void* cache, void* o_t, void* stream);
 
 /* Trainer backward of cpr_gdn_fwd for the loss  <dO, o> + <dHT, final>.
  * dHT and h0 may be NULL (zeros).  Outputs dq, dk [n_tok,H,d_k], dv

@@ -24,9 +24,11 @@ CPR_OK = 0
 ERRORS = {
     1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CONTRACT_MISMATCH",
     5: "UNALIGNED", 6: "CUDA", 7: "WORKSPACE", 8: "BAD_SEQLENS", 9: "DEVICE_TIMEOUT",
+    10: "COMMIT_DUE",
 }
 CPR_ERR_INVALID_ARG = 1
 CPR_ERR_UNSUPPORTED = 2
+CPR_ERR_COMMIT_DUE = 10
 CPR_DTYPE_F32 = 1
 CPR_DTYPE_BF16 = 2
 CPR_POLICY_SIMT_F32 = 1
@@ -94,6 +96,7 @@ def load_library(path: str = LIB_PATH):
         "cpr_gdn_fwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
         "cpr_gdn_prefill": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, SZ, P]),
         "cpr_gdn_decode_step": (I, [CP, P, P, P, P, P, P, I, I, P, P, P]),
+        "cpr_gdn_decode_step_nocommit": (I, [CP, P, P, P, P, P, P, I, I, P, P, P]),
         "cpr_gdn_bwd": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P, P, P, P,
                             P, SZ, P]),
         "cpr_gdn_fwd_train": (I, [CP, P, P, P, P, P, P, P, I, I64, I, P, P, P, P, SZ, P]),
@@ -422,17 +425,19 @@ def cpr_gdn_prefill(q, k, v, g, beta, cu_seqlens, h0=None, contract: Optional[Co
 
 def cpr_gdn_decode_step(q_t, k_t, v_t, g_t, beta_t, cache: DecodeCache,
                         contract: Optional[Contract] = None, digest: Optional[bytes] = None,
-                        out=None):
-    """One decode step; tokens [n_seq, H, d].  Returns o_t [n_seq, H, d_v] fp32."""
+                        out=None, no_commit: bool = False):
+    """One decode step; tokens [n_seq, H, d].  Returns o_t [n_seq, H, d_v] fp32.
+    no_commit=True (cpr_gdn_decode_step_nocommit): the caller states that no sequence
+    completes its chunk in this step; checked on the device (CPR_ERR_COMMIT_DUE)."""
     lib = load_library()
     c = contract or default_contract(q_t.dtype, q_t.shape[-1], v_t.shape[-1])
     specs, n_seq, H = _tok_specs(c, q_t, k_t, v_t, g_t, beta_t, sfx="_t")
     _check_cache(c, cache, n_seq, H)
     _validate(specs + [("out", out, torch.float32, (n_seq, H, c.d_v)), _blob("cache.blob", cache.blob)])
     o = out if out is not None else torch.empty(n_seq, H, c.d_v, dtype=torch.float32, device=q_t.device)
-    _check(lib.cpr_gdn_decode_step(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t),
-                                   _ptr(v_t), _ptr(g_t), _ptr(beta_t), n_seq, H,
-                                   _ptr(cache.blob), _ptr(o), _stream()))
+    fn = lib.cpr_gdn_decode_step_nocommit if no_commit else lib.cpr_gdn_decode_step
+    _check(fn(ctypes.byref(c), _dig(c, digest), _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(g_t),
+              _ptr(beta_t), n_seq, H, _ptr(cache.blob), _ptr(o), _stream()))
     return o
 
 

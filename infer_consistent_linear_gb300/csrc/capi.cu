@@ -445,7 +445,7 @@ int reading_b_forward(const cpr_contract* c, const uint8_t* digest, const void* 
 // every kernel before it reads past the header.
 int reading_b_step(const cpr_contract* c, const uint8_t* digest, const void* q_t, const void* k_t,
                    const void* v_t, const float* g_t, const float* beta_t, int n_seq, int H,
-                   void* cache, void* o_t, void* stream) {
+                   void* cache, void* o_t, void* stream, bool no_commit) {
     int rc = check_digest(c, digest);
     if (rc) return rc;
     rc = check_sizes(n_seq, 0, H);
@@ -471,13 +471,14 @@ int reading_b_step(const cpr_contract* c, const uint8_t* digest, const void* q_t
     a.state = reinterpret_cast<const float*>(cb + cl.state); a.run = reinterpret_cast<float*>(cb + cl.run);
     a.rk = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_k); a.rv = reinterpret_cast<__nv_bfloat16*>(cb + cl.rb_v);
     a.rg = reinterpret_cast<float*>(cb + cl.rb_g); a.rbeta = reinterpret_cast<float*>(cb + cl.rb_beta);
-    a.o = static_cast<float*>(o_t); a.err = err;
+    a.o = static_cast<float*>(o_t); a.err = err; a.no_commit = no_commit ? 1 : 0;
     cudaError_t e;
     {
         cpr::ProfScope ps("cpr_reading_b_step", st);
         e = cpr::rb_step_launch(a, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading-B step launch");
+    if (no_commit) return CPR_OK;   // the step kernel checked the claim
     // the commit: n_seq full chunks from the token rows; only completed ones run
     const WsLayout w = commit_ws(*c, n_seq, H);
     cpr::tc::TcArgs t{};
@@ -811,7 +812,16 @@ int cpr_gdn_decode_step(const cpr_contract* c, const uint8_t digest[32], const v
                         const void* k_t, const void* v_t, const float* g_t, const float* beta_t,
                         int n_seq, int H, void* cache, void* o_t, void* stream) {
     if (reading_b(c))
-        return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+        return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream, false);
+    return decode_impl(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
+}
+
+int cpr_gdn_decode_step_nocommit(const cpr_contract* c, const uint8_t digest[32], const void* q_t,
+                                 const void* k_t, const void* v_t, const float* g_t,
+                                 const float* beta_t, int n_seq, int H, void* cache, void* o_t,
+                                 void* stream) {
+    if (reading_b(c))
+        return reading_b_step(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream, true);
     return decode_impl(c, digest, q_t, k_t, v_t, g_t, beta_t, n_seq, H, cache, o_t, stream);
 }
 

@@ -190,20 +190,29 @@ __global__ void __launch_bounds__(256) k_rb(RbArgs a) {
 // (the chunk form's prep and state pass over the buffered chunk, launched after this
 // kernel) reads once the chunk is complete.  The last CTA moves every position on.  A
 // cache whose header is not this contract's is left untouched (nothing past its header
-// is read) and CPR_ERR_CONTRACT_MISMATCH is recorded.
+// is read) and CPR_ERR_CONTRACT_MISMATCH is recorded.  Under the caller's no-commit claim
+// every CTA reads every sequence's position: if one is C - 1 (its chunk would complete, but
+// no commit follows) every CTA leaves, nothing is written and CPR_ERR_COMMIT_DUE is recorded.
 __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
     constexpr int D = 128;
     __shared__ RecSmem<D> s;
     __shared__ int ok_s;
     const int tid = threadIdx.x, j = tid % D, part = tid / D;
     const int H = a.H, b = blockIdx.x / H, h = blockIdx.x % H;
-    if (tid < 32) {   // the header (a word per lane), then the position once it is right
+    if (tid < 32) {   // the header (a word per lane), then the positions once it is right
         bool ok = cache_header_ok(a.header, a.digest, a.hdr);
+        bool due = false;
+        if (ok && a.no_commit) {
+            bool d = false;
+            for (int sq = tid; sq < a.n_seq; sq += 32) d = d | (a.pos[sq] == kChunk - 1);
+            due = __any_sync(0xffffffffu, d);
+        }
         if (tid == 0) {
             const int p = ok ? a.pos[b] : -1;
             if (!(p >= 0 && p < kChunk)) ok = false;
             if (!ok) set_error(a.err, CPR_ERR_CONTRACT_MISMATCH);
-            ok_s = ok ? 1 + p : 0;
+            else if (due) set_error(a.err, CPR_ERR_COMMIT_DUE);
+            ok_s = (ok && !due) ? 1 + p : 0;
         }
     }
     __syncthreads();

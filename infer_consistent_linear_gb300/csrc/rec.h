@@ -95,6 +95,7 @@ struct RbStepArgs {           // reading B decode step (d = 128, bf16 io)
     float* rbeta;
     float* o;
     uint32_t* err;
+    int no_commit;            // the caller's claim that no sequence completes its chunk now
 };
 
 struct RbFillArgs {           // reading B prefill: the partial last chunk's rows into a cache

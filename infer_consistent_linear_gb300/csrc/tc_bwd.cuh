@@ -540,7 +540,7 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
     const int wn = w + (int)gridDim.x;         // the next item of this CTA
     const int h = w % H;
     if (nx_b < 0) locate(w);                   // the CTA's first item
-    const int b = nx_b, n = nx_n, seq0 = nx_seq0, T = nx_T;
+    const int n = nx_n, seq0 = nx_seq0, T = nx_T;
     nx_b = -1;
     const int t0 = seq0 + n * C;
     const int nrows = min(C, T - n * C);

@@ -175,6 +175,75 @@ def test_reading_b_decode_equals_reading_b_prefill():
     assert cpr.get_device_error() == 0
 
 
+def test_reading_b_nocommit_steps_same_bits():
+    """cpr_gdn_decode_step_nocommit on every step in which no sequence completes its chunk
+    (the caller tracks the positions from its own lengths) and cpr_gdn_decode_step on the
+    others: the same bits as a one-shot forward, and the same committed states."""
+    pre, steps, H = [100, 64, 0, 37, 130], 70, 2
+    full = [L + steps for L in pre]
+    x = make_inputs(full, H, 128, 128, io_dtype=torch.bfloat16, seed=10, h0_std=0.1).to(DEV)
+    cb = _rb()
+    o_full, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, h0=x.h0, contract=cb)
+    cu = x.cu_seqlens.tolist()
+    sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(len(pre))]).to(DEV)
+    cu_pre = torch.tensor([0] + torch.cumsum(torch.tensor(pre), 0).tolist(), dtype=torch.int32, device=DEV)
+    _, _, cache = cpr.cpr_gdn_prefill(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel], cu_pre,
+                                      h0=x.h0, contract=cb)
+    n_free = 0
+    for t in range(steps):
+        idx = torch.tensor([cu[b] + pre[b] + t for b in range(len(pre))], device=DEV)
+        free = all((pre[b] + t) % 64 != 63 for b in range(len(pre)))
+        n_free += free
+        ot = cpr.cpr_gdn_decode_step(x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx], cache, contract=cb,
+                                     no_commit=free)
+        assert_bitwise(f"reading-B decode step {t} (no_commit={free})", ot, o_full[idx])
+        for b in range(len(pre)):
+            n_done = pre[b] + t + 1
+            if n_done % 64 == 0:
+                sl = slice(cu[b], cu[b] + n_done)
+                _, fin = cpr.cpr_gdn_fwd(x.q[sl], x.k[sl], x.v[sl], x.g[sl], x.beta[sl],
+                                         torch.tensor([0, n_done], dtype=torch.int32, device=DEV),
+                                         h0=x.h0[b:b + 1], contract=_tc())
+                assert_bitwise(f"committed state seq {b} at {n_done}", cache.state()[b:b + 1], fin)
+    torch.cuda.synchronize()
+    assert cpr.get_device_error() == 0
+    assert 0 < n_free < steps
+
+
+def test_reading_b_nocommit_refused_when_a_chunk_completes():
+    """A no-commit step while a sequence sits at its chunk's last row (its step would
+    complete the chunk) is refused on the device: nothing is written, no position moves,
+    CPR_ERR_COMMIT_DUE is recorded; the ordinary step then runs as usual.  Under reading A,
+    whose step commits inside its own kernel, the claim changes nothing."""
+    x = make_inputs([64 + 63 + 1, 10 + 1], 2, 128, 128, io_dtype=torch.bfloat16, seed=12).to(DEV)
+    cu = x.cu_seqlens.tolist()
+    pre = [127, 10]
+    sel = torch.cat([torch.arange(cu[b], cu[b] + pre[b]) for b in range(2)]).to(DEV)
+    cu_pre = torch.tensor([0, 127, 137], dtype=torch.int32, device=DEV)
+    idx = torch.tensor([cu[0] + 127, cu[1] + 10], device=DEV)
+    tok = (x.q[idx], x.k[idx], x.v[idx], x.g[idx], x.beta[idx])
+    for c in (_rb(), _tc()):
+        o_full, _ = cpr.cpr_gdn_fwd(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, contract=c)
+        _, _, cache = cpr.cpr_gdn_prefill(x.q[sel], x.k[sel], x.v[sel], x.g[sel], x.beta[sel], cu_pre,
+                                          contract=c)
+        assert cpr.get_device_error(clear=True) == 0
+        if c.intra_order == cpr.CPR_ORDER_TOKENREC_V1:
+            before = cache.blob.clone()
+            o = torch.full((2, 2, 128), 7.0, device=DEV)
+            cpr.cpr_gdn_decode_step(*tok, cache, contract=c, out=o, no_commit=True)
+            torch.cuda.synchronize()
+            assert cpr.get_device_error(clear=True) == cpr.CPR_ERR_COMMIT_DUE
+            assert torch.equal(cache.blob, before)
+            assert bool((o == 7.0).all())
+            ot = cpr.cpr_gdn_decode_step(*tok, cache, contract=c)
+        else:
+            ot = cpr.cpr_gdn_decode_step(*tok, cache, contract=c, no_commit=True)
+        torch.cuda.synchronize()
+        assert cpr.get_device_error(clear=True) == 0
+        assert_bitwise(f"step after the claim ({'B' if c.intra_order == cpr.CPR_ORDER_TOKENREC_V1 else 'A'})",
+                       ot, o_full[idx])
+
+
 def test_reading_a_cache_refused_by_reading_b_decode():
     """A decode cache made under reading A carries reading A's digest and layout.  The
     binding refuses it for a reading-B decode step on the host (its layout is not reading
