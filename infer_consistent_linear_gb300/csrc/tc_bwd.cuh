@@ -688,10 +688,18 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         for (int j = 0; j < 32; ++j) scr[r * 65 + s0 + j] = __fadd_rn(scr[r * 65 + s0 + j], bloc[j]);
     }
     __syncthreads();
-    if (tid < C) {  // column sums colE_s = sum_{r > s} t_rs
+    if (tid < C) {  // column sums colE_s = sum_{r > s} t_rs, ascending r (16 loads, then their adds)
         const int s = tid;
         float acc = 0.f;
-        for (int rr = s + 1; rr < nrows; ++rr) acc = __fadd_rn(acc, scr[rr * 65 + s]);
+#pragma unroll
+        for (int r0 = 0; r0 < C; r0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = scr[(r0 + e) * 65 + s];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (r0 + e > s && r0 + e < nrows) acc = __fadd_rn(acc, v[e]);
+        }
         colE[s] = acc;
     }
     {
@@ -788,16 +796,32 @@ static __global__ void __launch_bounds__(256, 1) k_tc_grad(TcBwdArgs a) {
         float dgr = eL[rr];
         if (rr == Lr) {
             float sumL = 0.f, rs = 0.f;
-            for (int s = 0; s < Lr; ++s) sumL = __fadd_rn(sumL, dgam[s]);
+#pragma unroll
+            for (int s0 = 0; s0 < C; s0 += 16) {   // ascending s (16 loads, then their adds)
+                float v[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = dgam[s0 + e];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (s0 + e < Lr) sumL = __fadd_rn(sumL, v[e]);
+            }
             for (int w = 0; w < a.nsplit; ++w) rs = __fadd_rn(rs, red[w]);
             dgr = __fadd_rn(dgr, __fadd_rn(__fmul_rn(Gm[Lr], rs), sumL));
         }
         colE[rr] = (rr < nrows) ? dgr : 0.f;   // dgam_r
     }
     __syncthreads();
-    if (tid < nrows) {  // dg_s = sum_{r=s}^{L} dgam_r, from the last row down
+    if (tid < nrows) {  // dg_s = sum_{r=s}^{L} dgam_r, from the last row down (16 loads, then their adds)
         float acc = 0.f;
-        for (int rr = Lr; rr >= tid; --rr) acc = __fadd_rn(acc, colE[rr]);
+#pragma unroll
+        for (int r0 = C - 1; r0 >= 0; r0 -= 16) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = colE[r0 - e];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (r0 - e <= Lr && r0 - e >= tid) acc = __fadd_rn(acc, v[e]);
+        }
         a.dg[(size_t)(t0 + tid) * H + h] = acc;
     }
     {
