@@ -116,6 +116,23 @@ class _Nvml:
         return float(mhz.value), [n for n, b in self.BITS.items() if bits & b]
 
 
+def gpu_local_cpus(index):
+    """The host CPUs NVML names as nearest the GPU that torch calls `index` (read-only
+    query), intersected with the CPUs this process may run on; None when unknown."""
+    try:
+        import ctypes
+        n = _Nvml(index)
+        words = ((os.cpu_count() or 64) + 63) // 64
+        mask = (ctypes.c_ulong * words)()
+        if n.lib.nvmlDeviceGetCpuAffinity(n.h, ctypes.c_uint(words), mask) != 0:
+            return None
+        near = {w * 64 + b for w in range(words) for b in range(64) if (mask[w] >> b) & 1}
+        sel = near & os.sched_getaffinity(0)
+        return sel or None
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons while running: NVML every millisecond when the
     driver's library loads (a timed region can be a few milliseconds), else nvidia-smi every
@@ -459,7 +476,21 @@ def time_e2e(step, K, W, world):
     inputs host->device and its results device->host inside the timed region.  The copies
     run on their own streams with two sets of device buffers, so that step i + 1's upload
     and step i - 1's download overlap step i's kernels, as a serving loop would run them.
-    Returns (ms_per_step, h2d_bytes, d2h_bytes)."""
+    The host side runs on the CPUs nearest the GPU, as a serving process would be placed,
+    so that the pinned buffers (first touched here) live in that CPU's memory; the process's
+    CPU set is restored afterwards.  Returns (ms_per_step, h2d_bytes, d2h_bytes, cpus)."""
+    allowed = os.sched_getaffinity(0)
+    near = gpu_local_cpus(torch.cuda.current_device())
+    if near and near != allowed:
+        os.sched_setaffinity(0, near)
+    try:
+        r = _time_e2e(step, K, W, world)
+    finally:
+        os.sched_setaffinity(0, allowed)
+    return r + (len(near) if near else None,)
+
+
+def _time_e2e(step, K, W, world):
     cs = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     if step.op == "decode":
@@ -1289,9 +1320,10 @@ def main():
     value = value_of(name, ms, step.tokens_per_step(), world)
     e2e = None
     if not args.no_e2e:
-        e_ms, h2d, d2h = time_e2e(step, K, W, world)
+        e_ms, h2d, d2h, ncpu = time_e2e(step, K, W, world)
         e2e = {"value": value_of(name, e_ms, step.tokens_per_step(), world), "unit": unit,
-               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "host_cpus_near_gpu": ncpu}
     extra = {}
     if WORKLOADS[name]["op"] == "decode":
         extra["bitwise_decode_vs_prefill"] = decode_bitwise(step, n_dec)
