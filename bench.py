@@ -786,6 +786,55 @@ def decode_bitwise(step, n_done):
     return bool(torch.equal(ref.view(torch.int32), step.o_steps[:n_done].contiguous().view(torch.int32)))
 
 
+def decode_step_stats(step, K, W):
+    """The Decode workload's steps again, from the cache right after the prefill: first
+    each step timed on its own (events between steps), for the median; then the same W + K
+    steps with the last K captured once as a CUDA graph through the public API and
+    replayed, timed as a whole.  The replayed outputs are compared bit for bit with the
+    eager ones."""
+    res = {}
+    step.cache.blob.copy_(step.blob0)
+    step.t = 0
+    for _ in range(W):
+        step.run()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record()
+    for i in range(K):
+        step.run()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(K)]
+    res.update(us_per_step_median=round(statistics.median(per), 3), us_per_step_min=round(min(per), 3),
+               us_per_step_max=round(max(per), 3))
+    eager = step.o_steps[W:W + K].clone()
+    try:
+        step.cache.blob.copy_(step.blob0)
+        step.t = 0
+        for _ in range(W):
+            step.run()
+        torch.cuda.synchronize()
+        snap = step.cache.blob.clone()
+        step.o_steps[W:W + K].zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(K):
+                step.run()
+        torch.cuda.synchronize()
+        step.cache.blob.copy_(snap)      # capturing ran nothing; replay from the same cache
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        res["us_per_step_graph"] = round(s.elapsed_time(e) * 1e3 / K, 3)
+        res["graph_bitwise_equal_to_eager"] = bool(torch.equal(
+            eager.view(torch.int32), step.o_steps[W:W + K].contiguous().view(torch.int32)))
+        del g
+    except Exception as exc:   # reported, not fatal to the bench line
+        res["graph_error"] = f"{type(exc).__name__}: {exc}"
+    return res
+
+
 def secondary(name, dev, world, local, steps, warmup, pk, policy):
     n_dec = steps + warmup if WORKLOADS[name]["op"] == "decode" else 0
     st = OurStep(name, dev, n_decode_steps=n_dec, policy=policy)
@@ -797,6 +846,7 @@ def secondary(name, dev, world, local, steps, warmup, pk, policy):
            "kernels": kernel_table(prof, ms)}
     if WORKLOADS[name]["op"] == "decode":
         res["bitwise_decode_vs_prefill"] = decode_bitwise(st, n_dec)
+        res.update(decode_step_stats(st, steps, warmup))
     del st
     torch.cuda.empty_cache()
     return res
@@ -1327,6 +1377,7 @@ def main():
     extra = {}
     if WORKLOADS[name]["op"] == "decode":
         extra["bitwise_decode_vs_prefill"] = decode_bitwise(step, n_dec)
+        extra.update(decode_step_stats(step, K, W))
     line ={"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms, 4), "higher_is_better": hib, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16x3 MMA, f32 accumulate" if args.policy == "tc" else "f32",
