@@ -630,6 +630,7 @@ def roofline_for(step, prof, pk):
         ach = byt16 / avg_s / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "traffic_gbs": round(traffic / avg_s / 1e9, 1) if traffic else None,
                 "avg_launch_us": round(avg_s * 1e6, 2), "algo_bytes_per_launch": byt16,
                 "bytes_rule": "all of the step's algorithmic bytes, o counted in bf16 (1,032 B per "
                               "head-token forward) plus the states, over this kernel's launch time",
@@ -645,6 +646,7 @@ def roofline_for(step, prof, pk):
         ach = byt / avg_s / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "traffic_gbs": round(traffic / avg_s / 1e9, 1) if traffic else None,
                 "avg_launch_us": round(avg_s * 1e6, 2), "algo_bytes_per_launch": byt}
     fl = simt_kernel_flops_per_chunk(name, step.d)
     if fl is None:
