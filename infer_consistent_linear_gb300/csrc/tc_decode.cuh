@@ -125,8 +125,12 @@ __device__ __forceinline__ void store_row128(float* dst, const float (&v)[128]) 
 // products the prefill takes as M = 128 groups ([K; Q] K^T and [W'; Q] H) run here as
 // M = 64 groups over an A tile that holds just the two rows (p and p ^ 32): an output
 // element's bits do not depend on the instruction's M or N, nor on which row it sits in.
+// 160 threads: warps 0..3 do the unit's operand and epilogue work, warp 4 only issues the
+// MMA groups (about 56 cycles an instruction, during which the issuing warp does nothing else).
+constexpr int kDecThreads = 160, kDecIssuer = 128;
+
 template <int DVS>
-__global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     using S = DecSmem;
     extern __shared__ __align__(1024) unsigned char sm[];
     float* F = reinterpret_cast<float*>(sm + S::F);
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     fence_async_smem();
     tc_sync();
     if (has_next) pn = pos[un / H];
-    if (tid == 0) {
+    if (tid == kDecIssuer) {
         mma_tile<64, 64, D>(tmem, R1, sm + S::Kmn, false);
         mma_commit(mbar);
     }
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     fence_async_smem();
     tc_sync();
-    if (tid == 0) {
+    if (tid == kDecIssuer) {
         mma_tile_mj<64, D, C, false, true>(tmem, R1, sm + S::Kmn, false);
         mma_tile_mj<64, D, C, false, true>(tmem, R1 + 8192, sm + S::Kmn, true);
         mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 16384, sm + S::Vt, false);
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     __syncthreads();
     fence_async_smem();
     tc_sync();
-    if (tid == 0) {
+    if (tid == kDecIssuer) {
         mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hhi, false);
         mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hlo, true);
         mma_tile_mj<64, D, D, false, true>(tmem, R1 + 32768, sm + S::Hhi, true);
@@ -434,9 +438,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         else if (tid == lane_m64(p ^ 32)) store_row128(row2, v);
     }
     __syncthreads();
-    {
+    if (tid < D) {
         const float Gp = simt::gate(gams[p], gmls[p]);
-        const int j = tid;  // D == 128 == blockDim
+        const int j = tid;
         Dp[j] = __fsub_rn(Up[j], row1[j]);
         Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
     }
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
     }
     fence_async_smem();
     tc_sync();
-    if (tid == 0) {
+    if (tid == kDecIssuer) {
         mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt, false);
         mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt + 16384, true);
         mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 8192, sm + S::Dt, true);
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         if (lane == (p & 15)) store_row128(row1, v);
     }
     __syncthreads();
-    a.o[sh * D + tid] = __fadd_rn(Qs[tid], row1[tid]);
+    if (tid < D) a.o[sh * D + tid] = __fadd_rn(Qs[tid], row1[tid]);
     {
         // append row p to the cache (k and v as rows of their operand tiles; a committing
         // step clears those tiles for the next chunk instead)
@@ -492,7 +496,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
             else if (tid >= 32 && tid < 48)
                 *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(cv) + cm_off(p, (tid - 32) * 8, D)) = rowreg;
         }
-        cd[(size_t)p * D + tid] = Dp[tid];
+        if (tid < D) cd[(size_t)p * D + tid] = Dp[tid];
         if (tid < C) ct[p * C + tid] = trow[tid];
         if (tid == 0) {
             cg[p] = gams[p];
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         }
         fence_async_smem();
         tc_sync();
-        if (tid == 0) {
+        if (tid == kDecIssuer) {
             mma_tile_mj<128, D, C, true, true>(tmem, sm + S::Kmn, R1 + 16384, false);
             mma_tile_mj<128, D, C, true, true>(tmem, sm + S::Kmn, R1 + 32768, true);
             mma_commit(mbar);
@@ -556,7 +560,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
         const float GL = simt::gate(gams[Lr], gmls[Lr]);
         float v[32];
         const int d = tid;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D && tid < D; c0 += 32) {
             tmem_ld32(taddr_of(tmem, warp, c0), v);
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {
@@ -576,11 +580,11 @@ __global__ void __launch_bounds__(128, 1) k_tc_decode(TcDecArgs a) {
                 *reinterpret_cast<uint4*>(cst + 32768 + off) = lo;
             }
         }
-        for (int i = tid; i < C * D / 8; i += 128) {  // the next chunk starts with no K, V, Delta rows
+        for (int i = tid; i < C * D / 8; i += kDecThreads) {  // the next chunk starts with no K, V, Delta rows
             reinterpret_cast<uint4*>(ck)[i] = make_uint4(0u, 0u, 0u, 0u);
             reinterpret_cast<uint4*>(cv)[i] = make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int i = tid; i < 32768 / 16; i += 128) reinterpret_cast<uint4*>(cdt)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < 32768 / 16; i += kDecThreads) reinterpret_cast<uint4*>(cdt)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
     p = pn;

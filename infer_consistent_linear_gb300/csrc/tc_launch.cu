@@ -67,7 +67,7 @@ cudaError_t decode(const tc::TcDecArgs& a, cudaStream_t st) {
     const int64_t grid = units < nsm ? units : nsm;
     if (grid > 0) {
         ProfScope ps("cpr_tc_decode", st);
-        kern<<<(unsigned)grid, 128, sm, st>>>(a);
+        kern<<<(unsigned)grid, tc::kDecThreads, sm, st>>>(a);
     }
     return cudaGetLastError();
 }
