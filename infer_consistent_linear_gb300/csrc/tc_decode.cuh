@@ -268,24 +268,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     float* Hst = reinterpret_cast<float*>(a.cache + a.co.state) + sh * D * D;
     unsigned char* cst = a.cache + a.co.state_tiles + sh * 65536;     // state hi | lo tiles
     unsigned char* cdt = a.cache + a.co.delta_tiles + sh * 32768;     // Delta hi | lo tiles
-    {
-        // this unit's K and V tiles have landed: row p from the new token; the S1 operand
-        // (R1's first 16 KB) takes k_p as row p and q_p as row p ^ 32 (its other rows reach
-        // only accumulator rows never read)
-        const bool w = mbar_wait(bar_KV, ph_KV, a.err);
-        if (w) {
-            ph_KV ^= 1u;
-            pend_KV = false;
+    // once this unit's K and V tiles have landed (each thread waits itself): row p from the
+    // new token; the S1 operand (R1's first 16 KB) takes k_p as row p and q_p as row p ^ 32
+    // (its other rows reach only accumulator rows never read)
+    const bool wkv = mbar_wait(bar_KV, ph_KV, a.err);
+    if (wkv) {
+        ph_KV ^= 1u;
+        pend_KV = false;
+        if (tid < 16) {
+            *reinterpret_cast<uint4*>(R1 + cm_off(p ^ 32, tid * 8, D)) = rowreg;
+        } else if (tid < 32) {
+            *reinterpret_cast<uint4*>(sm + S::Kmn + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+            *reinterpret_cast<uint4*>(R1 + cm_off(p, (tid - 16) * 8, D)) = rowreg;
+        } else if (tid < 48) {
+            *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
         }
-        if (__syncthreads_or(!w)) { ok = false; break; }
-    }
-    if (tid < 16) {
-        *reinterpret_cast<uint4*>(R1 + cm_off(p ^ 32, tid * 8, D)) = rowreg;
-    } else if (tid < 32) {
-        *reinterpret_cast<uint4*>(sm + S::Kmn + cm_off(p, (tid - 16) * 8, D)) = rowreg;
-        *reinterpret_cast<uint4*>(R1 + cm_off(p, (tid - 16) * 8, D)) = rowreg;
-    } else if (tid < 48) {
-        *reinterpret_cast<uint4*>(sm + S::Vt + cm_off(p, (tid - 32) * 8, D)) = rowreg;
     }
     if (tid < p) {
         gams[tid] = cgv;
@@ -300,7 +297,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         bets[p] = bnew;
     }
     fence_async_smem();
-    tc_sync();
+    fence_before();
+    if (__syncthreads_or(!wkv)) { ok = false; break; }
+    fence_after();
     if (has_next) pn = pos[un / H];
     if (tid == kDecIssuer) {
         mma_tile<64, 64, D>(tmem, R1, sm + S::Kmn, false);
@@ -348,20 +347,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
                 if (s >= j && s < p) acc = f;
             }
         }
-        trow[j] = (j < p) ? -acc : (j == p ? 1.f : 0.f);
-    }
-    __syncthreads();
-    if (tid < 16) {
-        const int which = tid >> 3, s8 = tid & 7;
-        unsigned char* xhi = R1 + which * 16384;
-        const float* sc = which ? bets : bgs;
+        const float tj = (j < p) ? -acc : (j == p ? 1.f : 0.f);
+        trow[j] = tj;
+        // X row p, entry j: T_pj (b_j Gamma_j) and T_pj b_j, split hi + lo
+        const uint32_t off = cm_off(p, j, C);
+        __nv_bfloat16 hi, lo;
+        split_bf16(j <= p ? __fmul_rn(tj, bgs[j]) : 0.f, hi, lo);
+        *reinterpret_cast<__nv_bfloat16*>(R1 + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(R1 + 8192 + off) = lo;
+        split_bf16(j <= p ? __fmul_rn(tj, bets[j]) : 0.f, hi, lo);
+        *reinterpret_cast<__nv_bfloat16*>(R1 + 16384 + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(R1 + 24576 + off) = lo;
+    } else if (tid < C + C / 8) {  // P row p (R1 + 48 KB: hi, + 56 KB: lo), for P Delta
+        const int s8 = tid - C;
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int s = s8 * 8 + e;
-            x[e] = s <= p ? __fmul_rn(trow[s], sc[s]) : 0.f;
-        }
-        store8_split(xhi, xhi + 8192, cm_off(p, s8 * 8, C), x);
+        for (int e = 0; e < 8; ++e) x[e] = prow[s8 * 8 + e];
+        store8_split(R1 + 49152, R1 + 57344, cm_off(p, s8 * 8, C), x);
     }
     fence_async_smem();
     tc_sync();
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         for (int e = 0; e < 8; ++e) x[e] = Wp[d8 * 8 + e];
         store8_split(R1, R1 + 32768, cm_off(p, d8 * 8, D), x);
     }
+    fence_async_smem();
     {
         // the state tiles and the Delta tiles have landed (row p is written below, and rows
         // past it only meet zero P entries)
@@ -412,11 +415,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
             ph_D ^= 1u;
             pend_D = false;
         }
+        fence_before();
         if (__syncthreads_or(!(wh && wd))) { ok = false; break; }
+        fence_after();
     }
-    __syncthreads();
-    fence_async_smem();
-    tc_sync();
     if (tid == kDecIssuer) {
         mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hhi, false);
         mma_tile_mj<64, D, D, false, true>(tmem, R1, sm + S::Hlo, true);
@@ -438,15 +440,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         else if (tid == lane_m64(p ^ 32)) store_row128(row2, v);
     }
     __syncthreads();
-    if (tid < D) {
+    if (tid < D) {  // Delta row p, and its entry j in the Delta tiles, split hi + lo
         const float Gp = simt::gate(gams[p], gmls[p]);
         const int j = tid;
-        Dp[j] = __fsub_rn(Up[j], row1[j]);
+        const float dj = __fsub_rn(Up[j], row1[j]);
+        Dp[j] = dj;
         Qs[j] = __fmul_rn(Gp, __fmul_rn(a.scale, row2[j]));
+        __nv_bfloat16 hi, lo;
+        split_bf16(dj, hi, lo);
+        const uint32_t off = mn_off(j, p, D);
+        *reinterpret_cast<__nv_bfloat16*>(sm + S::Dt + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(sm + S::Dt + 16384 + off) = lo;
     }
-    // P row p (R1 + 0: hi, + 8 KB: lo); Delta row p into the Delta tiles and the cache
-    __syncthreads();
-    if (tid < D / 8) {
+    fence_async_smem();
+    tc_sync();
+    if (tid == kDecIssuer) {
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 49152, sm + S::Dt, false);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 49152, sm + S::Dt + 16384, true);
+        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 57344, sm + S::Dt, true);
+        mma_commit(mbar);
+    }
+    mma_out = true;
+    if (tid < D / 8) {  // the cache's copy of Delta row p, while P Delta runs
         const int j8 = tid;
         float x[8];
 #pragma unroll
@@ -454,26 +469,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         uint4 hi, lo;
         split8(x, hi, lo);
         const uint32_t off = mn_off(j8 * 8, p, D);
-        *reinterpret_cast<uint4*>(sm + S::Dt + off) = hi;
-        *reinterpret_cast<uint4*>(sm + S::Dt + 16384 + off) = lo;
         *reinterpret_cast<uint4*>(cdt + off) = hi;
         *reinterpret_cast<uint4*>(cdt + 16384 + off) = lo;
-    } else if (tid >= 64 && tid < 64 + C / 8) {
-        const int s8 = tid - 64;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = prow[s8 * 8 + e];
-        store8_split(R1, R1 + 8192, cm_off(p, s8 * 8, C), x);
     }
-    fence_async_smem();
-    tc_sync();
-    if (tid == kDecIssuer) {
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt, false);
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1, sm + S::Dt + 16384, true);
-        mma_tile_mj<64, D, C, false, true>(tmem + 128, R1 + 8192, sm + S::Dt, true);
-        mma_commit(mbar);
-    }
-    mma_out = true;
     if (!mma_wait()) { ok = false; break; }
     if (tid == 0 && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
         fence_async_smem();                    // (a committing unit stages its rows there first)
