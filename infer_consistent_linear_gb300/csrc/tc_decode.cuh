@@ -126,7 +126,8 @@ __device__ __forceinline__ void store_row128(float* dst, const float (&v)[128]) 
 // M = 64 groups over an A tile that holds just the two rows (p and p ^ 32): an output
 // element's bits do not depend on the instruction's M or N, nor on which row it sits in.
 // 160 threads: warps 0..3 do the unit's operand and epilogue work, warp 4 only issues the
-// MMA groups (about 56 cycles an instruction, during which the issuing warp does nothing else).
+// MMA groups (about 56 cycles an instruction, during which the issuing warp does nothing else)
+// and the bulk copies.
 constexpr int kDecThreads = 160, kDecIssuer = 128;
 
 template <int DVS>
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     }
     mma_out = true;
     if (!mma_wait()) { ok = false; break; }
-    if (tid == 0 && has_next && p != C - 1) {  // K and V are consumed (a committing unit still
+    if (tid == kDecIssuer && has_next && p != C - 1) {  // K and V are consumed (a committing unit still
         fence_async_smem();                    // needs K): the next unit's tiles
         issue_KV(un, pn);
     }
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     mma_out = true;
     if (has_next) load_rows(un, pn);   // the next unit's token rows land while A4 runs
     if (!mma_wait()) { ok = false; break; }
-    if (tid == 0 && has_next) {  // the state tiles are consumed: the next unit's
+    if (tid == kDecIssuer && has_next) {  // the state tiles are consumed: the next unit's
         fence_async_smem();
         issue_H(un);
     }
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         *reinterpret_cast<uint4*>(cdt + 16384 + off) = lo;
     }
     if (!mma_wait()) { ok = false; break; }
-    if (tid == 0 && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
+    if (tid == kDecIssuer && has_next && p != C - 1) {  // the Delta tiles are consumed: the next unit's
         fence_async_smem();                    // (a committing unit stages its rows there first)
         issue_D(un, pn);
     }
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     }
     if (p == C - 1) {  // resynchronise: commit the next chunk-start state
         const int Lr = C - 1;
-        if (tid == 0) {  // the chunk's other fp32 Delta rows (the Delta tiles are consumed)
+        if (tid == kDecIssuer) {  // the chunk's other fp32 Delta rows (the Delta tiles are consumed)
             fence_async_smem();
             mbar_expect_tx(bar_D, (uint32_t)p * D * 4);
             bulk_g2s(stage, cd, (uint32_t)p * D * 4, bar_D);
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         }
         mma_out = true;
         if (!mma_wait()) { ok = false; break; }
-        if (tid == 0 && has_next) {  // K and the staged rows are consumed: the next unit's
+        if (tid == kDecIssuer && has_next) {  // K and the staged rows are consumed: the next unit's
             fence_async_smem();      // K, V and Delta tiles
             issue_KV(un, pn);
             issue_D(un, pn);
