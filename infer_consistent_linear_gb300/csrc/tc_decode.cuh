@@ -308,6 +308,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     }
     mma_out = true;
     if (tid <= p) bgs[tid] = simt::bg_entry(bets[tid], gams[tid], gmls[tid]);
+    // while S1 runs: the exponentials of row p's A and P entries and Gamma_p (the factors
+    // a_entry, p_entry and the state scaling take, in their order)
+    const float Gp = simt::gate(gams[p], gmls[p]);
+    float Eps = 0.f, bEps = 0.f;
+    if (tid < C) {
+        Eps = simt::decay(gams[p], gmls[p], gams[tid], gmls[tid]);
+        bEps = __fmul_rn(bets[p], Eps);
+    }
     if (!mma_wait()) { ok = false; break; }
     if (warp == (p >> 4) || warp == ((p ^ 32) >> 4)) {   // the lane quarters of rows p, p ^ 32
         float v0[32], v1[32];
@@ -324,9 +332,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     __syncthreads();
     if (tid < C) {
         const int s = tid;
-        const float gp = gams[p], lp = gmls[p], bp = bets[p];
-        arow[s] = (s < p) ? simt::a_entry(bp, gp, lp, gams[s], gmls[s], row1[s]) : 0.f;
-        prow[s] = (s <= p) ? __fmul_rn(simt::decay(gp, lp, gams[s], gmls[s]), __fmul_rn(a.scale, row2[s])) : 0.f;
+        arow[s] = (s < p) ? __fmul_rn(bEps, row1[s]) : 0.f;
+        prow[s] = (s <= p) ? __fmul_rn(Eps, __fmul_rn(a.scale, row2[s])) : 0.f;
     }
     // X tiles (R1 + 0 .. 32 KB, row p only) and the T row
     __syncthreads();
@@ -442,7 +449,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     }
     __syncthreads();
     if (tid < D) {  // Delta row p, and its entry j in the Delta tiles, split hi + lo
-        const float Gp = simt::gate(gams[p], gmls[p]);
         const int j = tid;
         const float dj = __fsub_rn(Up[j], row1[j]);
         Dp[j] = dj;
