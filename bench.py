@@ -620,7 +620,8 @@ def roofline_for(step, prof, pk):
     units = step.kernel_units(name)
     traffic = None
     tr = load_traffic().get(f"{name}/{step.name}")
-    if tr and tr.get("kernel_src_sha") == kernel_src_sha(name):
+    # (stored for the full workload: a run on part of it, --n-seq, has none)
+    if tr and tr.get("kernel_src_sha") == kernel_src_sha(name) and not N_SEQ_OVERRIDE:
         traffic = tr.get("bytes_per_launch")
     tfl = tc_kernel_flops_per_chunk(name, step.d)
     if tfl is not None:
