@@ -53,6 +53,21 @@ struct TcDecArgs {
     uint32_t* err;
 };
 
+// A bulk copy (as bulk_g2s) with an L2 eviction-priority hint, a cache policy from
+// l2_policy: data read once per step can leave L2 before the data every step reads again.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src, uint32_t bytes, uint64_t* mbar,
+                                              uint64_t policy) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(mbar)), "l"(policy) : "memory");
+}
+template <bool LAST>
+__device__ __forceinline__ uint64_t l2_policy() {
+    uint64_t pol;
+    if (LAST) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 16 KB of zeros (never written) that fill the rows of a decode operand tile past the
 // unit's position: a bulk copy of it hits L2, where the cache's own zero rows cost HBM reads.
 static __device__ __align__(128) unsigned char kZeroTile[16384];
@@ -181,8 +196,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
     // hold data: the copies take the 8-row groups that contain them (2 KB each in every
     // tile) and the T rows below pu.  The rest of each tile, zero in the cache, is copied
     // from kZeroTile instead, which every CTA reads and so stays in L2.
+    const uint64_t pol_keep = l2_policy<true>();
     auto tile_g2s = [&](unsigned char* dst, const unsigned char* src, uint32_t head, uint64_t* bar) {
-        if (head) bulk_g2s(dst, src, head, bar);
+        if (head) bulk_g2s_hint(dst, src, head, bar, pol_keep);
         if (head < 16384u) bulk_g2s(dst + head, kZeroTile, 16384u - head, bar);
     };
     auto issue_KV = [&](int u, int pu) {   // K and V tiles and the T rows
@@ -190,11 +206,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tc_decode(TcDecArgs a) {
         mbar_expect_tx(bar_KV, 2 * 16384u + tr);
         tile_g2s(sm + S::Kmn, k_tile(u), kv, bar_KV);
         tile_g2s(sm + S::Vt, v_tile(u), kv, bar_KV);
-        if (tr) bulk_g2s(sm + S::Tt, a.cache + a.co.t_rows + (size_t)u * C * C * 4, tr, bar_KV);
+        if (tr) bulk_g2s_hint(sm + S::Tt, a.cache + a.co.t_rows + (size_t)u * C * C * 4, tr, bar_KV, pol_keep);
     };
+    // The state tiles (64 KB a unit, 134 MB a step on 2048 units) stream through L2 with the
+    // evict-first priority, and the chunk's K, V, Delta and T rows, which every step of the
+    // chunk reads again, are read with evict-last, so that they can stay in L2 from one step
+    // to the next.
+    const uint64_t pol_stream = l2_policy<false>();
     auto issue_H = [&](int u) {
         mbar_expect_tx(bar_H, 65536);
-        bulk_g2s(sm + S::Hhi, a.cache + a.co.state_tiles + (size_t)u * 65536, 65536, bar_H);
+        bulk_g2s_hint(sm + S::Hhi, a.cache + a.co.state_tiles + (size_t)u * 65536, 65536, bar_H, pol_stream);
     };
     auto issue_D = [&](int u, int pu) {  // the Delta hi and lo tiles
         const uint32_t dt = (uint32_t)((pu + 7) >> 3) * 2048u;
