@@ -114,6 +114,28 @@ __device__ __forceinline__ void token_loop(float (&hr)[D / 2], RecSmem<D>& s, co
     }
 }
 
+// fp32 load and store with an L2 cache policy (createpolicy), and the policy itself.
+__device__ __forceinline__ float ld_hint(const float* p, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" :: "l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_keep_policy(bool keep) {
+    uint64_t pol;
+    if (keep) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// A decode step's recurrent states (64 KB a (sequence, head); the native step's and reading
+// B's running states) are read and written once a step, and all of them together are a
+// little more than L2 holds.  Those of 3 (sequence, head) in every 8 are accessed with the
+// evict-last priority, so that they can stay in L2 from one step to the next, and the others
+// with evict-first.
+constexpr int kRunKeepOf8 = 3;
+
 template <int D, typename IO>
 __global__ void __launch_bounds__(2 * D) k_rec(RecArgs a) {
     __shared__ RecSmem<D> s;
@@ -139,14 +161,24 @@ __global__ void __launch_bounds__(2 * D) k_rec(RecArgs a) {
     // the state: column j, this thread's half of the rows
     float hr[D / 2];
     const float* hin = a.cu ? a.h0 : a.state;
+    const uint64_t pol = l2_keep_policy((int)(sh % 8) < kRunKeepOf8);   // (the decode step's)
 #pragma unroll
-    for (int i = 0; i < D / 2; ++i)
-        hr[i] = hin ? hin[(sh * D + part * (D / 2) + i) * D + j] : 0.f;
+    for (int i = 0; i < D / 2; ++i) {
+        hr[i] = 0.f;
+        if (hin) {
+            const float* src = hin + (sh * D + part * (D / 2) + i) * D + j;
+            hr[i] = a.cu ? *src : ld_hint(src, pol);
+        }
+    }
     token_loop<D, IO>(hr, s, q, k, v, a.g, a.beta, H, h, a.scale, t0, t1, a.o);
     float* hout = a.cu ? a.final_state : a.state;
     if (hout) {
 #pragma unroll
-        for (int i = 0; i < D / 2; ++i) hout[(sh * D + part * (D / 2) + i) * D + j] = hr[i];
+        for (int i = 0; i < D / 2; ++i) {
+            float* dst = hout + (sh * D + part * (D / 2) + i) * D + j;
+            if (a.cu) *dst = hr[i];
+            else st_hint(dst, hr[i], pol);
+        }
     }
 }
 
@@ -193,6 +225,7 @@ __global__ void __launch_bounds__(256) k_rb(RbArgs a) {
 // is read) and CPR_ERR_CONTRACT_MISMATCH is recorded.  Under the caller's no-commit claim
 // every CTA reads every sequence's position: if one is C - 1 (its chunk would complete, but
 // no commit follows) every CTA leaves, nothing is written and CPR_ERR_COMMIT_DUE is recorded.
+
 __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
     constexpr int D = 128;
     __shared__ RecSmem<D> s;
@@ -220,6 +253,7 @@ __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
     const int p = ok_s - 1;   // this step's row in its chunk
     const size_t sh = (size_t)b * H + h;
     float* run = a.run + sh * D * D;
+    const uint64_t pol = l2_keep_policy((int)(sh % 8) < kRunKeepOf8);
     float hr[D / 2];
     if (p == 0) {
         const float* st = a.state + sh * D * D;
@@ -231,11 +265,11 @@ __global__ void __launch_bounds__(256) k_rb_step(RbStepArgs a) {
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < D / 2; ++i) hr[i] = run[(part * (D / 2) + i) * D + j];
+        for (int i = 0; i < D / 2; ++i) hr[i] = ld_hint(run + (part * (D / 2) + i) * D + j, pol);
     }
     token_loop<D, __nv_bfloat16>(hr, s, a.q, a.k, a.v, a.g, a.beta, H, h, a.scale, b, b + 1, a.o);
 #pragma unroll
-    for (int i = 0; i < D / 2; ++i) run[(part * (D / 2) + i) * D + j] = hr[i];
+    for (int i = 0; i < D / 2; ++i) st_hint(run + (part * (D / 2) + i) * D + j, hr[i], pol);
     const size_t row = (size_t)b * kChunk + p;   // the chunk rows' token index
     if (tid < D) {
         a.rk[(row * H + h) * D + tid] = a.k[sh * D + tid];
