@@ -72,3 +72,32 @@ def test_step_bytes_follow_the_methods_per_head_token_figures():
     t.lens, t.op = [4096] * 8, "fwdbwd"
     assert bench.step_bytes(t, 2) == 524288 * (1032 + 1808) + 2 * 8 * 16 * 128 * 128 * 4
     assert bench.step_bytes(t, 4) == 524288 * (1288 + 2832) + 2 * 8 * 16 * 128 * 128 * 4
+
+
+class _DecodeStep:
+    """The parts of bench's decode step that roofline_for reads."""
+    name, d, H, op = "decode", 128, 32, "decode"
+    lens = [2048] * 64
+
+    def kernel_units(self, name):
+        return len(self.lens) * self.H
+
+
+def test_stored_traffic_only_for_the_full_workload(monkeypatch):
+    """profiles/traffic.json holds ncu DRAM bytes of a full-workload launch: the bench line
+    carries them only while the kernel's sources still hash to the stored key and the run
+    covers the whole workload (not --n-seq)."""
+    pk = {"bf16_tflops": 1941.2, "hbm_gbs": 6777.6, "sm_max_mhz": 2070}
+    prof = {"cpr_tc_decode": (512, 512 * 0.09)}
+    key = bench.kernel_src_sha("cpr_tc_decode")
+    monkeypatch.setattr(bench, "load_traffic", lambda: {
+        "cpr_tc_decode/decode": {"bytes_per_launch": 123456789, "kernel_src_sha": key}})
+    monkeypatch.setattr(bench, "N_SEQ_OVERRIDE", None)
+    r = bench.roofline_for(_DecodeStep(), prof, pk)
+    assert r["traffic"] == 123456789 and r["traffic_gbs"] == round(123456789 / 90e-6 / 1e9, 1)
+    monkeypatch.setattr(bench, "N_SEQ_OVERRIDE", 16)
+    assert bench.roofline_for(_DecodeStep(), prof, pk)["traffic"] is None
+    monkeypatch.setattr(bench, "N_SEQ_OVERRIDE", None)
+    monkeypatch.setattr(bench, "load_traffic", lambda: {
+        "cpr_tc_decode/decode": {"bytes_per_launch": 123456789, "kernel_src_sha": "0" * 16}})
+    assert bench.roofline_for(_DecodeStep(), prof, pk)["traffic"] is None
