@@ -227,3 +227,17 @@ def test_deployment_digest_needs_a_device(lib):
     assert lib.cpr_deployment_digest(out, None, 0) == 6
     assert "device" in lib.cpr_last_error().decode()
     assert lib.cpr_deployment_digest(None, None, 0) == 1
+
+
+def test_nocommit_step_checks_arguments_on_the_host(lib):
+    """cpr_gdn_decode_step_nocommit refuses a missing cache or a wrong digest before any
+    device work, under reading A (where it is the ordinary step) and reading B."""
+    a = cpr.default_contract(torch.bfloat16, 128, operand_policy=cpr.CPR_POLICY_TC_BF16X3, dv_splits=2)
+    b = cpr.Contract.from_buffer_copy(a)
+    b.intra_order = cpr.CPR_ORDER_TOKENREC_V1
+    p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    bad = (ctypes.c_uint8 * 32).from_buffer_copy(bytes(32))
+    for c in (a, b):
+        dig = (ctypes.c_uint8 * 32).from_buffer_copy(cpr.contract_digest(c))
+        assert lib.cpr_gdn_decode_step_nocommit(ctypes.byref(c), dig, *p[:5], 1, 1, None, p[6], None) == 1
+        assert lib.cpr_gdn_decode_step_nocommit(ctypes.byref(c), bad, *p[:5], 1, 1, p[5], p[6], None) == 4
